@@ -1,0 +1,570 @@
+/*
+ * ORACLE -- test infrastructure only.  Nothing in the product path links,
+ * loads or calls this file; only the tests, the smoke check and the bench's
+ * CPU-baseline leg do.
+ *
+ * A plain, single-threaded, deliberately slow statement of what the ONNX
+ * broadcast binary elementwise engine computes.  For every requested output
+ * element it decomposes the flat index over the FULL output shape, maps each
+ * dimension to the two inputs (index 0 on a size-1 dimension), reads both
+ * inputs, applies the operator and stores the result.  There is no
+ * coalescing, no loop family, no vectorisation and no blocking.
+ *
+ * Sources followed (page title -- section):
+ *  - "Binary Kernel Design" (onnx-light-cpu) -- "Operators and traversal":
+ *    right-aligned broadcasting, empty dimensions doing no work, the Mod
+ *    opset-28 sign rules, FLOAT16/BFLOAT16 through float conversion.
+ *  - "Binary Kernel Design" -- "Compute, scheduling, and safety": validation of
+ *    integer division, modulo and shifts; one byte per BOOL.
+ *  - 0verkilll/onnx "ops" package docs -- BatchNormalizationOp (inference
+ *    formula, channel axis 1), PReluOp (x >= 0 ? x : slope*x, slope broadcast
+ *    to the data), ClipOp (optional min/max bounds), Add/Sub/Mul.
+ *  - ncnn operators.md -- batchnorm, bias, binaryop, clip.
+ * Where the pages are silent the plain reading is taken (IEEE-754 binary32
+ * round-to-nearest-even arithmetic without contraction, two's-complement wrap
+ * for integers, C99 pow/fmod semantics, ONNX type lists).
+ *
+ * Compile with -ffp-contract=off and without fast-math: every float operation
+ * below must round on its own.
+ *
+ * Parity pins: every function here is pinned by tests/test_oracle_pins.py
+ * against numpy/Python library routines, closed forms, the sign tables that
+ * follow from the Mod rules, and brute force over tiny shapes.  Integer Pow
+ * with a negative exponent is the one reading with no outside pin (parity
+ * unpinned beyond its closed-form cases).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ---- the oracle's own operator and type codes (no shared header) ---- */
+enum {
+    OR_ADD = 0, OR_SUB, OR_MUL, OR_DIV, OR_MOD, OR_POW,
+    OR_EQUAL, OR_LESS, OR_GREATER, OR_LESS_EQUAL, OR_GREATER_EQUAL,
+    OR_AND, OR_OR, OR_XOR,
+    OR_BITWISE_AND, OR_BITWISE_OR, OR_BITWISE_XOR,
+    OR_BITSHIFT, OR_PRELU,
+    OR_BATCHNORM, OR_CLIP,
+    OR_NUM_OPS
+};
+enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL, OT_NUM };
+
+/* return codes */
+enum { OR_OK = 0, OR_SHAPES = 1, OR_ARGS = 2, OR_TYPE = 3, OR_ATTR = 4 };
+/* per-element validation findings, OR-ed into *status */
+enum { OR_ST_DIV_BY_ZERO = 1u, OR_ST_SHIFT_RANGE = 2u };
+
+#define OR_MAX_RANK 8
+
+static int size_of(int t)
+{
+    switch (t) {
+    case OT_F32: case OT_I32: case OT_U32: return 4;
+    case OT_F16: case OT_BF16: return 2;
+    case OT_I64: return 8;
+    case OT_U8: case OT_BOOL: return 1;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* half and bfloat16 <-> float, written out from the IEEE-754 binary16 and   */
+/* bfloat16 encodings.  Widening is exact; narrowing rounds to nearest, ties */
+/* to even, overflows to infinity and keeps NaN a NaN.                       */
+/* ------------------------------------------------------------------------ */
+static float bits_to_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t f32_to_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+float oracle_half_to_float(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) << 31;
+    uint32_t exp = (h >> 10) & 0x1F;
+    uint32_t man = h & 0x3FF;
+    if (exp == 0) {
+        /* zero or subnormal: man * 2^-24, exact in binary32 */
+        float v = (float)man * 5.9604644775390625e-08f;
+        return sign ? -v : v;
+    }
+    if (exp == 31) return bits_to_f32(sign | 0x7F800000u | (man << 13));
+    return bits_to_f32(sign | ((exp - 15 + 127) << 23) | (man << 13));
+}
+
+/* shift a positive integer right by s bits, rounding to nearest, ties to even */
+static uint32_t shift_round_even(uint32_t m, int s)
+{
+    if (s <= 0) return m;
+    if (s > 31) return 0;
+    uint32_t q = m >> s;
+    uint32_t rem = m & ((1u << s) - 1u);
+    uint32_t half = 1u << (s - 1);
+    if (rem > half || (rem == half && (q & 1u))) q += 1;
+    return q;
+}
+
+uint16_t oracle_float_to_half(float f)
+{
+    uint32_t x = f32_to_bits(f);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ax = x & 0x7FFFFFFFu;
+    if (ax > 0x7F800000u) return sign | 0x7E00u;           /* NaN stays NaN */
+    if (ax == 0x7F800000u) return sign | 0x7C00u;          /* infinity */
+    int e = (int)(ax >> 23) - 127;                          /* unbiased exponent */
+    uint32_t m = (ax & 0x7FFFFFu) | (ax >= 0x00800000u ? 0x800000u : 0u);
+    if (ax < 0x00800000u) e = -126;                          /* binary32 subnormal */
+    if (e >= -14) {
+        /* half normal range: keep 10 fraction bits, round the other 13 */
+        uint32_t q = shift_round_even(m, 13);                /* 11-bit significand, may carry */
+        int he = e + 15;
+        if (q == 0x800u) { q = 0x400u; he += 1; }            /* carry into the exponent */
+        if (he >= 31) return sign | 0x7C00u;                 /* overflow -> infinity */
+        return sign | (uint16_t)((uint32_t)he << 10) | (uint16_t)(q & 0x3FFu);
+    }
+    /* half subnormal range: value = q * 2^-24, q = m * 2^(e-23) * 2^24 */
+    int s = 13 + (-14 - e);                                  /* extra shift below 2^-14 */
+    uint32_t q = shift_round_even(m, s);                     /* q <= 0x400 */
+    return sign | (uint16_t)q;                               /* 0x400 is the smallest normal */
+}
+
+float oracle_bf16_to_float(uint16_t b) { return bits_to_f32((uint32_t)b << 16); }
+
+uint16_t oracle_float_to_bf16(float f)
+{
+    uint32_t x = f32_to_bits(f);
+    if ((x & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((x >> 16) | 0x0040u);   /* NaN */
+    uint32_t hi = x >> 16;
+    uint32_t lo = x & 0xFFFFu;
+    if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1;   /* carries reach inf */
+    return (uint16_t)hi;
+}
+
+/* ------------------------------------------------------------------------ */
+/* element access                                                            */
+/* ------------------------------------------------------------------------ */
+static int is_float_type(int t) { return t == OT_F32 || t == OT_F16 || t == OT_BF16; }
+static int is_signed_int(int t) { return t == OT_I32 || t == OT_I64; }
+static int is_int_type(int t) { return t == OT_I32 || t == OT_I64 || t == OT_U8 || t == OT_U32; }
+
+static float load_float(const void *p, int t, int64_t i)
+{
+    if (t == OT_F32) return ((const float *)p)[i];
+    if (t == OT_F16) return oracle_half_to_float(((const uint16_t *)p)[i]);
+    return oracle_bf16_to_float(((const uint16_t *)p)[i]);
+}
+
+static void store_float(void *p, int t, int64_t i, float v)
+{
+    if (t == OT_F32) ((float *)p)[i] = v;
+    else if (t == OT_F16) ((uint16_t *)p)[i] = oracle_float_to_half(v);
+    else ((uint16_t *)p)[i] = oracle_float_to_bf16(v);
+}
+
+/* integers travel as their value in int64 (uint32 fits), wrapped on store */
+static int64_t load_int(const void *p, int t, int64_t i)
+{
+    switch (t) {
+    case OT_I32: return ((const int32_t *)p)[i];
+    case OT_I64: return ((const int64_t *)p)[i];
+    case OT_U8: case OT_BOOL: return ((const uint8_t *)p)[i];
+    case OT_U32: return ((const uint32_t *)p)[i];
+    }
+    return 0;
+}
+
+static void store_int(void *p, int t, int64_t i, uint64_t v)
+{
+    switch (t) {
+    case OT_I32: ((uint32_t *)p)[i] = (uint32_t)v; break;
+    case OT_I64: ((uint64_t *)p)[i] = v; break;
+    case OT_U8: case OT_BOOL: ((uint8_t *)p)[i] = (uint8_t)v; break;
+    case OT_U32: ((uint32_t *)p)[i] = (uint32_t)v; break;
+    }
+}
+
+static int bits_of(int t) { return 8 * size_of(t); }
+
+/* reinterpret a wrapped bit pattern of width w as a signed value */
+static int64_t as_signed(uint64_t v, int w)
+{
+    if (w == 64) return (int64_t)v;
+    uint64_t m = (1ull << w) - 1ull;
+    v &= m;
+    if (v >> (w - 1)) return (int64_t)(v | ~m);
+    return (int64_t)v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* descriptor rules (which operator accepts which type; attribute checks)    */
+/* ------------------------------------------------------------------------ */
+int oracle_type_allowed(int op, int t)
+{
+    switch (op) {
+    case OR_ADD: case OR_SUB: case OR_MUL: case OR_DIV: case OR_MOD:
+    case OR_LESS: case OR_GREATER: case OR_LESS_EQUAL: case OR_GREATER_EQUAL:
+    case OR_CLIP:
+        return t != OT_BOOL && t >= 0 && t < OT_NUM;
+    case OR_POW:
+        return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64;
+    case OR_EQUAL:
+        return t >= 0 && t < OT_NUM;
+    case OR_AND: case OR_OR: case OR_XOR:
+        return t == OT_BOOL;
+    case OR_BITWISE_AND: case OR_BITWISE_OR: case OR_BITWISE_XOR:
+        return is_int_type(t);
+    case OR_BITSHIFT:
+        return t == OT_U8 || t == OT_U32;
+    case OR_PRELU:
+        return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64 ||
+               t == OT_U32;
+    case OR_BATCHNORM:
+        return is_float_type(t);
+    }
+    return 0;
+}
+
+int oracle_output_type(int op, int t)
+{
+    if (op >= OR_EQUAL && op <= OR_XOR) return OT_BOOL;
+    return t;
+}
+
+/*
+ * Descriptor check.  Mod: opset 10..28; floating inputs need fmod=1 before
+ * opset 28 ("Binary Kernel Design", Operators and traversal); fmod in {0,1}.
+ * BitShift: direction 0 (LEFT) or 1 (RIGHT).
+ */
+int oracle_check_descriptor(int op, int opset, int fmod, int direction, int ta, int tb)
+{
+    if (op < 0 || op >= OR_NUM_OPS) return OR_ARGS;
+    if (ta != tb) return OR_TYPE;
+    if (!oracle_type_allowed(op, ta)) return OR_TYPE;
+    if (op == OR_MOD) {
+        if (opset < 10 || opset > 28) return OR_ATTR;
+        if (fmod != 0 && fmod != 1) return OR_ATTR;
+        if (is_float_type(ta) && fmod == 0 && opset < 28) return OR_ATTR;
+    }
+    if (op == OR_BITSHIFT && direction != 0 && direction != 1) return OR_ATTR;
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* scalar semantics                                                          */
+/* ------------------------------------------------------------------------ */
+static float float_mod(float a, float b, int fmod_flag)
+{
+    float r = fmodf(a, b);                 /* exact truncated remainder, sign of a */
+    if (fmod_flag) return r;
+    /* floor remainder: a nonzero result takes the divisor's sign by adding b,
+       an exact zero takes the divisor's sign */
+    if (r == 0.0f) return copysignf(0.0f, b);
+    if (signbit(r) != signbit(b)) r = r + b;
+    return r;
+}
+
+static float float_op(int op, float a, float b, int fmod_flag)
+{
+    switch (op) {
+    case OR_ADD: return a + b;
+    case OR_SUB: return a - b;
+    case OR_MUL: return a * b;
+    case OR_DIV: return a / b;
+    case OR_MOD: return float_mod(a, b, fmod_flag);
+    case OR_POW: return (float)pow((double)a, (double)b);
+    case OR_PRELU: return (a >= 0.0f) ? a : b * a;      /* slope * x below zero */
+    }
+    return 0.0f;
+}
+
+static int float_cmp(int op, float a, float b)
+{
+    switch (op) {
+    case OR_EQUAL: return a == b;
+    case OR_LESS: return a < b;
+    case OR_GREATER: return a > b;
+    case OR_LESS_EQUAL: return a <= b;
+    case OR_GREATER_EQUAL: return a >= b;
+    }
+    return 0;
+}
+
+static int int_cmp(int op, int64_t a, int64_t b)
+{
+    switch (op) {
+    case OR_EQUAL: return a == b;
+    case OR_LESS: return a < b;
+    case OR_GREATER: return a > b;
+    case OR_LESS_EQUAL: return a <= b;
+    case OR_GREATER_EQUAL: return a >= b;
+    }
+    return 0;
+}
+
+/* integer operator on values a, b of type t; returns the wrapped bit pattern */
+static uint64_t int_op(int op, int t, int64_t a, int64_t b, int fmod_flag, int direction,
+                       uint32_t *status)
+{
+    int w = bits_of(t);
+    int sgn = is_signed_int(t);
+    uint64_t ua = (uint64_t)a, ub = (uint64_t)b;
+    switch (op) {
+    case OR_ADD: return ua + ub;
+    case OR_SUB: return ua - ub;
+    case OR_MUL: return ua * ub;
+    case OR_DIV:
+        if (b == 0) { *status |= OR_ST_DIV_BY_ZERO; return 0; }
+        if (sgn && b == -1) return 0ull - ua;                 /* INT_MIN / -1 wraps */
+        return (uint64_t)(a / b);                              /* C truncation */
+    case OR_MOD: {
+        if (b == 0) { *status |= OR_ST_DIV_BY_ZERO; return 0; }
+        if (sgn && b == -1) return 0;
+        int64_t r = a % b;                                     /* truncated, sign of a */
+        if (!fmod_flag && r != 0 && ((r < 0) != (b < 0))) r += b;   /* floor: sign of b */
+        return (uint64_t)r;
+    }
+    case OR_POW: {
+        if (b < 0) {
+            if (a == 0) { *status |= OR_ST_DIV_BY_ZERO; return 0; }
+            if (a == 1) return 1;
+            if (a == -1) return (b & 1) ? (uint64_t)-1 : 1;
+            return 0;                                          /* trunc(1 / a^|b|) */
+        }
+        uint64_t result = 1, base = ua;
+        uint64_t e = ub;
+        while (e) {                                            /* square and multiply */
+            if (e & 1u) result *= base;
+            base *= base;
+            e >>= 1;
+        }
+        return result;
+    }
+    case OR_BITWISE_AND: return ua & ub;
+    case OR_BITWISE_OR: return ua | ub;
+    case OR_BITWISE_XOR: return ua ^ ub;
+    case OR_BITSHIFT: {
+        uint64_t s = ub;
+        if (s >= (uint64_t)w) { *status |= OR_ST_SHIFT_RANGE; return 0; }
+        uint64_t mask = (w == 64) ? ~0ull : ((1ull << w) - 1ull);
+        return direction == 0 ? ((ua << s) & mask) : ((ua & mask) >> s);
+    }
+    case OR_PRELU:                                             /* x >= 0 ? x : slope * x */
+        return (!sgn || as_signed(ua, w) >= 0) ? ua : ub * ua;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* broadcasting                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * NumPy-style broadcast of two shapes: right-align, then each dimension pair
+ * must be equal or contain a 1; the output takes the larger (0 pairs with 1
+ * and gives 0).  Rank-0 shapes are scalars.
+ */
+int oracle_broadcast_shape(const int64_t *sa, int ra, const int64_t *sb, int rb,
+                           int64_t *so, int *ro)
+{
+    if (ra < 0 || rb < 0 || ra > OR_MAX_RANK || rb > OR_MAX_RANK) return OR_ARGS;
+    int r = ra > rb ? ra : rb;
+    for (int d = 0; d < r; ++d) {
+        int ia = d - (r - ra), ib = d - (r - rb);
+        int64_t x = ia >= 0 ? sa[ia] : 1;
+        int64_t y = ib >= 0 ? sb[ib] : 1;
+        if (x < 0 || y < 0) return OR_ARGS;
+        if (x == y) so[d] = x;
+        else if (x == 1) so[d] = y;
+        else if (y == 1) so[d] = x;
+        else return OR_SHAPES;
+    }
+    *ro = r;
+    return OR_OK;
+}
+
+/* dense row-major strides of `shape` right-aligned into rank r; 0 on size-1 dims */
+static void aligned_strides(const int64_t *shape, int rank, int r, int64_t *stride)
+{
+    int64_t s = 1;
+    for (int d = r - 1; d >= 0; --d) {
+        int i = d - (r - rank);
+        int64_t n = i >= 0 ? shape[i] : 1;
+        stride[d] = (n == 1) ? 0 : s;
+        s *= n;
+    }
+}
+
+static int64_t numel(const int64_t *shape, int rank)
+{
+    int64_t n = 1;
+    for (int d = 0; d < rank; ++d) n *= shape[d];
+    return n;
+}
+
+/* element offsets into A and B of flat output index f (full multi-index) */
+static void offsets_of(int64_t f, const int64_t *so, int r, const int64_t *sta,
+                       const int64_t *stb, int64_t *oa, int64_t *ob)
+{
+    int64_t a = 0, b = 0;
+    for (int d = r - 1; d >= 0; --d) {
+        int64_t idx = f % so[d];
+        f /= so[d];
+        a += idx * sta[d];
+        b += idx * stb[d];
+    }
+    *oa = a;
+    *ob = b;
+}
+
+/* channel index (axis 1 of the output) of flat output index f */
+static int64_t channel_of(int64_t f, const int64_t *so, int r)
+{
+    for (int d = r - 1; d > 1; --d) f /= so[d];
+    return f % so[1];
+}
+
+/* exposed for the planner tests: A and B offsets of each listed output index */
+int oracle_offsets(const int64_t *sa, int ra, const int64_t *sb, int rb, const int64_t *idx,
+                   int64_t n, int64_t *oa, int64_t *ob)
+{
+    int64_t so[OR_MAX_RANK], sta[OR_MAX_RANK], stb[OR_MAX_RANK];
+    int r;
+    int rc = oracle_broadcast_shape(sa, ra, sb, rb, so, &r);
+    if (rc) return rc;
+    aligned_strides(sa, ra, r, sta);
+    aligned_strides(sb, rb, r, stb);
+    for (int64_t i = 0; i < n; ++i) offsets_of(idx[i], so, r, sta, stb, &oa[i], &ob[i]);
+    return OR_OK;
+}
+
+/*
+ * Evaluate output elements at the flat indices idx[0..n) (idx == NULL means
+ * every element 0..numel-1, in order) and store them densely in out.
+ *
+ * Operands:
+ *  - ordinary ops: A and B of types ta == tb, broadcast against each other;
+ *  - PRelu: B (slope) must broadcast to A's shape, out shape == A shape;
+ *  - BatchNormalization (inference): A = x [N, C, ...] (rank >= 2), B = [4, C]
+ *    holding scale, bias, mean, var rows; per element, in binary32 and in the
+ *    order written, y = (x - mean) / sqrt(var + eps) * scale + bias;
+ *  - Clip: B = [2] holding {min, max}; has_min / has_max say which bound
+ *    applies; y = x, then raised to min if below it, then lowered to max if
+ *    above it.
+ * Out shape: see oracle_output_shape.
+ */
+int oracle_output_shape(int op, const int64_t *sa, int ra, const int64_t *sb, int rb,
+                        int64_t *so, int *ro)
+{
+    if (op == OR_BATCHNORM) {
+        if (ra < 2 || rb != 2 || sb[0] != 4 || sb[1] != sa[1]) return OR_SHAPES;
+        for (int d = 0; d < ra; ++d) so[d] = sa[d];
+        *ro = ra;
+        return OR_OK;
+    }
+    if (op == OR_CLIP) {
+        if (!(rb == 1 && sb[0] == 2)) return OR_SHAPES;
+        for (int d = 0; d < ra; ++d) so[d] = sa[d];
+        *ro = ra;
+        return OR_OK;
+    }
+    int rc = oracle_broadcast_shape(sa, ra, sb, rb, so, ro);
+    if (rc) return rc;
+    if (op == OR_PRELU) {
+        /* slope broadcasts one way only: the output keeps the data's shape */
+        if (*ro != ra) return OR_SHAPES;
+        for (int d = 0; d < ra; ++d)
+            if (so[d] != sa[d]) return OR_SHAPES;
+    }
+    return OR_OK;
+}
+
+int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_min, int has_max,
+                const int64_t *sa, int ra, const int64_t *sb, int rb,
+                const void *A, const void *B, void *out,
+                const int64_t *idx, int64_t n_idx, uint32_t *status)
+{
+    int64_t so[OR_MAX_RANK], sta[OR_MAX_RANK], stb[OR_MAX_RANK];
+    int r;
+    *status = 0;
+    if (op < 0 || op >= OR_NUM_OPS || !oracle_type_allowed(op, t)) return OR_TYPE;
+    int rc = oracle_output_shape(op, sa, ra, sb, rb, so, &r);
+    if (rc) return rc;
+    int64_t total = numel(so, r);
+    int64_t count = idx ? n_idx : total;
+    int to = oracle_output_type(op, t);
+    aligned_strides(sa, ra, r, sta);
+    if (op != OR_BATCHNORM && op != OR_CLIP) aligned_strides(sb, rb, r, stb);
+    else for (int d = 0; d < r; ++d) stb[d] = 0;
+
+    for (int64_t k = 0; k < count; ++k) {
+        int64_t f = idx ? idx[k] : k;
+        if (f < 0 || f >= total) return OR_ARGS;
+        int64_t oa, ob;
+        offsets_of(f, so, r, sta, stb, &oa, &ob);
+
+        if (op == OR_BATCHNORM) {
+            int64_t C = sb[1], c = channel_of(f, so, r);
+            float x = load_float(A, t, oa);
+            float scale = load_float(B, t, 0 * C + c);
+            float bias = load_float(B, t, 1 * C + c);
+            float mean = load_float(B, t, 2 * C + c);
+            float var = load_float(B, t, 3 * C + c);
+            float y = (x - mean) / sqrtf(var + eps) * scale + bias;
+            store_float(out, t, k, y);
+            continue;
+        }
+        if (op == OR_CLIP) {
+            if (is_float_type(t)) {
+                float y = load_float(A, t, oa);
+                if (has_min) { float lo = load_float(B, t, 0); if (y < lo) y = lo; }
+                if (has_max) { float hi = load_float(B, t, 1); if (y > hi) y = hi; }
+                store_float(out, t, k, y);
+            } else {
+                int64_t y = load_int(A, t, oa);
+                if (has_min) { int64_t lo = load_int(B, t, 0); if (y < lo) y = lo; }
+                if (has_max) { int64_t hi = load_int(B, t, 1); if (y > hi) y = hi; }
+                store_int(out, t, k, (uint64_t)y);
+            }
+            continue;
+        }
+        if (to == OT_BOOL) {
+            int v;
+            if (op == OR_AND || op == OR_OR || op == OR_XOR) {
+                int x = load_int(A, t, oa) != 0, y = load_int(B, t, ob) != 0;
+                v = op == OR_AND ? (x && y) : op == OR_OR ? (x || y) : (x != y);
+            } else if (is_float_type(t)) {
+                v = float_cmp(op, load_float(A, t, oa), load_float(B, t, ob));
+            } else if (t == OT_BOOL) {
+                v = int_cmp(op, load_int(A, t, oa) != 0, load_int(B, t, ob) != 0);
+            } else {
+                v = int_cmp(op, load_int(A, t, oa), load_int(B, t, ob));
+            }
+            ((uint8_t *)out)[k] = (uint8_t)(v ? 1 : 0);
+            continue;
+        }
+        if (is_float_type(t)) {
+            float y = float_op(op, load_float(A, t, oa), load_float(B, t, ob), fmod_flag);
+            store_float(out, t, k, y);
+        } else {
+            uint64_t y = int_op(op, t, load_int(A, t, oa), load_int(B, t, ob), fmod_flag,
+                                direction, status);
+            store_int(out, t, k, y);
+        }
+    }
+    return OR_OK;
+}
+
+/* bulk forms of the conversions above, for the pin tests */
+void oracle_f32_to_f16_n(const float *x, uint16_t *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_float_to_half(x[i]);
+}
+void oracle_f32_to_bf16_n(const float *x, uint16_t *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_float_to_bf16(x[i]);
+}
+void oracle_f16_to_f32_n(const uint16_t *x, float *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_half_to_float(x[i]);
+}
+void oracle_bf16_to_f32_n(const uint16_t *x, float *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_bf16_to_float(x[i]);
+}

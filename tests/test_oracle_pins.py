@@ -1,0 +1,644 @@
+"""Pins of the oracle against things other than itself (CPU only).
+
+Each test checks the oracle against a library routine that does not share the
+oracle's code (numpy / torch ufuncs, Python integers, exact rational
+arithmetic with ``fractions``, arbitrary precision ``mpmath``), a closed form
+or worked table under ``tests/golden/`` (each with its citation), an identity,
+or brute force over tiny shapes.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+from conftest import assert_bits_equal, ulp_distance
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def f32(*v):
+    return np.array(v, dtype=np.float32)
+
+
+def bf16_bits(x_f32):
+    return torch.from_numpy(np.ascontiguousarray(x_f32, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_to_f32(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16) \
+        .float().numpy()
+
+
+SPECIALS = f32(0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45, 1.17549435e-38,
+               3.4028235e38, -3.4028235e38, 65504.0, 65520.0, 6.1035156e-05, 5.9604645e-08,
+               2.9802322e-08, 0.5, 3.0, -7.0, 1e30, 1e-30)
+
+
+def float_corpus(n, seed):
+    """Random float32 bit patterns (all exponents) plus values of moderate size and specials."""
+    bits = datagen.raw_u32(seed, 0, n).view(np.float32)
+    mid = datagen.normal(seed, 1, n) * np.float32(100.0)
+    return np.concatenate([bits, mid, SPECIALS])
+
+
+# --------------------------------------------------------------------------- conversions
+
+def stratified_f32_bits():
+    """All 2^16 upper halves times low halves that sit on and around every rounding boundary."""
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = np.array([0x0000, 0x0001, 0x0FFF, 0x1000, 0x1001, 0x1FFF, 0x2000, 0x3000, 0x7FFF,
+                     0x8000, 0x8001, 0xC000, 0xE000, 0xF000, 0xFFFF, 0x5A5A], dtype=np.uint32)
+    rnd = datagen.raw_u32(7, 0, 16) & 0xFFFF
+    lows = np.concatenate([lows, rnd.astype(np.uint32)])
+    return (hi[:, None] | lows[None, :]).reshape(-1).view(np.float32)
+
+
+def test_half_widening_exhaustive():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    got = oracle.f16_bits_to_f32(bits)
+    want = bits.view(np.float16).astype(np.float32)
+    assert_bits_equal(got, want, "float32", "half->float")
+
+
+def test_bf16_widening_exhaustive():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    got = oracle.bf16_bits_to_f32(bits)
+    want = bf16_to_f32(bits)
+    assert_bits_equal(got, want, "float32", "bf16->float")
+
+
+def test_half_narrowing_matches_numpy():
+    x = stratified_f32_bits()
+    got = oracle.f32_to_f16_bits(x)
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    assert_bits_equal(got.view(np.float16), want.view(np.float16), "float16", "float->half")
+
+
+def test_bf16_narrowing_matches_torch():
+    x = stratified_f32_bits()
+    got = oracle.f32_to_bf16_bits(x)
+    want = bf16_bits(x)
+    assert_bits_equal(got, want, "bfloat16", "float->bf16")
+
+
+# --------------------------------------------------------------------------- broadcasting
+
+def all_small_shapes():
+    shapes = [()]
+    for r in (1, 2, 3):
+        for flat in range(4 ** r):
+            shapes.append(tuple((flat // 4 ** k) % 4 for k in range(r))[::-1])
+    return shapes
+
+
+def test_broadcast_shape_brute_force():
+    shapes = all_small_shapes()
+    assert len(shapes) == 85
+    for sa in shapes:
+        for sb in shapes:
+            try:
+                want = np.broadcast_shapes(sa, sb)
+            except ValueError:
+                want = None
+            try:
+                got = oracle.output_shape("Add", sa, sb)
+            except ValueError as e:
+                assert str(e) == "incompatible_shapes"
+                got = None
+            assert got == want, (sa, sb, got, want)
+
+
+def test_broadcast_values_brute_force():
+    """Every compatible pair of tiny shapes: oracle Add/Sub == numpy broadcasting, bit for bit."""
+    shapes = all_small_shapes()
+    for sa in shapes:
+        for sb in shapes:
+            try:
+                np.broadcast_shapes(sa, sb)
+            except ValueError:
+                continue
+            a = datagen.make("uniform", "float32", sa, 0, 0)
+            b = datagen.make("uniform", "float32", sb, 0, 1)
+            for op, fn in (("Add", np.add), ("Sub", np.subtract)):
+                got, st = oracle.run(op, a, b, "float32")
+                assert st == 0
+                assert_bits_equal(got, fn(a, b), "float32", "%s %s %s" % (op, sa, sb))
+
+
+def test_offsets_match_numpy_index_mapping():
+    sa, sb = (2, 1, 4, 1), (3, 1, 5)
+    out_shape = np.broadcast_shapes(sa, sb)
+    n = int(np.prod(out_shape))
+    ia = np.broadcast_to(np.arange(np.prod(sa)).reshape(sa), out_shape).reshape(-1)
+    ib = np.broadcast_to(np.arange(np.prod(sb)).reshape(sb), out_shape).reshape(-1)
+    oa, ob = oracle.offsets(sa, sb, np.arange(n))
+    assert (oa == ia).all() and (ob == ib).all()
+
+
+def test_empty_dims_do_no_work():
+    """numel 0: no element is read (NULL inputs are fine) and the output is untouched."""
+    lib = oracle._load()
+    sa = np.array([0, 3], np.int64)
+    sb = np.array([3], np.int64)
+    st = np.zeros(1, np.uint32)
+    rc = lib.oracle_eval(oracle.OPS.index("Div"), oracle.DTYPES.index("int32"), 0, 0, 0.0, 1, 1,
+                         sa.ctypes.data, 2, sb.ctypes.data, 1, None, None, None, None, 0,
+                         st.ctypes.data)
+    assert rc == 0 and st[0] == 0
+    out, st2 = oracle.run("Add", np.zeros((2, 0, 3), np.float32), np.zeros((1, 3), np.float32),
+                          "float32")
+    assert out.shape == (2, 0, 3) and st2 == 0
+
+
+def test_coalescing_and_unit_dims_do_not_change_results():
+    x = datagen.make("normal", "bfloat16", (8, 4, 16, 16), 2, 0)
+    b = datagen.make("uniform", "bfloat16", (4, 1, 1), 2, 1, lo=-0.5, hi=0.5)
+    full, _ = oracle.run("Add", x, b, "bfloat16")
+    merged, _ = oracle.run("Add", x.reshape(8, 4, 256), b.reshape(4, 1), "bfloat16")
+    unit, _ = oracle.run("Add", x.reshape(1, 8, 4, 1, 16, 16), b.reshape(1, 4, 1, 1, 1),
+                         "bfloat16")
+    assert full.tobytes() == merged.tobytes() == unit.tobytes()
+
+
+# --------------------------------------------------------------------------- float arithmetic
+
+@pytest.mark.parametrize("op,fn", [("Add", np.add), ("Sub", np.subtract), ("Mul", np.multiply),
+                                   ("Div", np.divide)])
+def test_f32_arith_matches_numpy(op, fn):
+    a = float_corpus(20000, 11)
+    b = float_corpus(20000, 12)
+    b = np.roll(b, 7)
+    got, st = oracle.run(op, a, b, "float32")
+    with np.errstate(all="ignore"):
+        want = fn(a, b)
+    assert st == 0
+    assert_bits_equal(got, want, "float32", op)
+
+
+@pytest.mark.parametrize("op,fn", [("Add", np.add), ("Sub", np.subtract), ("Mul", np.multiply),
+                                   ("Div", np.divide), ("Mod", np.remainder)])
+def test_f16_arith_matches_numpy_half(op, fn):
+    """numpy float16 ufuncs widen to float, operate and round once: the same semantics."""
+    a = np.concatenate([datagen.raw_u32(13, 0, 30000).astype(np.uint16).view(np.float16),
+                        datagen.make("normal", "float16", (30000,), 13, 1)])
+    b = np.concatenate([datagen.raw_u32(13, 2, 30000).astype(np.uint16).view(np.float16),
+                        datagen.make("normal", "float16", (30000,), 13, 3)])
+    got, st = oracle.run(op, a, b, "float16")
+    with np.errstate(all="ignore"):
+        want = fn(a, b)
+    assert_bits_equal(got, want, "float16", op)
+
+
+@pytest.mark.parametrize("op,fn", [("Add", torch.add), ("Sub", torch.sub), ("Mul", torch.mul),
+                                   ("Div", torch.div)])
+def test_bf16_arith_matches_torch(op, fn):
+    a = np.concatenate([datagen.raw_u32(14, 0, 30000).astype(np.uint16),
+                        datagen.make("normal", "bfloat16", (30000,), 14, 1)])
+    b = np.concatenate([datagen.raw_u32(14, 2, 30000).astype(np.uint16),
+                        datagen.make("normal", "bfloat16", (30000,), 14, 3)])
+    got, _ = oracle.run(op, a, b, "bfloat16")
+    ta = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    tb = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+    want = fn(ta, tb).view(torch.int16).numpy().view(np.uint16)
+    assert_bits_equal(got, want, "bfloat16", op)
+
+
+def test_f32_identities():
+    a = float_corpus(5000, 15)
+    b = np.roll(float_corpus(5000, 16), 3)
+    run = lambda op, x, y: oracle.run(op, x, y, "float32")[0]
+    negzero = f32(-0.0).reshape(())
+    one = f32(1.0).reshape(())
+    assert_bits_equal(run("Add", a, negzero), a, "float32", "A + (-0) == A")
+    assert_bits_equal(run("Mul", a, one), a, "float32", "A * 1 == A")
+    assert_bits_equal(run("Div", a, one), a, "float32", "A / 1 == A")
+    assert_bits_equal(run("Add", a, b), run("Add", b, a), "float32", "Add commutes")
+    assert_bits_equal(run("Mul", a, b), run("Mul", b, a), "float32", "Mul commutes")
+    assert_bits_equal(run("Sub", a, b), run("Add", a, -b), "float32", "A - B == A + (-B)")
+    # A + (+0) is not an identity: -0 + +0 = +0
+    assert run("Add", f32(-0.0), f32(0.0)).view(np.uint32)[0] == 0
+
+
+# --------------------------------------------------------------------------- Mod
+
+def rn32(x: Fraction) -> float:
+    """Round an exact rational to binary32, nearest, ties to even (subnormals, overflow)."""
+    if x == 0:
+        return 0.0
+    sign = -1.0 if x < 0 else 1.0
+    x = abs(x)
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while Fraction(2) ** e > x:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= x:
+        e += 1
+    e = max(e, -126)
+    quantum = Fraction(2) ** (e - 23)
+    m = x / quantum
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = n * quantum
+    if val >= Fraction(2) ** 128:
+        return sign * math.inf
+    return sign * float(val)
+
+
+def exact_mod(a: float, b: float, fmod_flag: int) -> float:
+    """Mod from exact rationals: truncated remainder, then the floor rule of opset 28."""
+    fa, fb = Fraction(a), Fraction(b)
+    q = fa / fb
+    t = q.numerator // q.denominator if q >= 0 else -((-q.numerator) // q.denominator)
+    r = fa - t * fb
+    if fmod_flag:
+        return math.copysign(0.0, a) if r == 0 else float(r)
+    if r == 0:
+        return math.copysign(0.0, b)
+    if (r < 0) != (fb < 0):
+        return rn32(r + fb)
+    return float(r)
+
+
+def mod_inputs(n, seed):
+    a = np.concatenate([datagen.uniform_zeros(seed, 0, n, -100, 100, 0.01),
+                        datagen.raw_u32(seed, 2, n).view(np.float32)])
+    b = np.concatenate([datagen.uniform_reject(seed, 1, n, -7, 7, 0.01),
+                        datagen.raw_u32(seed, 3, n).view(np.float32)])
+    ok = np.isfinite(a) & np.isfinite(b) & (b != 0)
+    return a[ok], b[ok]
+
+
+@pytest.mark.parametrize("fmod_flag", [0, 1])
+def test_f32_mod_exact_rational(fmod_flag):
+    a, b = mod_inputs(3000, 21)
+    got, st = oracle.run("Mod", a, b, "float32", fmod=fmod_flag)
+    want = np.array([exact_mod(float(x), float(y), fmod_flag) for x, y in zip(a, b)], np.float32)
+    assert st == 0
+    assert_bits_equal(got, want, "float32", "Mod fmod=%d" % fmod_flag)
+
+
+def test_f32_mod_matches_numpy_remainder():
+    """numpy.remainder is the floor remainder with a divisor-signed zero (fmod=0)."""
+    a = float_corpus(20000, 22)
+    b = np.roll(float_corpus(20000, 23), 5)
+    got, _ = oracle.run("Mod", a, b, "float32", fmod=0)
+    with np.errstate(all="ignore"):
+        want = np.remainder(a, b)
+    assert_bits_equal(got, want, "float32", "Mod fmod=0 vs numpy.remainder")
+
+
+def test_mod_sign_table():
+    for dtype, a, b, fm, want in read_golden("mod_sign_rules.txt"):
+        fm = int(fm)
+        if dtype in ("float32", "float16", "bfloat16"):
+            av, bv = f32(float(a)), f32(float(b))
+            if dtype == "float16":
+                av, bv = av.astype(np.float16), bv.astype(np.float16)
+            elif dtype == "bfloat16":
+                av, bv = bf16_bits(av), bf16_bits(bv)
+            got, _ = oracle.run("Mod", av, bv, dtype, fmod=fm)
+            g = got.astype(np.float32) if dtype == "float16" else \
+                bf16_to_f32(got) if dtype == "bfloat16" else got
+            w = float(want)
+            assert g[0] == w and math.copysign(1, g[0]) == math.copysign(1, w), \
+                (dtype, a, b, fm, g[0], w)
+        else:
+            st = datagen.STORAGE[dtype]
+            got, _ = oracle.run("Mod", np.array([int(a)]).astype(st), np.array([int(b)]).astype(st),
+                                dtype, fmod=fm)
+            assert int(got[0]) == int(want), (dtype, a, b, fm, got[0])
+
+
+def test_mod_specials():
+    nan, inf = np.nan, np.inf
+    a = f32(nan, inf, -inf, 5.0, 5.0, 5.0, -5.0, 5.0, -0.0)
+    b = f32(2.0, 2.0, 2.0, 0.0, -0.0, nan, inf, -inf, inf)
+    g0, _ = oracle.run("Mod", a, b, "float32", fmod=0)
+    g1, _ = oracle.run("Mod", a, b, "float32", fmod=1)
+    assert np.isnan(g0[:6]).all() and np.isnan(g1[:6]).all()
+    # fmod(a, +-inf) = a; the floor rule then moves a sign mismatch to the divisor
+    assert g1[6] == -5.0 and g1[7] == 5.0
+    assert g0[6] == inf and g0[7] == -inf
+    assert g0[8] == 0.0 and not math.copysign(1, g0[8]) < 0
+    assert g1[8] == 0.0 and math.copysign(1, g1[8]) < 0
+
+
+# --------------------------------------------------------------------------- integers
+
+INT_LIMITS = {"int32": (-(1 << 31), (1 << 31) - 1), "int64": (-(1 << 63), (1 << 63) - 1),
+              "uint8": (0, 255), "uint32": (0, (1 << 32) - 1)}
+
+
+def wrap(v, dtype):
+    lo, hi = INT_LIMITS[dtype]
+    m = hi - lo + 1
+    return (v - lo) % m + lo
+
+
+def int_pairs(dtype):
+    lo, hi = INT_LIMITS[dtype]
+    small = list(range(max(lo, -40), min(hi, 40) + 1))
+    edges = [lo, lo + 1, hi, hi - 1, 0, 1, 2, 3, 7, 255, 256]
+    edges += [lo // 2, hi // 3] if dtype != "uint8" else [128, 129]
+    vals = sorted(set(v for v in small + edges if lo <= v <= hi))
+    a, b = np.meshgrid(np.array(vals, dtype=object), np.array(vals, dtype=object))
+    return a.reshape(-1), b.reshape(-1)
+
+
+def trunc_div(a, b):
+    q = abs(a) // abs(b)
+    return q if (a >= 0) == (b >= 0) else -q
+
+
+@pytest.mark.parametrize("dtype", ["int32", "int64", "uint8", "uint32"])
+def test_int_arith_matches_python_integers(dtype):
+    a, b = int_pairs(dtype)
+    st_t = datagen.STORAGE[dtype]
+    A = np.array([int(x) for x in a], dtype=object).astype(st_t)
+    B = np.array([int(x) for x in b], dtype=object).astype(st_t)
+    nz = b != 0
+    for op in ("Add", "Sub", "Mul", "Div", "Mod", "BitwiseAnd", "BitwiseOr", "BitwiseXor"):
+        fmods = (0, 1) if op == "Mod" else (0,)
+        for fm in fmods:
+            got, st = oracle.run(op, A, B, dtype, fmod=fm)
+            want = []
+            for x, y in zip(a, b):
+                x, y = int(x), int(y)
+                if op == "Add": v = x + y
+                elif op == "Sub": v = x - y
+                elif op == "Mul": v = x * y
+                elif op == "Div": v = trunc_div(x, y) if y else 0
+                elif op == "Mod":
+                    if y == 0: v = 0
+                    elif fm: v = x - trunc_div(x, y) * y
+                    else: v = x % y
+                elif op == "BitwiseAnd": v = (x & y)
+                elif op == "BitwiseOr": v = (x | y)
+                else: v = (x ^ y)
+                want.append(wrap(v, dtype))
+            want = np.array(want, dtype=object).astype(st_t)
+            assert (got == want).all(), (op, fm, dtype)
+            if op in ("Div", "Mod"):
+                assert st == (0 if nz.all() else oracle.STATUS_DIV_BY_ZERO)
+
+
+def test_int_division_by_zero_sets_status():
+    a = np.array([5, 7, -9], np.int32)
+    _, st = oracle.run("Div", a, np.array([1, 0, 2], np.int32), "int32")
+    assert st == oracle.STATUS_DIV_BY_ZERO
+    _, st = oracle.run("Mod", a, np.array([1, 3, 2], np.int32), "int32")
+    assert st == 0
+
+
+@pytest.mark.parametrize("dtype", ["uint8", "uint32"])
+def test_bitshift_matches_numpy(dtype):
+    w = 8 * np.dtype(datagen.STORAGE[dtype]).itemsize
+    a = datagen.make("bits", dtype, (4096,), 5, 0)
+    for s in range(w):
+        b = np.full(a.shape, s, datagen.STORAGE[dtype])
+        gl, st_l = oracle.run("BitShift", a, b, dtype, direction=0)
+        gr, st_r = oracle.run("BitShift", a, b, dtype, direction=1)
+        assert st_l == 0 and st_r == 0
+        assert (gl == np.left_shift(a, b)).all() and (gr == np.right_shift(a, b)).all()
+    _, st = oracle.run("BitShift", a, np.full(a.shape, w, datagen.STORAGE[dtype]), dtype,
+                       direction=1)
+    assert st == oracle.STATUS_SHIFT_RANGE
+    _, st = oracle.run("BitShift", a, np.full(a.shape, w - 1, datagen.STORAGE[dtype]), dtype)
+    assert st == 0
+
+
+@pytest.mark.parametrize("dtype", ["int32", "int64"])
+def test_int_pow_matches_python(dtype):
+    st_t = datagen.STORAGE[dtype]
+    bases = list(range(-12, 13)) + [INT_LIMITS[dtype][0], INT_LIMITS[dtype][1], 3 ** 19]
+    exps = list(range(0, 70))
+    a = np.array([x for x in bases for _ in exps], dtype=object)
+    b = np.array([y for _ in bases for y in exps], dtype=object)
+    got, st = oracle.run("Pow", a.astype(st_t), b.astype(st_t), dtype)
+    want = np.array([wrap(pow(int(x), int(y)), dtype) for x, y in zip(a, b)],
+                    dtype=object).astype(st_t)
+    assert st == 0 and (got == want).all()
+
+
+def test_int_pow_negative_exponent_reading():
+    """Reading (no outside pin): trunc(1 / base^|e|), base 0 flags division by zero."""
+    a = np.array([1, -1, -1, 2, -3, 7], np.int32)
+    b = np.array([-5, -3, -4, -1, -2, -1], np.int32)
+    got, st = oracle.run("Pow", a, b, "int32")
+    assert list(got) == [1, -1, 1, 0, 0, 0] and st == 0
+    _, st = oracle.run("Pow", np.array([0], np.int32), np.array([-1], np.int32), "int32")
+    assert st == oracle.STATUS_DIV_BY_ZERO
+
+
+# --------------------------------------------------------------------------- Pow (float)
+
+def test_f32_pow_within_half_ulp_of_mpmath():
+    import mpmath
+    mpmath.mp.prec = 200
+    n = 1500
+    base = np.concatenate([datagen.uniform(31, 0, n, 1e-3, 50.0),
+                           -np.floor(datagen.uniform(31, 1, n, 1.0, 20.0))])
+    expo = np.concatenate([datagen.uniform(31, 2, n, -12.0, 12.0),
+                           np.floor(datagen.uniform(31, 3, n, -9.0, 10.0))]).astype(np.float32)
+    base = base.astype(np.float32)
+    got, _ = oracle.run("Pow", base, expo, "float32")
+    want = []
+    for x, y in zip(base, expo):
+        v = mpmath.power(mpmath.mpf(float(x)), mpmath.mpf(float(y)))
+        sign, man, exp, _ = mpmath.mpf(v)._mpf_
+        want.append(rn32((-1) ** sign * Fraction(int(man)) * Fraction(2) ** int(exp)))
+    want = np.array(want, np.float32)
+    d = ulp_distance(got, want, "float32")
+    assert d.max() <= 1, d.max()
+    assert (d == 0).mean() > 0.999
+
+
+def test_pow_special_values():
+    for x, y, want in read_golden("pow_special_values.txt"):
+        got, _ = oracle.run("Pow", f32(float(x)), f32(float(y)), "float32")
+        g = float(got[0])
+        if want == "nan":
+            assert math.isnan(g), (x, y, g)
+        else:
+            w = float(want)
+            assert g == w and math.copysign(1, g) == math.copysign(1, w), (x, y, g, w)
+
+
+# --------------------------------------------------------------------------- comparisons/logic
+
+CMP = [("Equal", np.equal), ("Less", np.less), ("Greater", np.greater),
+       ("LessOrEqual", np.less_equal), ("GreaterOrEqual", np.greater_equal)]
+
+
+@pytest.mark.parametrize("op,fn", CMP)
+def test_comparisons_match_numpy(op, fn):
+    a = float_corpus(5000, 41)
+    b = np.concatenate([np.roll(a[:-len(SPECIALS)], 1), SPECIALS[::-1]])
+    b[::3] = a[::3]                                # many equal pairs
+    got, _ = oracle.run(op, a, b, "float32")
+    assert got.dtype == np.uint8 and (got == fn(a, b).astype(np.uint8)).all()
+    h_a, h_b = a.astype(np.float16), b.astype(np.float16)
+    got, _ = oracle.run(op, h_a, h_b, "float16")
+    assert (got == fn(h_a, h_b).astype(np.uint8)).all()
+    bf_a, bf_b = bf16_bits(a), bf16_bits(b)
+    got, _ = oracle.run(op, bf_a, bf_b, "bfloat16")
+    assert (got == fn(bf16_to_f32(bf_a), bf16_to_f32(bf_b)).astype(np.uint8)).all()
+    for dtype in ("int32", "int64", "uint8", "uint32"):
+        ia = datagen.make("bits", dtype, (3000,), 42, 0)
+        ib = datagen.make("bits", dtype, (3000,), 42, 1)
+        ib[::4] = ia[::4]
+        got, _ = oracle.run(op, ia, ib, dtype)
+        assert (got == fn(ia, ib).astype(np.uint8)).all()
+
+
+def test_comparisons_nan_and_signed_zero():
+    a = f32(np.nan, np.nan, 0.0, -0.0)
+    b = f32(np.nan, 1.0, -0.0, 0.0)
+    for op, _ in CMP:
+        got, _ = oracle.run(op, a, b, "float32")
+        assert got[0] == 0 and got[1] == 0
+    eq, _ = oracle.run("Equal", a, b, "float32")
+    assert eq[2] == 1 and eq[3] == 1
+
+
+@pytest.mark.parametrize("op,fn", [("And", np.logical_and), ("Or", np.logical_or),
+                                   ("Xor", np.logical_xor)])
+def test_logical_matches_numpy(op, fn):
+    a = datagen.make("bool", "bool", (5000,), 43, 0)
+    b = datagen.make("bool", "bool", (5000,), 43, 1)
+    got, _ = oracle.run(op, a, b, "bool")
+    assert (got == fn(a, b).astype(np.uint8)).all()
+    x, _ = oracle.run("Xor", a, a, "bool")
+    assert not x.any()
+
+
+def test_less_is_mirrored_greater():
+    a = float_corpus(4000, 44)
+    b = np.roll(a, 11)
+    lt, _ = oracle.run("Less", a, b, "float32")
+    gt, _ = oracle.run("Greater", b, a, "float32")
+    le, _ = oracle.run("LessOrEqual", a, b, "float32")
+    eq, _ = oracle.run("Equal", a, b, "float32")
+    assert (lt == gt).all()
+    ok = ~(np.isnan(a) | np.isnan(b))
+    assert (le[ok] == (lt | eq)[ok]).all()
+
+
+# --------------------------------------------------------------------------- PRelu / BN / Clip
+
+def test_prelu_closed_forms():
+    for row in read_golden("prelu_clip_closed_form.txt"):
+        op, x, p1, p2, want = row
+        if op == "prelu":
+            got, _ = oracle.run("PRelu", f32(float(x)), f32(float(p1)), "float32")
+        else:
+            got, _ = oracle.run("Clip", f32(float(x)), f32(float(p1), float(p2)), "float32")
+        g, w = float(got[0]), float(want)
+        assert g == w and math.copysign(1, g) == math.copysign(1, w), row
+
+
+@pytest.mark.parametrize("dtype", ["float32", "float16"])
+def test_prelu_matches_numpy_where(dtype):
+    x = datagen.make("normal", dtype, (64, 3, 5), 45, 0)
+    s = datagen.make("uniform", dtype, (3, 1), 45, 1, lo=0.0, hi=0.3)
+    got, _ = oracle.run("PRelu", x, s, dtype)
+    want = np.where(x >= 0, x, np.broadcast_to(s, x.shape) * x)
+    assert_bits_equal(got, want, dtype, "PRelu")
+    one, _ = oracle.run("PRelu", x, np.ones((3, 1), datagen.STORAGE[dtype]), dtype)
+    assert_bits_equal(one, x, dtype, "PRelu slope 1 is the identity")
+
+
+def test_prelu_is_unidirectional():
+    with pytest.raises(ValueError, match="incompatible_shapes"):
+        oracle.run("PRelu", np.zeros((3, 1), np.float32), np.zeros((3, 4), np.float32), "float32")
+
+
+def test_batchnorm_closed_forms():
+    for x, mean, var, eps, scale, bias, want in read_golden("batchnorm_closed_form.txt"):
+        xs = f32(float(x)).reshape(1, 1)
+        params = f32(float(scale), float(bias), float(mean), float(var)).reshape(4, 1)
+        got, _ = oracle.run("BatchNormalization", xs, params, "float32", eps=float(eps))
+        g, w = float(got[0, 0]), float(want)
+        assert g == w and math.copysign(1, g) == math.copysign(1, w), (x, g, w)
+
+
+def test_batchnorm_identity_and_channel_axis():
+    x = datagen.make("normal", "float32", (2, 3, 4, 5), 46, 0)
+    ident = np.zeros((4, 3), np.float32)
+    ident[0] = 1.0
+    ident[1] = -0.0
+    ident[3] = 1.0
+    got, _ = oracle.run("BatchNormalization", x, ident, "float32", eps=0.0)
+    assert_bits_equal(got, x, "float32", "BN identity")
+    # only channel 1 gets a shift: everything else stays bit-identical
+    p = ident.copy()
+    p[1, 1] = 10.0
+    got, _ = oracle.run("BatchNormalization", x, p, "float32", eps=0.0)
+    assert_bits_equal(got[:, [0, 2]], x[:, [0, 2]], "float32", "BN other channels")
+    assert_bits_equal(got[:, 1], x[:, 1] + np.float32(10.0), "float32", "BN channel 1")
+
+
+def test_batchnorm_within_float64_bound():
+    """Five correctly rounded binary32 steps stay within a few ulp of the exact value."""
+    x = datagen.make("normal", "float32", (4, 8, 33), 47, 0)
+    p = np.stack([datagen.normal(47, 1, 8), datagen.normal(47, 2, 8), datagen.normal(47, 3, 8),
+                  datagen.uniform(47, 4, 8, 0.1, 2.0)]).astype(np.float32)
+    got, _ = oracle.run("BatchNormalization", x, p, "float32", eps=1e-5)
+    sc, bi, mu, va = (p[i].astype(np.float64)[None, :, None] for i in range(4))
+    exact = (x.astype(np.float64) - mu) / np.sqrt(va + np.float64(np.float32(1e-5))) * sc + bi
+    err = np.abs(got.astype(np.float64) - exact)
+    scale = np.abs(exact) + np.abs(bi) + np.abs(sc) * np.abs(x.astype(np.float64) - mu)
+    assert (err <= 8 * 2.0 ** -24 * scale + 1e-30).all()
+
+
+def test_clip_matches_numpy_and_bounds_are_optional():
+    x = float_corpus(5000, 48)
+    lohi = f32(-2.5, 3.0)
+    got, _ = oracle.run("Clip", x, lohi, "float32")
+    ok = ~np.isnan(x)
+    assert_bits_equal(got[ok], np.minimum(np.maximum(x[ok], lohi[0]), lohi[1]), "float32", "Clip")
+    assert np.isnan(got[~ok]).all()
+    only_max, _ = oracle.run("Clip", x, lohi, "float32", has_min=False)
+    assert_bits_equal(only_max[ok], np.minimum(x[ok], lohi[1]), "float32", "Clip max only")
+    none, _ = oracle.run("Clip", x, lohi, "float32", has_min=False, has_max=False)
+    assert_bits_equal(none, x, "float32", "Clip without bounds")
+    xi = datagen.make("bits", "int32", (3000,), 48, 1)
+    gi, _ = oracle.run("Clip", xi, np.array([-1000, 5000], np.int32), "int32")
+    assert (gi == np.clip(xi, -1000, 5000)).all()
+
+
+# --------------------------------------------------------------------------- descriptor
+
+def test_descriptor_rules_from_the_mod_section():
+    cd = oracle.check_descriptor
+    assert cd("Mod", 28, 0, 0, "float32", "float32") == "ok"
+    assert cd("Mod", 27, 0, 0, "float32", "float32") == "invalid_attr"
+    assert cd("Mod", 27, 1, 0, "float16", "float16") == "ok"
+    assert cd("Mod", 10, 0, 0, "int32", "int32") == "ok"
+    assert cd("Mod", 9, 1, 0, "int32", "int32") == "invalid_attr"
+    assert cd("Mod", 28, 2, 0, "int32", "int32") == "invalid_attr"
+    assert cd("BitShift", 11, 0, 2, "uint8", "uint8") == "invalid_attr"
+    assert cd("BitShift", 11, 0, 1, "int32", "int32") == "unsupported_type"
+    assert cd("And", 7, 0, 0, "float32", "float32") == "unsupported_type"
+    assert cd("Add", 14, 0, 0, "float32", "float16") == "unsupported_type"
+    for op in ("Equal", "Less", "Greater", "LessOrEqual", "GreaterOrEqual", "And", "Or", "Xor"):
+        assert oracle.output_type(op, "bool" if op in ("And", "Or", "Xor") else "int32") == "bool"
+    assert oracle.output_type("Add", "bfloat16") == "bfloat16"
