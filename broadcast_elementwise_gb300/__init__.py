@@ -1,0 +1,364 @@
+"""GB300-native ONNX broadcast binary elementwise engine: Python binding.
+
+A thin ctypes binding of ``libebin.so``, whose C ABI (``include/ebin.h``) is
+the product's boundary.  The ``ebin_*`` functions here have the C names and
+only marshal arguments; every step of the path (descriptor checks, planning,
+the plan cache, validation and the elementwise kernels) runs in the library.
+PyTorch is used for device memory and streams only.
+
+Importing this package loads the library and fails loudly if it is missing:
+there is no CPU or eager fallback.
+
+Typical use::
+
+    import torch, broadcast_elementwise_gb300 as eb
+    y = eb.binary("Add", x, b)                   # allocates y, runs on the current stream
+
+    desc = eb.Descriptor("Mod", "float32", fmod=0, opset=28)
+    plan = eb.Plan(desc, a.shape, b.shape)
+    eb.execute(plan, a, b, out)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libebin.so")
+
+OPS = {"Add": 0, "Sub": 1, "Mul": 2, "Div": 3, "Mod": 4, "Pow": 5,
+       "Equal": 6, "Less": 7, "Greater": 8, "LessOrEqual": 9, "GreaterOrEqual": 10,
+       "And": 11, "Or": 12, "Xor": 13,
+       "BitwiseAnd": 14, "BitwiseOr": 15, "BitwiseXor": 16,
+       "BitShift": 17, "PRelu": 18, "BatchNormalization": 19, "Clip": 20}
+DTYPES = {"float32": 1, "uint8": 2, "int32": 6, "int64": 7, "bool": 9, "float16": 10,
+          "uint32": 12, "bfloat16": 16}
+DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
+ITEMSIZE = {"float32": 4, "uint8": 1, "int32": 4, "int64": 8, "bool": 1, "float16": 2,
+            "uint32": 4, "bfloat16": 2}
+FAMILIES = {"auto": -1, "empty": 0, "contiguous": 1, "left_scalar": 2, "right_scalar": 3,
+            "repeated_block": 4, "inner_vector_outer": 5, "general_strided": 6}
+FAMILY_NAMES = {v: k for k, v in FAMILIES.items()}
+STATUS = {0: "ok", 1: "invalid_arg", 2: "unsupported_op", 3: "unsupported_type",
+          4: "invalid_attr", 5: "incompatible_shapes", 6: "rank_too_large", 7: "alias",
+          8: "cuda", 9: "family"}
+DEVICE_DIV_BY_ZERO = 0x1
+DEVICE_SHIFT_RANGE = 0x2
+MAX_RANK = 8
+PLAN_CACHE_CAPACITY = 8
+
+
+class EbinError(RuntimeError):
+    """A non-OK status returned by the C ABI; ``.code`` holds its name."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.code = STATUS.get(status, "unknown")
+        super().__init__("%s: %s" % (where, self.code))
+
+
+class ebin_attrs(ctypes.Structure):
+    _fields_ = [("fmod", ctypes.c_int32), ("direction", ctypes.c_int32),
+                ("epsilon", ctypes.c_float), ("clip_has_min", ctypes.c_int32),
+                ("clip_has_max", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libebin.so is not built (%s); run __graft_entry__.build() or "
+                          "python -m broadcast_elementwise_gb300._build" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    p_i64 = ctypes.POINTER(ctypes.c_int64)
+    sigs = {
+        "ebin_descriptor_create": (i32, [i32, i32, ctypes.POINTER(ebin_attrs), i32, i32,
+                                         ctypes.POINTER(vp)]),
+        "ebin_descriptor_output_dtype": (i32, [vp, ctypes.POINTER(ctypes.c_int)]),
+        "ebin_descriptor_id": (i32, [vp, ctypes.POINTER(ctypes.c_uint64)]),
+        "ebin_descriptor_destroy": (None, [vp]),
+        "ebin_plan_create": (i32, [vp, p_i64, i32, p_i64, i32, ctypes.POINTER(vp)]),
+        "ebin_plan_create_forced": (i32, [vp, p_i64, i32, p_i64, i32, i32, ctypes.POINTER(vp)]),
+        "ebin_plan_output_shape": (i32, [vp, p_i64, ctypes.POINTER(ctypes.c_int)]),
+        "ebin_plan_numel": (i32, [vp, p_i64]),
+        "ebin_plan_family": (i32, [vp, ctypes.POINTER(ctypes.c_int)]),
+        "ebin_plan_geometry": (i32, [vp, ctypes.POINTER(ctypes.c_int), p_i64, p_i64, p_i64]),
+        "ebin_plan_release": (None, [vp]),
+        "ebin_plan_cache_stats": (i32, [ctypes.POINTER(ctypes.c_uint64),
+                                        ctypes.POINTER(ctypes.c_uint64),
+                                        ctypes.POINTER(ctypes.c_int)]),
+        "ebin_plan_cache_clear": (None, []),
+        "ebin_execute": (i32, [vp, vp, vp, vp, vp]),
+        "ebin_execute_host": (i32, [vp, vp, vp, vp, vp, vp, vp, vp]),
+        "ebin_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_uint32)]),
+        "ebin_launch_count": (ctypes.c_uint64, []),
+        "ebin_dtype_size": (ctypes.c_size_t, [i32]),
+        "ebin_status_string": (ctypes.c_char_p, [i32]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise EbinError(status, where)
+
+
+def _shape(shape):
+    dims = [int(d) for d in shape]
+    arr = (ctypes.c_int64 * max(1, len(dims)))(*dims)
+    return arr, len(dims)
+
+
+def _ptr(x) -> int | None:
+    """Device address of a tensor (or an int address, or None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------- the C ABI, by name
+
+def ebin_descriptor_create(op, opset, attrs, dtype_a, dtype_b) -> int:
+    out = ctypes.c_void_p()
+    _check(lib.ebin_descriptor_create(op, opset, ctypes.byref(attrs) if attrs else None,
+                                      dtype_a, dtype_b, ctypes.byref(out)),
+           "ebin_descriptor_create")
+    return out.value
+
+
+def ebin_descriptor_output_dtype(desc) -> int:
+    v = ctypes.c_int()
+    _check(lib.ebin_descriptor_output_dtype(desc, ctypes.byref(v)), "ebin_descriptor_output_dtype")
+    return v.value
+
+
+def ebin_descriptor_id(desc) -> int:
+    v = ctypes.c_uint64()
+    _check(lib.ebin_descriptor_id(desc, ctypes.byref(v)), "ebin_descriptor_id")
+    return v.value
+
+
+def ebin_descriptor_destroy(desc) -> None:
+    lib.ebin_descriptor_destroy(desc)
+
+
+def ebin_plan_create(desc, shape_a, shape_b) -> int:
+    sa, ra = _shape(shape_a)
+    sb, rb = _shape(shape_b)
+    out = ctypes.c_void_p()
+    _check(lib.ebin_plan_create(desc, sa, ra, sb, rb, ctypes.byref(out)), "ebin_plan_create")
+    return out.value
+
+
+def ebin_plan_create_forced(desc, shape_a, shape_b, family) -> int:
+    sa, ra = _shape(shape_a)
+    sb, rb = _shape(shape_b)
+    out = ctypes.c_void_p()
+    _check(lib.ebin_plan_create_forced(desc, sa, ra, sb, rb, family, ctypes.byref(out)),
+           "ebin_plan_create_forced")
+    return out.value
+
+
+def ebin_plan_output_shape(plan) -> tuple:
+    shape = (ctypes.c_int64 * MAX_RANK)()
+    rank = ctypes.c_int()
+    _check(lib.ebin_plan_output_shape(plan, shape, ctypes.byref(rank)), "ebin_plan_output_shape")
+    return tuple(shape[i] for i in range(rank.value))
+
+
+def ebin_plan_numel(plan) -> int:
+    v = ctypes.c_int64()
+    _check(lib.ebin_plan_numel(plan, ctypes.byref(v)), "ebin_plan_numel")
+    return v.value
+
+
+def ebin_plan_family(plan) -> int:
+    v = ctypes.c_int()
+    _check(lib.ebin_plan_family(plan, ctypes.byref(v)), "ebin_plan_family")
+    return v.value
+
+
+def ebin_plan_geometry(plan):
+    rank = ctypes.c_int()
+    n, sa, sb = ((ctypes.c_int64 * MAX_RANK)() for _ in range(3))
+    _check(lib.ebin_plan_geometry(plan, ctypes.byref(rank), n, sa, sb), "ebin_plan_geometry")
+    r = rank.value
+    return [n[i] for i in range(r)], [sa[i] for i in range(r)], [sb[i] for i in range(r)]
+
+
+def ebin_plan_release(plan) -> None:
+    lib.ebin_plan_release(plan)
+
+
+def ebin_plan_cache_stats():
+    h, m, s = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_int()
+    _check(lib.ebin_plan_cache_stats(ctypes.byref(h), ctypes.byref(m), ctypes.byref(s)),
+           "ebin_plan_cache_stats")
+    return h.value, m.value, s.value
+
+
+def ebin_plan_cache_clear() -> None:
+    lib.ebin_plan_cache_clear()
+
+
+def ebin_execute(plan, A, B, out, stream) -> None:
+    _check(lib.ebin_execute(plan, A, B, out, stream), "ebin_execute")
+
+
+def ebin_execute_host(plan, host_a, host_b, host_out, dev_a, dev_b, dev_out, stream) -> None:
+    _check(lib.ebin_execute_host(plan, host_a, host_b, host_out, dev_a, dev_b, dev_out, stream),
+           "ebin_execute_host")
+
+
+def ebin_get_device_status(stream) -> int:
+    v = ctypes.c_uint32()
+    _check(lib.ebin_get_device_status(stream, ctypes.byref(v)), "ebin_get_device_status")
+    return v.value
+
+
+def ebin_launch_count() -> int:
+    return int(lib.ebin_launch_count())
+
+
+def ebin_dtype_size(dtype) -> int:
+    return int(lib.ebin_dtype_size(dtype))
+
+
+def ebin_status_string(status) -> str:
+    return lib.ebin_status_string(status).decode()
+
+
+# ----------------------------------------------------------------- thin object wrappers
+
+def _dtype_code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    if isinstance(dtype, str):
+        return DTYPES[dtype]
+    return DTYPES[torch_dtype_name(dtype)]
+
+
+def torch_dtype_name(t) -> str:
+    import torch
+    table = {torch.float32: "float32", torch.float16: "float16", torch.bfloat16: "bfloat16",
+             torch.int32: "int32", torch.int64: "int64", torch.uint8: "uint8",
+             torch.bool: "bool", torch.uint32: "uint32"}
+    return table[t]
+
+
+def torch_dtype(name: str):
+    import torch
+    return {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16,
+            "int32": torch.int32, "int64": torch.int64, "uint8": torch.uint8,
+            "bool": torch.bool, "uint32": torch.uint32}[name]
+
+
+class Descriptor:
+    """Owns an ebin descriptor (operator, opset, attributes, element type)."""
+
+    def __init__(self, op: str, dtype, *, opset: int = 28, fmod: int = 0, direction: int = 0,
+                 epsilon: float = 1e-5, has_min: bool = True, has_max: bool = True):
+        self.op = op
+        self.dtype = DTYPE_NAMES[_dtype_code(dtype)]
+        attrs = ebin_attrs(int(fmod), int(direction), float(epsilon), int(bool(has_min)),
+                           int(bool(has_max)))
+        code = _dtype_code(dtype)
+        self.handle = ebin_descriptor_create(OPS[op], int(opset), attrs, code, code)
+        self.out_dtype = DTYPE_NAMES[ebin_descriptor_output_dtype(self.handle)]
+        self.id = ebin_descriptor_id(self.handle)
+
+    def close(self):
+        if self.handle:
+            ebin_descriptor_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Plan:
+    """Holds one plan reference for (descriptor, shape_a, shape_b)."""
+
+    def __init__(self, desc: Descriptor, shape_a, shape_b, family: str | None = None):
+        self.desc = desc
+        self.shape_a = tuple(int(d) for d in shape_a)
+        self.shape_b = tuple(int(d) for d in shape_b)
+        if family is None:
+            self.handle = ebin_plan_create(desc.handle, self.shape_a, self.shape_b)
+        else:
+            self.handle = ebin_plan_create_forced(desc.handle, self.shape_a, self.shape_b,
+                                                  FAMILIES[family])
+        self.output_shape = ebin_plan_output_shape(self.handle)
+        self.numel = ebin_plan_numel(self.handle)
+        self.family = FAMILY_NAMES[ebin_plan_family(self.handle)]
+
+    def geometry(self):
+        return ebin_plan_geometry(self.handle)
+
+    def close(self):
+        if self.handle:
+            ebin_plan_release(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def execute(plan: Plan, A, B, out, stream=None) -> None:
+    """Enqueue the plan on device buffers (torch tensors or int addresses)."""
+    ebin_execute(plan.handle, _ptr(A), _ptr(B), _ptr(out), _stream(stream))
+
+
+def get_device_status(stream=None) -> int:
+    return ebin_get_device_status(_stream(stream))
+
+
+_descriptors: dict = {}
+
+
+def descriptor(op: str, dtype, **attrs) -> Descriptor:
+    """A process-wide Descriptor per (op, dtype, attributes), so plans stay cached."""
+    key = (op, _dtype_code(dtype), tuple(sorted(attrs.items())))
+    d = _descriptors.get(key)
+    if d is None:
+        d = _descriptors[key] = Descriptor(op, dtype, **attrs)
+    return d
+
+
+def binary(op: str, a, b, out=None, *, stream=None, **attrs):
+    """One-shot call on torch CUDA tensors: returns ``out`` (allocated if None).
+
+    Inputs that are not contiguous are copied first (on the current stream).
+    """
+    import torch
+    desc = descriptor(op, a.dtype, **attrs)
+    plan = Plan(desc, a.shape, b.shape if b is not None else (2,))
+    if out is None:
+        out = torch.empty(plan.output_shape, dtype=torch_dtype(desc.out_dtype), device=a.device)
+    a_c = a.contiguous()
+    b_c = b.contiguous() if b is not None else None
+    execute(plan, a_c, b_c, out, stream)
+    return out

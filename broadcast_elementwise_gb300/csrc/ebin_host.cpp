@@ -1,0 +1,673 @@
+// Host side of the ebin C ABI: descriptors, the broadcast planner, the
+// 8-entry plan LRU, execution (alias check, family dispatch, launch) and the
+// per-stream device status word.
+//
+// Follows "Binary Kernel Design" (onnx-light-cpu):
+//   Prepared execution      -- descriptor built once per node; plans cached in
+//                              a bounded 8-entry LRU keyed on a monotonic
+//                              descriptor id, the types and both shapes; a miss
+//                              builds and validates a fresh plan.
+//   Operators and traversal -- right-align, zero strides for broadcast dims,
+//                              drop unit dims, coalesce, pick a loop family;
+//                              empty dims do no work.
+//   Compute, scheduling, and safety -- validation before the math; one byte
+//                              per BOOL; aliasing only when type and shape equal
+//                              the output's.
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <list>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "ebin.h"
+#include "ebin_launch.h"
+
+using ebin::Fam;
+using ebin::Geom;
+using ebin::kMaxRank;
+
+// ------------------------------------------------------------------ types
+namespace {
+
+int dt_class(ebin_dtype t) {
+    switch (t) {
+    case EBIN_FLOAT32: return ebin::DT_F32;
+    case EBIN_FLOAT16: return ebin::DT_F16;
+    case EBIN_BFLOAT16: return ebin::DT_BF16;
+    case EBIN_INT32: return ebin::DT_I32;
+    case EBIN_INT64: return ebin::DT_I64;
+    case EBIN_UINT8: return ebin::DT_U8;
+    case EBIN_UINT32: return ebin::DT_U32;
+    case EBIN_BOOL: return ebin::DT_BOOL;
+    }
+    return -1;
+}
+
+bool is_float(ebin_dtype t) {
+    return t == EBIN_FLOAT32 || t == EBIN_FLOAT16 || t == EBIN_BFLOAT16;
+}
+bool is_int(ebin_dtype t) {
+    return t == EBIN_INT32 || t == EBIN_INT64 || t == EBIN_UINT8 || t == EBIN_UINT32;
+}
+bool is_signed_int(ebin_dtype t) { return t == EBIN_INT32 || t == EBIN_INT64; }
+
+// Type manifest: which element type each operator accepts (A and B share it).
+bool type_legal(int op, ebin_dtype t) {
+    if (dt_class(t) < 0) return false;
+    switch (op) {
+    case EBIN_OP_ADD: case EBIN_OP_SUB: case EBIN_OP_MUL: case EBIN_OP_DIV: case EBIN_OP_MOD:
+    case EBIN_OP_LESS: case EBIN_OP_GREATER: case EBIN_OP_LESS_OR_EQUAL:
+    case EBIN_OP_GREATER_OR_EQUAL: case EBIN_OP_CLIP:
+        return is_float(t) || is_int(t);
+    case EBIN_OP_POW: return is_float(t) || is_signed_int(t);
+    case EBIN_OP_EQUAL: return true;
+    case EBIN_OP_AND: case EBIN_OP_OR: case EBIN_OP_XOR: return t == EBIN_BOOL;
+    case EBIN_OP_BITWISE_AND: case EBIN_OP_BITWISE_OR: case EBIN_OP_BITWISE_XOR: return is_int(t);
+    case EBIN_OP_BITSHIFT: return t == EBIN_UINT8 || t == EBIN_UINT32;
+    case EBIN_OP_PRELU: return is_float(t) || is_signed_int(t) || t == EBIN_UINT32;
+    case EBIN_OP_BATCHNORM: return is_float(t);
+    }
+    return false;
+}
+
+ebin_dtype output_type(int op, ebin_dtype t) {
+    return (op >= EBIN_OP_EQUAL && op <= EBIN_OP_XOR) ? EBIN_BOOL : t;
+}
+
+// Operators whose kernels can meet invalid elements and report them.
+bool validates(int op, ebin_dtype t) {
+    if ((op == EBIN_OP_DIV || op == EBIN_OP_MOD) && is_int(t)) return true;
+    if (op == EBIN_OP_POW && is_signed_int(t)) return true;
+    return op == EBIN_OP_BITSHIFT;
+}
+
+// B is an ordinary broadcast tensor (not the BN parameter block or Clip bounds).
+bool plain_b(int op) { return op != EBIN_OP_BATCHNORM && op != EBIN_OP_CLIP; }
+
+// Output keeps A's shape: B broadcasts one way.
+bool one_way(int op) {
+    return op == EBIN_OP_PRELU || op == EBIN_OP_BATCHNORM || op == EBIN_OP_CLIP;
+}
+
+std::atomic<uint64_t> g_next_id{1};
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+struct ebin_descriptor_s {
+    uint64_t id;
+    int op;
+    int opset;
+    ebin_attrs attrs;
+    ebin_dtype dt;
+    ebin_dtype out_dt;
+};
+
+struct ebin_plan_s {
+    std::atomic<int> refs{1};
+    // cache key
+    uint64_t desc_id = 0;
+    ebin_dtype dt = EBIN_FLOAT32;
+    int rank_a = 0, rank_b = 0;
+    int64_t shape_a[kMaxRank] = {};
+    int64_t shape_b[kMaxRank] = {};
+    // what execution needs (copied: a plan may outlive its descriptor)
+    int op = 0;
+    ebin_attrs attrs{};
+    ebin_dtype out_dt = EBIN_FLOAT32;
+    int rank_out = 0;
+    int64_t shape_out[kMaxRank] = {};
+    int64_t numel = 0, numel_a = 0, numel_b = 0;
+    Geom g{};
+    int family = ebin::FAM_EMPTY;
+    int64_t plane = 0;
+};
+
+// ------------------------------------------------------------------ descriptor
+extern "C" ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_attrs *attrs,
+                                              ebin_dtype dtype_a, ebin_dtype dtype_b,
+                                              ebin_descriptor_t *out) {
+    if (!out) return EBIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if ((int)op < 0 || (int)op >= EBIN_OP_COUNT) return EBIN_ERR_UNSUPPORTED_OP;
+    ebin_attrs a{0, 0, EBIN_DEFAULT_EPSILON, 1, 1};
+    if (attrs) a = *attrs;
+    if (dtype_a != dtype_b || !type_legal(op, dtype_a)) return EBIN_ERR_UNSUPPORTED_TYPE;
+    if (op == EBIN_OP_MOD) {
+        // "Mod tracks schema version 28 while retaining minimum opset 10";
+        // floating fmod=0 (floor remainder) only from opset 28.
+        if (opset < 10 || opset > 28) return EBIN_ERR_INVALID_ATTR;
+        if (a.fmod != 0 && a.fmod != 1) return EBIN_ERR_INVALID_ATTR;
+        if (is_float(dtype_a) && a.fmod == 0 && opset < 28) return EBIN_ERR_INVALID_ATTR;
+    }
+    if (op == EBIN_OP_BITSHIFT && a.direction != 0 && a.direction != 1)
+        return EBIN_ERR_INVALID_ATTR;
+    auto *d = new ebin_descriptor_s;
+    d->id = g_next_id.fetch_add(1);
+    d->op = op;
+    d->opset = opset;
+    d->attrs = a;
+    d->dt = dtype_a;
+    d->out_dt = output_type(op, dtype_a);
+    *out = d;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_descriptor_output_dtype(ebin_descriptor_t desc, ebin_dtype *out) {
+    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
+    *out = desc->out_dt;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_descriptor_id(ebin_descriptor_t desc, uint64_t *id) {
+    if (!desc || !id) return EBIN_ERR_INVALID_ARG;
+    *id = desc->id;
+    return EBIN_OK;
+}
+
+// ------------------------------------------------------------------ planner
+namespace {
+
+int64_t product(const int64_t *s, int r) {
+    int64_t n = 1;
+    for (int i = 0; i < r; ++i) n *= s[i];
+    return n;
+}
+
+// Loop family for a coalesced geometry, or EBIN_ERR_FAMILY through *ok when a
+// forced family cannot traverse it.
+int family_of(const ebin_plan_s &p, int forced, bool *ok) {
+    *ok = true;
+    if (p.numel == 0) return ebin::FAM_EMPTY;
+    const Geom &g = p.g;
+    const int r = g.rank;
+    const int64_t G = 16 / (int64_t)ebin_dtype_size(p.dt);
+    const int64_t inner = g.n[r - 1];
+    const bool contig = r == 1 && g.sa[0] == 1 && g.sb[0] == 1;
+    const bool left = r == 1 && g.sa[0] == 0 && g.sb[0] == 1 && plain_b(p.op);
+    const bool right = r == 1 && g.sa[0] == 1 && g.sb[0] == 0;
+    bool block = false;
+    if (r == 2 && inner % G == 0) {
+        const bool a_dense = g.sa[0] == inner && g.sa[1] == 1;
+        const bool b_dense = g.sb[0] == inner && g.sb[1] == 1;
+        auto bcast = [](const int64_t *s) {
+            return (s[0] == 1 && s[1] == 0) || (s[0] == 0 && s[1] == 1);
+        };
+        block = (a_dense && bcast(g.sb)) || (b_dense && bcast(g.sa) && plain_b(p.op));
+    }
+    const int64_t ia = g.sa[r - 1], ib = g.sb[r - 1];
+    const bool inner_ok = inner % G == 0 && (ia == 0 || ia == 1) && (ib == 0 || ib == 1) &&
+                          (ia == 1 || ib == 1) && (ia == 1 || plain_b(p.op));
+    switch (forced) {
+    case EBIN_FAMILY_AUTO:
+        if (contig) return ebin::FAM_CONTIGUOUS;
+        if (left) return ebin::FAM_LEFT_SCALAR;
+        if (right) return ebin::FAM_RIGHT_SCALAR;
+        if (block) return ebin::FAM_REPEATED_BLOCK;
+        if (inner_ok && inner >= 64) return ebin::FAM_INNER_VECTOR_OUTER;
+        return ebin::FAM_GENERAL_STRIDED;
+    case EBIN_FAMILY_CONTIGUOUS: *ok = contig; return forced;
+    case EBIN_FAMILY_LEFT_SCALAR: *ok = left; return forced;
+    case EBIN_FAMILY_RIGHT_SCALAR: *ok = right; return forced;
+    case EBIN_FAMILY_REPEATED_BLOCK: *ok = block; return forced;
+    case EBIN_FAMILY_INNER_VECTOR_OUTER: *ok = inner_ok; return forced;
+    case EBIN_FAMILY_GENERAL_STRIDED: return forced;
+    default: *ok = false; return forced;
+    }
+}
+
+ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
+                       int rb, int forced, ebin_plan_s **out) {
+    if (ra < 0 || rb < 0) return EBIN_ERR_INVALID_ARG;
+    if (ra > kMaxRank || rb > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
+    if ((ra > 0 && !sa) || (rb > 0 && !sb)) return EBIN_ERR_INVALID_ARG;
+    for (int i = 0; i < ra; ++i)
+        if (sa[i] < 0) return EBIN_ERR_INVALID_ARG;
+    for (int i = 0; i < rb; ++i)
+        if (sb[i] < 0) return EBIN_ERR_INVALID_ARG;
+
+    // The logical shape B broadcasts with.  BatchNormalization: B = [4, C]
+    // holds four parameter rows of C and broadcasts as [1, C, 1, ...] along
+    // x's channel axis 1.  Clip: B = [2] holds {min, max}, a scalar pair.
+    int64_t lb[kMaxRank];
+    int rlb = rb;
+    int64_t plane = 0;
+    if (d.op == EBIN_OP_BATCHNORM) {
+        if (ra < 2 || rb != 2 || sb[0] != 4 || sb[1] != sa[1]) return EBIN_ERR_INCOMPATIBLE_SHAPES;
+        rlb = ra;
+        for (int i = 0; i < ra; ++i) lb[i] = (i == 1) ? sa[1] : 1;
+        plane = sa[1];
+    } else if (d.op == EBIN_OP_CLIP) {
+        if (rb != 1 || sb[0] != 2) return EBIN_ERR_INCOMPATIBLE_SHAPES;
+        rlb = 0;
+    } else {
+        for (int i = 0; i < rb; ++i) lb[i] = sb[i];
+    }
+
+    // 1. right-align and broadcast
+    const int r = std::max(ra, rlb);
+    int64_t so[kMaxRank], xa[kMaxRank], xb[kMaxRank];
+    for (int i = 0; i < r; ++i) {
+        const int ia = i - (r - ra), ib = i - (r - rlb);
+        xa[i] = ia >= 0 ? sa[ia] : 1;
+        xb[i] = ib >= 0 ? lb[ib] : 1;
+        if (xa[i] == xb[i]) so[i] = xa[i];
+        else if (xa[i] == 1) so[i] = xb[i];
+        else if (xb[i] == 1) so[i] = xa[i];
+        else return EBIN_ERR_INCOMPATIBLE_SHAPES;
+    }
+    if (one_way(d.op)) {
+        if (r != ra) return EBIN_ERR_INCOMPATIBLE_SHAPES;
+        for (int i = 0; i < r; ++i)
+            if (so[i] != sa[i]) return EBIN_ERR_INCOMPATIBLE_SHAPES;
+    }
+
+    auto *p = new ebin_plan_s;
+    p->desc_id = d.id;
+    p->dt = d.dt;
+    p->rank_a = ra;
+    p->rank_b = rb;
+    for (int i = 0; i < ra; ++i) p->shape_a[i] = sa[i];
+    for (int i = 0; i < rb; ++i) p->shape_b[i] = sb[i];
+    p->op = d.op;
+    p->attrs = d.attrs;
+    p->out_dt = d.out_dt;
+    p->rank_out = r;
+    for (int i = 0; i < r; ++i) p->shape_out[i] = so[i];
+    p->numel = product(so, r);
+    p->numel_a = product(sa, ra);
+    p->numel_b = product(sb, rb);
+    p->plane = plane;
+
+    // 2. dense strides, zero on broadcast dims
+    int64_t st_a[kMaxRank], st_b[kMaxRank];
+    int64_t acc_a = 1, acc_b = 1;
+    for (int i = r - 1; i >= 0; --i) {
+        st_a[i] = xa[i] == 1 ? 0 : acc_a;
+        st_b[i] = xb[i] == 1 ? 0 : acc_b;
+        acc_a *= xa[i];
+        acc_b *= xb[i];
+    }
+    // 3. drop output dims of extent 1;  4. merge adjacent compatible dims
+    Geom g{};
+    int k = 0;
+    for (int i = 0; i < r; ++i) {
+        if (so[i] == 1) continue;
+        if (k > 0 && g.sa[k - 1] == st_a[i] * so[i] && g.sb[k - 1] == st_b[i] * so[i]) {
+            // the previous (outer) dim continues this one: fold it in
+            g.n[k - 1] *= so[i];
+            g.sa[k - 1] = st_a[i];
+            g.sb[k - 1] = st_b[i];
+            continue;
+        }
+        g.n[k] = so[i];
+        g.sa[k] = st_a[i];
+        g.sb[k] = st_b[i];
+        ++k;
+    }
+    if (k == 0) {  // a single element
+        g.n[0] = 1;
+        g.sa[0] = 1;
+        g.sb[0] = 1;
+        k = 1;
+    }
+    g.rank = k;
+    p->g = g;
+
+    // 5. loop family
+    bool ok = true;
+    p->family = family_of(*p, forced, &ok);
+    if (!ok) {
+        delete p;
+        return EBIN_ERR_FAMILY;
+    }
+    *out = p;
+    return EBIN_OK;
+}
+
+// ------------------------------------------------------------------ plan cache
+std::mutex g_cache_mu;
+std::list<ebin_plan_s *> g_cache;  // most recently used first
+uint64_t g_hits = 0, g_misses = 0;
+
+void plan_unref(ebin_plan_s *p) {
+    if (p && p->refs.fetch_sub(1) == 1) delete p;
+}
+
+bool key_equal(const ebin_plan_s &p, uint64_t id, const int64_t *sa, int ra, const int64_t *sb,
+               int rb) {
+    if (p.desc_id != id || p.rank_a != ra || p.rank_b != rb) return false;
+    for (int i = 0; i < ra; ++i)
+        if (p.shape_a[i] != sa[i]) return false;
+    for (int i = 0; i < rb; ++i)
+        if (p.shape_b[i] != sb[i]) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" void ebin_descriptor_destroy(ebin_descriptor_t desc) {
+    if (!desc) return;
+    std::list<ebin_plan_s *> dropped;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        for (auto it = g_cache.begin(); it != g_cache.end();) {
+            if ((*it)->desc_id == desc->id) {
+                dropped.push_back(*it);
+                it = g_cache.erase(it);
+            } else {
+                ++it;
+            }
+        }
+    }
+    for (auto *p : dropped) plan_unref(p);
+    delete desc;
+}
+
+extern "C" ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *shape_a,
+                                        int rank_a, const int64_t *shape_b, int rank_b,
+                                        ebin_plan_t *out) {
+    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (rank_a < 0 || rank_b < 0) return EBIN_ERR_INVALID_ARG;
+    if (rank_a > kMaxRank || rank_b > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
+    if ((rank_a > 0 && !shape_a) || (rank_b > 0 && !shape_b)) return EBIN_ERR_INVALID_ARG;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        for (auto it = g_cache.begin(); it != g_cache.end(); ++it) {
+            if (key_equal(**it, desc->id, shape_a, rank_a, shape_b, rank_b)) {
+                ebin_plan_s *p = *it;
+                g_cache.splice(g_cache.begin(), g_cache, it);
+                p->refs.fetch_add(1);
+                ++g_hits;
+                *out = p;
+                return EBIN_OK;
+            }
+        }
+        ++g_misses;
+    }
+    ebin_plan_s *p = nullptr;
+    const ebin_status st = build_plan(*desc, shape_a, rank_a, shape_b, rank_b, EBIN_FAMILY_AUTO, &p);
+    if (st != EBIN_OK) return st;
+    ebin_plan_s *evicted = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        p->refs.fetch_add(1);  // the cache's reference
+        g_cache.push_front(p);
+        if ((int)g_cache.size() > EBIN_PLAN_CACHE_CAPACITY) {
+            evicted = g_cache.back();
+            g_cache.pop_back();
+        }
+    }
+    plan_unref(evicted);
+    *out = p;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape_a,
+                                               int rank_a, const int64_t *shape_b, int rank_b,
+                                               ebin_family family, ebin_plan_t *out) {
+    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    ebin_plan_s *p = nullptr;
+    const ebin_status st = build_plan(*desc, shape_a, rank_a, shape_b, rank_b, (int)family, &p);
+    if (st != EBIN_OK) return st;
+    *out = p;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_plan_output_shape(ebin_plan_t plan, int64_t *shape, int *rank) {
+    if (!plan || !shape || !rank) return EBIN_ERR_INVALID_ARG;
+    *rank = plan->rank_out;
+    for (int i = 0; i < plan->rank_out; ++i) shape[i] = plan->shape_out[i];
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_plan_numel(ebin_plan_t plan, int64_t *numel) {
+    if (!plan || !numel) return EBIN_ERR_INVALID_ARG;
+    *numel = plan->numel;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_plan_family(ebin_plan_t plan, ebin_family *family) {
+    if (!plan || !family) return EBIN_ERR_INVALID_ARG;
+    *family = (ebin_family)plan->family;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_plan_geometry(ebin_plan_t plan, int *rank, int64_t *n,
+                                          int64_t *stride_a, int64_t *stride_b) {
+    if (!plan || !rank || !n || !stride_a || !stride_b) return EBIN_ERR_INVALID_ARG;
+    *rank = plan->g.rank;
+    for (int i = 0; i < plan->g.rank; ++i) {
+        n[i] = plan->g.n[i];
+        stride_a[i] = plan->g.sa[i];
+        stride_b[i] = plan->g.sb[i];
+    }
+    return EBIN_OK;
+}
+
+extern "C" void ebin_plan_release(ebin_plan_t plan) { plan_unref(plan); }
+
+extern "C" ebin_status ebin_plan_cache_stats(uint64_t *hits, uint64_t *misses, int *size) {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    if (hits) *hits = g_hits;
+    if (misses) *misses = g_misses;
+    if (size) *size = (int)g_cache.size();
+    return EBIN_OK;
+}
+
+extern "C" void ebin_plan_cache_clear(void) {
+    std::list<ebin_plan_s *> dropped;
+    {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        dropped.swap(g_cache);
+        g_hits = 0;
+        g_misses = 0;
+    }
+    for (auto *p : dropped) plan_unref(p);
+}
+
+// ------------------------------------------------------------------ execution
+namespace {
+
+std::mutex g_dev_mu;
+std::map<std::pair<int, uintptr_t>, uint32_t *> g_status_words;
+int g_sm_count[128] = {0};
+
+int sm_count(int dev) {
+    if (dev >= 0 && dev < 128 && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev >= 0 && dev < 128) g_sm_count[dev] = n;
+    return n;
+}
+
+// The status word of (device, stream), allocated and zeroed (stream-ordered)
+// on first use.
+uint32_t *status_word(int dev, cudaStream_t stream, bool create) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    const auto key = std::make_pair(dev, (uintptr_t)stream);
+    auto it = g_status_words.find(key);
+    if (it != g_status_words.end()) return it->second;
+    if (!create) return nullptr;
+    uint32_t *w = nullptr;
+    if (cudaMalloc(&w, sizeof(uint32_t)) != cudaSuccess) return nullptr;
+    if (cudaMemsetAsync(w, 0, sizeof(uint32_t), stream) != cudaSuccess) {
+        cudaFree(w);
+        return nullptr;
+    }
+    g_status_words[key] = w;
+    return w;
+}
+
+bool overlaps(const void *p, int64_t pb, const void *q, int64_t qb) {
+    const uintptr_t a = (uintptr_t)p, b = (uintptr_t)q;
+    return pb > 0 && qb > 0 && a < b + (uintptr_t)qb && b < a + (uintptr_t)pb;
+}
+
+}  // namespace
+
+cudaError_t ebin::launch(const Launch &L) {
+#define EBIN_PICK(g)                                                                      \
+    switch (L.dt) {                                                                       \
+    case 0: return launch_##g##_0(L);                                                     \
+    case 1: return launch_##g##_1(L);                                                     \
+    case 2: return launch_##g##_2(L);                                                     \
+    case 3: return launch_##g##_3(L);                                                     \
+    case 4: return launch_##g##_4(L);                                                     \
+    case 5: return launch_##g##_5(L);                                                     \
+    case 6: return launch_##g##_6(L);                                                     \
+    case 7: return launch_##g##_7(L);                                                     \
+    default: return cudaErrorInvalidValue;                                                \
+    }
+    switch (L.op) {
+    case EBIN_OP_ADD: case EBIN_OP_SUB: case EBIN_OP_MUL: case EBIN_OP_DIV: EBIN_PICK(arith)
+    case EBIN_OP_MOD: EBIN_PICK(mod)
+    case EBIN_OP_POW: EBIN_PICK(pow)
+    case EBIN_OP_EQUAL: case EBIN_OP_LESS: case EBIN_OP_GREATER: case EBIN_OP_LESS_OR_EQUAL:
+    case EBIN_OP_GREATER_OR_EQUAL: EBIN_PICK(cmp)
+    case EBIN_OP_AND: case EBIN_OP_OR: case EBIN_OP_XOR: case EBIN_OP_BITWISE_AND:
+    case EBIN_OP_BITWISE_OR: case EBIN_OP_BITWISE_XOR: case EBIN_OP_BITSHIFT: EBIN_PICK(logic)
+    case EBIN_OP_PRELU: case EBIN_OP_BATCHNORM: case EBIN_OP_CLIP: EBIN_PICK(chan)
+    default: return cudaErrorInvalidValue;
+    }
+#undef EBIN_PICK
+}
+
+extern "C" ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
+                                    void *stream) {
+    if (!plan) return EBIN_ERR_INVALID_ARG;
+    const ebin_plan_s &p = *plan;
+    if (p.numel == 0) return EBIN_OK;  // empty dims: no work, nothing read
+    const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max);
+    if (!A || !out || (b_needed && !B)) return EBIN_ERR_INVALID_ARG;
+
+    // Aliasing: an input may share storage with out only as the identical
+    // buffer of the output's type and element count; a broadcast input or a
+    // parameter block is never overwritten in place.
+    const int64_t isz = (int64_t)ebin_dtype_size(p.dt);
+    const int64_t out_bytes = p.numel * (int64_t)ebin_dtype_size(p.out_dt);
+    if (overlaps(A, p.numel_a * isz, out, out_bytes)) {
+        if (!(A == out && p.numel_a == p.numel && p.dt == p.out_dt)) return EBIN_ERR_ALIAS;
+    }
+    if (B && overlaps(B, p.numel_b * isz, out, out_bytes)) {
+        if (!(plain_b(p.op) && B == out && p.numel_b == p.numel && p.dt == p.out_dt))
+            return EBIN_ERR_ALIAS;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EBIN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    ebin::Launch L{};
+    L.op = p.op;
+    L.dt = dt_class(p.dt);
+    L.family = p.family;
+    L.g = p.g;
+    L.numel = p.numel;
+    L.A = A;
+    L.B = B;
+    L.out = out;
+    L.args.fmod = p.attrs.fmod;
+    L.args.direction = p.attrs.direction;
+    L.args.eps = p.attrs.epsilon;
+    L.args.has_min = p.attrs.clip_has_min;
+    L.args.has_max = p.attrs.clip_has_max;
+    L.args.plane = p.plane;
+    L.stream = s;
+    L.num_sms = sm_count(dev);
+    L.status = nullptr;
+    if (validates(p.op, p.dt)) {
+        L.status = status_word(dev, s, true);
+        if (!L.status) return EBIN_ERR_CUDA;
+    }
+    // The vector families move 16-byte packs: pointers off that alignment
+    // take the general kernel, which reads element by element.
+    if (L.family != ebin::FAM_GENERAL_STRIDED) {
+        const uintptr_t G = 16 / (uintptr_t)isz;
+        const uintptr_t out_align = G * (uintptr_t)ebin_dtype_size(p.out_dt);
+        const bool aligned = ((uintptr_t)A % 16 == 0) && (!B || (uintptr_t)B % 16 == 0) &&
+                             ((uintptr_t)out % out_align == 0);
+        if (!aligned) L.family = ebin::FAM_GENERAL_STRIDED;
+    }
+    const cudaError_t e = ebin::launch(L);
+    g_launches.fetch_add(1);
+    return e == cudaSuccess ? EBIN_OK : EBIN_ERR_CUDA;
+}
+
+extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, const void *host_b,
+                                         void *host_out, void *dev_a, void *dev_b, void *dev_out,
+                                         void *stream) {
+    if (!plan) return EBIN_ERR_INVALID_ARG;
+    const ebin_plan_s &p = *plan;
+    if (p.numel == 0) return EBIN_OK;
+    if (!host_a || !host_out || !dev_a || !dev_out) return EBIN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t isz = ebin_dtype_size(p.dt);
+    if (cudaMemcpyAsync(dev_a, host_a, (size_t)p.numel_a * isz, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return EBIN_ERR_CUDA;
+    if (host_b && dev_b) {
+        if (cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+            return EBIN_ERR_CUDA;
+    }
+    const ebin_status st = ebin_execute(plan, dev_a, dev_b, dev_out, stream);
+    if (st != EBIN_OK) return st;
+    if (cudaMemcpyAsync(host_out, dev_out, (size_t)p.numel * ebin_dtype_size(p.out_dt),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return EBIN_ERR_CUDA;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_get_device_status(void *stream, uint32_t *bits) {
+    if (!bits) return EBIN_ERR_INVALID_ARG;
+    *bits = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EBIN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t *w = status_word(dev, s, false);
+    if (!w) return cudaStreamSynchronize(s) == cudaSuccess ? EBIN_OK : EBIN_ERR_CUDA;
+    uint32_t h = 0;
+    if (cudaMemcpyAsync(&h, w, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return EBIN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return EBIN_ERR_CUDA;
+    if (cudaMemsetAsync(w, 0, sizeof(uint32_t), s) != cudaSuccess) return EBIN_ERR_CUDA;
+    *bits = h;
+    return EBIN_OK;
+}
+
+extern "C" uint64_t ebin_launch_count(void) { return g_launches.load(); }
+
+extern "C" size_t ebin_dtype_size(ebin_dtype t) {
+    switch (t) {
+    case EBIN_FLOAT32: case EBIN_INT32: case EBIN_UINT32: return 4;
+    case EBIN_FLOAT16: case EBIN_BFLOAT16: return 2;
+    case EBIN_INT64: return 8;
+    case EBIN_UINT8: case EBIN_BOOL: return 1;
+    }
+    return 0;
+}
+
+extern "C" const char *ebin_status_string(ebin_status s) {
+    switch (s) {
+    case EBIN_OK: return "ok";
+    case EBIN_ERR_INVALID_ARG: return "invalid argument";
+    case EBIN_ERR_UNSUPPORTED_OP: return "unsupported operator";
+    case EBIN_ERR_UNSUPPORTED_TYPE: return "unsupported type";
+    case EBIN_ERR_INVALID_ATTR: return "invalid attribute";
+    case EBIN_ERR_INCOMPATIBLE_SHAPES: return "incompatible shapes";
+    case EBIN_ERR_RANK_TOO_LARGE: return "rank too large";
+    case EBIN_ERR_ALIAS: return "input aliases the output";
+    case EBIN_ERR_CUDA: return "CUDA error";
+    case EBIN_ERR_FAMILY: return "loop family cannot traverse this plan";
+    }
+    return "unknown status";
+}

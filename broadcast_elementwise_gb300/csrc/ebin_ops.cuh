@@ -1,0 +1,350 @@
+// Element types and per-element operator functors of the broadcast binary
+// engine (device side).
+//
+// Semantics follow "Binary Kernel Design" (onnx-light-cpu), section
+// "Operators and traversal" (operator set; Mod opset-28 sign rules; FLOAT16
+// and BFLOAT16 computed through float) and section "Compute, scheduling, and
+// safety" (validation of integer division, modulo and shifts; one byte per
+// BOOL); BatchNormalization, PRelu and Clip follow the 0verkilll/onnx "ops"
+// docs (BatchNormalizationOp, PReluOp, ClipOp) and ncnn operators.md
+// (batchnorm, bias, clip).
+//
+// Floating arithmetic uses the round-to-nearest intrinsics (__fadd_rn, ...)
+// so that nothing is contracted into an FMA: every step rounds alone, as in
+// IEEE-754 binary32.  Half and bfloat16 widen exactly to float, operate in
+// float and round once (round to nearest even) on the way out.
+#pragma once
+
+#include <cstdint>
+#include <type_traits>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ebin_launch.h"
+
+namespace ebin {
+
+// One byte per BOOL; any nonzero byte reads as true, results are 0 or 1.
+struct Bool8 {
+    uint8_t v;
+};
+
+constexpr uint32_t kErrDivByZero = 0x1u;
+constexpr uint32_t kErrShiftRange = 0x2u;
+
+// ---------------------------------------------------------------- type traits
+template <class T> struct Tr;
+
+template <> struct Tr<float> {
+    using C = float;
+    static constexpr bool kFloat = true;
+    __device__ __forceinline__ static float in(float x) { return x; }
+    __device__ __forceinline__ static float out(float v) { return v; }
+};
+template <> struct Tr<__half> {
+    using C = float;
+    static constexpr bool kFloat = true;
+    __device__ __forceinline__ static float in(__half x) { return __half2float(x); }
+    __device__ __forceinline__ static __half out(float v) { return __float2half_rn(v); }
+};
+template <> struct Tr<__nv_bfloat16> {
+    using C = float;
+    static constexpr bool kFloat = true;
+    __device__ __forceinline__ static float in(__nv_bfloat16 x) { return __bfloat162float(x); }
+    __device__ __forceinline__ static __nv_bfloat16 out(float v) { return __float2bfloat16_rn(v); }
+};
+template <class I, class U, bool S> struct IntTr {
+    using C = I;
+    using UT = U;
+    static constexpr bool kFloat = false;
+    static constexpr bool kSigned = S;
+    static constexpr int kBits = 8 * sizeof(I);
+    __device__ __forceinline__ static I in(I x) { return x; }
+    __device__ __forceinline__ static I out(I v) { return v; }
+};
+template <> struct Tr<int32_t> : IntTr<int32_t, uint32_t, true> {};
+template <> struct Tr<int64_t> : IntTr<int64_t, uint64_t, true> {};
+template <> struct Tr<uint8_t> : IntTr<uint8_t, uint8_t, false> {};
+template <> struct Tr<uint32_t> : IntTr<uint32_t, uint32_t, false> {};
+template <> struct Tr<Bool8> {
+    using C = bool;
+    static constexpr bool kFloat = false;
+    __device__ __forceinline__ static bool in(Bool8 x) { return x.v != 0; }
+};
+
+template <class T> constexpr bool is_float_v = std::is_same_v<T, float> ||
+                                               std::is_same_v<T, __half> ||
+                                               std::is_same_v<T, __nv_bfloat16>;
+template <class T> constexpr bool is_int_v = std::is_same_v<T, int32_t> ||
+                                             std::is_same_v<T, int64_t> ||
+                                             std::is_same_v<T, uint8_t> ||
+                                             std::is_same_v<T, uint32_t>;
+template <class T> constexpr bool is_bool_v = std::is_same_v<T, Bool8>;
+template <class T> constexpr bool is_signed_int_v = std::is_same_v<T, int32_t> ||
+                                                    std::is_same_v<T, int64_t>;
+
+// Common shape of an operator functor whose B operand is an ordinary
+// broadcast tensor of the input type.
+template <class T, class O> struct PlainB {
+    using In = T;
+    using Out = O;
+    using BV = T;
+    static constexpr bool kPlainB = true;
+    __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &) {
+        return B[off];
+    }
+};
+
+// ---------------------------------------------------------------- exact fmod
+//
+// Truncated remainder r = a - trunc(a/b)*b, exact, for finite a and nonzero
+// finite b.  Fast path (|a/b| < 2^23): q = trunc(RN(|a|/|b|)).  Because RN is
+// monotone and every integer below 2^24 is representable, q is either
+// n = trunc(|a|/|b|) or n + 1.  |a| >= |b| makes |a| a multiple of ulp(|b|),
+// so |a| - q|b| is a multiple of ulp(|b|) smaller than |b| in magnitude: it is
+// representable and the single rounding of fmaf(-q, |b|, |a|) is exact.  A
+// negative result means q was n + 1, and adding |b| back is exact as well.
+// Larger quotients, infinities, NaNs and zero divisors go to CUDA's fmodf.
+__device__ __forceinline__ float fmod_exact(float a, float b) {
+    const float aa = fabsf(a), ab = fabsf(b);
+    if (aa < ab) return a;                         // includes a = +-0 (b finite or inf)
+    if (!(aa < INFINITY) || !(ab > 0.0f) || !(ab < INFINITY)) return fmodf(a, b);
+    const float q = truncf(__fdiv_rn(aa, ab));
+    if (q < 8388608.0f) {
+        float r = fmaf(-q, ab, aa);
+        if (r < 0.0f) r = __fadd_rn(r, ab);
+        return copysignf(r, a);                    // a zero result keeps the dividend's sign
+    }
+    return fmodf(a, b);
+}
+
+// Mod with opset-28 rules: fmod=1 truncated; fmod=0 floor remainder where a
+// nonzero result with the wrong sign gets b added (one rounded add) and an
+// exact zero takes the divisor's sign.
+__device__ __forceinline__ float mod_float(float a, float b, int fmod_flag) {
+    float r = fmod_exact(a, b);
+    if (fmod_flag) return r;
+    if (r == 0.0f) return copysignf(0.0f, b);
+    if (signbit(r) != signbit(b)) r = __fadd_rn(r, b);
+    return r;
+}
+
+// ---------------------------------------------------------------- arithmetic
+enum ArithK { K_ADD = 0, K_SUB = 1, K_MUL = 2, K_DIV = 3 };
+
+template <class T, int K> struct OpArith : PlainB<T, T> {
+    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kValidates = (K == K_DIV) && is_int_v<T>;
+    __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
+        if constexpr (is_float_v<T>) {
+            const float x = Tr<T>::in(a), y = Tr<T>::in(b);
+            float r;
+            if constexpr (K == K_ADD) r = __fadd_rn(x, y);
+            else if constexpr (K == K_SUB) r = __fsub_rn(x, y);
+            else if constexpr (K == K_MUL) r = __fmul_rn(x, y);
+            else r = __fdiv_rn(x, y);
+            return Tr<T>::out(r);
+        } else {
+            using U = typename Tr<T>::UT;
+            if constexpr (K == K_ADD) return (T)((U)a + (U)b);
+            else if constexpr (K == K_SUB) return (T)((U)a - (U)b);
+            else if constexpr (K == K_MUL) return (T)((U)a * (U)b);
+            else {
+                if (b == 0) { err |= kErrDivByZero; return (T)0; }
+                if constexpr (Tr<T>::kSigned) {
+                    if (b == (T)-1) return (T)((U)0 - (U)a);    // INT_MIN / -1 wraps
+                }
+                return (T)(a / b);                               // truncates toward zero
+            }
+        }
+    }
+};
+
+template <class T> struct OpMod : PlainB<T, T> {
+    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kValidates = is_int_v<T>;
+    __device__ __forceinline__ static T apply(T a, T b, const OpArgs &p, uint32_t &err) {
+        if constexpr (is_float_v<T>) {
+            return Tr<T>::out(mod_float(Tr<T>::in(a), Tr<T>::in(b), p.fmod));
+        } else {
+            if (b == 0) { err |= kErrDivByZero; return (T)0; }
+            if constexpr (Tr<T>::kSigned) {
+                if (b == (T)-1) return (T)0;
+                T r = a % b;                                     // sign of the dividend
+                if (!p.fmod && r != 0 && ((r < 0) != (b < 0))) r = (T)(r + b);
+                return r;
+            } else {
+                return (T)(a % b);
+            }
+        }
+    }
+};
+
+template <class T> struct OpPow : PlainB<T, T> {
+    static constexpr bool kLegal = is_float_v<T> || is_signed_int_v<T>;
+    static constexpr bool kValidates = is_signed_int_v<T>;
+    __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
+        if constexpr (is_float_v<T>) {
+            // C pow semantics evaluated in binary64, rounded once to binary32
+            const double r = pow((double)Tr<T>::in(a), (double)Tr<T>::in(b));
+            return Tr<T>::out(__double2float_rn(r));
+        } else {
+            using U = typename Tr<T>::UT;
+            if (b < 0) {
+                if (a == 0) { err |= kErrDivByZero; return (T)0; }
+                if (a == 1) return (T)1;
+                if (a == (T)-1) return (b & 1) ? (T)-1 : (T)1;
+                return (T)0;                                     // trunc(1 / a^|b|)
+            }
+            U result = 1, base = (U)a, e = (U)b;
+            while (e) {                                          // square and multiply, wrapping
+                if (e & 1u) result *= base;
+                base *= base;
+                e >>= 1;
+            }
+            return (T)result;
+        }
+    }
+};
+
+// ---------------------------------------------------------------- comparisons
+enum CmpK { K_EQ = 0, K_LT = 1, K_GT = 2, K_LE = 3, K_GE = 4 };
+
+template <class C, int K> __device__ __forceinline__ bool compare(C x, C y) {
+    if constexpr (K == K_EQ) return x == y;
+    else if constexpr (K == K_LT) return x < y;
+    else if constexpr (K == K_GT) return x > y;
+    else if constexpr (K == K_LE) return x <= y;
+    else return x >= y;
+}
+
+template <class T, int K> struct OpCmp : PlainB<T, Bool8> {
+    static constexpr bool kLegal = is_float_v<T> || is_int_v<T> || (K == K_EQ && is_bool_v<T>);
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static Bool8 apply(T a, T b, const OpArgs &, uint32_t &) {
+        return Bool8{(uint8_t)(compare<typename Tr<T>::C, K>(Tr<T>::in(a), Tr<T>::in(b)) ? 1 : 0)};
+    }
+};
+
+// ---------------------------------------------------------------- logical / bitwise / shift
+enum LogicK { K_AND = 0, K_OR = 1, K_XOR = 2 };
+
+template <class T, int K> struct OpLogic : PlainB<T, Bool8> {
+    static constexpr bool kLegal = is_bool_v<T>;
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static Bool8 apply(T a, T b, const OpArgs &, uint32_t &) {
+        const bool x = a.v != 0, y = b.v != 0;
+        bool r;
+        if constexpr (K == K_AND) r = x && y;
+        else if constexpr (K == K_OR) r = x || y;
+        else r = x != y;
+        return Bool8{(uint8_t)(r ? 1 : 0)};
+    }
+};
+
+template <class T, int K> struct OpBitwise : PlainB<T, T> {
+    static constexpr bool kLegal = is_int_v<T>;
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &) {
+        if constexpr (K == K_AND) return (T)(a & b);
+        else if constexpr (K == K_OR) return (T)(a | b);
+        else return (T)(a ^ b);
+    }
+};
+
+template <class T> struct OpShift : PlainB<T, T> {
+    static constexpr bool kLegal = std::is_same_v<T, uint8_t> || std::is_same_v<T, uint32_t>;
+    static constexpr bool kValidates = true;
+    __device__ __forceinline__ static T apply(T a, T b, const OpArgs &p, uint32_t &err) {
+        if constexpr (kLegal) {
+            constexpr uint32_t w = 8 * sizeof(T);
+            const uint32_t s = (uint32_t)b;
+            if (s >= w) { err |= kErrShiftRange; return (T)0; }
+            return p.direction == 0 ? (T)((uint32_t)a << s) : (T)((uint32_t)a >> s);
+        } else {
+            return a;
+        }
+    }
+};
+
+// ---------------------------------------------------------------- per-channel operators
+template <class T> struct OpPRelu : PlainB<T, T> {
+    static constexpr bool kLegal = is_float_v<T> || is_signed_int_v<T> ||
+                                   std::is_same_v<T, uint32_t>;
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static T apply(T a, T slope, const OpArgs &, uint32_t &) {
+        if constexpr (is_float_v<T>) {
+            const float x = Tr<T>::in(a);
+            if (x >= 0.0f) return a;                             // keeps -0 and exact bits
+            return Tr<T>::out(__fmul_rn(Tr<T>::in(slope), x));
+        } else if constexpr (Tr<T>::kSigned) {
+            using U = typename Tr<T>::UT;
+            return a >= 0 ? a : (T)((U)slope * (U)a);
+        } else {
+            return a;                                            // unsigned: never below zero
+        }
+    }
+};
+
+// Inference BatchNormalization: y = (x - mean) / sqrt(var + eps) * scale + bias,
+// each step rounded in binary32 in the order written.  B holds four rows
+// (scale, bias, mean, var) of `plane` elements; the per-channel sqrt is formed
+// when the parameters are loaded.
+struct BNParams {
+    float scale, bias, mean, d;
+};
+
+template <class T> struct OpBN {
+    using In = T;
+    using Out = T;
+    using BV = BNParams;
+    static constexpr bool kPlainB = false;
+    static constexpr bool kLegal = is_float_v<T>;
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
+        BNParams r;
+        r.scale = Tr<T>::in(B[off]);
+        r.bias = Tr<T>::in(B[off + p.plane]);
+        r.mean = Tr<T>::in(B[off + 2 * p.plane]);
+        const float var = Tr<T>::in(B[off + 3 * p.plane]);
+        r.d = __fsqrt_rn(__fadd_rn(var, p.eps));
+        return r;
+    }
+    __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
+        float t = __fsub_rn(Tr<T>::in(a), q.mean);
+        t = __fdiv_rn(t, q.d);
+        t = __fmul_rn(t, q.scale);
+        return Tr<T>::out(__fadd_rn(t, q.bias));
+    }
+};
+
+// Clip: y = x, raised to min when below it, then lowered to max when above it.
+// B = {min, max}; an absent bound is never applied.  The element offset is
+// ignored: the two bounds are shared by every element.
+template <class T> struct ClipParams {
+    typename Tr<T>::C lo, hi;
+};
+
+template <class T> struct OpClip {
+    using In = T;
+    using Out = T;
+    using BV = ClipParams<T>;
+    static constexpr bool kPlainB = false;
+    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static BV loadB(const T *B, int64_t, const OpArgs &p) {
+        BV r{};
+        if (p.has_min) r.lo = Tr<T>::in(B[0]);
+        if (p.has_max) r.hi = Tr<T>::in(B[1]);
+        return r;
+    }
+    __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &p, uint32_t &) {
+        auto y = Tr<T>::in(a);
+        if (p.has_min && y < q.lo) y = q.lo;
+        if (p.has_max && y > q.hi) y = q.hi;
+        return Tr<T>::out(y);
+    }
+};
+
+}  // namespace ebin

@@ -1,0 +1,286 @@
+/*
+ * ebin -- ONNX broadcast binary elementwise engine for one NVIDIA GB300 GPU.
+ *
+ * C ABI.  Plain pointers and sizes only; no C++ or PyTorch types.
+ *
+ * The engine follows the three-stage statement of "Binary Kernel Design"
+ * (onnx-light-cpu), section "Prepared execution": a descriptor is built once
+ * per node, a plan is built (or fetched from a bounded 8-entry LRU) once per
+ * pair of concrete input shapes, and the plan is executed on device buffers.
+ *
+ * Threading: every entry point is thread-safe.  Descriptors and plans are
+ * immutable after creation and may be shared between host threads and CUDA
+ * streams.
+ *
+ * Streams: `stream` arguments are a cudaStream_t passed as void* (NULL = the
+ * legacy default stream).  Kernels are enqueued; nothing synchronises unless
+ * stated.
+ *
+ * Device pointers: A, B and out of ebin_execute are device (or managed)
+ * memory on the current CUDA device, owned by the caller, laid out dense
+ * row-major (C order) in the element type of the descriptor.
+ */
+#ifndef EBIN_H
+#define EBIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EBIN_MAX_RANK 8
+#define EBIN_PLAN_CACHE_CAPACITY 8
+#define EBIN_DEFAULT_EPSILON 1e-5f
+
+/* Return codes.  Host-detectable errors are returned synchronously. */
+typedef enum ebin_status {
+    EBIN_OK = 0,
+    EBIN_ERR_INVALID_ARG = 1,         /* NULL handle, NULL buffer with work to do, bad rank/dim */
+    EBIN_ERR_UNSUPPORTED_OP = 2,      /* operator code out of range */
+    EBIN_ERR_UNSUPPORTED_TYPE = 3,    /* type pair not in the operator's manifest */
+    EBIN_ERR_INVALID_ATTR = 4,        /* Mod fmod/opset, BitShift direction */
+    EBIN_ERR_INCOMPATIBLE_SHAPES = 5, /* not broadcastable (or not one-way for PRelu/BN/Clip) */
+    EBIN_ERR_RANK_TOO_LARGE = 6,      /* an input rank above EBIN_MAX_RANK */
+    EBIN_ERR_ALIAS = 7,               /* an input overlaps out without being identical to it */
+    EBIN_ERR_CUDA = 8,                /* a CUDA runtime call or kernel launch failed */
+    EBIN_ERR_FAMILY = 9               /* a forced loop family cannot traverse this plan */
+} ebin_status;
+
+/*
+ * Operators.  The nineteen binary operators of "Binary Kernel Design",
+ * section "Operators and traversal" (arithmetic, comparisons, logical,
+ * bitwise, BitShift, PRelu), plus the two broadcasts that inference
+ * BatchNormalization and Clip reduce to (0verkilll/onnx "ops" docs,
+ * BatchNormalizationOp and ClipOp; ncnn operators.md, batchnorm and clip).
+ * Bias (ncnn operators.md, bias) is EBIN_OP_ADD with B shaped [C,1,1].
+ */
+typedef enum ebin_op {
+    EBIN_OP_ADD = 0,
+    EBIN_OP_SUB = 1,
+    EBIN_OP_MUL = 2,
+    EBIN_OP_DIV = 3,
+    EBIN_OP_MOD = 4,              /* attrs.fmod; opset 10..28 */
+    EBIN_OP_POW = 5,
+    EBIN_OP_EQUAL = 6,            /* comparisons write one byte per BOOL (0 or 1) */
+    EBIN_OP_LESS = 7,
+    EBIN_OP_GREATER = 8,
+    EBIN_OP_LESS_OR_EQUAL = 9,
+    EBIN_OP_GREATER_OR_EQUAL = 10,
+    EBIN_OP_AND = 11,             /* BOOL in, BOOL out; a nonzero byte is true */
+    EBIN_OP_OR = 12,
+    EBIN_OP_XOR = 13,
+    EBIN_OP_BITWISE_AND = 14,
+    EBIN_OP_BITWISE_OR = 15,
+    EBIN_OP_BITWISE_XOR = 16,
+    EBIN_OP_BITSHIFT = 17,        /* attrs.direction */
+    EBIN_OP_PRELU = 18,           /* B = slope, broadcast one way to A */
+    EBIN_OP_BATCHNORM = 19,       /* inference; B = [4, C]: scale, bias, mean, var rows */
+    EBIN_OP_CLIP = 20,            /* B = [2]: {min, max}; attrs.clip_has_min/max */
+    EBIN_OP_COUNT = 21
+} ebin_op;
+
+/* Element types, numbered as ONNX TensorProto.DataType. */
+typedef enum ebin_dtype {
+    EBIN_FLOAT32 = 1,
+    EBIN_UINT8 = 2,
+    EBIN_INT32 = 6,
+    EBIN_INT64 = 7,
+    EBIN_BOOL = 9,                /* one byte per element */
+    EBIN_FLOAT16 = 10,
+    EBIN_UINT32 = 12,
+    EBIN_BFLOAT16 = 16
+} ebin_dtype;
+
+/*
+ * Loop families ("Binary Kernel Design", section "Operators and traversal",
+ * loop-family table).  Each has its own kernel; the selection rule is stated
+ * at ebin_plan_create.
+ */
+typedef enum ebin_family {
+    EBIN_FAMILY_AUTO = -1,            /* only as a request to ebin_plan_create_forced */
+    EBIN_FAMILY_EMPTY = 0,            /* zero output elements: nothing is launched or read */
+    EBIN_FAMILY_CONTIGUOUS = 1,
+    EBIN_FAMILY_LEFT_SCALAR = 2,
+    EBIN_FAMILY_RIGHT_SCALAR = 3,
+    EBIN_FAMILY_REPEATED_BLOCK = 4,
+    EBIN_FAMILY_INNER_VECTOR_OUTER = 5,
+    EBIN_FAMILY_GENERAL_STRIDED = 6
+} ebin_family;
+
+/* Device status bits ("Compute, scheduling, and safety": validation before the math). */
+#define EBIN_DEVICE_DIV_BY_ZERO 0x1u  /* integer Div/Mod by 0, or integer 0 to a negative power */
+#define EBIN_DEVICE_SHIFT_RANGE 0x2u  /* BitShift count >= the element width in bits */
+
+/*
+ * Operator attributes.  Pass NULL to ebin_descriptor_create for the defaults
+ * (fmod 0, direction LEFT, epsilon 1e-5, both Clip bounds present).
+ *   fmod          Mod only: 0 = floor remainder (result and exact zeros take
+ *                 the divisor's sign), 1 = truncated remainder (the dividend's
+ *                 sign, including a signed zero).  Floating Mod with fmod 0
+ *                 needs opset 28 ("Binary Kernel Design", Operators and
+ *                 traversal).
+ *   direction     BitShift only: 0 = LEFT, 1 = RIGHT.
+ *   epsilon       BatchNormalization only.
+ *   clip_has_min  Clip only: nonzero if B[0] is a lower bound.
+ *   clip_has_max  Clip only: nonzero if B[1] is an upper bound.
+ */
+typedef struct ebin_attrs {
+    int32_t fmod;
+    int32_t direction;
+    float epsilon;
+    int32_t clip_has_min;
+    int32_t clip_has_max;
+} ebin_attrs;
+
+typedef struct ebin_descriptor_s *ebin_descriptor_t;
+typedef struct ebin_plan_s *ebin_plan_t;
+
+/*
+ * Build a descriptor ("Binary Kernel Design", Prepared execution: "built once
+ * for the node"): checks the operator, opset and attributes, checks that
+ * (dtype_a, dtype_b) is a registered type pair of the operator and resolves the
+ * output type.  Each descriptor receives a fresh, never reused, monotonic id.
+ *
+ *   op, opset      operator and the node's opset (only Mod reads opset: 10..28)
+ *   attrs          may be NULL (defaults above); copied, not retained
+ *   dtype_a/b      element types of A and B; they must be equal
+ *   out            receives the new descriptor; the caller owns it
+ * Errors: INVALID_ARG (out NULL), UNSUPPORTED_OP, UNSUPPORTED_TYPE, INVALID_ATTR.
+ */
+ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_attrs *attrs,
+                                   ebin_dtype dtype_a, ebin_dtype dtype_b,
+                                   ebin_descriptor_t *out);
+
+/* Output element type: BOOL for comparisons and logical operators, else dtype_a. */
+ebin_status ebin_descriptor_output_dtype(ebin_descriptor_t desc, ebin_dtype *out);
+
+/* The descriptor's monotonic identity (the plan cache keys on it, never on the pointer). */
+ebin_status ebin_descriptor_id(ebin_descriptor_t desc, uint64_t *id);
+
+/*
+ * Free a descriptor.  Cached plans built from it are dropped from the LRU;
+ * plans the caller still holds stay valid (they copy what they need).
+ */
+void ebin_descriptor_destroy(ebin_descriptor_t desc);
+
+/*
+ * Plan the broadcast of concrete input shapes ("Binary Kernel Design",
+ * Operators and traversal; Prepared execution for the cache):
+ *   1. right-align the shapes (a rank-0 shape is a scalar) and check that each
+ *      dimension pair is equal or contains a 1 (0 pairs only with 0 or 1);
+ *      PRelu, BatchNormalization and Clip broadcast one way: out == A's shape;
+ *   2. give broadcast dimensions zero strides;
+ *   3. drop dimensions of output extent 1;
+ *   4. merge adjacent dimensions i, i+1 when stride[i] == stride[i+1] * n[i+1]
+ *      holds for A, B and out;
+ *   5. pick the loop family:
+ *        numel == 0                                   -> EMPTY
+ *        rank 1, strides (A,B) (1,1) / (0,1) / (1,0)  -> CONTIGUOUS / LEFT_ / RIGHT_SCALAR
+ *        rank 2, one input dense and the other with strides (1,0) (one value
+ *        per row) or (0,1) (one row block reused), row length a multiple of
+ *        the vector width                              -> REPEATED_BLOCK
+ *        innermost extent >= 64 and a multiple of the vector width
+ *                                                      -> INNER_VECTOR_OUTER
+ *        otherwise                                     -> GENERAL_STRIDED
+ *      (vector width = 16 bytes / element size of A).
+ * The result is looked up in, or inserted into, a process-wide LRU of
+ * EBIN_PLAN_CACHE_CAPACITY plans keyed on (descriptor id, types, both shapes);
+ * a miss always builds and validates a fresh plan.
+ *
+ * Shapes: shape_a[rank_a], shape_b[rank_b], dims >= 0.  For BatchNormalization
+ * B is [4, C] with C == shape_a[1] (rank_a >= 2); for Clip B is [2].
+ *   out            receives a plan reference; release it with ebin_plan_release
+ * Errors: INVALID_ARG, RANK_TOO_LARGE, INCOMPATIBLE_SHAPES.
+ */
+ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *shape_a, int rank_a,
+                             const int64_t *shape_b, int rank_b, ebin_plan_t *out);
+
+/*
+ * As ebin_plan_create, but force a loop family (for testing every kernel on
+ * the same inputs).  Forced plans bypass the cache.  GENERAL_STRIDED can run
+ * every plan; the others only geometries they can traverse (else FAMILY).
+ * With zero output elements the family is always EMPTY.
+ */
+ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape_a, int rank_a,
+                                    const int64_t *shape_b, int rank_b, ebin_family family,
+                                    ebin_plan_t *out);
+
+/* Output shape: `shape` must hold EBIN_MAX_RANK entries; *rank receives its rank. */
+ebin_status ebin_plan_output_shape(ebin_plan_t plan, int64_t *shape, int *rank);
+
+/* Number of output elements. */
+ebin_status ebin_plan_numel(ebin_plan_t plan, int64_t *numel);
+
+/* The selected loop family. */
+ebin_status ebin_plan_family(ebin_plan_t plan, ebin_family *family);
+
+/*
+ * The coalesced traversal: *rank dims with extents n[] and element strides of
+ * A and B (0 on broadcast dims); out is dense.  Arrays hold EBIN_MAX_RANK.
+ */
+ebin_status ebin_plan_geometry(ebin_plan_t plan, int *rank, int64_t *n, int64_t *stride_a,
+                               int64_t *stride_b);
+
+/* Drop one reference; the plan is freed when no caller and no cache slot holds it. */
+void ebin_plan_release(ebin_plan_t plan);
+
+/* Plan cache counters since the last clear, and its current size (<= 8). */
+ebin_status ebin_plan_cache_stats(uint64_t *hits, uint64_t *misses, int *size);
+
+/* Empty the plan cache and zero its counters (held plans stay valid). */
+void ebin_plan_cache_clear(void);
+
+/*
+ * Run a plan on device buffers ("Binary Kernel Design", Compute, scheduling,
+ * and safety): one kernel of the plan's family is enqueued on `stream`.
+ *   A, B, out   device pointers of the plan's input and output shapes (dense).
+ *               B may be NULL only for Clip without bounds.  With zero output
+ *               elements nothing is read or written and NULL is accepted.
+ *               An input may alias out only if it is the same pointer and has
+ *               the output's type and shape; any other overlap is ALIAS.
+ *               Pointers not aligned to 16 bytes run the general kernel.
+ *   stream      cudaStream_t as void* (NULL = legacy default stream)
+ * Returns once the kernel is enqueued.  Invalid elements (integer division by
+ * zero, shift counts out of range) do not stop the kernel: they write 0 and set
+ * bits in the stream's status word, read with ebin_get_device_status.
+ * Errors: INVALID_ARG, ALIAS, CUDA.
+ */
+ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
+                         void *stream);
+
+/*
+ * End-to-end form of ebin_execute for callers whose data lives in host
+ * memory: enqueues on `stream` the copies host_a -> dev_a and host_b -> dev_b,
+ * the kernel, and the copy dev_out -> host_out.  All six buffers belong to the
+ * caller and are sized for the plan; host buffers should be pinned for the
+ * copies to overlap.  Does not synchronise: host_out is valid after the
+ * stream completes.  Errors as ebin_execute.
+ */
+ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, const void *host_b,
+                              void *host_out, void *dev_a, void *dev_b, void *dev_out,
+                              void *stream);
+
+/*
+ * Read and clear the device status word of `stream` on the current device:
+ * synchronises the stream, returns the OR of the EBIN_DEVICE_* bits raised
+ * since the last call, then zeroes the word (stream-ordered).  A stream that
+ * never ran a validating operator reports 0.
+ */
+ebin_status ebin_get_device_status(void *stream, uint32_t *bits);
+
+/* Kernels this library has launched in this process (for launch accounting). */
+uint64_t ebin_launch_count(void);
+
+/* Bytes per element of a type (0 if unknown). */
+size_t ebin_dtype_size(ebin_dtype dtype);
+
+/* A static, human-readable name for a status code. */
+const char *ebin_status_string(ebin_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EBIN_H */

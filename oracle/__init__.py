@@ -45,9 +45,23 @@ STATUS_SHIFT_RANGE = 2
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
 
 
+def _elf_matches_host(path: str) -> bool:
+    """True if the shared object at `path` was built for this machine's CPU."""
+    import platform
+    import struct
+    want = {"x86_64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+        return want is None or struct.unpack("<H", head[18:20])[0] == want
+    except (OSError, struct.error):
+        return False
+
+
 def build(force: bool = False) -> str:
     """Compile liboracle.so next to its source (plain C, no GPU needed)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if (force or not os.path.exists(_LIB) or not _elf_matches_host(_LIB)
+            or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)):
         tmp = _LIB + ".tmp%d" % os.getpid()
         subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)

@@ -1,0 +1,137 @@
+"""GPU behaviour around the kernels: validation status, aliasing, alignment
+fallback, streams, the host-buffer entry point and launch accounting."""
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from conftest import assert_bits_equal
+from engine_util import inputs_for, run_engine, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+eb = pytest.importorskip("broadcast_elementwise_gb300")
+
+
+def test_division_by_zero_sets_status_and_clears():
+    a = np.arange(1, 100001, dtype=np.int32)
+    b = np.ones(100000, np.int32)
+    b[777] = 0
+    got, bits, _ = run_engine("Div", "int32", a, b)
+    want, wbits = oracle.run("Div", a, b, "int32")
+    assert bits == eb.DEVICE_DIV_BY_ZERO == wbits
+    assert (got == want).all()
+    # read-and-clear: the next read on the stream is clean
+    assert eb.get_device_status() == 0
+    got, bits, _ = run_engine("Mod", "int32", a, np.full(1, 7, np.int32).reshape(()),
+                              attrs={"fmod": 0})
+    assert bits == 0
+
+
+def test_scalar_zero_divisor_and_negative_power():
+    a = datagen.make("bits", "int64", (5000,), 1, 0)
+    _, bits, fam = run_engine("Mod", "int64", a, np.zeros((), np.int64), attrs={"fmod": 1})
+    assert fam == "right_scalar" and bits == eb.DEVICE_DIV_BY_ZERO
+    base = np.array([0, 2, 3], np.int32)
+    _, bits, _ = run_engine("Pow", "int32", base, np.array([-1], np.int32))
+    assert bits == eb.DEVICE_DIV_BY_ZERO
+
+
+@pytest.mark.parametrize("dtype", ["uint8", "uint32"])
+def test_shift_range(dtype):
+    w = 8 * np.dtype(datagen.STORAGE[dtype]).itemsize
+    a = datagen.make("bits", dtype, (4096,), 2, 0)
+    for direction in (0, 1):
+        for s in range(w):
+            b = np.array([s], datagen.STORAGE[dtype])
+            got, bits, _ = run_engine("BitShift", dtype, a, b, attrs={"direction": direction})
+            want, _ = oracle.run("BitShift", a, b, dtype, direction=direction)
+            assert bits == 0 and (got == want).all(), (direction, s)
+        _, bits, _ = run_engine("BitShift", dtype, a, np.array([w], datagen.STORAGE[dtype]),
+                                attrs={"direction": direction})
+        assert bits == eb.DEVICE_SHIFT_RANGE
+
+
+def test_status_words_are_per_stream():
+    a = torch.arange(1, 1025, dtype=torch.int32, device="cuda")
+    z = torch.zeros(1024, dtype=torch.int32, device="cuda")
+    o = torch.ones(1024, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(a)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    d = eb.descriptor("Div", "int32")
+    p = eb.Plan(d, (1024,), (1024,))
+    eb.execute(p, a, z, out, stream=s1)
+    eb.execute(p, a, o, out, stream=s2)
+    assert eb.get_device_status(s2) == 0
+    assert eb.get_device_status(s1) == eb.DEVICE_DIV_BY_ZERO
+    assert eb.get_device_status(s1) == 0
+
+
+def test_in_place_execution():
+    a, b = inputs_for("Add", "float32", (1000, 256), (256,), seed=3)
+    want, _ = oracle.run("Add", a, b, "float32")
+    dA, dB = to_device(a), to_device(b)
+    p = eb.Plan(eb.descriptor("Add", "float32"), a.shape, b.shape)
+    eb.execute(p, dA, dB, dA)                             # out == A: allowed
+    torch.cuda.synchronize()
+    assert_bits_equal(dA.cpu().numpy().view(np.float32).reshape(want.shape), want, "float32")
+
+
+def test_misaligned_pointers_take_the_general_kernel():
+    a, b = inputs_for("Mul", "float32", (100001,), (100001,), seed=4)
+    want, _ = oracle.run("Mul", a, b, "float32")
+    dA = to_device(np.concatenate([np.zeros(1, np.float32), a]))
+    dB = to_device(np.concatenate([np.zeros(3, np.float32), b]))
+    out = torch.zeros((100001 + 1) * 4, dtype=torch.uint8, device="cuda")
+    p = eb.Plan(eb.descriptor("Mul", "float32"), a.shape, b.shape)
+    eb.execute(p, dA.data_ptr() + 4, dB.data_ptr() + 12, out.data_ptr() + 4)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.float32)[1:]
+    assert_bits_equal(got, want, "float32")
+
+
+def test_execute_host_round_trip():
+    a, b = inputs_for("Sub", "bfloat16", (64, 3000), (64, 1), seed=5)
+    want, _ = oracle.run("Sub", a, b, "bfloat16")
+    p = eb.Plan(eb.descriptor("Sub", "bfloat16"), a.shape, b.shape)
+    ha = torch.from_numpy(a.reshape(-1).view(np.int16).copy()).pin_memory()
+    hb = torch.from_numpy(b.reshape(-1).view(np.int16).copy()).pin_memory()
+    ho = torch.empty(p.numel, dtype=torch.int16).pin_memory()
+    da = torch.empty_like(ha, device="cuda")
+    db = torch.empty_like(hb, device="cuda")
+    do = torch.empty_like(ho, device="cuda")
+    s = torch.cuda.current_stream()
+    eb.ebin_execute_host(p.handle, ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), da.data_ptr(),
+                         db.data_ptr(), do.data_ptr(), s.cuda_stream)
+    s.synchronize()
+    assert_bits_equal(ho.numpy().view(np.uint16).reshape(want.shape), want, "bfloat16")
+
+
+def test_launch_count_and_binary_helper():
+    x = torch.randn(4, 8, 32, 32, device="cuda")
+    bias = torch.randn(8, 1, 1, device="cuda")
+    before = eb.ebin_launch_count()
+    y = eb.binary("Add", x, bias)
+    torch.cuda.synchronize()
+    assert eb.ebin_launch_count() == before + 1
+    want, _ = oracle.run("Add", x.cpu().numpy(), bias.cpu().numpy(), "float32")
+    assert_bits_equal(y.cpu().numpy(), want, "float32")
+    e = eb.binary("Add", torch.empty(0, 5, device="cuda"), torch.empty(5, device="cuda"))
+    assert e.shape == (0, 5) and eb.ebin_launch_count() == before + 1
+
+
+def test_plan_outlives_cache_eviction_on_device():
+    eb.ebin_plan_cache_clear()
+    d = eb.descriptor("Mul", "float32")
+    keep = eb.Plan(d, (64, 64), (64,))
+    for i in range(12):
+        eb.Plan(d, (i + 1, 64), (64,))                     # evicts `keep` from the cache
+    a, b = inputs_for("Mul", "float32", (64, 64), (64,), seed=6)
+    want, _ = oracle.run("Mul", a, b, "float32")
+    dA, dB = to_device(a), to_device(b)
+    out = torch.empty(64 * 64 * 4, dtype=torch.uint8, device="cuda")
+    eb.execute(keep, dA, dB, out)
+    torch.cuda.synchronize()
+    assert_bits_equal(out.cpu().numpy().view(np.float32).reshape(64, 64), want, "float32")

@@ -1,0 +1,126 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the oracle.
+
+Every (operator, type) of the manifest runs on shapes chosen to land in each
+loop family (with ragged tails and several CTAs of work), once with the
+family the planner picks and once forced through the general strided kernel.
+Results must be bit-identical (any NaN matches any NaN; signed zeros by
+bits), except floating Pow, which must be within 2 ulp of the oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from conftest import assert_bits_equal, ulp_distance
+from engine_util import FLOATS, MANIFEST, ONE_WAY, inputs_for, run_engine
+
+pytestmark = pytest.mark.gpu
+
+TWO_WAY_CASES = [
+    ("contiguous", (300007,), (300007,)),
+    ("right_scalar", (300007,), ()),
+    ("left_scalar", (1,), (300007,)),
+    ("repeated_block", (300, 256), (300, 1)),
+    ("repeated_block", (300, 256), (256,)),
+    ("repeated_block", (300, 1), (300, 256)),
+    ("repeated_block", (256,), (300, 256)),
+    ("inner_vector_outer", (4, 16, 3, 256), (16, 1, 1)),
+    ("inner_vector_outer", (6, 1, 5, 1), (1, 7, 1, 256)),
+    ("general_strided", (2, 3, 4, 5), (3, 1, 5)),
+    ("general_strided", (7, 1, 93), (1, 5, 93)),
+    ("general_strided", (33, 65), (33, 1)),
+    ("empty", (0, 5), (5,)),
+    ("contiguous", (), ()),
+]
+PRELU_CASES = [
+    ("inner_vector_outer", (4, 16, 3, 256), (16, 1, 1)),
+    ("repeated_block", (300, 256), (256,)),
+    ("repeated_block", (300, 256), (300, 1)),
+    ("right_scalar", (300007,), (1,)),
+    ("contiguous", (50001,), (50001,)),
+    ("general_strided", (2, 3, 4, 5), (3, 1, 5)),
+]
+BN_CASES = [
+    ("inner_vector_outer", (4, 16, 8, 32), (4, 16)),
+    ("repeated_block", (300, 64), (4, 64)),
+    ("general_strided", (3, 16, 9, 11), (4, 16)),
+    ("contiguous", (1, 64), (4, 64)),
+    ("empty", (0, 16, 4), (4, 16)),
+]
+CLIP_CASES = [
+    ("right_scalar", (300007,), (2,)),
+    ("right_scalar", (40, 77), (2,)),
+    ("contiguous", (1,), (2,)),
+]
+
+
+def cases_for(op):
+    if op == "PRelu":
+        return PRELU_CASES
+    if op == "BatchNormalization":
+        return BN_CASES
+    if op == "Clip":
+        return CLIP_CASES
+    return TWO_WAY_CASES
+
+
+def attr_variants(op):
+    if op == "Mod":
+        return [{"fmod": 0}, {"fmod": 1}]
+    if op == "BitShift":
+        return [{"direction": 0}, {"direction": 1}]
+    if op == "BatchNormalization":
+        return [{"epsilon": 1e-5}]
+    return [{}]
+
+
+def oracle_kwargs(attrs):
+    kw = {}
+    if "fmod" in attrs:
+        kw["fmod"] = attrs["fmod"]
+    if "direction" in attrs:
+        kw["direction"] = attrs["direction"]
+    if "epsilon" in attrs:
+        kw["eps"] = attrs["epsilon"]
+    return kw
+
+
+def compare(op, dtype, got, want, what):
+    if op == "Pow" and dtype in FLOATS:
+        d = ulp_distance(got, want, dtype)
+        assert d.max(initial=0) <= 2, "%s: Pow differs by %d ulp" % (what, d.max())
+    else:
+        otype = "bool" if got.dtype == np.uint8 and op in (
+            "Equal", "Less", "Greater", "LessOrEqual", "GreaterOrEqual", "And", "Or",
+            "Xor") else dtype
+        assert_bits_equal(got, want, otype, what)
+
+
+PAIRS = [(op, dt) for op, dts in MANIFEST.items() for dt in dts]
+
+
+@pytest.mark.parametrize("op,dtype", PAIRS, ids=["%s-%s" % p for p in PAIRS])
+def test_parity_all_families(op, dtype):
+    for attrs in attr_variants(op):
+        for i, (fam, sa, sb) in enumerate(cases_for(op)):
+            a, b = inputs_for(op, dtype, sa, sb, seed=i)
+            want, want_bits = oracle.run(op, a, b, dtype, **oracle_kwargs(attrs))
+            for forced in (None, "general_strided"):
+                what = "%s %s %s %s x %s forced=%s" % (op, dtype, attrs, sa, sb, forced)
+                got, bits, family = run_engine(op, dtype, a, b, family=forced, attrs=attrs)
+                if forced is None:
+                    assert family == fam, (what, family)
+                compare(op, dtype, got, want, what)
+                assert bits == want_bits, (what, bits, want_bits)
+
+
+@pytest.mark.parametrize("op,dtype", [("Add", "float32"), ("Greater", "float16"),
+                                      ("Mod", "int32"), ("Xor", "bool"), ("Sub", "uint8")])
+def test_inner_vector_kernel_on_other_geometries(op, dtype):
+    """The inner-vector kernel forced onto contiguous, scalar and block geometries."""
+    for i, (sa, sb) in enumerate([((300032,), (300032,)), ((300032,), ()), ((1,), (300032,)),
+                                  ((300, 256), (256,)), ((300, 256), (300, 1))]):
+        a, b = inputs_for(op, dtype, sa, sb, seed=40 + i)
+        want, _ = oracle.run(op, a, b, dtype)
+        got, _, fam = run_engine(op, dtype, a, b, family="inner_vector_outer")
+        assert fam == "inner_vector_outer"
+        compare(op, dtype, got, want, "%s %s %s %s" % (op, dtype, sa, sb))

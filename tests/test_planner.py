@@ -1,0 +1,263 @@
+"""Host logic of the C ABI, run on the CPU (no kernel is launched here).
+
+The library loads without a GPU; descriptor creation, planning, the plan
+cache, the alias check and empty executions never touch CUDA.
+"""
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+eb = pytest.importorskip("broadcast_elementwise_gb300")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ALL_DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool"]
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "ebin.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ebin_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(eb.lib, n), n
+
+
+def test_descriptor_rules_match_oracle():
+    for op, dt, opset, fmod, direction in itertools.product(
+            list(eb.OPS), ALL_DTYPES, (9, 10, 27, 28, 29), (0, 1, 2), (0, 1, 2)):
+        want = oracle.check_descriptor(op, opset, fmod, direction, dt, dt)
+        try:
+            d = eb.Descriptor(op, dt, opset=opset, fmod=fmod, direction=direction)
+            got = "ok"
+            assert d.out_dtype == oracle.output_type(op, dt)
+            d.close()
+        except eb.EbinError as e:
+            got = e.code
+        # the oracle only applies opset/fmod to Mod and direction to BitShift, as the engine does
+        assert got == want, (op, dt, opset, fmod, direction, got, want)
+
+
+def test_descriptor_rejects_mixed_types_and_bad_ops():
+    with pytest.raises(eb.EbinError) as e:
+        eb.ebin_descriptor_create(2, 14, None, eb.DTYPES["float32"], eb.DTYPES["float16"])
+    assert e.value.code == "unsupported_type"
+    with pytest.raises(eb.EbinError) as e:
+        eb.ebin_descriptor_create(99, 14, None, 1, 1)
+    assert e.value.code == "unsupported_op"
+
+
+def test_descriptor_ids_are_monotonic():
+    ids = [eb.Descriptor("Add", "float32").id for _ in range(5)]
+    assert ids == sorted(ids) and len(set(ids)) == 5
+
+
+def small_shapes():
+    shapes = [()]
+    for r in (1, 2, 3):
+        shapes += list(itertools.product((0, 1, 2, 3), repeat=r))
+    return shapes
+
+
+def test_output_shapes_brute_force():
+    d = eb.Descriptor("Add", "float32")
+    for sa in small_shapes():
+        for sb in small_shapes():
+            try:
+                want = oracle.output_shape("Add", sa, sb)
+            except ValueError:
+                want = None
+            try:
+                p = eb.Plan(d, sa, sb)
+                got = p.output_shape
+                p.close()
+            except eb.EbinError as e:
+                assert e.code == "incompatible_shapes"
+                got = None
+            assert got == want, (sa, sb)
+
+
+def flat_offsets(n, sa, sb, idx):
+    """Offsets of flat output indices through a coalesced geometry."""
+    oa = np.zeros(idx.size, np.int64)
+    ob = np.zeros(idx.size, np.int64)
+    rem = idx.copy()
+    for d in range(len(n) - 1, -1, -1):
+        i = rem % n[d]
+        rem //= n[d]
+        oa += i * sa[d]
+        ob += i * sb[d]
+    return oa, ob
+
+
+SHAPE_PAIRS = [((2, 3, 4, 5), (3, 1, 5)), ((8, 64, 16, 16), (64, 1, 1)),
+               ((64, 1, 32, 1), (1, 8, 1, 64)), ((4096,), ()), ((40, 96), (40, 1)),
+               ((40, 96), (96,)), ((1, 96), (40, 96)), ((7, 1, 9), (1, 5, 9)),
+               ((2, 1, 3, 1, 4), (1, 5, 1, 6, 1)), ((3, 4, 5), (3, 4, 5)), ((1, 1, 1), (1,)),
+               ((6, 1, 1, 7), (1, 1, 1)), ((2, 3, 1, 1, 5, 1, 7, 2), (3, 4, 1, 5, 6, 1, 2))]
+
+
+@pytest.mark.parametrize("sa,sb", SHAPE_PAIRS)
+def test_coalesced_geometry_preserves_the_element_mapping(sa, sb):
+    d = eb.Descriptor("Add", "float32")
+    p = eb.Plan(d, sa, sb)
+    n, gsa, gsb = p.geometry()
+    total = p.numel
+    idx = np.arange(total, dtype=np.int64)
+    want_a, want_b = oracle.offsets(sa, sb, idx)
+    got_a, got_b = flat_offsets(n, gsa, gsb, idx)
+    assert int(np.prod(n)) == total
+    assert (got_a == want_a).all() and (got_b == want_b).all()
+    # coalescing is maximal: no adjacent pair could still merge
+    for i in range(len(n) - 1):
+        assert not (gsa[i] == gsa[i + 1] * n[i + 1] and gsb[i] == gsb[i + 1] * n[i + 1])
+    assert all(x > 1 for x in n) or total == 1
+
+
+def family(op, dt, sa, sb, **kw):
+    d = eb.Descriptor(op, dt, **kw)
+    p = eb.Plan(d, sa, sb)
+    return p.family, p.geometry()
+
+
+def test_families_of_the_benchmark_workloads():
+    assert family("Add", "float32", (2, 3, 4, 5), (3, 1, 5))[0] == "general_strided"
+    assert family("Mul", "float32", (1 << 28,), (1 << 28,))[0] == "contiguous"
+    f, (n, sa, sb) = family("Add", "bfloat16", (8, 64, 256, 256), (64, 1, 1))
+    assert f == "inner_vector_outer" and n == [8, 64, 65536] and sb == [0, 1, 0]
+    assert family("PRelu", "bfloat16", (8, 64, 256, 256), (64, 1, 1))[0] == "inner_vector_outer"
+    assert family("BatchNormalization", "bfloat16", (8, 64, 256, 256), (4, 64))[0] == \
+        "inner_vector_outer"
+    assert family("Mod", "float32", (4096, 4096), (1,), fmod=1)[0] == "right_scalar"
+    assert family("Mod", "float32", (4096, 4096), (), fmod=0)[0] == "right_scalar"
+    assert family("Mod", "float32", (4096, 4096), (4096, 1), fmod=0)[0] == "repeated_block"
+    assert family("Mod", "int32", (4096, 4096), (4096, 1))[0] == "repeated_block"
+    f, (n, sa, sb) = family("Greater", "float16", (64, 1, 512, 1), (1, 32, 1, 1024))
+    assert f == "inner_vector_outer" and n == [64, 32, 512, 1024]
+    assert family("BitShift", "uint32", (1 << 26,), (1,), direction=1)[0] == "right_scalar"
+    assert family("Add", "float32", (1,), (1 << 20,))[0] == "left_scalar"
+    assert family("Add", "float32", (0, 5), (5,))[0] == "empty"
+    assert family("Clip", "float32", (30, 40), (2,))[0] == "right_scalar"
+    assert family("BatchNormalization", "float32", (300, 64), (4, 64))[0] == "repeated_block"
+
+
+def test_one_way_broadcasts():
+    for op, sb in (("PRelu", (3, 4)), ("BatchNormalization", (4, 5)), ("Clip", (3,))):
+        d = eb.Descriptor(op, "float32")
+        with pytest.raises(eb.EbinError) as e:
+            eb.Plan(d, (3, 1), sb)
+        assert e.value.code == "incompatible_shapes"
+    d = eb.Descriptor("BatchNormalization", "float32")
+    with pytest.raises(eb.EbinError):
+        eb.Plan(d, (8,), (4, 8))                     # rank 1 has no channel axis
+    assert eb.Plan(d, (2, 8, 3), (4, 8)).output_shape == (2, 8, 3)
+
+
+def test_rank_and_dims_are_checked():
+    d = eb.Descriptor("Add", "float32")
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (1,) * 9, (1,))
+    assert e.value.code == "rank_too_large"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (3, -1), (1,))
+    assert e.value.code == "invalid_arg"
+    assert eb.Plan(d, (1,) * 8, (2,) * 8).output_shape == (2,) * 8
+
+
+def test_forced_families():
+    d = eb.Descriptor("Add", "float32")
+    for fam in ("general_strided", "inner_vector_outer"):
+        assert eb.Plan(d, (40, 96), (40, 1), family=fam).family == fam
+    assert eb.Plan(d, (4096,), (), family="general_strided").family == "general_strided"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (2, 3, 4, 5), (3, 1, 5), family="contiguous")
+    assert e.value.code == "family"
+    with pytest.raises(eb.EbinError):
+        eb.Plan(d, (40, 90), (40, 1), family="inner_vector_outer")   # 90 % 4 != 0
+    assert eb.Plan(d, (0, 4), (4,), family="contiguous").family == "empty"
+
+
+def test_plan_cache_is_an_8_entry_lru():
+    eb.ebin_plan_cache_clear()
+    d = eb.Descriptor("Sub", "int32")
+    plans = [eb.Plan(d, (i + 1, 3), (3,)) for i in range(8)]
+    h, m, s = eb.ebin_plan_cache_stats()
+    assert (h, m, s) == (0, 8, 8)
+    again = eb.Plan(d, (1, 3), (3,))                  # hit; becomes most recent
+    assert again.handle == plans[0].handle
+    assert eb.ebin_plan_cache_stats() == (1, 8, 8)
+    eb.Plan(d, (100, 3), (3,))                        # miss; evicts the LRU entry (2, 3)
+    assert eb.ebin_plan_cache_stats() == (1, 9, 8)
+    fresh = eb.Plan(d, (2, 3), (3,))                  # was evicted: a miss, a new plan
+    assert eb.ebin_plan_cache_stats()[1] == 10
+    assert fresh.handle != plans[1].handle
+    # the evicted plan is still usable by its holder
+    assert plans[1].output_shape == (2, 3)
+    eb.Plan(d, (1, 3), (3,))
+    assert eb.ebin_plan_cache_stats()[0] == 2
+
+
+def test_destroyed_descriptor_never_hits():
+    eb.ebin_plan_cache_clear()
+    d = eb.Descriptor("Mul", "float32")
+    p = eb.Plan(d, (5, 7), (7,))
+    old_id = d.id
+    d.close()
+    assert p.output_shape == (5, 7)                   # held plan outlives its descriptor
+    d2 = eb.Descriptor("Mul", "float32")
+    assert d2.id != old_id
+    eb.Plan(d2, (5, 7), (7,))
+    h, m, _ = eb.ebin_plan_cache_stats()
+    assert h == 0 and m == 2
+
+
+def test_empty_execute_reads_nothing():
+    d = eb.Descriptor("Div", "int32")
+    p = eb.Plan(d, (0, 5), (5,))
+    before = eb.ebin_launch_count()
+    eb.ebin_execute(p.handle, None, None, None, None)
+    assert eb.ebin_launch_count() == before
+
+
+def test_alias_rule():
+    d = eb.Descriptor("Add", "float32")
+    p = eb.Plan(d, (4, 8), (8,))
+    base = 1 << 40                                     # never dereferenced: the check fails first
+    with pytest.raises(eb.EbinError) as e:            # A overlaps out, shifted by one element
+        eb.ebin_execute(p.handle, base, base + 4096, base + 4, None)
+    assert e.value.code == "alias"
+    with pytest.raises(eb.EbinError) as e:            # broadcast B inside out
+        eb.ebin_execute(p.handle, base + 8192, base + 16, base, None)
+    assert e.value.code == "alias"
+    dc = eb.Descriptor("Greater", "float32")
+    pc = eb.Plan(dc, (4, 8), (4, 8))
+    with pytest.raises(eb.EbinError) as e:            # BOOL out over a float input
+        eb.ebin_execute(pc.handle, base, base + 4096, base, None)
+    assert e.value.code == "alias"
+    db = eb.Descriptor("BatchNormalization", "float32")
+    pb = eb.Plan(db, (4, 8), (4, 8))
+    with pytest.raises(eb.EbinError) as e:            # parameter block never aliases out
+        eb.ebin_execute(pb.handle, base + 4096, base, base, None)
+    assert e.value.code == "alias"
+
+
+def test_null_buffers_rejected():
+    d = eb.Descriptor("Add", "float32")
+    p = eb.Plan(d, (4,), (4,))
+    with pytest.raises(eb.EbinError) as e:
+        eb.ebin_execute(p.handle, None, 16, 32, None)
+    assert e.value.code == "invalid_arg"
+
+
+def test_dtype_sizes_and_strings():
+    for name, code in eb.DTYPES.items():
+        assert eb.ebin_dtype_size(code) == eb.ITEMSIZE[name]
+    assert eb.ebin_status_string(7) == "input aliases the output"
