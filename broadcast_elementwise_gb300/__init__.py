@@ -66,7 +66,7 @@ class ebin_attrs(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libebin.so is not built (%s); run __graft_entry__.build() or "
-                          "python -m broadcast_elementwise_gb300._build" % LIB_PATH)
+                          "python broadcast_elementwise_gb300/_build.py" % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     p_i64 = ctypes.POINTER(ctypes.c_int64)
