@@ -51,6 +51,10 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-families", action="store_true", help="skip the per-workload table")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--only", default=None,
+                    help="time one workload case alone (for profiling), e.g. mul_f32_contiguous")
+    ap.add_argument("--scale-log2", type=int, default=0,
+                    help="with --only: shrink the 1-D workloads by 2^S")
     return ap.parse_args()
 
 
@@ -445,8 +449,46 @@ def run_reference(args, dist: Dist):
     print(json.dumps(out), flush=True)
 
 
+def run_one_case(args):
+    """One workload alone: warmup, then --steps launches timed one by one."""
+    import torch
+
+    import broadcast_elementwise_gb300 as eb
+    from datagen import workloads
+
+    c = workloads.by_name(args.only, scale_log2=args.scale_log2)
+    a, b = c.make_a(), c.make_b()
+    desc = eb.descriptor(c.op, c.dtype, **c.attrs)
+    plan = eb.Plan(desc, c.shape_a, c.shape_b)
+    da, db = upload(a), upload(b)
+    osz = eb.ITEMSIZE[desc.out_dtype]
+    out = torch.empty(plan.numel * osz, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        eb.execute(plan, da, db, out, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s0, s1 in evs:
+        s0.record(stream)
+        eb.execute(plan, da, db, out, stream=stream)
+        s1.record(stream)
+    torch.cuda.synchronize()
+    if eb.get_device_status(stream) != 0:
+        raise RuntimeError("device status set")
+    ts = [x.elapsed_time(y) * 1e-3 for x, y in evs]
+    nbytes = a.size * eb.ITEMSIZE[c.dtype] + b.size * eb.ITEMSIZE[c.dtype] + plan.numel * osz
+    med = statistics.median(ts)
+    print(json.dumps({"case": c.name, "family": plan.family, "numel": plan.numel,
+                      "bytes": nbytes, "us_median": round(med * 1e6, 2),
+                      "gbs": round(nbytes / med / 1e9, 1)}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.only:
+        run_one_case(args)
+        return
     dist = Dist()
     try:
         if args.impl == "reference":
