@@ -90,6 +90,7 @@ def _load():
         "ebin_execute": (i32, [vp, vp, vp, vp, vp]),
         "ebin_execute_host": (i32, [vp, vp, vp, vp, vp, vp, vp, vp]),
         "ebin_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_uint32)]),
+        "ebin_execute_noalloc": (i32, [vp, vp, vp, vp, vp, i32, ctypes.POINTER(ctypes.c_uint32)]),
         "ebin_launch_count": (ctypes.c_uint64, []),
         "ebin_dtype_size": (ctypes.c_size_t, [i32]),
         "ebin_status_string": (ctypes.c_char_p, [i32]),
@@ -225,6 +226,18 @@ def ebin_execute(plan, A, B, out, stream) -> None:
 def ebin_execute_host(plan, host_a, host_b, host_out, dev_a, dev_b, dev_out, stream) -> None:
     _check(lib.ebin_execute_host(plan, host_a, host_b, host_out, dev_a, dev_b, dev_out, stream),
            "ebin_execute_host")
+
+
+def ebin_execute_noalloc(plan, A, B, out, stream, status_slot, want_status=True):
+    """Marshal ebin_execute_noalloc; returns the status bits (0 when not requested)."""
+    bits = ctypes.c_uint32(0)
+    _check(lib.ebin_execute_noalloc(plan, A, B, out, stream, int(status_slot),
+                                    ctypes.byref(bits) if want_status else None),
+           "ebin_execute_noalloc")
+    return bits.value
+
+
+NOALLOC_STATUS_SLOTS = 64
 
 
 def ebin_get_device_status(stream) -> int:

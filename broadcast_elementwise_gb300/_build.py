@@ -74,6 +74,10 @@ def _jobs():
     host_obj = os.path.join(OBJDIR, "ebin_host.o")
     jobs.append((host_obj, [host_src] + heads,
                  [nvcc, *ARCH, *NVCC_FLAGS, "-c", host_src, "-o", host_obj]))
+    noalloc_src = os.path.join(CSRC, "ebin_noalloc.cu")
+    noalloc_obj = os.path.join(OBJDIR, "ebin_noalloc.o")
+    jobs.append((noalloc_obj, [noalloc_src] + heads,
+                 [nvcc, *ARCH, *NVCC_FLAGS, "-c", noalloc_src, "-o", noalloc_obj]))
     for g in GROUPS:
         src = os.path.join(CSRC, "k_%s.cu" % g)
         for dt in range(N_DT):

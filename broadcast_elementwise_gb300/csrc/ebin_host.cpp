@@ -26,6 +26,7 @@
 
 #include "ebin.h"
 #include "ebin_launch.h"
+#include "ebin_plan.h"
 
 using ebin::Fam;
 using ebin::Geom;
@@ -108,25 +109,6 @@ struct ebin_descriptor_s {
     ebin_dtype out_dt;
 };
 
-struct ebin_plan_s {
-    std::atomic<int> refs{1};
-    // cache key
-    uint64_t desc_id = 0;
-    ebin_dtype dt = EBIN_FLOAT32;
-    int rank_a = 0, rank_b = 0;
-    int64_t shape_a[kMaxRank] = {};
-    int64_t shape_b[kMaxRank] = {};
-    // what execution needs (copied: a plan may outlive its descriptor)
-    int op = 0;
-    ebin_attrs attrs{};
-    ebin_dtype out_dt = EBIN_FLOAT32;
-    int rank_out = 0;
-    int64_t shape_out[kMaxRank] = {};
-    int64_t numel = 0, numel_a = 0, numel_b = 0;
-    Geom g{};
-    int family = ebin::FAM_EMPTY;
-    int64_t plane = 0;
-};
 
 // ------------------------------------------------------------------ descriptor
 extern "C" ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_attrs *attrs,
@@ -645,6 +627,8 @@ extern "C" ebin_status ebin_get_device_status(void *stream, uint32_t *bits) {
 }
 
 extern "C" uint64_t ebin_launch_count(void) { return g_launches.load(); }
+
+void ebin::count_launch() { g_launches.fetch_add(1); }
 
 extern "C" size_t ebin_dtype_size(ebin_dtype t) {
     switch (t) {

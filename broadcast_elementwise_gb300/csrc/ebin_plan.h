@@ -1,0 +1,34 @@
+// The plan object behind ebin_plan_t, shared by the translation units that
+// execute plans.  Not part of the public C ABI.
+#pragma once
+
+#include <atomic>
+#include <cstdint>
+
+#include "ebin.h"
+#include "ebin_launch.h"
+
+struct ebin_plan_s {
+    std::atomic<int> refs{1};
+    // cache key
+    uint64_t desc_id = 0;
+    ebin_dtype dt = EBIN_FLOAT32;
+    int rank_a = 0, rank_b = 0;
+    int64_t shape_a[ebin::kMaxRank] = {};
+    int64_t shape_b[ebin::kMaxRank] = {};
+    // what execution needs (copied: a plan may outlive its descriptor)
+    int op = 0;
+    ebin_attrs attrs{};
+    ebin_dtype out_dt = EBIN_FLOAT32;
+    int rank_out = 0;
+    int64_t shape_out[ebin::kMaxRank] = {};
+    int64_t numel = 0, numel_a = 0, numel_b = 0;
+    ebin::Geom g{};
+    int family = ebin::FAM_EMPTY;
+    int64_t plane = 0;
+};
+
+namespace ebin {
+// Add one to the process-wide kernel launch count (ebin_launch_count).
+void count_launch();
+}  // namespace ebin

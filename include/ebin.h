@@ -270,6 +270,36 @@ ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, const void *
  */
 ebin_status ebin_get_device_status(void *stream, uint32_t *bits);
 
+/*
+ * Execute without any allocation by the library.  No counterpart in the pages:
+ * this entry point exists for callers that cannot let a library allocate
+ * device memory -- an application whose device memory is wholly owned by its
+ * own arena allocator, a plugin whose host framework forbids allocation while
+ * work is being enqueued, or a latency-critical loop that cannot absorb the
+ * implicit synchronisation of cudaMalloc.  ebin_execute would cudaMalloc a
+ * per-stream status word the first time a validating operator (integer Div,
+ * Mod, Pow; BitShift) runs on a stream; this call runs the same kernels with
+ * the status word taken from a fixed array compiled into the library instead
+ * (EBIN_NOALLOC_STATUS_SLOTS words = 256 bytes, held on every device that
+ * loads the library until the process exits).
+ *
+ *   plan, A, B, out, stream   as for ebin_execute (same checks and errors)
+ *   status_slot               which word of the array this call uses,
+ *                             0 <= slot < EBIN_NOALLOC_STATUS_SLOTS; anything
+ *                             else returns EBIN_ERR_INVALID_ARG
+ *   status_bits               NULL, or a host word that receives the
+ *                             EBIN_DEVICE_* bits of this call; with a non-NULL
+ *                             pointer the call waits for `stream` to finish
+ * The slot is zeroed (stream-ordered) at the start of every call.  All calls
+ * share the array: calls that use the same slot and overlap on the GPU race on
+ * it.  The first call on a device looks up the array's device address once
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define EBIN_NOALLOC_STATUS_SLOTS 64
+ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, const void *B, void *out,
+                                 void *stream, int status_slot, uint32_t *status_bits);
+
 /* Kernels this library has launched in this process (for launch accounting). */
 uint64_t ebin_launch_count(void);
 
