@@ -4,19 +4,28 @@
 // Families ("Binary Kernel Design", section "Operators and traversal",
 // loop-family table), each a kernel template instantiated per operator and
 // element type:
-//   k_contiguous   A, B and out advance together             (Contiguous)
-//   k_scalar       one operand is a single value             (Left / right scalar)
-//   k_rows<2-D>    rank 2: one value per row, or one row block reused for every
-//                  row                                        (Repeated contiguous block)
-//   k_rows<N-D>    vectorised inner rows, incremental outer offsets
-//                                                             (Inner-vector / outer broadcast)
-//   k_rows<G=1>    any coalesced strides, element at a time  (General strided)
+//   k_contiguous        A, B and out advance together          (Contiguous)
+//   k_scalar            one operand is a single value          (Left / right scalar)
+//   k_rows<NOPREFIX>    rank-2 plans: one value per row, or one row block
+//                       reused by every row                    (Repeated contiguous block)
+//   k_rows<G>           vectorised inner rows, outer offsets advanced by
+//                       constant steps                          (Inner-vector / outer broadcast)
+//   k_rows<G=1, any>    any coalesced strides, element by element (General strided)
 //
-// Memory access: the dense streams move in 16-byte vectors (ld.global.nc with
-// L1::no_allocate for inputs that are read once); a warp's 32 lanes touch 512
-// consecutive bytes per access.  Offsets advance incrementally ("division and
-// modulo are not performed for every output element"): each lane decomposes
-// its first index once and afterwards only adds and carries.
+// GB300 design points (all measured on the part):
+//  * One tile per CTA ("one-shot" grid): a grid-stride persistent loop reached
+//    ~6.5 TB/s on the contiguous fp32 stream, one tile per CTA ~7.1 TB/s.
+//  * Dense streams move as 16-byte vectors: ld.global.nc.L1::no_allocate for
+//    inputs read once, st.global.cs (evict-first) for outputs.  A warp touches
+//    512 consecutive bytes per access (16 sectors per request).
+//  * Row traversal: a tile is (outer prefix index, a run of rows along the
+//    dimension next to the inner one, a chunk of columns).  A thread owns one
+//    column group and walks its rows with constant offset steps -- "offsets
+//    advance incrementally; division and modulo are not performed for every
+//    output element".  The tile index is split with precomputed
+//    Granlund-Montgomery divisors (multiply-high and shifts), once per thread.
+//    An operand whose run stride is 0 (a row block reused by every row) stays
+//    in registers for the whole run.
 //
 // Validation ("Compute, scheduling, and safety"): operators that can meet an
 // invalid element (integer division by zero, shift counts) write 0 for it and
@@ -25,6 +34,7 @@
 #pragma once
 
 #include <cstring>
+#include <type_traits>
 
 #include "ebin_ops.cuh"
 
@@ -50,15 +60,70 @@ __device__ __forceinline__ Pack<T, G> ld_stream(const T *p) {
     return out;
 }
 
+// Streaming (evict-first) store of a pack of 1..16 bytes.
 template <class T, int G>
-__device__ __forceinline__ void st_pack(T *p, const Pack<T, G> &v) {
-    *reinterpret_cast<Pack<T, G> *>(p) = v;
+__device__ __forceinline__ void st_stream(T *p, const Pack<T, G> &v) {
+    constexpr int kBytes = (int)sizeof(T) * G;
+    if constexpr (kBytes == 16) {
+        uint32_t w[4];
+        memcpy(w, &v, 16);
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3])
+                     : "memory");
+    } else if constexpr (kBytes == 8) {
+        uint32_t w[2];
+        memcpy(w, &v, 8);
+        asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1])
+                     : "memory");
+    } else if constexpr (kBytes == 4) {
+        uint32_t w;
+        memcpy(&w, &v, 4);
+        asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(w) : "memory");
+    } else if constexpr (kBytes == 2) {
+        uint16_t w;
+        memcpy(&w, &v, 2);
+        asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(w) : "memory");
+    } else {
+        static_assert(kBytes == 1, "pack size");
+        uint32_t w = 0;
+        memcpy(&w, &v, 1);
+        asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(w) : "memory");
+    }
 }
 
 template <class Op>
 __device__ __forceinline__ void flush_err(uint32_t *status, uint32_t err) {
     if constexpr (Op::kValidates) {
         if (err) atomicOr(status, err);
+    }
+}
+
+// Operators with a whole-group form (Op::kPack) use it for groups of a multiple of 4.
+template <class Op, class = void> struct HasPack : std::false_type {};
+template <class Op>
+struct HasPack<Op, std::void_t<decltype(Op::kPack)>> : std::bool_constant<Op::kPack> {};
+
+// o[k] = op(a[k], b[k]) for one group of G elements.  SA / SB: the operand is
+// one value for the whole group (a[0] / b[0]), not G values.
+template <class Op, int G, bool SA = false, bool SB = false>
+__device__ __forceinline__ void compute_group(const typename Op::In *a, const typename Op::BV *b,
+                                              typename Op::Out *o, const OpArgs &args,
+                                              uint32_t &err) {
+    if constexpr (HasPack<Op>::value && G % 4 == 0) {
+        if constexpr (SA || SB) {
+            typename Op::In ta[G], tb[G];
+#pragma unroll
+            for (int k = 0; k < G; ++k) {
+                ta[k] = a[SA ? 0 : k];
+                tb[k] = b[SB ? 0 : k];
+            }
+            Op::template apply_pack<G>(ta, tb, o);
+        } else {
+            Op::template apply_pack<G>(a, b, o);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < G; ++k) o[k] = Op::apply(a[SA ? 0 : k], b[SB ? 0 : k], args, err);
     }
 }
 
@@ -72,22 +137,43 @@ struct KArgs {
     uint32_t *status;
 };
 
-// Row traversal (k_rows): the coalesced dims split into an inner row of
-// `inner` elements (= cols groups of G) and up to kMaxRank-1 outer digits,
-// stored right-aligned in on/osa/osb (digit kMaxRank-2 is next to the row).
-// Unused digits have a huge extent so that no carry ever reaches them.
-struct RowArgs {
-    int64_t cols;          // groups per row
-    int64_t ngroups;       // rows * cols
-    int64_t per_warp;      // groups handled by each warp (multiple of 32)
-    int64_t ia, ib;        // inner element strides of A and B (general kernel)
-    int32_t outer;         // number of live outer digits
-    int64_t on[kMaxRank - 1];
-    int64_t osa[kMaxRank - 1];
-    int64_t osb[kMaxRank - 1];
+// ---------------------------------------------------------------- invariant division
+// n / d for 0 <= n < 2^32 and 1 <= d < 2^32 with one multiply-high, a
+// subtract, an add and two shifts: the unsigned method of Granlund and
+// Montgomery, "Division by invariant integers using multiplication" (PLDI
+// 1994), section 4: l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+// q = (t + ((n - t) >> min(l,1))) >> max(l-1,0) with t = mulhi(m, n).
+struct FastDiv {
+    uint32_t m;
+    uint32_t s1;
+    uint32_t s2;
 };
 
+inline FastDiv make_fastdiv(uint64_t d) {
+    FastDiv f{1, 0, 0};
+    if (d == 0 || d >= (1ull << 32)) return f;  // unused: the wide path divides directly
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    f.m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+    f.s1 = l < 1 ? l : 1;
+    f.s2 = l > 0 ? l - 1 : 0;
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv &f) {
+    const uint32_t t = __umulhi(f.m, n);
+    return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
+// q = n / d; 32-bit fast path unless `wide` (some index may reach 2^32).
+__device__ __forceinline__ int64_t udiv(int64_t n, int64_t d, const FastDiv &f, bool wide) {
+    if (!wide) return (int64_t)fastdiv((uint32_t)n, f);
+    return n / d;
+}
+
 // ---------------------------------------------------------------- Contiguous
+// One tile of kThreads*U groups of G elements per CTA; a ragged tail of
+// numel % G elements is finished element by element.
 template <class Op, int U>
 __global__ void __launch_bounds__(kThreads) k_contiguous(KArgs p) {
     using In = typename Op::In;
@@ -103,19 +189,18 @@ __global__ void __launch_bounds__(kThreads) k_contiguous(KArgs p) {
     for (int64_t base = (int64_t)blockIdx.x * (kThreads * U) + threadIdx.x; base < ng;
          base += step) {
         Pack<In, G> a[U];
-        BV b[U][G];
+        Pack<In, G> bp[U];   // plain B: one 16-byte pack per group
+        BV bv[Op::kPlainB ? 1 : U][G];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t g = base + (int64_t)u * kThreads;
             if (g < ng) {
                 a[u] = ld_stream<In, G>(A + g * G);
                 if constexpr (Op::kPlainB) {
-                    const Pack<In, G> t = ld_stream<In, G>(B + g * G);
-#pragma unroll
-                    for (int k = 0; k < G; ++k) b[u][k] = t.v[k];
+                    bp[u] = ld_stream<In, G>(B + g * G);
                 } else {
 #pragma unroll
-                    for (int k = 0; k < G; ++k) b[u][k] = Op::loadB(B, g * G + k, p.args);
+                    for (int k = 0; k < G; ++k) bv[u][k] = Op::loadB(B, g * G + k, p.args);
                 }
             }
         }
@@ -124,13 +209,12 @@ __global__ void __launch_bounds__(kThreads) k_contiguous(KArgs p) {
             const int64_t g = base + (int64_t)u * kThreads;
             if (g < ng) {
                 Pack<Out, G> o;
-#pragma unroll
-                for (int k = 0; k < G; ++k) o.v[k] = Op::apply(a[u].v[k], b[u][k], p.args, err);
-                st_pack<Out, G>(O + g * G, o);
+                if constexpr (Op::kPlainB) compute_group<Op, G>(a[u].v, bp[u].v, o.v, p.args, err);
+                else compute_group<Op, G>(a[u].v, bv[u], o.v, p.args, err);
+                st_stream<Out, G>(O + g * G, o);
             }
         }
     }
-    // ragged tail (numel % G elements)
     for (int64_t e = ng * G + (int64_t)blockIdx.x * kThreads + threadIdx.x; e < p.numel;
          e += (int64_t)gridDim.x * kThreads)
         O[e] = Op::apply(A[e], Op::loadB(B, e, p.args), p.args, err);
@@ -171,12 +255,9 @@ __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
             const int64_t g = base + (int64_t)u * kThreads;
             if (g < ng) {
                 Pack<Out, G> o;
-#pragma unroll
-                for (int k = 0; k < G; ++k) {
-                    if constexpr (SCALAR_A) o.v[k] = Op::apply(sa, d[u].v[k], p.args, err);
-                    else o.v[k] = Op::apply(d[u].v[k], sb, p.args, err);
-                }
-                st_pack<Out, G>(O + g * G, o);
+                if constexpr (SCALAR_A) compute_group<Op, G, true, false>(&sa, d[u].v, o.v, p.args, err);
+                else compute_group<Op, G, false, true>(d[u].v, &sb, o.v, p.args, err);
+                st_stream<Out, G>(O + g * G, o);
             }
         }
     }
@@ -190,141 +271,142 @@ __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
 
 // ---------------------------------------------------------------- Row traversal
 //
-// Repeated block, inner-vector/outer-broadcast and general strided.  The
-// output is split into rows of `cols` groups of G elements; every warp owns a
-// contiguous range of `per_warp` groups.  Lane l handles groups
-// begin + l, begin + l + 32, ...: each access of the warp covers 32
-// consecutive groups.  A lane decomposes its first group once; every further
-// step adds 32 to its column and carries whole rows into the outer digits,
-// updating the A and B row offsets by the digits' strides.
-//
+// The coalesced dims split into: prefix digits (dims 0..rank-3), the run dim
+// (rank-2, extent M, strides smA/smB) and the inner row (rank-1, L elements =
+// cols groups of G).  A CTA of tpr*rs threads handles one tile:
+// (prefix index, run index, column chunk); rs rows advance in parallel, each
+// thread walks kr of its rows rs apart.
+struct RowArgs {
+    int64_t L;            // inner elements per row
+    int64_t cols;         // groups per row = L / G
+    int64_t M;            // extent of the run dim (1 for rank-1 plans)
+    int64_t smA, smB;     // A and B strides along the run dim
+    int64_t ia, ib;       // inner element strides (general kernel)
+    int32_t tpr;          // threads per row
+    int32_t rs;           // rows in parallel (threads = tpr * rs)
+    int32_t kr;           // rows per thread per tile
+    int32_t wide;         // an index may reach 2^32: divide in 64 bits
+    int64_t cc;           // column chunks per row = ceil(cols / tpr)
+    int64_t runs;         // run tiles per prefix index = ceil(M / (rs * kr))
+    int32_t nprefix;      // prefix digits (rank - 2, at least 0)
+    int64_t pn[kMaxRank];
+    int64_t psa[kMaxRank];
+    int64_t psb[kMaxRank];
+    FastDiv f_cc, f_runs, f_tpr;
+    FastDiv f_pn[kMaxRank];
+};
+
 // IA / IB: 1 = the operand advances along the row (vector loads), 0 = it is
-// constant along the row (one value per row, read once per step), 2 = any
-// inner stride (G must be 1).  TWO_D: exactly one outer digit (rank-2 plans),
-// so the carry is a single add.
-template <class Op, int G, int IA, int IB, bool TWO_D, int U>
+// constant along the row (one value per row), 2 = any inner stride (G == 1).
+// NOPREFIX: rank <= 2, no prefix digits to decode.
+template <class Op, int G, int IA, int IB, bool NOPREFIX>
 __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
-    constexpr int D = kMaxRank - 1;
     static_assert(G == 1 || (IA != 2 && IB != 2), "runtime inner strides need G == 1");
+    constexpr bool kVecA = IA == 1 && G > 1;
+    constexpr bool kVecB = IB == 1 && G > 1;
     const In *A = static_cast<const In *>(p.A);
     const In *B = static_cast<const In *>(p.B);
     Out *O = static_cast<Out *>(p.out);
 
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t begin = warp * r.per_warp;
-    const int64_t end = min(begin + r.per_warp, r.ngroups);
-    if (begin >= end) return;
+    const int t = threadIdx.x;
+    if (t >= r.tpr * r.rs) return;
+    const bool wide = r.wide != 0;
+    // tile -> (prefix index, run index, column chunk), the column chunk fastest
+    const int64_t tile = blockIdx.x;
+    const int64_t q1 = udiv(tile, r.cc, r.f_cc, wide);
+    const int64_t ci = tile - q1 * r.cc;
+    const int64_t pi = udiv(q1, r.runs, r.f_runs, wide);
+    const int64_t ri = q1 - pi * r.runs;
+    const int rsub = r.rs == 1 ? 0 : (int)fastdiv((uint32_t)t, r.f_tpr);
+    const int64_t c = ci * r.tpr + (t - rsub * r.tpr);
+    if (c >= r.cols) return;
+    const int64_t m0 = ri * (int64_t)(r.rs * r.kr) + rsub;
+    if (m0 >= r.M) return;
 
-    // first group of this lane -> (row digits, column)
-    int64_t g = begin + lane;
-    int64_t row = g / r.cols;
-    int64_t col = g - row * r.cols;
-    int64_t idx[D];
-    int64_t rowA = 0, rowB = 0;
-    if constexpr (TWO_D) {
-        idx[D - 1] = row;
-        rowA = row * r.osa[D - 1];
-        rowB = row * r.osb[D - 1];
-    } else {
+    int64_t baseA = 0, baseB = 0;
+    if constexpr (!NOPREFIX) {
+        int64_t rem = pi;
 #pragma unroll
-        for (int d = D - 1; d >= 0; --d) {
-            if (d >= D - r.outer) {
-                const int64_t q = row / r.on[d];
-                idx[d] = row - q * r.on[d];
-                row = q;
-                rowA += idx[d] * r.osa[d];
-                rowB += idx[d] * r.osb[d];
-            } else {
-                idx[d] = 0;
+        for (int d = kMaxRank - 1; d >= 0; --d) {
+            if (d < r.nprefix) {
+                const int64_t q = udiv(rem, r.pn[d], r.f_pn[d], wide);
+                const int64_t digit = rem - q * r.pn[d];
+                rem = q;
+                baseA += digit * r.psa[d];
+                baseB += digit * r.psb[d];
             }
         }
     }
+    int64_t offA = baseA + m0 * r.smA + (IA == 1 ? c * G : IA == 2 ? c * r.ia : 0);
+    int64_t offB = baseB + m0 * r.smB + (IB == 1 ? c * G : IB == 2 ? c * r.ib : 0);
+    int64_t offO = (pi * r.M + m0) * r.L + c * G;
+    const int64_t stepA = (int64_t)r.rs * r.smA;
+    const int64_t stepB = (int64_t)r.rs * r.smB;
+    const int64_t stepO = (int64_t)r.rs * r.L;
+    const int64_t left = (r.M - m0 + r.rs - 1) / r.rs;
+    const int n = (int)(left < r.kr ? left : r.kr);
 
+    // UR rows per iteration: all their loads are issued before any result is
+    // stored.  An operand whose run stride is 0 is read once and kept.  Dense
+    // operands stay 16-byte packs; an operand constant along the row is one value.
+    constexpr bool kBElem = kVecB && !Op::kPlainB;   // per-element parameter blocks
+    constexpr int UR = kBElem ? 1 : ((kVecA && kVecB) || !Op::kPlainB) ? 2 : 4;
+    using APack = std::conditional_t<kVecA, Pack<In, G>, Pack<In, 1>>;
+    using BPack = std::conditional_t<kVecB && Op::kPlainB, Pack<In, G>, Pack<BV, kBElem ? G : 1>>;
+    const bool reloadA = stepA != 0, reloadB = stepB != 0;
+    auto load_a = [&](int64_t off) {
+        APack r;
+        if constexpr (kVecA) r = ld_stream<In, G>(A + off);
+        else r.v[0] = A[off];
+        return r;
+    };
+    auto load_b = [&](int64_t off) {
+        BPack r;
+        if constexpr (kVecB && Op::kPlainB) {
+            r = ld_stream<In, G>(B + off);
+        } else if constexpr (kBElem) {
+#pragma unroll
+            for (int k = 0; k < G; ++k) r.v[k] = Op::loadB(B, off + k, p.args);
+        } else {
+            r.v[0] = Op::loadB(B, off, p.args);
+        }
+        return r;
+    };
+    APack ah{};
+    BPack bh{};
+    if (!reloadA) ah = load_a(offA);
+    if (!reloadB) bh = load_b(offB);
     uint32_t err = 0;
-    while (g < end) {
-        int64_t offA[U], offB[U], gs[U];
+    for (int j0 = 0; j0 < n; j0 += UR) {
+        APack a[UR];
+        BPack b[UR];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            gs[u] = g;
-            offA[u] = rowA + (IA == 1 ? col * G : IA == 0 ? 0 : col * r.ia);
-            offB[u] = rowB + (IB == 1 ? col * G : IB == 0 ? 0 : col * r.ib);
-            // advance this lane by 32 groups
-            g += 32;
-            col += 32;
-            while (col >= r.cols) {
-                col -= r.cols;
-                if constexpr (TWO_D) {
-                    rowA += r.osa[D - 1];
-                    rowB += r.osb[D - 1];
-                } else {
-#pragma unroll
-                    for (int d = D - 1; d >= 0; --d) {
-                        idx[d] += 1;
-                        rowA += r.osa[d];
-                        rowB += r.osb[d];
-                        if (idx[d] < r.on[d]) break;
-                        idx[d] = 0;
-                        rowA -= r.on[d] * r.osa[d];
-                        rowB -= r.on[d] * r.osb[d];
-                    }
-                }
-            }
-        }
-        // A: a vector per group, or one value per row (IA == 0)
-        // B: a vector per group (IB == 1), or one value per row (IB == 0)
-        Pack<In, G> a[U];
-        In as[U];
-        BV b[U][G];
-        BV bs[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (gs[u] < end) {
-                if constexpr (IA == 1 && G > 1) a[u] = ld_stream<In, G>(A + offA[u]);
-                else as[u] = A[offA[u]];
-                if constexpr (IB == 1 && G > 1 && Op::kPlainB) {
-                    const Pack<In, G> t = ld_stream<In, G>(B + offB[u]);
-#pragma unroll
-                    for (int k = 0; k < G; ++k) b[u][k] = t.v[k];
-                } else if constexpr (IB == 1 && G > 1) {
-#pragma unroll
-                    for (int k = 0; k < G; ++k) b[u][k] = Op::loadB(B, offB[u] + k, p.args);
-                } else {
-                    bs[u] = Op::loadB(B, offB[u], p.args);
-                }
+        for (int u = 0; u < UR; ++u) {
+            if (j0 + u < n) {
+                a[u] = reloadA ? load_a(offA + u * stepA) : ah;
+                b[u] = reloadB ? load_b(offB + u * stepB) : bh;
             }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (gs[u] < end) {
+        for (int u = 0; u < UR; ++u) {
+            if (j0 + u < n) {
                 Pack<Out, G> o;
-#pragma unroll
-                for (int k = 0; k < G; ++k) {
-                    const In x = (IA == 1 && G > 1) ? a[u].v[k] : as[u];
-                    if constexpr (IB == 1 && G > 1) o.v[k] = Op::apply(x, b[u][k], p.args, err);
-                    else o.v[k] = Op::apply(x, bs[u], p.args, err);
-                }
-                if constexpr (G > 1) st_pack<Out, G>(O + gs[u] * G, o);
-                else O[gs[u]] = o.v[0];
+                compute_group<Op, G, !kVecA, !kVecB>(a[u].v, b[u].v, o.v, p.args, err);
+                if constexpr (G > 1) st_stream<Out, G>(O + offO + u * stepO, o);
+                else O[offO + u * stepO] = o.v[0];
             }
         }
+        offA += UR * stepA;
+        offB += UR * stepB;
+        offO += UR * stepO;
     }
     flush_err<Op>(p.status, err);
 }
 
 // ---------------------------------------------------------------- launch helpers
-template <class K>
-int blocks_per_sm(K kernel) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess ||
-        n < 1)
-        n = 1;
-    return n;
-}
-
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <class Op>
@@ -339,91 +421,112 @@ KArgs kargs(const Launch &L) {
     return k;
 }
 
-constexpr int kUnrollFlat = 4;
-constexpr int kUnrollRows = 2;
+constexpr int kUnrollFlat = 2;
+constexpr int64_t kMaxGrid = 0x7FFFFFFF;
 
 template <class Op>
 cudaError_t run_contiguous(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    auto kernel = k_contiguous<Op, kUnrollFlat>;
-    static const int bps = blocks_per_sm(kernel);
     const int64_t ng = L.numel / G;
     int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
-    grid = std::min<int64_t>(grid, (int64_t)L.num_sms * bps);
-    kernel<<<(unsigned)std::max<int64_t>(grid, 1), kThreads, 0, L.stream>>>(kargs<Op>(L));
+    grid = std::min<int64_t>(grid, kMaxGrid);
+    k_contiguous<Op, kUnrollFlat><<<(unsigned)grid, kThreads, 0, L.stream>>>(kargs<Op>(L));
     return cudaGetLastError();
 }
 
 template <class Op, bool SCALAR_A>
 cudaError_t run_scalar(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    auto kernel = k_scalar<Op, SCALAR_A, kUnrollFlat>;
-    static const int bps = blocks_per_sm(kernel);
     const int64_t ng = L.numel / G;
     int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
-    grid = std::min<int64_t>(grid, (int64_t)L.num_sms * bps);
-    kernel<<<(unsigned)std::max<int64_t>(grid, 1), kThreads, 0, L.stream>>>(kargs<Op>(L));
+    grid = std::min<int64_t>(grid, kMaxGrid);
+    k_scalar<Op, SCALAR_A, kUnrollFlat><<<(unsigned)grid, kThreads, 0, L.stream>>>(kargs<Op>(L));
     return cudaGetLastError();
 }
 
-// Fill RowArgs from the coalesced geometry with rows of `inner` elements
-// split into groups of G.
-inline RowArgs row_args(const Geom &g, int G) {
-    RowArgs r;
+// Tile shape for a row traversal with rows of `cols` groups: threads per row,
+// rows in parallel and rows per thread, aiming at enough CTAs for several waves.
+inline RowArgs row_args(const Geom &g, int G, int num_sms) {
+    RowArgs r{};
     const int rank = g.rank;
-    const int64_t inner = g.n[rank - 1];
-    r.cols = inner / G;
-    r.ngroups = 0;
-    r.per_warp = 0;
+    r.L = g.n[rank - 1];
+    r.cols = r.L / G;
     r.ia = g.sa[rank - 1];
     r.ib = g.sb[rank - 1];
-    r.outer = rank - 1;
-    constexpr int D = kMaxRank - 1;
-    int64_t rows = 1;
-    for (int d = 0; d < D; ++d) {
-        r.on[d] = (int64_t)1 << 62;
-        r.osa[d] = 0;
-        r.osb[d] = 0;
+    if (rank >= 2) {
+        r.M = g.n[rank - 2];
+        r.smA = g.sa[rank - 2];
+        r.smB = g.sb[rank - 2];
+    } else {
+        r.M = 1;
+        r.smA = 0;
+        r.smB = 0;
     }
-    for (int i = 0; i < rank - 1; ++i) {
-        const int d = D - (rank - 1) + i;
-        r.on[d] = g.n[i];
-        r.osa[d] = g.sa[i];
-        r.osb[d] = g.sb[i];
-        rows *= g.n[i];
+    r.nprefix = rank >= 2 ? rank - 2 : 0;
+    int64_t P = 1;
+    for (int i = 0; i < r.nprefix; ++i) {
+        r.pn[i] = g.n[i];
+        r.psa[i] = g.sa[i];
+        r.psb[i] = g.sb[i];
+        r.f_pn[i] = make_fastdiv((uint64_t)g.n[i]);
+        P *= g.n[i];
     }
-    r.ngroups = rows * r.cols;
+    if (r.cols >= kThreads) {
+        r.tpr = kThreads;
+        r.rs = 1;
+    } else {
+        r.tpr = (int32_t)r.cols;
+        r.rs = (int32_t)(kThreads / r.cols);
+        if (r.rs > r.M) r.rs = (int32_t)r.M;
+    }
+    r.cc = ceil_div(r.cols, r.tpr);
+    // rows per thread: keep >= ~16 CTAs per SM in flight, at most 16 rows each
+    const int64_t groups = P * r.M * r.cols;
+    const int64_t per_cta = (int64_t)r.tpr * r.rs;
+    int64_t kr = groups / (per_cta * (int64_t)num_sms * 16);
+    kr = std::max<int64_t>(1, std::min<int64_t>(16, kr));
+    kr = std::min<int64_t>(kr, ceil_div(r.M, r.rs));
+    r.kr = (int32_t)kr;
+    r.runs = ceil_div(r.M, (int64_t)r.rs * r.kr);
+    r.f_cc = make_fastdiv((uint64_t)r.cc);
+    r.f_runs = make_fastdiv((uint64_t)r.runs);
+    r.f_tpr = make_fastdiv((uint64_t)r.tpr);
+    const int64_t tiles = P * r.runs * r.cc;
+    r.wide = tiles >= (1ll << 31) ? 1 : 0;
+    for (int i = 0; i < r.nprefix; ++i)
+        if (r.pn[i] >= (1ll << 32)) r.wide = 1;
+    if (r.cc >= (1ll << 32) || r.runs >= (1ll << 32)) r.wide = 1;
     return r;
 }
 
-template <class Op, int G, int IA, int IB, bool TWO_D>
-cudaError_t run_rows_kernel(const Launch &L, RowArgs r) {
-    auto kernel = k_rows<Op, G, IA, IB, TWO_D, kUnrollRows>;
-    static const int bps = blocks_per_sm(kernel);
-    const int64_t warps_max = (int64_t)L.num_sms * bps * (kThreads / 32);
-    // at least 4 steps of 32 groups per warp before spreading wider
-    int64_t warps = std::min<int64_t>(warps_max, std::max<int64_t>(1, ceil_div(r.ngroups, 32 * 4)));
-    r.per_warp = ceil_div(ceil_div(r.ngroups, warps), 32) * 32;
-    warps = ceil_div(r.ngroups, r.per_warp);
-    const int64_t grid = ceil_div(warps, kThreads / 32);
-    kernel<<<(unsigned)std::max<int64_t>(grid, 1), kThreads, 0, L.stream>>>(kargs<Op>(L), r);
+inline int64_t row_tiles(const RowArgs &r) {
+    int64_t P = 1;
+    for (int i = 0; i < r.nprefix; ++i) P *= r.pn[i];
+    return P * r.runs * r.cc;
+}
+
+template <class Op, int G, int IA, int IB, bool NOPREFIX>
+cudaError_t run_rows_kernel(const Launch &L, const RowArgs &r) {
+    const int64_t tiles = row_tiles(r);
+    if (tiles > kMaxGrid) return cudaErrorInvalidConfiguration;
+    k_rows<Op, G, IA, IB, NOPREFIX>
+        <<<(unsigned)tiles, r.tpr * r.rs, 0, L.stream>>>(kargs<Op>(L), r);
     return cudaGetLastError();
 }
 
-template <class Op, bool TWO_D>
+template <class Op, bool NOPREFIX>
 cudaError_t run_rows_vector(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    const RowArgs r = row_args(L.g, G);
-    const int64_t ia = r.ia, ib = r.ib;
-    if (ia == 1 && ib == 1) return run_rows_kernel<Op, G, 1, 1, TWO_D>(L, r);
-    if (ia == 1 && ib == 0) return run_rows_kernel<Op, G, 1, 0, TWO_D>(L, r);
-    if (ia == 0 && ib == 1) return run_rows_kernel<Op, G, 0, 1, TWO_D>(L, r);
+    const RowArgs r = row_args(L.g, G, L.num_sms);
+    if (r.ia == 1 && r.ib == 1) return run_rows_kernel<Op, G, 1, 1, NOPREFIX>(L, r);
+    if (r.ia == 1 && r.ib == 0) return run_rows_kernel<Op, G, 1, 0, NOPREFIX>(L, r);
+    if (r.ia == 0 && r.ib == 1) return run_rows_kernel<Op, G, 0, 1, NOPREFIX>(L, r);
     return cudaErrorInvalidValue;
 }
 
 template <class Op>
 cudaError_t run_general(const Launch &L) {
-    const RowArgs r = row_args(L.g, 1);
+    const RowArgs r = row_args(L.g, 1, L.num_sms);
     return run_rows_kernel<Op, 1, 2, 2, false>(L, r);
 }
 
@@ -439,7 +542,9 @@ cudaError_t launch_op(const Launch &L) {
         case FAM_LEFT_SCALAR:
             if constexpr (Op::kPlainB) return run_scalar<Op, true>(L);
             else return cudaErrorInvalidValue;
-        case FAM_REPEATED_BLOCK: return run_rows_vector<Op, true>(L);
+        case FAM_REPEATED_BLOCK:
+            if (L.g.rank == 2) return run_rows_vector<Op, true>(L);
+            return run_rows_vector<Op, false>(L);
         case FAM_INNER_VECTOR_OUTER: return run_rows_vector<Op, false>(L);
         case FAM_GENERAL_STRIDED: return run_general<Op>(L);
         default: return cudaErrorInvalidValue;
@@ -464,6 +569,3 @@ template <> struct DtType<DT_BOOL> { using type = Bool8; };
 #define EBIN_CAT2(a, b) a##b
 #define EBIN_CAT(a, b) EBIN_CAT2(a, b)
 #define EBIN_GROUP_FN(g) EBIN_CAT(launch_##g##_, EBIN_DT)
-
-namespace ebin {
-}  // namespace ebin

@@ -16,6 +16,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
 #include <type_traits>
 
 #include <cuda_bf16.h>
@@ -219,11 +220,52 @@ template <class C, int K> __device__ __forceinline__ bool compare(C x, C y) {
     else return x >= y;
 }
 
+template <class T> constexpr bool is_half_like_v = std::is_same_v<T, __half> ||
+                                                   std::is_same_v<T, __nv_bfloat16>;
+
+// Two-lane comparison masks (0xFFFF per true lane, NaN compares false).
+template <int K, class T2>
+__device__ __forceinline__ unsigned cmp_mask2(T2 a, T2 b) {
+    if constexpr (K == K_EQ) return __heq2_mask(a, b);
+    else if constexpr (K == K_LT) return __hlt2_mask(a, b);
+    else if constexpr (K == K_GT) return __hgt2_mask(a, b);
+    else if constexpr (K == K_LE) return __hle2_mask(a, b);
+    else return __hge2_mask(a, b);
+}
+
 template <class T, int K> struct OpCmp : PlainB<T, Bool8> {
     static constexpr bool kLegal = is_float_v<T> || is_int_v<T> || (K == K_EQ && is_bool_v<T>);
     static constexpr bool kValidates = false;
+    // half and bfloat16 compare exactly in their own format, two lanes per
+    // instruction; the comparison of the exact float widenings is the same
+    static constexpr bool kPack = is_half_like_v<T>;
     __device__ __forceinline__ static Bool8 apply(T a, T b, const OpArgs &, uint32_t &) {
         return Bool8{(uint8_t)(compare<typename Tr<T>::C, K>(Tr<T>::in(a), Tr<T>::in(b)) ? 1 : 0)};
+    }
+    // G results (G a multiple of 4): two packed compares per four lanes, the
+    // lane masks narrowed to one 0/1 byte each.
+    template <int G>
+    __device__ __forceinline__ static void apply_pack(const T *a, const T *b, Bool8 *o) {
+        static_assert(G % 4 == 0, "packs of four");
+        using T2 = std::conditional_t<std::is_same_v<T, __half>, __half2, __nv_bfloat162>;
+#pragma unroll
+        for (int k = 0; k < G; k += 4) {
+            T2 a0, a1, b0, b1;
+            if constexpr (std::is_same_v<T, __half>) {
+                a0 = __halves2half2(a[k], a[k + 1]);
+                a1 = __halves2half2(a[k + 2], a[k + 3]);
+                b0 = __halves2half2(b[k], b[k + 1]);
+                b1 = __halves2half2(b[k + 2], b[k + 3]);
+            } else {
+                a0 = __halves2bfloat162(a[k], a[k + 1]);
+                a1 = __halves2bfloat162(a[k + 2], a[k + 3]);
+                b0 = __halves2bfloat162(b[k], b[k + 1]);
+                b1 = __halves2bfloat162(b[k + 2], b[k + 3]);
+            }
+            const unsigned m0 = cmp_mask2<K>(a0, b0), m1 = cmp_mask2<K>(a1, b1);
+            const uint32_t w = __byte_perm(m0, m1, 0x6420) & 0x01010101u;
+            memcpy(o + k, &w, 4);
+        }
     }
 };
 
