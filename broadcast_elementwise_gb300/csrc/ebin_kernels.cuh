@@ -103,13 +103,27 @@ template <class Op, class = void> struct HasPack : std::false_type {};
 template <class Op>
 struct HasPack<Op, std::void_t<decltype(Op::kPack)>> : std::bool_constant<Op::kPack> {};
 
+// Operators that prepare a B shared by many elements (Op::kPrep, Op::prep,
+// Op::apply_prep) -- e.g. the reciprocal of a Mod divisor.
+template <class Op, class = void> struct HasPrep : std::false_type {};
+template <class Op>
+struct HasPrep<Op, std::void_t<decltype(Op::kPrep)>> : std::bool_constant<Op::kPrep> {};
+
+struct PrepNone {
+    using PB = int;
+};
+
 // o[k] = op(a[k], b[k]) for one group of G elements.  SA / SB: the operand is
 // one value for the whole group (a[0] / b[0]), not G values.
 template <class Op, int G, bool SA = false, bool SB = false>
 __device__ __forceinline__ void compute_group(const typename Op::In *a, const typename Op::BV *b,
                                               typename Op::Out *o, const OpArgs &args,
                                               uint32_t &err) {
-    if constexpr (HasPack<Op>::value && G % 4 == 0) {
+    if constexpr (SB && HasPrep<Op>::value) {
+        const typename Op::PB pb = Op::prep(b[0]);
+#pragma unroll
+        for (int k = 0; k < G; ++k) o[k] = Op::apply_prep(a[SA ? 0 : k], pb, args, err);
+    } else if constexpr (HasPack<Op>::value && G % 4 == 0) {
         if constexpr (SA || SB) {
             typename Op::In ta[G], tb[G];
 #pragma unroll
@@ -239,6 +253,10 @@ __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
     BV sb{};
     if constexpr (SCALAR_A) sa = A[0];
     else sb = Op::loadB(B, 0, p.args);
+    // a right scalar that the operator can prepare is prepared once per thread
+    using PrepT = typename std::conditional_t<HasPrep<Op>::value, Op, PrepNone>::PB;
+    PrepT pb{};
+    if constexpr (!SCALAR_A && HasPrep<Op>::value) pb = Op::prep(sb);
     const int64_t ng = p.numel / G;
     uint32_t err = 0;
     const int64_t step = (int64_t)gridDim.x * (kThreads * U);
@@ -255,8 +273,14 @@ __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
             const int64_t g = base + (int64_t)u * kThreads;
             if (g < ng) {
                 Pack<Out, G> o;
-                if constexpr (SCALAR_A) compute_group<Op, G, true, false>(&sa, d[u].v, o.v, p.args, err);
-                else compute_group<Op, G, false, true>(d[u].v, &sb, o.v, p.args, err);
+                if constexpr (SCALAR_A) {
+                    compute_group<Op, G, true, false>(&sa, d[u].v, o.v, p.args, err);
+                } else if constexpr (HasPrep<Op>::value) {
+#pragma unroll
+                    for (int k = 0; k < G; ++k) o.v[k] = Op::apply_prep(d[u].v[k], pb, p.args, err);
+                } else {
+                    compute_group<Op, G, false, true>(d[u].v, &sb, o.v, p.args, err);
+                }
                 st_stream<Out, G>(O + g * G, o);
             }
         }
@@ -274,8 +298,9 @@ __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
 // The coalesced dims split into: prefix digits (dims 0..rank-3), the run dim
 // (rank-2, extent M, strides smA/smB) and the inner row (rank-1, L elements =
 // cols groups of G).  A CTA of tpr*rs threads handles one tile:
-// (prefix index, run index, column chunk); rs rows advance in parallel, each
-// thread walks kr of its rows rs apart.
+// (prefix index, run index, column chunk).  rs rows advance in parallel; each
+// thread covers V column groups of its rows (tpr groups apart, so a warp's
+// accesses stay contiguous) and walks kr of its rows, rs apart.
 struct RowArgs {
     int64_t L;            // inner elements per row
     int64_t cols;         // groups per row = L / G
@@ -286,20 +311,22 @@ struct RowArgs {
     int32_t rs;           // rows in parallel (threads = tpr * rs)
     int32_t kr;           // rows per thread per tile
     int32_t wide;         // an index may reach 2^32: divide in 64 bits
-    int64_t cc;           // column chunks per row = ceil(cols / tpr)
+    int64_t cc;           // column chunks per row = ceil(cols / (tpr * V))
     int64_t runs;         // run tiles per prefix index = ceil(M / (rs * kr))
     int32_t nprefix;      // prefix digits (rank - 2, at least 0)
     int64_t pn[kMaxRank];
     int64_t psa[kMaxRank];
     int64_t psb[kMaxRank];
-    FastDiv f_cc, f_runs, f_tpr;
+    FastDiv f_cc, f_runs, f_tpr, f_rs;
     FastDiv f_pn[kMaxRank];
 };
 
 // IA / IB: 1 = the operand advances along the row (vector loads), 0 = it is
 // constant along the row (one value per row), 2 = any inner stride (G == 1).
-// NOPREFIX: rank <= 2, no prefix digits to decode.
-template <class Op, int G, int IA, int IB, bool NOPREFIX>
+// NOPREFIX: rank <= 2, no prefix digits to decode.  V: column groups per
+// thread per row.  UR: rows per iteration whose loads are all issued before
+// any store.
+template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, int UR>
 __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     using In = typename Op::In;
     using Out = typename Op::Out;
@@ -307,6 +334,7 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     static_assert(G == 1 || (IA != 2 && IB != 2), "runtime inner strides need G == 1");
     constexpr bool kVecA = IA == 1 && G > 1;
     constexpr bool kVecB = IB == 1 && G > 1;
+    constexpr bool kBElem = kVecB && !Op::kPlainB;   // per-element parameter blocks
     const In *A = static_cast<const In *>(p.A);
     const In *B = static_cast<const In *>(p.B);
     Out *O = static_cast<Out *>(p.out);
@@ -321,10 +349,13 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     const int64_t pi = udiv(q1, r.runs, r.f_runs, wide);
     const int64_t ri = q1 - pi * r.runs;
     const int rsub = r.rs == 1 ? 0 : (int)fastdiv((uint32_t)t, r.f_tpr);
-    const int64_t c = ci * r.tpr + (t - rsub * r.tpr);
-    if (c >= r.cols) return;
+    const int64_t c0 = ci * (int64_t)r.tpr * V + (t - rsub * r.tpr);
+    if (c0 >= r.cols) return;
     const int64_t m0 = ri * (int64_t)(r.rs * r.kr) + rsub;
     if (m0 >= r.M) return;
+    bool ok[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) ok[v] = c0 + (int64_t)v * r.tpr < r.cols;
 
     int64_t baseA = 0, baseB = 0;
     if constexpr (!NOPREFIX) {
@@ -340,63 +371,88 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
             }
         }
     }
-    int64_t offA = baseA + m0 * r.smA + (IA == 1 ? c * G : IA == 2 ? c * r.ia : 0);
-    int64_t offB = baseB + m0 * r.smB + (IB == 1 ? c * G : IB == 2 ? c * r.ib : 0);
-    int64_t offO = (pi * r.M + m0) * r.L + c * G;
+    // element offsets of group v: off + v * vstep
+    const int64_t vstepA = IA == 1 ? (int64_t)r.tpr * G : IA == 2 ? (int64_t)r.tpr * r.ia : 0;
+    const int64_t vstepB = IB == 1 ? (int64_t)r.tpr * G : IB == 2 ? (int64_t)r.tpr * r.ib : 0;
+    const int64_t vstepO = (int64_t)r.tpr * G;
+    int64_t offA = baseA + m0 * r.smA + (IA == 1 ? c0 * G : IA == 2 ? c0 * r.ia : 0);
+    int64_t offB = baseB + m0 * r.smB + (IB == 1 ? c0 * G : IB == 2 ? c0 * r.ib : 0);
+    int64_t offO = (pi * r.M + m0) * r.L + c0 * G;
     const int64_t stepA = (int64_t)r.rs * r.smA;
     const int64_t stepB = (int64_t)r.rs * r.smB;
     const int64_t stepO = (int64_t)r.rs * r.L;
-    const int64_t left = (r.M - m0 + r.rs - 1) / r.rs;
+    // this thread's rows in the run: ceil((M - m0) / rs), at most kr
+    const int64_t rows_left = r.M - m0 + r.rs - 1;
+    const int64_t left = wide ? rows_left / r.rs : (int64_t)fastdiv((uint32_t)rows_left, r.f_rs);
     const int n = (int)(left < r.kr ? left : r.kr);
 
-    // UR rows per iteration: all their loads are issued before any result is
-    // stored.  An operand whose run stride is 0 is read once and kept.  Dense
-    // operands stay 16-byte packs; an operand constant along the row is one value.
-    constexpr bool kBElem = kVecB && !Op::kPlainB;   // per-element parameter blocks
-    constexpr int UR = kBElem ? 1 : ((kVecA && kVecB) || !Op::kPlainB) ? 2 : 4;
+    // Dense operands stay 16-byte packs; an operand constant along the row is
+    // one value.  An operand whose run stride is 0 is read once and kept.
     using APack = std::conditional_t<kVecA, Pack<In, G>, Pack<In, 1>>;
     using BPack = std::conditional_t<kVecB && Op::kPlainB, Pack<In, G>, Pack<BV, kBElem ? G : 1>>;
+    constexpr int VA = (IA == 0) ? 1 : V;   // a row-constant operand is the same for all v
+    constexpr int VB = (IB == 0) ? 1 : V;
     const bool reloadA = stepA != 0, reloadB = stepB != 0;
     auto load_a = [&](int64_t off) {
-        APack r;
-        if constexpr (kVecA) r = ld_stream<In, G>(A + off);
-        else r.v[0] = A[off];
-        return r;
+        APack x;
+        if constexpr (kVecA) x = ld_stream<In, G>(A + off);
+        else x.v[0] = A[off];
+        return x;
     };
     auto load_b = [&](int64_t off) {
-        BPack r;
+        BPack x;
         if constexpr (kVecB && Op::kPlainB) {
-            r = ld_stream<In, G>(B + off);
+            x = ld_stream<In, G>(B + off);
         } else if constexpr (kBElem) {
 #pragma unroll
-            for (int k = 0; k < G; ++k) r.v[k] = Op::loadB(B, off + k, p.args);
+            for (int k = 0; k < G; ++k) x.v[k] = Op::loadB(B, off + k, p.args);
         } else {
-            r.v[0] = Op::loadB(B, off, p.args);
+            x.v[0] = Op::loadB(B, off, p.args);
         }
-        return r;
+        return x;
     };
-    APack ah{};
-    BPack bh{};
-    if (!reloadA) ah = load_a(offA);
-    if (!reloadB) bh = load_b(offB);
+    APack ah[VA];
+    BPack bh[VB];
+    if (!reloadA) {
+#pragma unroll
+        for (int v = 0; v < VA; ++v)
+            if (ok[v]) ah[v] = load_a(offA + v * vstepA);
+    }
+    if (!reloadB) {
+#pragma unroll
+        for (int v = 0; v < VB; ++v)
+            if (ok[v]) bh[v] = load_b(offB + v * vstepB);
+    }
     uint32_t err = 0;
     for (int j0 = 0; j0 < n; j0 += UR) {
-        APack a[UR];
-        BPack b[UR];
+        APack a[UR][VA];
+        BPack b[UR][VB];
 #pragma unroll
         for (int u = 0; u < UR; ++u) {
             if (j0 + u < n) {
-                a[u] = reloadA ? load_a(offA + u * stepA) : ah;
-                b[u] = reloadB ? load_b(offB + u * stepB) : bh;
+#pragma unroll
+                for (int v = 0; v < VA; ++v)
+                    if (ok[v]) a[u][v] = reloadA ? load_a(offA + u * stepA + v * vstepA) : ah[v];
+#pragma unroll
+                for (int v = 0; v < VB; ++v)
+                    if (ok[v]) b[u][v] = reloadB ? load_b(offB + u * stepB + v * vstepB) : bh[v];
             }
         }
 #pragma unroll
         for (int u = 0; u < UR; ++u) {
             if (j0 + u < n) {
-                Pack<Out, G> o;
-                compute_group<Op, G, !kVecA, !kVecB>(a[u].v, b[u].v, o.v, p.args, err);
-                if constexpr (G > 1) st_stream<Out, G>(O + offO + u * stepO, o);
-                else O[offO + u * stepO] = o.v[0];
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    if (ok[v]) {
+                        Pack<Out, G> o;
+                        compute_group<Op, G, !kVecA, !kVecB>(a[u][IA == 0 ? 0 : v].v,
+                                                            b[u][IB == 0 ? 0 : v].v, o.v,
+                                                            p.args, err);
+                        const int64_t oo = offO + u * stepO + v * vstepO;
+                        if constexpr (G > 1) st_stream<Out, G>(O + oo, o);
+                        else O[oo] = o.v[0];
+                    }
+                }
             }
         }
         offA += UR * stepA;
@@ -444,9 +500,10 @@ cudaError_t run_scalar(const Launch &L) {
     return cudaGetLastError();
 }
 
-// Tile shape for a row traversal with rows of `cols` groups: threads per row,
-// rows in parallel and rows per thread, aiming at enough CTAs for several waves.
-inline RowArgs row_args(const Geom &g, int G, int num_sms) {
+// Tile shape for a row traversal with rows of `cols` groups and V groups per
+// thread per row: threads per row, rows in parallel and rows per thread,
+// aiming at enough CTAs for several waves.
+inline RowArgs row_args(const Geom &g, int G, int V, int num_sms) {
     RowArgs r{};
     const int rank = g.rank;
     r.L = g.n[rank - 1];
@@ -471,18 +528,19 @@ inline RowArgs row_args(const Geom &g, int G, int num_sms) {
         r.f_pn[i] = make_fastdiv((uint64_t)g.n[i]);
         P *= g.n[i];
     }
-    if (r.cols >= kThreads) {
+    const int64_t per_thread_cols = ceil_div(r.cols, V);
+    if (per_thread_cols >= kThreads) {
         r.tpr = kThreads;
         r.rs = 1;
     } else {
-        r.tpr = (int32_t)r.cols;
-        r.rs = (int32_t)(kThreads / r.cols);
+        r.tpr = (int32_t)per_thread_cols;
+        r.rs = (int32_t)(kThreads / per_thread_cols);
         if (r.rs > r.M) r.rs = (int32_t)r.M;
     }
-    r.cc = ceil_div(r.cols, r.tpr);
+    r.cc = ceil_div(r.cols, (int64_t)r.tpr * V);
     // rows per thread: keep >= ~16 CTAs per SM in flight, at most 16 rows each
     const int64_t groups = P * r.M * r.cols;
-    const int64_t per_cta = (int64_t)r.tpr * r.rs;
+    const int64_t per_cta = (int64_t)r.tpr * r.rs * V;
     int64_t kr = groups / (per_cta * (int64_t)num_sms * 16);
     kr = std::max<int64_t>(1, std::min<int64_t>(16, kr));
     kr = std::min<int64_t>(kr, ceil_div(r.M, r.rs));
@@ -491,11 +549,12 @@ inline RowArgs row_args(const Geom &g, int G, int num_sms) {
     r.f_cc = make_fastdiv((uint64_t)r.cc);
     r.f_runs = make_fastdiv((uint64_t)r.runs);
     r.f_tpr = make_fastdiv((uint64_t)r.tpr);
+    r.f_rs = make_fastdiv((uint64_t)r.rs);
     const int64_t tiles = P * r.runs * r.cc;
     r.wide = tiles >= (1ll << 31) ? 1 : 0;
     for (int i = 0; i < r.nprefix; ++i)
         if (r.pn[i] >= (1ll << 32)) r.wide = 1;
-    if (r.cc >= (1ll << 32) || r.runs >= (1ll << 32)) r.wide = 1;
+    if (r.cc >= (1ll << 32) || r.runs >= (1ll << 32) || r.M + r.rs >= (1ll << 32)) r.wide = 1;
     return r;
 }
 
@@ -505,29 +564,50 @@ inline int64_t row_tiles(const RowArgs &r) {
     return P * r.runs * r.cc;
 }
 
-template <class Op, int G, int IA, int IB, bool NOPREFIX>
-cudaError_t run_rows_kernel(const Launch &L, const RowArgs &r) {
+template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, int UR>
+cudaError_t run_rows_kernel(const Launch &L) {
+    const RowArgs r = row_args(L.g, G, V, L.num_sms);
     const int64_t tiles = row_tiles(r);
     if (tiles > kMaxGrid) return cudaErrorInvalidConfiguration;
-    k_rows<Op, G, IA, IB, NOPREFIX>
+    k_rows<Op, G, IA, IB, NOPREFIX, V, UR>
         <<<(unsigned)tiles, r.tpr * r.rs, 0, L.stream>>>(kargs<Op>(L), r);
     return cudaGetLastError();
 }
 
+// Column groups per thread per row (V) and rows per iteration (UR).  Measured
+// on GB300 (per-channel bf16 x[8,64,256,256], Greater fp16 to BOOL
+// [64,32,512,1024]): two groups per thread per row and one row per iteration
+// for a dense A (5.0 TB/s against 4.4 with one group and four rows); four
+// groups when A is one value per row (5.35 TB/s against 4.3).
+template <class Op, int IA, int IB>
+struct RowShape {
+    static constexpr bool kElemB = IB == 1 && !Op::kPlainB;
+    static constexpr int V = kElemB ? 1 : (IA == 0 ? 4 : 2);
+    static constexpr int UR = 1;
+};
+
 template <class Op, bool NOPREFIX>
 cudaError_t run_rows_vector(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    const RowArgs r = row_args(L.g, G, L.num_sms);
-    if (r.ia == 1 && r.ib == 1) return run_rows_kernel<Op, G, 1, 1, NOPREFIX>(L, r);
-    if (r.ia == 1 && r.ib == 0) return run_rows_kernel<Op, G, 1, 0, NOPREFIX>(L, r);
-    if (r.ia == 0 && r.ib == 1) return run_rows_kernel<Op, G, 0, 1, NOPREFIX>(L, r);
+    const int64_t ia = L.g.sa[L.g.rank - 1], ib = L.g.sb[L.g.rank - 1];
+    if (ia == 1 && ib == 1) {
+        using S = RowShape<Op, 1, 1>;
+        return run_rows_kernel<Op, G, 1, 1, NOPREFIX, S::V, S::UR>(L);
+    }
+    if (ia == 1 && ib == 0) {
+        using S = RowShape<Op, 1, 0>;
+        return run_rows_kernel<Op, G, 1, 0, NOPREFIX, S::V, S::UR>(L);
+    }
+    if (ia == 0 && ib == 1) {
+        using S = RowShape<Op, 0, 1>;
+        return run_rows_kernel<Op, G, 0, 1, NOPREFIX, S::V, S::UR>(L);
+    }
     return cudaErrorInvalidValue;
 }
 
 template <class Op>
 cudaError_t run_general(const Launch &L) {
-    const RowArgs r = row_args(L.g, 1, L.num_sms);
-    return run_rows_kernel<Op, 1, 2, 2, false>(L, r);
+    return run_rows_kernel<Op, 1, 2, 2, false, 1, 2>(L);
 }
 
 // Launch the kernel of L.family for operator functor Op.

@@ -162,6 +162,51 @@ template <class T, int K> struct OpArith : PlainB<T, T> {
     }
 };
 
+// A divisor that stays the same for many elements (a scalar, or one value per
+// row) is prepared once: with r = RN(1/|b|), q = trunc(|a| * r) is within one
+// of n = trunc(|a|/|b|) whenever |a|/|b| < 2^22 (two roundings of relative
+// size 2^-24 each).  fmaf(-q, |b|, |a|) is exact for q = n and for q = n + 1
+// (the results are multiples of ulp(|b|) below |b| in magnitude); a negative
+// result takes |b| back (exact), and a result >= |b| means q = n - 1, which is
+// redone with n (exact).  Anything outside that range -- NaN, infinities, zero
+// or subnormal divisors, huge quotients -- goes to fmod_exact.
+struct ModPrep {
+    float b, ab, rcp;
+    bool fast;
+};
+
+__device__ __forceinline__ ModPrep mod_prep(float b) {
+    ModPrep p;
+    p.b = b;
+    p.ab = fabsf(b);
+    p.fast = p.ab >= 0x1p-125f && p.ab <= 0x1p125f;   // excludes 0, subnormals, inf, NaN
+    p.rcp = __frcp_rn(p.ab);
+    return p;
+}
+
+__device__ __forceinline__ float fmod_prepared(float a, const ModPrep &p) {
+    const float aa = fabsf(a);
+    if (aa < p.ab) return a;
+    if (p.fast && aa < INFINITY) {
+        const float q = truncf(__fmul_rn(aa, p.rcp));
+        if (q < 4194304.0f) {
+            float r = fmaf(-q, p.ab, aa);
+            if (r < 0.0f) r = __fadd_rn(r, p.ab);
+            else if (r >= p.ab) r = fmaf(-__fadd_rn(q, 1.0f), p.ab, aa);
+            return copysignf(r, a);
+        }
+    }
+    return fmod_exact(a, p.b);
+}
+
+// fmod=1: truncated remainder as is; fmod=0: floor rule of opset 28
+__device__ __forceinline__ float floor_adjust(float r, float b, int fmod_flag) {
+    if (fmod_flag) return r;
+    if (r == 0.0f) return copysignf(0.0f, b);
+    if (signbit(r) != signbit(b)) r = __fadd_rn(r, b);
+    return r;
+}
+
 template <class T> struct OpMod : PlainB<T, T> {
     static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
     static constexpr bool kValidates = is_int_v<T>;
@@ -179,6 +224,14 @@ template <class T> struct OpMod : PlainB<T, T> {
                 return (T)(a % b);
             }
         }
+    }
+    // floating Mod with a divisor shared by a whole group (see ModPrep)
+    static constexpr bool kPrep = is_float_v<T>;
+    using PB = ModPrep;
+    __device__ __forceinline__ static ModPrep prep(T b) { return mod_prep(Tr<T>::in(b)); }
+    __device__ __forceinline__ static T apply_prep(T a, const ModPrep &pb, const OpArgs &p,
+                                                   uint32_t &) {
+        return Tr<T>::out(floor_adjust(fmod_prepared(Tr<T>::in(a), pb), pb.b, p.fmod));
     }
 };
 

@@ -135,3 +135,34 @@ def test_plan_outlives_cache_eviction_on_device():
     eb.execute(keep, dA, dB, out)
     torch.cuda.synchronize()
     assert_bits_equal(out.cpu().numpy().view(np.float32).reshape(64, 64), want, "float32")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
+def test_mod_with_shared_divisor_is_exact(dtype):
+    """Scalar and per-row divisors take the prepared-reciprocal path: stress it
+    with dividends at, next to and between multiples of the divisor, raw bit
+    patterns, and divisors across the exponent range."""
+    divisors = [1.0, 3.0, -2.5, 0.1, 7.0e-3, -1.0e-30, 6.5e20, 1.5e-38, 1e-44, 0.0, -0.0,
+                np.inf, np.nan, 65504.0, 3.3333333, -1234.5678]
+    rng = np.random.default_rng(99)
+    for i, d in enumerate(divisors):
+        bq = datagen.float_to(np.array([d], np.float32), dtype)
+        dv = float(bq.astype(np.float32)[0]) if dtype != "bfloat16" else \
+            float((bq.astype(np.uint32) << 16).view(np.float32)[0])
+        k = rng.integers(-5000000, 5000000, 4096).astype(np.float64)
+        cand = np.concatenate([k * dv, k * dv + dv * 0.5, np.nextafter(k * dv, np.inf),
+                               (rng.random(4096) - 0.5) * 2e6]).astype(np.float32)
+        with np.errstate(all="ignore"):
+            a = np.concatenate([datagen.float_to(np.nan_to_num(cand, nan=1.0), dtype),
+                                datagen.make("bits", dtype, (8192,), 70, i)]).reshape(-1)
+        a = a[: (a.size // 64) * 64]
+        for fmod in (0, 1):
+            got, bits, fam = run_engine("Mod", dtype, a, bq.reshape(()), attrs={"fmod": fmod})
+            want, _ = oracle.run("Mod", a, bq.reshape(()), dtype, fmod=fmod)
+            assert fam == "right_scalar"
+            assert_bits_equal(got, want, dtype, "Mod scalar %r fmod=%d" % (d, fmod))
+            rows = a.reshape(64, -1)
+            bcol = np.repeat(bq, 64).reshape(64, 1)
+            got, _, fam = run_engine("Mod", dtype, rows, bcol, attrs={"fmod": fmod})
+            want, _ = oracle.run("Mod", rows, bcol, dtype, fmod=fmod)
+            assert_bits_equal(got, want, dtype, "Mod rows %r fmod=%d" % (d, fmod))
