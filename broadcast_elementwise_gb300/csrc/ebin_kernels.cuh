@@ -314,6 +314,7 @@ struct RowArgs {
     int64_t cc;           // column chunks per row = ceil(cols / (tpr * V))
     int64_t runs;         // run tiles per prefix index = ceil(M / (rs * kr))
     int32_t nprefix;      // prefix digits (rank - 2, at least 0)
+    int32_t pack_ok;      // rows are a whole number of V*G packs: pack stores stay aligned
     int64_t pn[kMaxRank];
     int64_t psa[kMaxRank];
     int64_t psb[kMaxRank];
@@ -324,20 +325,20 @@ struct RowArgs {
 // IA / IB: 1 = the operand advances along the row (vector loads), 0 = it is
 // constant along the row (one value per row), 2 = any inner stride (G == 1).
 // NOPREFIX: rank <= 2, no prefix digits to decode.  V: column groups per
-// thread per row.  UR: rows per iteration whose loads are all issued before
-// any store.
-template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, int UR>
+// thread per row.  PACKED: the V groups are adjacent and their outputs form
+// one store of V*G*sizeof(Out) <= 16 bytes (outputs narrower than inputs,
+// e.g. comparisons writing BOOL); otherwise they are tpr groups apart.
+// Pointers advance by constant steps from row to row.
+template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, bool PACKED>
 __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
     static_assert(G == 1 || (IA != 2 && IB != 2), "runtime inner strides need G == 1");
+    static_assert(!PACKED || V * G * (int)sizeof(Out) <= 16, "packed output fits one store");
     constexpr bool kVecA = IA == 1 && G > 1;
     constexpr bool kVecB = IB == 1 && G > 1;
     constexpr bool kBElem = kVecB && !Op::kPlainB;   // per-element parameter blocks
-    const In *A = static_cast<const In *>(p.A);
-    const In *B = static_cast<const In *>(p.B);
-    Out *O = static_cast<Out *>(p.out);
 
     const int t = threadIdx.x;
     if (t >= r.tpr * r.rs) return;
@@ -349,13 +350,16 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     const int64_t pi = udiv(q1, r.runs, r.f_runs, wide);
     const int64_t ri = q1 - pi * r.runs;
     const int rsub = r.rs == 1 ? 0 : (int)fastdiv((uint32_t)t, r.f_tpr);
-    const int64_t c0 = ci * (int64_t)r.tpr * V + (t - rsub * r.tpr);
+    const int64_t lane = ci * (int64_t)r.tpr + (t - rsub * r.tpr);
+    // first column group of this thread, and the distance between its groups
+    const int64_t c0 = PACKED ? lane * V : lane + (ci * (int64_t)r.tpr) * (V - 1);
+    const int64_t cstep = PACKED ? 1 : r.tpr;
     if (c0 >= r.cols) return;
     const int64_t m0 = ri * (int64_t)(r.rs * r.kr) + rsub;
     if (m0 >= r.M) return;
     bool ok[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) ok[v] = c0 + (int64_t)v * r.tpr < r.cols;
+    for (int v = 0; v < V; ++v) ok[v] = c0 + v * cstep < r.cols;
 
     int64_t baseA = 0, baseB = 0;
     if constexpr (!NOPREFIX) {
@@ -371,13 +375,15 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
             }
         }
     }
-    // element offsets of group v: off + v * vstep
-    const int64_t vstepA = IA == 1 ? (int64_t)r.tpr * G : IA == 2 ? (int64_t)r.tpr * r.ia : 0;
-    const int64_t vstepB = IB == 1 ? (int64_t)r.tpr * G : IB == 2 ? (int64_t)r.tpr * r.ib : 0;
-    const int64_t vstepO = (int64_t)r.tpr * G;
-    int64_t offA = baseA + m0 * r.smA + (IA == 1 ? c0 * G : IA == 2 ? c0 * r.ia : 0);
-    int64_t offB = baseB + m0 * r.smB + (IB == 1 ? c0 * G : IB == 2 ? c0 * r.ib : 0);
-    int64_t offO = (pi * r.M + m0) * r.L + c0 * G;
+    // element distance between the thread's groups v and v+1
+    const int64_t vstepA = IA == 1 ? cstep * G : IA == 2 ? cstep * r.ia : 0;
+    const int64_t vstepB = IB == 1 ? cstep * G : IB == 2 ? cstep * r.ib : 0;
+    const int64_t vstepO = cstep * G;
+    const In *pa = static_cast<const In *>(p.A) + baseA + m0 * r.smA +
+                   (IA == 1 ? c0 * G : IA == 2 ? c0 * r.ia : 0);
+    const In *pb = static_cast<const In *>(p.B) + baseB + m0 * r.smB +
+                   (IB == 1 ? c0 * G : IB == 2 ? c0 * r.ib : 0);
+    Out *po = static_cast<Out *>(p.out) + (pi * r.M + m0) * r.L + c0 * G;
     const int64_t stepA = (int64_t)r.rs * r.smA;
     const int64_t stepB = (int64_t)r.rs * r.smB;
     const int64_t stepO = (int64_t)r.rs * r.L;
@@ -393,71 +399,73 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     constexpr int VA = (IA == 0) ? 1 : V;   // a row-constant operand is the same for all v
     constexpr int VB = (IB == 0) ? 1 : V;
     const bool reloadA = stepA != 0, reloadB = stepB != 0;
-    auto load_a = [&](int64_t off) {
+    auto load_a = [&](const In *q) {
         APack x;
-        if constexpr (kVecA) x = ld_stream<In, G>(A + off);
-        else x.v[0] = A[off];
+        if constexpr (kVecA) x = ld_stream<In, G>(q);
+        else x.v[0] = *q;
         return x;
     };
-    auto load_b = [&](int64_t off) {
+    auto load_b = [&](const In *q) {
         BPack x;
         if constexpr (kVecB && Op::kPlainB) {
-            x = ld_stream<In, G>(B + off);
+            x = ld_stream<In, G>(q);
         } else if constexpr (kBElem) {
 #pragma unroll
-            for (int k = 0; k < G; ++k) x.v[k] = Op::loadB(B, off + k, p.args);
+            for (int k = 0; k < G; ++k) x.v[k] = Op::loadB(q, k, p.args);
         } else {
-            x.v[0] = Op::loadB(B, off, p.args);
+            x.v[0] = Op::loadB(q, 0, p.args);
         }
         return x;
     };
-    APack ah[VA];
-    BPack bh[VB];
-    if (!reloadA) {
-#pragma unroll
-        for (int v = 0; v < VA; ++v)
-            if (ok[v]) ah[v] = load_a(offA + v * vstepA);
-    }
-    if (!reloadB) {
-#pragma unroll
-        for (int v = 0; v < VB; ++v)
-            if (ok[v]) bh[v] = load_b(offB + v * vstepB);
-    }
+    APack a[VA];
+    BPack b[VB];
     uint32_t err = 0;
-    for (int j0 = 0; j0 < n; j0 += UR) {
-        APack a[UR][VA];
-        BPack b[UR][VB];
+    for (int j = 0; j < n; ++j) {
+        if (j == 0 || reloadA) {
 #pragma unroll
-        for (int u = 0; u < UR; ++u) {
-            if (j0 + u < n) {
-#pragma unroll
-                for (int v = 0; v < VA; ++v)
-                    if (ok[v]) a[u][v] = reloadA ? load_a(offA + u * stepA + v * vstepA) : ah[v];
-#pragma unroll
-                for (int v = 0; v < VB; ++v)
-                    if (ok[v]) b[u][v] = reloadB ? load_b(offB + u * stepB + v * vstepB) : bh[v];
-            }
+            for (int v = 0; v < VA; ++v)
+                if (ok[v]) a[v] = load_a(pa + v * vstepA);
         }
+        if (j == 0 || reloadB) {
 #pragma unroll
-        for (int u = 0; u < UR; ++u) {
-            if (j0 + u < n) {
+            for (int v = 0; v < VB; ++v)
+                if (ok[v]) b[v] = load_b(pb + v * vstepB);
+        }
+        if constexpr (PACKED) {
+            Pack<Out, V * G> o;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                compute_group<Op, G, !kVecA, !kVecB>(a[IA == 0 ? 0 : v].v, b[IB == 0 ? 0 : v].v,
+                                                    o.v + v * G, p.args, err);
+            if (r.pack_ok && ok[V - 1]) {
+                st_stream<Out, V * G>(po, o);
+            } else {
+                // rows that are not a whole number of packs: one aligned store per group
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     if (ok[v]) {
-                        Pack<Out, G> o;
-                        compute_group<Op, G, !kVecA, !kVecB>(a[u][IA == 0 ? 0 : v].v,
-                                                            b[u][IB == 0 ? 0 : v].v, o.v,
-                                                            p.args, err);
-                        const int64_t oo = offO + u * stepO + v * vstepO;
-                        if constexpr (G > 1) st_stream<Out, G>(O + oo, o);
-                        else O[oo] = o.v[0];
+                        Pack<Out, G> og;
+#pragma unroll
+                        for (int k = 0; k < G; ++k) og.v[k] = o.v[v * G + k];
+                        st_stream<Out, G>(po + v * G, og);
                     }
                 }
             }
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                if (ok[v]) {
+                    Pack<Out, G> o;
+                    compute_group<Op, G, !kVecA, !kVecB>(a[IA == 0 ? 0 : v].v,
+                                                        b[IB == 0 ? 0 : v].v, o.v, p.args, err);
+                    if constexpr (G > 1) st_stream<Out, G>(po + v * vstepO, o);
+                    else po[v * vstepO] = o.v[0];
+                }
+            }
         }
-        offA += UR * stepA;
-        offB += UR * stepB;
-        offO += UR * stepO;
+        pa += stepA;
+        pb += stepB;
+        po += stepO;
     }
     flush_err<Op>(p.status, err);
 }
@@ -538,6 +546,7 @@ inline RowArgs row_args(const Geom &g, int G, int V, int num_sms) {
         if (r.rs > r.M) r.rs = (int32_t)r.M;
     }
     r.cc = ceil_div(r.cols, (int64_t)r.tpr * V);
+    r.pack_ok = (r.L % ((int64_t)V * G) == 0) ? 1 : 0;
     // rows per thread: keep >= ~16 CTAs per SM in flight, at most 16 rows each
     const int64_t groups = P * r.M * r.cols;
     const int64_t per_cta = (int64_t)r.tpr * r.rs * V;
@@ -564,26 +573,31 @@ inline int64_t row_tiles(const RowArgs &r) {
     return P * r.runs * r.cc;
 }
 
-template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, int UR>
+template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, bool PACKED>
 cudaError_t run_rows_kernel(const Launch &L) {
     const RowArgs r = row_args(L.g, G, V, L.num_sms);
     const int64_t tiles = row_tiles(r);
     if (tiles > kMaxGrid) return cudaErrorInvalidConfiguration;
-    k_rows<Op, G, IA, IB, NOPREFIX, V, UR>
+    k_rows<Op, G, IA, IB, NOPREFIX, V, PACKED>
         <<<(unsigned)tiles, r.tpr * r.rs, 0, L.stream>>>(kargs<Op>(L), r);
     return cudaGetLastError();
 }
 
-// Column groups per thread per row (V) and rows per iteration (UR).  Measured
-// on GB300 (per-channel bf16 x[8,64,256,256], Greater fp16 to BOOL
-// [64,32,512,1024]): two groups per thread per row and one row per iteration
-// for a dense A (5.0 TB/s against 4.4 with one group and four rows); four
-// groups when A is one value per row (5.35 TB/s against 4.3).
+// Column groups per thread per row (V), measured on GB300.  Outputs narrower
+// than the inputs (comparisons to BOOL) take adjacent groups whose results make
+// one 16-byte store (Greater fp16 -> BOOL [64,32,512,1024]: 7.6 TB/s, against
+// 5.1 with groups a row-width apart).  Otherwise two groups a row-width apart
+// for a dense A (per-channel bf16: 5.0 TB/s, against 4.4 with one group and
+// four rows per iteration) and four when A is one value per row.
 template <class Op, int IA, int IB>
 struct RowShape {
+    using In = typename Op::In;
+    using Out = typename Op::Out;
+    static constexpr int G = 16 / (int)sizeof(In);
     static constexpr bool kElemB = IB == 1 && !Op::kPlainB;
-    static constexpr int V = kElemB ? 1 : (IA == 0 ? 4 : 2);
-    static constexpr int UR = 1;
+    static constexpr int kPackV = 16 / (G * (int)sizeof(Out));
+    static constexpr bool PACKED = !kElemB && sizeof(Out) < sizeof(In) && kPackV >= 2;
+    static constexpr int V = PACKED ? (kPackV > 4 ? 4 : kPackV) : kElemB ? 1 : (IA == 0 ? 4 : 2);
 };
 
 template <class Op, bool NOPREFIX>
@@ -592,22 +606,22 @@ cudaError_t run_rows_vector(const Launch &L) {
     const int64_t ia = L.g.sa[L.g.rank - 1], ib = L.g.sb[L.g.rank - 1];
     if (ia == 1 && ib == 1) {
         using S = RowShape<Op, 1, 1>;
-        return run_rows_kernel<Op, G, 1, 1, NOPREFIX, S::V, S::UR>(L);
+        return run_rows_kernel<Op, G, 1, 1, NOPREFIX, S::V, S::PACKED>(L);
     }
     if (ia == 1 && ib == 0) {
         using S = RowShape<Op, 1, 0>;
-        return run_rows_kernel<Op, G, 1, 0, NOPREFIX, S::V, S::UR>(L);
+        return run_rows_kernel<Op, G, 1, 0, NOPREFIX, S::V, S::PACKED>(L);
     }
     if (ia == 0 && ib == 1) {
         using S = RowShape<Op, 0, 1>;
-        return run_rows_kernel<Op, G, 0, 1, NOPREFIX, S::V, S::UR>(L);
+        return run_rows_kernel<Op, G, 0, 1, NOPREFIX, S::V, S::PACKED>(L);
     }
     return cudaErrorInvalidValue;
 }
 
 template <class Op>
 cudaError_t run_general(const Launch &L) {
-    return run_rows_kernel<Op, 1, 2, 2, false, 1, 2>(L);
+    return run_rows_kernel<Op, 1, 2, 2, false, 2, false>(L);
 }
 
 // Launch the kernel of L.family for operator functor Op.

@@ -124,3 +124,18 @@ def test_inner_vector_kernel_on_other_geometries(op, dtype):
         got, _, fam = run_engine(op, dtype, a, b, family="inner_vector_outer")
         assert fam == "inner_vector_outer"
         compare(op, dtype, got, want, "%s %s %s %s" % (op, dtype, sa, sb))
+
+
+@pytest.mark.parametrize("op", ["Greater", "Equal", "LessOrEqual"])
+@pytest.mark.parametrize("dtype,inner", [("float32", 72), ("float16", 72), ("bfloat16", 88),
+                                         ("int64", 70), ("int32", 68)])
+def test_packed_compare_rows_with_ragged_ends(op, dtype, inner):
+    """Comparisons write adjacent groups as one narrow pack; rows whose width
+    is not a multiple of the pack finish group by group."""
+    for i, (sa, sb) in enumerate([((9, 1, inner), (1, 3, inner)), ((5, 1, 7, 1), (1, 3, 1, inner)),
+                                  ((40, inner), (inner,))]):
+        a, b = inputs_for(op, dtype, sa, sb, seed=60 + i)
+        want, _ = oracle.run(op, a, b, dtype)
+        got, _, fam = run_engine(op, dtype, a, b)
+        assert fam in ("inner_vector_outer", "repeated_block"), fam
+        compare(op, dtype, got, want, "%s %s %s x %s" % (op, dtype, sa, sb))
