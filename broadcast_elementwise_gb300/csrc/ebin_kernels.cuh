@@ -91,6 +91,16 @@ __device__ __forceinline__ void st_stream(T *p, const Pack<T, G> &v) {
     }
 }
 
+// Programmatic dependent launch.  Every kernel first lets the next grid on its
+// stream be scheduled (it is launched once all CTAs of this grid have started),
+// then waits until the grids it depends on have finished and their memory is
+// visible, before its first global access.  The next kernel's launch then
+// overlaps this kernel's last wave instead of following its completion.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <class Op>
 __device__ __forceinline__ void flush_err(uint32_t *status, uint32_t err) {
     if constexpr (Op::kValidates) {
@@ -190,6 +200,7 @@ __device__ __forceinline__ int64_t udiv(int64_t n, int64_t d, const FastDiv &f, 
 // numel % G elements is finished element by element.
 template <class Op, int U>
 __global__ void __launch_bounds__(kThreads) k_contiguous(KArgs p) {
+    pdl_enter();
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
@@ -241,6 +252,7 @@ __global__ void __launch_bounds__(kThreads) k_contiguous(KArgs p) {
 // registers; operand order is preserved.
 template <class Op, bool SCALAR_A, int U>
 __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
+    pdl_enter();
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
@@ -331,6 +343,7 @@ struct RowArgs {
 // Pointers advance by constant steps from row to row.
 template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, bool PACKED>
 __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
+    pdl_enter();
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
@@ -485,6 +498,23 @@ KArgs kargs(const Launch &L) {
     return k;
 }
 
+// Launch with programmatic stream serialization (see pdl_enter).
+template <class... KParams, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KParams...), int64_t grid, int block, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kUnrollFlat = 2;
 constexpr int64_t kMaxGrid = 0x7FFFFFFF;
 
@@ -494,8 +524,7 @@ cudaError_t run_contiguous(const Launch &L) {
     const int64_t ng = L.numel / G;
     int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
     grid = std::min<int64_t>(grid, kMaxGrid);
-    k_contiguous<Op, kUnrollFlat><<<(unsigned)grid, kThreads, 0, L.stream>>>(kargs<Op>(L));
-    return cudaGetLastError();
+    return launch_pdl(k_contiguous<Op, kUnrollFlat>, grid, kThreads, L.stream, kargs<Op>(L));
 }
 
 template <class Op, bool SCALAR_A>
@@ -504,8 +533,7 @@ cudaError_t run_scalar(const Launch &L) {
     const int64_t ng = L.numel / G;
     int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
     grid = std::min<int64_t>(grid, kMaxGrid);
-    k_scalar<Op, SCALAR_A, kUnrollFlat><<<(unsigned)grid, kThreads, 0, L.stream>>>(kargs<Op>(L));
-    return cudaGetLastError();
+    return launch_pdl(k_scalar<Op, SCALAR_A, kUnrollFlat>, grid, kThreads, L.stream, kargs<Op>(L));
 }
 
 // Tile shape for a row traversal with rows of `cols` groups and V groups per
@@ -578,9 +606,8 @@ cudaError_t run_rows_kernel(const Launch &L) {
     const RowArgs r = row_args(L.g, G, V, L.num_sms);
     const int64_t tiles = row_tiles(r);
     if (tiles > kMaxGrid) return cudaErrorInvalidConfiguration;
-    k_rows<Op, G, IA, IB, NOPREFIX, V, PACKED>
-        <<<(unsigned)tiles, r.tpr * r.rs, 0, L.stream>>>(kargs<Op>(L), r);
-    return cudaGetLastError();
+    return launch_pdl(k_rows<Op, G, IA, IB, NOPREFIX, V, PACKED>, tiles, r.tpr * r.rs, L.stream,
+                      kargs<Op>(L), r);
 }
 
 // Column groups per thread per row (V), measured on GB300.  Outputs narrower

@@ -166,3 +166,27 @@ def test_mod_with_shared_divisor_is_exact(dtype):
             got, _, fam = run_engine("Mod", dtype, rows, bcol, attrs={"fmod": fmod})
             want, _ = oracle.run("Mod", rows, bcol, dtype, fmod=fmod)
             assert_bits_equal(got, want, dtype, "Mod rows %r fmod=%d" % (d, fmod))
+
+
+def test_chained_launches_see_previous_results():
+    """Back-to-back kernels overlap their launch with the previous kernel's
+    tail; each must still read the finished output of the one before."""
+    x = datagen.make("normal", "float32", (64, 4096), 5, 0)
+    bias = datagen.make("uniform", "float32", (4096,), 5, 1, lo=-0.5, hi=0.5)
+    scale = datagen.make("uniform", "float32", (64, 1), 5, 2, lo=0.5, hi=1.5)
+    want = x
+    for k in range(6):
+        want, _ = oracle.run("Add" if k % 2 == 0 else "Mul", want, bias if k % 2 == 0 else scale,
+                             "float32")
+    cur = to_device(x)
+    bufs = [torch.empty_like(cur) for _ in range(2)]
+    dB, dS = to_device(bias), to_device(scale)
+    p_add = eb.Plan(eb.descriptor("Add", "float32"), x.shape, bias.shape)
+    p_mul = eb.Plan(eb.descriptor("Mul", "float32"), x.shape, scale.shape)
+    for k in range(6):
+        out = bufs[k % 2]
+        eb.execute(p_add if k % 2 == 0 else p_mul, cur, dB if k % 2 == 0 else dS, out)
+        cur = out
+    torch.cuda.synchronize()
+    assert_bits_equal(cur.cpu().numpy().view(np.float32).reshape(want.shape), want, "float32",
+                      "six chained launches")
