@@ -42,7 +42,15 @@ namespace ebin {
 
 constexpr int kThreads = 256;
 
-template <class T, int G> struct alignas(sizeof(T) * G) Pack {
+// A pack of G elements is aligned to its size when that is a power of two up to
+// 16 bytes (so it moves as one vector access); other packs (parameter blocks)
+// keep the element's natural alignment.
+template <class T, int G> constexpr size_t pack_align() {
+    constexpr size_t n = sizeof(T) * G;
+    return (n <= 16 && (n & (n - 1)) == 0) ? n : alignof(T);
+}
+
+template <class T, int G> struct alignas(pack_align<T, G>()) Pack {
     T v[G];
 };
 
@@ -131,8 +139,7 @@ __device__ __forceinline__ void compute_group(const typename Op::In *a, const ty
                                               uint32_t &err) {
     if constexpr (SB && HasPrep<Op>::value) {
         const typename Op::PB pb = Op::prep(b[0]);
-#pragma unroll
-        for (int k = 0; k < G; ++k) o[k] = Op::apply_prep(a[SA ? 0 : k], pb, args, err);
+        Op::template apply_prep_group<G, SA>(a, pb, o, args, err);
     } else if constexpr (HasPack<Op>::value && G % 4 == 0) {
         if constexpr (SA || SB) {
             typename Op::In ta[G], tb[G];
@@ -288,8 +295,7 @@ __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
                 if constexpr (SCALAR_A) {
                     compute_group<Op, G, true, false>(&sa, d[u].v, o.v, p.args, err);
                 } else if constexpr (HasPrep<Op>::value) {
-#pragma unroll
-                    for (int k = 0; k < G; ++k) o.v[k] = Op::apply_prep(d[u].v[k], pb, p.args, err);
+                    Op::template apply_prep_group<G, false>(d[u].v, pb, o.v, p.args, err);
                 } else {
                     compute_group<Op, G, false, true>(d[u].v, &sb, o.v, p.args, err);
                 }

@@ -233,6 +233,32 @@ template <class T> struct OpMod : PlainB<T, T> {
                                                    uint32_t &) {
         return Tr<T>::out(floor_adjust(fmod_prepared(Tr<T>::in(a), pb), pb.b, p.fmod));
     }
+    // G elements at once: the fast path for all of them without branches, and
+    // one uniform branch to the exact fmod if any element needs it.
+    template <int G, bool SA>
+    __device__ __forceinline__ static void apply_prep_group(const T *a, const ModPrep &pb, T *o,
+                                                            const OpArgs &p, uint32_t &) {
+        float x[G], r[G];
+        bool slow = !pb.fast;
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+            x[k] = Tr<T>::in(a[SA ? 0 : k]);
+            const float aa = fabsf(x[k]);
+            const float q = truncf(__fmul_rn(aa, pb.rcp));
+            float rr = fmaf(-q, pb.ab, aa);
+            rr = rr < 0.0f ? __fadd_rn(rr, pb.ab) : rr;
+            rr = rr >= pb.ab ? fmaf(-__fadd_rn(q, 1.0f), pb.ab, aa) : rr;
+            const bool small = aa < pb.ab;
+            r[k] = small ? x[k] : copysignf(rr, x[k]);
+            slow = slow | (!small & !((aa < INFINITY) & (q < 4194304.0f)));
+        }
+        if (slow) {
+#pragma unroll
+            for (int k = 0; k < G; ++k) r[k] = fmod_exact(x[k], pb.b);
+        }
+#pragma unroll
+        for (int k = 0; k < G; ++k) o[k] = Tr<T>::out(floor_adjust(r[k], pb.b, p.fmod));
+    }
 };
 
 template <class T> struct OpPow : PlainB<T, T> {
@@ -385,7 +411,9 @@ template <class T> struct OpPRelu : PlainB<T, T> {
 // Inference BatchNormalization: y = (x - mean) / sqrt(var + eps) * scale + bias,
 // each step rounded in binary32 in the order written.  B holds four rows
 // (scale, bias, mean, var) of `plane` elements; the per-channel sqrt is formed
-// when the parameters are loaded.
+// when the parameters are loaded.  (A per-channel reciprocal with a
+// remainder-checked correction was measured slower than the IEEE divide on
+// GB300, so the divide stays.)
 struct BNParams {
     float scale, bias, mean, d;
 };

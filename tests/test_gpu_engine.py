@@ -190,3 +190,32 @@ def test_chained_launches_see_previous_results():
     torch.cuda.synchronize()
     assert_bits_equal(cur.cpu().numpy().view(np.float32).reshape(want.shape), want, "float32",
                       "six chained launches")
+
+
+@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
+def test_batchnorm_division_is_exact(dtype):
+    """BatchNormalization divides by one prepared value per channel: stress the
+    proof-checked fast division and its fallback with channel divisors across
+    the exponent range (and 0, NaN, infinity) and raw-bit-pattern inputs."""
+    var = np.array([1.0, 3.0, 0.0, -1.0, 1e-30, 1e30, 2.0 ** -80, 2.0 ** 90, 0.75, 1e-6,
+                    np.inf, np.nan, 5.0, 0.2, 123456.0, 7e-3], np.float32)
+    C = var.size
+    eps = 0.0 if dtype == "float32" else 1e-5
+    mean = np.array([0.0, 1.0, -2.0, 0.5, 0.0, 3.0, -0.0, 1e20, 0.25, -1e-3, 0.0, 1.0, 7.0,
+                     -3.0, 0.0, 0.5], np.float32)
+    scale = np.array([1.0, 2.0, -1.0, 0.5, 1.0, 1e-3, 3.0, 1.0, -2.0, 1.0, 1.0, 1.0, 0.1,
+                      1.0, 1e10, 1.0], np.float32)
+    bias = np.array([-0.0, 0.5, 0.0, 1.0, -0.0, 2.0, -1.0, 0.0, 0.0, 4.0, 0.0, 0.0, -0.5,
+                     0.0, 1.0, -0.0], np.float32)
+    params = datagen.float_to(np.stack([scale, bias, mean, var]), dtype)
+    x = np.concatenate([datagen.make("bits", dtype, (2, C, 512), 80, 0).reshape(-1),
+                        datagen.make("normal", dtype, (2, C, 512), 80, 1).reshape(-1)])
+    x = x.reshape(4, C, 512)
+    got, _, fam = run_engine("BatchNormalization", dtype, x, params, attrs={"epsilon": eps})
+    want, _ = oracle.run("BatchNormalization", x, params, dtype, eps=eps)
+    assert fam == "inner_vector_outer"
+    assert_bits_equal(got, want, dtype, "BN per-channel rows")
+    x2 = x.reshape(4 * 512, C)   # rank 2: one parameter set per element
+    got, _, _ = run_engine("BatchNormalization", dtype, x2, params, attrs={"epsilon": eps})
+    want, _ = oracle.run("BatchNormalization", x2, params, dtype, eps=eps)
+    assert_bits_equal(got, want, dtype, "BN rank-2")
