@@ -207,6 +207,73 @@ __device__ __forceinline__ float floor_adjust(float r, float b, int fmod_flag) {
     return r;
 }
 
+// An int32 divisor shared by many elements is prepared once: d = |b| and
+// m0 = trunc(2^32 * rcp_rz(float_ru(d))) <= 2^32 / d (every rounding is toward
+// the underestimate; 2^32 itself saturates to 2^32 - 1), within a relative
+// 2^-22 plus one unit of 2^32 / d.  For n = |a| <= 2^31:
+//   q1 = mulhi(n, m0) <= floor(n/d) and misses it by less than n*2^-22/d + 1.5,
+//   so r1 = n - q1*d lies in [0, 2d + 2^9) and fits 32 bits (for d > 2^30 the
+//   miss is at most 1 and r1 < 2d <= 2^32);
+//   q2 = mulhi(r1, m0) misses floor(r1/d) by at most 1, so r2 = r1 - q2*d lies
+//   in [0, 2d), and min(r2, r2 - d) taken unsigned (r2 - d wraps above r2
+//   when r2 < d) is n mod d.
+// Then the truncated remainder is +-(n mod d) with the dividend's sign, and
+// the floor remainder is the magnitude x = n mod d, or d - x when that is
+// nonzero and the signs differ, with the divisor's sign.
+struct IModPrep {
+    int32_t b;
+    uint32_t d, nd, m0;
+    int32_t sb;     // 0 or -1: the divisor's sign as a mask
+    bool zero;
+};
+
+__device__ __forceinline__ IModPrep imod_prep(int32_t b) {
+    IModPrep p;
+    p.b = b;
+    p.d = b < 0 ? 0u - (uint32_t)b : (uint32_t)b;
+    p.nd = 0u - p.d;
+    p.sb = b >> 31;
+    p.zero = b == 0;
+    const float r = __frcp_rz(__uint2float_ru(p.zero ? 1u : p.d));
+    p.m0 = __float2uint_rz(r * 4294967296.0f);
+    return p;
+}
+
+__device__ __forceinline__ uint32_t umod_prepared(uint32_t n, const IModPrep &p) {
+    const uint32_t r1 = n + __umulhi(n, p.m0) * p.nd;
+    const uint32_t r2 = r1 + __umulhi(r1, p.m0) * p.nd;
+    return umin(r2, r2 + p.nd);
+}
+
+// Truncated remainder (fmod=1) and floor remainder (fmod=0) of int32 a by the
+// prepared nonzero divisor.
+// |a| as unsigned; PTX abs.s32 leaves INT_MIN as is, whose bits read 2^31.
+__device__ __forceinline__ uint32_t uabs32(int32_t a) {
+    int32_t r;
+    asm("abs.s32 %0, %1;" : "=r"(r) : "r"(a));
+    return (uint32_t)r;
+}
+// (Sign flips are done unsigned: (v ^ s) - s negates v when s = -1.)
+__device__ __forceinline__ int32_t imod_trunc(int32_t a, const IModPrep &p) {
+    const uint32_t sa = (uint32_t)(a >> 31);
+    const uint32_t x = umod_prepared(uabs32(a), p);
+    return (int32_t)((x ^ sa) - sa);
+}
+__device__ __forceinline__ int32_t imod_floor(int32_t a, const IModPrep &p) {
+    const uint32_t x = umod_prepared(uabs32(a), p);
+    const uint32_t y = (x != 0u && (a ^ p.b) < 0) ? p.d - x : x;
+    return (int32_t)((y ^ (uint32_t)p.sb) - (uint32_t)p.sb);
+}
+// The floor remainder for a divisor known positive / known negative.
+__device__ __forceinline__ int32_t imod_floor_pos(int32_t a, const IModPrep &p) {
+    const uint32_t x = umod_prepared(uabs32(a), p);
+    return (int32_t)((a < 0 && x != 0u) ? p.d - x : x);
+}
+__device__ __forceinline__ int32_t imod_floor_neg(int32_t a, const IModPrep &p) {
+    const uint32_t x = umod_prepared(uabs32(a), p);
+    return (int32_t)((a > 0 && x != 0u) ? x - p.d : 0u - x);
+}
+
 template <class T> struct OpMod : PlainB<T, T> {
     static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
     static constexpr bool kValidates = is_int_v<T>;
@@ -225,39 +292,68 @@ template <class T> struct OpMod : PlainB<T, T> {
             }
         }
     }
-    // floating Mod with a divisor shared by a whole group (see ModPrep)
-    static constexpr bool kPrep = is_float_v<T>;
-    using PB = ModPrep;
-    __device__ __forceinline__ static ModPrep prep(T b) { return mod_prep(Tr<T>::in(b)); }
-    __device__ __forceinline__ static T apply_prep(T a, const ModPrep &pb, const OpArgs &p,
-                                                   uint32_t &) {
-        return Tr<T>::out(floor_adjust(fmod_prepared(Tr<T>::in(a), pb), pb.b, p.fmod));
+    // Mod with a divisor shared by a whole group: floating (see ModPrep) and
+    // int32 (see IModPrep)
+    static constexpr bool kPrep = is_float_v<T> || std::is_same_v<T, int32_t>;
+    using PB = std::conditional_t<std::is_same_v<T, int32_t>, IModPrep, ModPrep>;
+    __device__ __forceinline__ static PB prep(T b) {
+        if constexpr (std::is_same_v<T, int32_t>) return imod_prep(b);
+        else return mod_prep(Tr<T>::in(b));
     }
-    // G elements at once: the fast path for all of them without branches, and
-    // one uniform branch to the exact fmod if any element needs it.
+    __device__ __forceinline__ static T apply_prep(T a, const PB &pb, const OpArgs &p,
+                                                   uint32_t &err) {
+        if constexpr (std::is_same_v<T, int32_t>) {
+            if (pb.zero) { err |= kErrDivByZero; return (T)0; }
+            return p.fmod ? imod_trunc(a, pb) : imod_floor(a, pb);
+        } else {
+            return Tr<T>::out(floor_adjust(fmod_prepared(Tr<T>::in(a), pb), pb.b, p.fmod));
+        }
+    }
+    // G elements at once.  Floating: the fast path for all of them without
+    // branches, and one uniform branch to the exact fmod if any element needs
+    // it.  int32: the prepared remainder for each.
     template <int G, bool SA>
-    __device__ __forceinline__ static void apply_prep_group(const T *a, const ModPrep &pb, T *o,
-                                                            const OpArgs &p, uint32_t &) {
-        float x[G], r[G];
-        bool slow = !pb.fast;
+    __device__ __forceinline__ static void apply_prep_group(const T *a, const PB &pb, T *o,
+                                                            const OpArgs &p, uint32_t &err) {
+        if constexpr (std::is_same_v<T, int32_t>) {
+            if (pb.zero) {
+                err |= kErrDivByZero;
 #pragma unroll
-        for (int k = 0; k < G; ++k) {
-            x[k] = Tr<T>::in(a[SA ? 0 : k]);
-            const float aa = fabsf(x[k]);
-            const float q = truncf(__fmul_rn(aa, pb.rcp));
-            float rr = fmaf(-q, pb.ab, aa);
-            rr = rr < 0.0f ? __fadd_rn(rr, pb.ab) : rr;
-            rr = rr >= pb.ab ? fmaf(-__fadd_rn(q, 1.0f), pb.ab, aa) : rr;
-            const bool small = aa < pb.ab;
-            r[k] = small ? x[k] : copysignf(rr, x[k]);
-            slow = slow | (!small & !((aa < INFINITY) & (q < 4194304.0f)));
+                for (int k = 0; k < G; ++k) o[k] = 0;
+                return;
+            }
+            if (p.fmod) {
+#pragma unroll
+                for (int k = 0; k < G; ++k) o[k] = imod_trunc(a[SA ? 0 : k], pb);
+            } else if (pb.sb == 0) {
+#pragma unroll
+                for (int k = 0; k < G; ++k) o[k] = imod_floor_pos(a[SA ? 0 : k], pb);
+            } else {
+#pragma unroll
+                for (int k = 0; k < G; ++k) o[k] = imod_floor_neg(a[SA ? 0 : k], pb);
+            }
+        } else {
+            float x[G], r[G];
+            bool slow = !pb.fast;
+#pragma unroll
+            for (int k = 0; k < G; ++k) {
+                x[k] = Tr<T>::in(a[SA ? 0 : k]);
+                const float aa = fabsf(x[k]);
+                const float q = truncf(__fmul_rn(aa, pb.rcp));
+                float rr = fmaf(-q, pb.ab, aa);
+                rr = rr < 0.0f ? __fadd_rn(rr, pb.ab) : rr;
+                rr = rr >= pb.ab ? fmaf(-__fadd_rn(q, 1.0f), pb.ab, aa) : rr;
+                const bool small = aa < pb.ab;
+                r[k] = small ? x[k] : copysignf(rr, x[k]);
+                slow = slow | (!small & !((aa < INFINITY) & (q < 4194304.0f)));
+            }
+            if (slow) {
+#pragma unroll
+                for (int k = 0; k < G; ++k) r[k] = fmod_exact(x[k], pb.b);
+            }
+#pragma unroll
+            for (int k = 0; k < G; ++k) o[k] = Tr<T>::out(floor_adjust(r[k], pb.b, p.fmod));
         }
-        if (slow) {
-#pragma unroll
-            for (int k = 0; k < G; ++k) r[k] = fmod_exact(x[k], pb.b);
-        }
-#pragma unroll
-        for (int k = 0; k < G; ++k) o[k] = Tr<T>::out(floor_adjust(r[k], pb.b, p.fmod));
     }
 };
 

@@ -168,6 +168,45 @@ def test_mod_with_shared_divisor_is_exact(dtype):
             assert_bits_equal(got, want, dtype, "Mod rows %r fmod=%d" % (d, fmod))
 
 
+def test_int32_mod_with_shared_divisor_is_exact():
+    """int32 scalar and per-row divisors take the prepared multiply-high path:
+    stress it with divisors across the range (1, -1, powers of two and their
+    neighbours, 2^31 - 1, INT_MIN) and dividends at the extremes, at multiples
+    of the divisor and one either side, and raw bit patterns."""
+    i32 = np.iinfo(np.int32)
+    divisors = [1, -1, 2, -2, 3, 7, -7, 10, 1000, -999, 65535, 65536, 65537, (1 << 24) + 1,
+                (1 << 30) - 1, 1 << 30, i32.max, -i32.max, i32.min, 123456789, -987654321]
+    rng = np.random.default_rng(123)
+    for i, d in enumerate(divisors):
+        k = rng.integers(-(2 ** 31) // max(abs(d), 1), 2 ** 31 // max(abs(d), 1), 2048,
+                         dtype=np.int64)
+        cand = np.concatenate([k * d, k * d + 1, k * d - 1,
+                               [i32.min, i32.max, i32.min + 1, 0, 1, -1, d, -d if d != i32.min
+                                else 0]])
+        cand = cand[(cand >= i32.min) & (cand <= i32.max)].astype(np.int32)
+        a = np.concatenate([cand, datagen.make("bits", "int32", (4096,), 71, i)])
+        a = a[: (a.size // 256) * 256]             # rows of a multiple of 4 elements
+        bq = np.array([d], np.int32)
+        for fmod in (0, 1):
+            got, bits, fam = run_engine("Mod", "int32", a, bq.reshape(()), attrs={"fmod": fmod})
+            want, wbits = oracle.run("Mod", a, bq.reshape(()), "int32", fmod=fmod)
+            assert fam == "right_scalar" and bits == wbits == 0
+            assert_bits_equal(got, want, "int32", "Mod int32 scalar %d fmod=%d" % (d, fmod))
+            rows = a.reshape(64, -1)
+            bcol = np.repeat(bq, 64).reshape(64, 1)
+            got, _, fam = run_engine("Mod", "int32", rows, bcol, attrs={"fmod": fmod})
+            want, _ = oracle.run("Mod", rows, bcol, "int32", fmod=fmod)
+            assert fam == "repeated_block"
+            assert_bits_equal(got, want, "int32", "Mod int32 rows %d fmod=%d" % (d, fmod))
+    # a zero divisor among per-row divisors: that row reads 0 and the status is set
+    rows = datagen.make("bits", "int32", (8, 512), 72, 0)
+    bcol = np.array([3, -5, 0, 7, 1, -1, 100, 9], np.int32).reshape(8, 1)
+    got, bits, _ = run_engine("Mod", "int32", rows, bcol, attrs={"fmod": 0})
+    want, wbits = oracle.run("Mod", rows, bcol, "int32", fmod=0)
+    assert bits == wbits == eb.DEVICE_DIV_BY_ZERO
+    assert_bits_equal(got, want, "int32", "Mod int32 rows with a zero divisor")
+
+
 def test_chained_launches_see_previous_results():
     """Back-to-back kernels overlap their launch with the previous kernel's
     tail; each must still read the finished output of the one before."""
