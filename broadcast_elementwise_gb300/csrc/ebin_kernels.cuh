@@ -122,7 +122,7 @@ template <class Op>
 struct HasPack<Op, std::void_t<decltype(Op::kPack)>> : std::bool_constant<Op::kPack> {};
 
 // Operators that prepare a B shared by many elements (Op::kPrep, Op::prep,
-// Op::apply_prep) -- e.g. the reciprocal of a Mod divisor.
+// Op::apply_prep_group) -- e.g. the reciprocal of a Mod divisor.
 template <class Op, class = void> struct HasPrep : std::false_type {};
 template <class Op>
 struct HasPrep<Op, std::void_t<decltype(Op::kPrep)>> : std::bool_constant<Op::kPrep> {};

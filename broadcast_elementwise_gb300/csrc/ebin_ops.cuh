@@ -162,17 +162,26 @@ template <class T, int K> struct OpArith : PlainB<T, T> {
     }
 };
 
-// A divisor that stays the same for many elements (a scalar, or one value per
-// row) is prepared once: with r = RN(1/|b|), q = trunc(|a| * r) is within one
-// of n = trunc(|a|/|b|) whenever |a|/|b| < 2^22 (two roundings of relative
-// size 2^-24 each).  fmaf(-q, |b|, |a|) is exact for q = n and for q = n + 1
-// (the results are multiples of ulp(|b|) below |b| in magnitude); a negative
-// result takes |b| back (exact), and a result >= |b| means q = n - 1, which is
-// redone with n (exact).  Anything outside that range -- NaN, infinities, zero
-// or subnormal divisors, huge quotients -- goes to fmod_exact.
+// A floating divisor that stays the same for many elements (a scalar, or one
+// value per row) is prepared once: ab = |b|, rcp = RD(1/ab) and
+// lim = RN(2^21 * ab) (exact, or infinity when ab > 2^107, where every finite
+// |a| / ab is below 2^21 anyway).  For |a| < lim:
+//   p = RD(|a| * rcp) <= |a|/ab and, with two downward roundings of relative
+//   size 2^-23, p > |a|/ab - 1/2, so q = trunc(p) is n = trunc(|a|/ab) or n - 1;
+//   r0 = fmaf(-q, ab, |a|) and r1 = fmaf(-(q + 1), ab, |a|) (q + 1 exact): for
+//   q = n, r0 is the remainder and r1 = r0 - ab < 0; for q = n - 1, r1 is the
+//   remainder (>= 0).  Each value that is used is a multiple of ulp(ab) of
+//   magnitude at most ab (|a| >= ab makes |a| a multiple of ulp(ab)), hence
+//   representable, and each FMA rounds once, so it is exact.  |a| < ab needs no
+//   special case (q = 0, r0 = |a|).
+// The truncated remainder is then that magnitude with the dividend's sign; the
+// floor rule adds b to a nonzero remainder of the other sign (one rounded
+// operation) and gives an exact zero the divisor's sign.  Zero, subnormal,
+// huge, infinite or NaN divisors, NaN or infinite dividends and quotients of
+// 2^21 or more take the exact general path (mod_float) for the whole group.
 struct ModPrep {
-    float b, ab, rcp;
-    bool fast;
+    float b, ab, rcp, lim;
+    bool fast, neg;
 };
 
 __device__ __forceinline__ ModPrep mod_prep(float b) {
@@ -180,31 +189,10 @@ __device__ __forceinline__ ModPrep mod_prep(float b) {
     p.b = b;
     p.ab = fabsf(b);
     p.fast = p.ab >= 0x1p-125f && p.ab <= 0x1p125f;   // excludes 0, subnormals, inf, NaN
-    p.rcp = __frcp_rn(p.ab);
+    p.neg = signbit(b);
+    p.rcp = __frcp_rd(p.fast ? p.ab : 1.0f);
+    p.lim = __fmul_rn(p.ab, 2097152.0f);
     return p;
-}
-
-__device__ __forceinline__ float fmod_prepared(float a, const ModPrep &p) {
-    const float aa = fabsf(a);
-    if (aa < p.ab) return a;
-    if (p.fast && aa < INFINITY) {
-        const float q = truncf(__fmul_rn(aa, p.rcp));
-        if (q < 4194304.0f) {
-            float r = fmaf(-q, p.ab, aa);
-            if (r < 0.0f) r = __fadd_rn(r, p.ab);
-            else if (r >= p.ab) r = fmaf(-__fadd_rn(q, 1.0f), p.ab, aa);
-            return copysignf(r, a);
-        }
-    }
-    return fmod_exact(a, p.b);
-}
-
-// fmod=1: truncated remainder as is; fmod=0: floor rule of opset 28
-__device__ __forceinline__ float floor_adjust(float r, float b, int fmod_flag) {
-    if (fmod_flag) return r;
-    if (r == 0.0f) return copysignf(0.0f, b);
-    if (signbit(r) != signbit(b)) r = __fadd_rn(r, b);
-    return r;
 }
 
 // An int32 divisor shared by many elements is prepared once: d = |b| and
@@ -245,24 +233,18 @@ __device__ __forceinline__ uint32_t umod_prepared(uint32_t n, const IModPrep &p)
     return umin(r2, r2 + p.nd);
 }
 
-// Truncated remainder (fmod=1) and floor remainder (fmod=0) of int32 a by the
-// prepared nonzero divisor.
 // |a| as unsigned; PTX abs.s32 leaves INT_MIN as is, whose bits read 2^31.
 __device__ __forceinline__ uint32_t uabs32(int32_t a) {
     int32_t r;
     asm("abs.s32 %0, %1;" : "=r"(r) : "r"(a));
     return (uint32_t)r;
 }
-// (Sign flips are done unsigned: (v ^ s) - s negates v when s = -1.)
+// Truncated remainder (fmod=1) of int32 a by the prepared nonzero divisor.
+// (The sign flip is done unsigned: (v ^ s) - s negates v when s = -1.)
 __device__ __forceinline__ int32_t imod_trunc(int32_t a, const IModPrep &p) {
     const uint32_t sa = (uint32_t)(a >> 31);
     const uint32_t x = umod_prepared(uabs32(a), p);
     return (int32_t)((x ^ sa) - sa);
-}
-__device__ __forceinline__ int32_t imod_floor(int32_t a, const IModPrep &p) {
-    const uint32_t x = umod_prepared(uabs32(a), p);
-    const uint32_t y = (x != 0u && (a ^ p.b) < 0) ? p.d - x : x;
-    return (int32_t)((y ^ (uint32_t)p.sb) - (uint32_t)p.sb);
 }
 // The floor remainder for a divisor known positive / known negative.
 __device__ __forceinline__ int32_t imod_floor_pos(int32_t a, const IModPrep &p) {
@@ -300,18 +282,9 @@ template <class T> struct OpMod : PlainB<T, T> {
         if constexpr (std::is_same_v<T, int32_t>) return imod_prep(b);
         else return mod_prep(Tr<T>::in(b));
     }
-    __device__ __forceinline__ static T apply_prep(T a, const PB &pb, const OpArgs &p,
-                                                   uint32_t &err) {
-        if constexpr (std::is_same_v<T, int32_t>) {
-            if (pb.zero) { err |= kErrDivByZero; return (T)0; }
-            return p.fmod ? imod_trunc(a, pb) : imod_floor(a, pb);
-        } else {
-            return Tr<T>::out(floor_adjust(fmod_prepared(Tr<T>::in(a), pb), pb.b, p.fmod));
-        }
-    }
-    // G elements at once.  Floating: the fast path for all of them without
-    // branches, and one uniform branch to the exact fmod if any element needs
-    // it.  int32: the prepared remainder for each.
+    // G elements at once, all taking the fast path without branches, with one
+    // uniform branch per group to the general path and one on the divisor's
+    // sign and the fmod attribute.
     template <int G, bool SA>
     __device__ __forceinline__ static void apply_prep_group(const T *a, const PB &pb, T *o,
                                                             const OpArgs &p, uint32_t &err) {
@@ -334,25 +307,32 @@ template <class T> struct OpMod : PlainB<T, T> {
             }
         } else {
             float x[G], r[G];
-            bool slow = !pb.fast;
+            bool ok = pb.fast;
 #pragma unroll
             for (int k = 0; k < G; ++k) {
                 x[k] = Tr<T>::in(a[SA ? 0 : k]);
                 const float aa = fabsf(x[k]);
-                const float q = truncf(__fmul_rn(aa, pb.rcp));
-                float rr = fmaf(-q, pb.ab, aa);
-                rr = rr < 0.0f ? __fadd_rn(rr, pb.ab) : rr;
-                rr = rr >= pb.ab ? fmaf(-__fadd_rn(q, 1.0f), pb.ab, aa) : rr;
-                const bool small = aa < pb.ab;
-                r[k] = small ? x[k] : copysignf(rr, x[k]);
-                slow = slow | (!small & !((aa < INFINITY) & (q < 4194304.0f)));
+                ok = ok & (aa < pb.lim);
+                const float q = truncf(__fmul_rd(aa, pb.rcp));
+                const float r0 = fmaf(-q, pb.ab, aa);
+                const float r1 = fmaf(-__fadd_rn(q, 1.0f), pb.ab, aa);
+                r[k] = r1 < 0.0f ? r0 : r1;
             }
-            if (slow) {
+            if (!ok) {
 #pragma unroll
-                for (int k = 0; k < G; ++k) r[k] = fmod_exact(x[k], pb.b);
+                for (int k = 0; k < G; ++k) o[k] = Tr<T>::out(mod_float(x[k], pb.b, p.fmod));
+            } else if (p.fmod) {
+#pragma unroll
+                for (int k = 0; k < G; ++k) o[k] = Tr<T>::out(copysignf(r[k], x[k]));
+            } else if (!pb.neg) {
+#pragma unroll
+                for (int k = 0; k < G; ++k)
+                    o[k] = Tr<T>::out((x[k] < 0.0f && r[k] != 0.0f) ? __fsub_rn(pb.ab, r[k]) : r[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < G; ++k)
+                    o[k] = Tr<T>::out((x[k] > 0.0f && r[k] != 0.0f) ? __fsub_rn(r[k], pb.ab) : -r[k]);
             }
-#pragma unroll
-            for (int k = 0; k < G; ++k) o[k] = Tr<T>::out(floor_adjust(r[k], pb.b, p.fmod));
         }
     }
 };
