@@ -359,7 +359,8 @@ def run_ours(args, dist: Dist):
         e2e = {"value": round(aggregate(bytes_per_step * args.e2e_steps, dist.world, e2e_s), 1),
                "unit": UNIT, "h2d_bytes_per_step": 4 * n * 4, "d2h_bytes_per_step": 2 * n * 4,
                "steps": args.e2e_steps,
-               "api": "ebin_execute_host (pinned host buffers, copies on the stream)"}
+               "api": "ebin_execute_host (pinned host buffers; contiguous plans pipelined in "
+                      "chunks over two copy streams)"}
         del hA, hBm, hBd, hOm, hOd
 
     # the oracle on a bounded sample, host cores, rank 0 only

@@ -523,11 +523,12 @@ cudaError_t ebin::launch(const Launch &L) {
 #undef EBIN_PICK
 }
 
-extern "C" ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
-                                    void *stream) {
-    if (!plan) return EBIN_ERR_INVALID_ARG;
-    const ebin_plan_s &p = *plan;
-    if (p.numel == 0) return EBIN_OK;  // empty dims: no work, nothing read
+namespace {
+
+// Checks and launch description shared by the execute entry points: the
+// buffer, alias and alignment rules of ebin_execute, and the status word.
+ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, void *out,
+                           cudaStream_t s, ebin::Launch &L) {
     const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max);
     if (!A || !out || (b_needed && !B)) return EBIN_ERR_INVALID_ARG;
 
@@ -546,9 +547,7 @@ extern "C" ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void 
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return EBIN_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    ebin::Launch L{};
+    L = ebin::Launch{};
     L.op = p.op;
     L.dt = dt_class(p.dt);
     L.family = p.family;
@@ -579,10 +578,85 @@ extern "C" ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void 
                              ((uintptr_t)out % out_align == 0);
         if (!aligned) L.family = ebin::FAM_GENERAL_STRIDED;
     }
+    return EBIN_OK;
+}
+
+ebin_status launch_counted(const ebin::Launch &L) {
     const cudaError_t e = ebin::launch(L);
     g_launches.fetch_add(1);
     return e == cudaSuccess ? EBIN_OK : EBIN_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
+                                    void *stream) {
+    if (!plan) return EBIN_ERR_INVALID_ARG;
+    const ebin_plan_s &p = *plan;
+    if (p.numel == 0) return EBIN_OK;  // empty dims: no work, nothing read
+    ebin::Launch L;
+    const ebin_status st = prepare_launch(p, A, B, out, static_cast<cudaStream_t>(stream), L);
+    if (st != EBIN_OK) return st;
+    return launch_counted(L);
+}
+
+namespace {
+
+// Host-buffer pipeline of one device: an input-copy and an output-copy stream
+// beside the caller's, and reusable events.  Created on first use, kept until
+// the process exits; `mu` makes one call's enqueue sequence atomic.
+constexpr int kPipeChunks = 32;                 // at most this many chunks per call
+constexpr int64_t kPipeMinChunk = int64_t(1) << 20;   // elements
+constexpr int64_t kPipeGrain = 4096;            // chunk sizes are multiples of this
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t copied[kPipeChunks] = {}, computed[kPipeChunks] = {};
+};
+HostPipe g_pipes[128];
+
+HostPipe *host_pipe(int dev) {
+    if (dev < 0 || dev >= 128) return nullptr;
+    HostPipe &h = g_pipes[dev];
+    std::lock_guard<std::mutex> lk(h.mu);
+    if (h.ready) return &h;
+    const unsigned ev = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.start, ev) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.done, ev) == cudaSuccess;
+    for (int c = 0; ok && c < kPipeChunks; ++c)
+        ok = cudaEventCreateWithFlags(&h.copied[c], ev) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h.computed[c], ev) == cudaSuccess;
+    if (!ok) return nullptr;   // partially created handles stay unused
+    h.ready = true;
+    return &h;
+}
+
+// Copies in, kernel, copies out, one after the other on the caller's stream.
+ebin_status host_serial(const ebin_plan_s &p, const ebin::Launch &L, const void *host_a,
+                        const void *host_b, void *host_out, void *dev_a, void *dev_b,
+                        void *dev_out, cudaStream_t s) {
+    const size_t isz = ebin_dtype_size(p.dt);
+    if (cudaMemcpyAsync(dev_a, host_a, (size_t)p.numel_a * isz, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return EBIN_ERR_CUDA;
+    if (host_b && dev_b && p.numel_b > 0) {
+        if (cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+            return EBIN_ERR_CUDA;
+    }
+    const ebin_status st = launch_counted(L);
+    if (st != EBIN_OK) return st;
+    if (cudaMemcpyAsync(host_out, dev_out, (size_t)p.numel * ebin_dtype_size(p.out_dt),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return EBIN_ERR_CUDA;
+    return EBIN_OK;
+}
+
+}  // namespace
 
 extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, const void *host_b,
                                          void *host_out, void *dev_a, void *dev_b, void *dev_out,
@@ -591,20 +665,74 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
     const ebin_plan_s &p = *plan;
     if (p.numel == 0) return EBIN_OK;
     if (!host_a || !host_out || !dev_a || !dev_out) return EBIN_ERR_INVALID_ARG;
+    if (host_b && !dev_b) return EBIN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t isz = ebin_dtype_size(p.dt);
-    if (cudaMemcpyAsync(dev_a, host_a, (size_t)p.numel_a * isz, cudaMemcpyHostToDevice, s) !=
-        cudaSuccess)
+    ebin::Launch L;
+    ebin_status st = prepare_launch(p, dev_a, host_b ? dev_b : nullptr, dev_out, s, L);
+    if (st != EBIN_OK) return st;
+
+    // Streaming families whose output range [o, o+n) reads only the same range
+    // of each dense operand (and all of a scalar one) run as a pipeline of
+    // chunks: chunk c+1 is copied in while chunk c computes and chunk c-1 is
+    // copied out, on two copy streams beside the caller's.
+    const bool streaming = L.family == ebin::FAM_CONTIGUOUS ||
+                           L.family == ebin::FAM_LEFT_SCALAR ||
+                           L.family == ebin::FAM_RIGHT_SCALAR;
+    int dev = 0;
+    HostPipe *hp = nullptr;
+    if (streaming && p.numel >= 2 * kPipeMinChunk && cudaGetDevice(&dev) == cudaSuccess)
+        hp = host_pipe(dev);
+    if (!hp) return host_serial(p, L, host_a, host_b, host_out, dev_a, dev_b, dev_out, s);
+
+    const size_t isz = ebin_dtype_size(p.dt), osz = ebin_dtype_size(p.out_dt);
+    const bool a_dense = p.numel_a == p.numel, b_dense = p.numel_b == p.numel;
+    const int64_t want = std::max(kPipeMinChunk, (p.numel + kPipeChunks - 1) / kPipeChunks);
+    const int64_t chunk = (want + kPipeGrain - 1) / kPipeGrain * kPipeGrain;
+    const int nchunks = (int)((p.numel + chunk - 1) / chunk);
+
+    std::lock_guard<std::mutex> lk(hp->mu);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // the copy streams start after everything already queued on the caller's
+    if (!ok(cudaEventRecord(hp->start, s)) || !ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
+        !ok(cudaStreamWaitEvent(hp->out, hp->start, 0)))
         return EBIN_ERR_CUDA;
-    if (host_b && dev_b) {
-        if (cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess)
+    // a scalar operand is copied whole, first
+    if (!a_dense && !ok(cudaMemcpyAsync(dev_a, host_a, (size_t)p.numel_a * isz,
+                                        cudaMemcpyHostToDevice, hp->in)))
+        return EBIN_ERR_CUDA;
+    if (host_b && !b_dense && p.numel_b > 0 &&
+        !ok(cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz, cudaMemcpyHostToDevice,
+                            hp->in)))
+        return EBIN_ERR_CUDA;
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t off = (int64_t)c * chunk;
+        const int64_t n = std::min(chunk, p.numel - off);
+        const size_t ib = (size_t)off * isz, nb = (size_t)n * isz;
+        if (a_dense && !ok(cudaMemcpyAsync((char *)dev_a + ib, (const char *)host_a + ib, nb,
+                                           cudaMemcpyHostToDevice, hp->in)))
+            return EBIN_ERR_CUDA;
+        if (host_b && b_dense &&
+            !ok(cudaMemcpyAsync((char *)dev_b + ib, (const char *)host_b + ib, nb,
+                                cudaMemcpyHostToDevice, hp->in)))
+            return EBIN_ERR_CUDA;
+        if (!ok(cudaEventRecord(hp->copied[c], hp->in)) ||
+            !ok(cudaStreamWaitEvent(s, hp->copied[c], 0)))
+            return EBIN_ERR_CUDA;
+        ebin::Launch Lc = L;
+        Lc.numel = n;
+        Lc.A = a_dense ? (const void *)((const char *)dev_a + ib) : dev_a;
+        Lc.B = (host_b && b_dense) ? (const void *)((const char *)dev_b + ib) : L.B;
+        Lc.out = (char *)dev_out + (size_t)off * osz;
+        if ((st = launch_counted(Lc)) != EBIN_OK) return st;
+        if (!ok(cudaEventRecord(hp->computed[c], s)) ||
+            !ok(cudaStreamWaitEvent(hp->out, hp->computed[c], 0)) ||
+            !ok(cudaMemcpyAsync((char *)host_out + (size_t)off * osz,
+                                (const char *)dev_out + (size_t)off * osz, (size_t)n * osz,
+                                cudaMemcpyDeviceToHost, hp->out)))
             return EBIN_ERR_CUDA;
     }
-    const ebin_status st = ebin_execute(plan, dev_a, dev_b, dev_out, stream);
-    if (st != EBIN_OK) return st;
-    if (cudaMemcpyAsync(host_out, dev_out, (size_t)p.numel * ebin_dtype_size(p.out_dt),
-                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    // the caller's stream completes only after the last output copy
+    if (!ok(cudaEventRecord(hp->done, hp->out)) || !ok(cudaStreamWaitEvent(s, hp->done, 0)))
         return EBIN_ERR_CUDA;
     return EBIN_OK;
 }

@@ -252,11 +252,23 @@ ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *o
 
 /*
  * End-to-end form of ebin_execute for callers whose data lives in host
- * memory: enqueues on `stream` the copies host_a -> dev_a and host_b -> dev_b,
- * the kernel, and the copy dev_out -> host_out.  All six buffers belong to the
- * caller and are sized for the plan; host buffers should be pinned for the
- * copies to overlap.  Does not synchronise: host_out is valid after the
- * stream completes.  Errors as ebin_execute.
+ * memory: copies host_a -> dev_a and host_b -> dev_b, runs the kernel, and
+ * copies dev_out -> host_out.  All six buffers belong to the caller and are
+ * sized for the plan (host_b / dev_b NULL where ebin_execute takes B = NULL);
+ * host buffers should be pinned for the copies to run asynchronously.
+ *
+ * Contiguous and scalar-family plans of at least 2^21 elements run as a
+ * pipeline: the output range is cut into at most 32 chunks (multiples of 4096
+ * elements, at least 2^20), and chunk c+1 is copied in while chunk c computes
+ * on `stream` and chunk c-1 is copied out.  The copies go on two streams per
+ * device that the library creates on first use and keeps; events order them
+ * after the work already queued on `stream`, and `stream` itself waits for the
+ * last output copy.  Other plans enqueue copies, kernel and copy-back on
+ * `stream` one after another.
+ *
+ * Does not synchronise: host_out is valid once `stream` has completed.
+ * Errors as ebin_execute (checks on the device buffers), and INVALID_ARG for
+ * host_b without dev_b.
  */
 ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, const void *host_b,
                               void *host_out, void *dev_a, void *dev_b, void *dev_out,

@@ -109,6 +109,71 @@ def test_execute_host_round_trip():
     assert_bits_equal(ho.numpy().view(np.uint16).reshape(want.shape), want, "bfloat16")
 
 
+def _host_run(op, dtype, a, b, attrs=None, stream=None):
+    """ebin_execute_host with pinned host buffers; returns (out, family, launches)."""
+    p = eb.Plan(eb.descriptor(op, dtype, **(attrs or {})), a.shape, b.shape)
+    view = {1: np.uint8, 2: np.int16, 4: np.int32, 8: np.int64}
+    isz = eb.ITEMSIZE[dtype]
+    osz = eb.ITEMSIZE[eb.descriptor(op, dtype, **(attrs or {})).out_dtype]
+    ha = torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(view[isz]).copy()).pin_memory()
+    hb = torch.from_numpy(np.ascontiguousarray(b).reshape(-1).view(view[isz]).copy()).pin_memory()
+    ho = torch.empty(p.numel * osz, dtype=torch.uint8).pin_memory()
+    da, db = torch.empty_like(ha, device="cuda"), torch.empty_like(hb, device="cuda")
+    do = torch.empty(p.numel * osz, dtype=torch.uint8, device="cuda")
+    s = stream or torch.cuda.current_stream()
+    before = eb.ebin_launch_count()
+    eb.ebin_execute_host(p.handle, ha.data_ptr(), hb.data_ptr(), ho.data_ptr(), da.data_ptr(),
+                         db.data_ptr(), do.data_ptr(), s.cuda_stream)
+    s.synchronize()
+    return ho.numpy(), p.family, eb.ebin_launch_count() - before
+
+
+@pytest.mark.parametrize("op,dtype,sa,sb,fam,chunks", [
+    ("Mul", "float32", (5000003,), (5000003,), "contiguous", 5),
+    ("Add", "bfloat16", (3000001,), (), "right_scalar", 3),
+    ("Sub", "int32", (1,), (2500000,), "left_scalar", 3),
+    ("Greater", "float16", (2621447,), (2621447,), "contiguous", 3),
+    ("Div", "float32", (1 << 21,), (1 << 21,), "contiguous", 2),
+])
+def test_execute_host_pipelined(op, dtype, sa, sb, fam, chunks):
+    """Large contiguous and scalar plans run as a pipeline of chunks over two
+    copy streams; ragged lengths end in a short chunk."""
+    a, b = inputs_for(op, dtype, sa, sb, seed=81)
+    want, _ = oracle.run(op, a, b, dtype)
+    got, family, launches = _host_run(op, dtype, a, b)
+    assert family == fam and launches == chunks
+    otype = "bool" if op == "Greater" else dtype
+    ov = {"float32": np.float32, "bfloat16": np.uint16, "int32": np.int32, "bool": np.uint8}[otype]
+    assert_bits_equal(got.view(ov).reshape(want.shape), want, otype, op)
+
+
+def test_execute_host_pipelined_status_and_ordering():
+    """The device status word is raised through the chunked path, and two
+    calls queued back to back on one stream reuse the device buffers in order."""
+    n = 3 << 20
+    a = datagen.make("bits", "int32", (n,), 82, 0)
+    got, fam, launches = _host_run("Mod", "int32", a, np.zeros((), np.int32), {"fmod": 0})
+    assert fam == "right_scalar" and launches == 3
+    assert eb.get_device_status() == eb.DEVICE_DIV_BY_ZERO
+    assert eb.get_device_status() == 0
+    # two pipelined calls on the same buffers without a synchronisation between them
+    x1, y1 = inputs_for("Add", "float32", (n,), (n,), seed=83)
+    x2, y2 = inputs_for("Mul", "float32", (n,), (n,), seed=84)
+    p1 = eb.Plan(eb.descriptor("Add", "float32"), (n,), (n,))
+    p2 = eb.Plan(eb.descriptor("Mul", "float32"), (n,), (n,))
+    pin = lambda v: torch.from_numpy(v.copy()).pin_memory()
+    h = [pin(x1), pin(y1), pin(x2), pin(y2)]
+    o1, o2 = torch.empty(n).pin_memory(), torch.empty(n).pin_memory()
+    da, db, do = (torch.empty(n, device="cuda") for _ in range(3))
+    s = torch.cuda.current_stream()
+    for p, ha, hb, ho in ((p1, h[0], h[1], o1), (p2, h[2], h[3], o2)):
+        eb.ebin_execute_host(p.handle, ha.data_ptr(), hb.data_ptr(), ho.data_ptr(),
+                             da.data_ptr(), db.data_ptr(), do.data_ptr(), s.cuda_stream)
+    s.synchronize()
+    assert_bits_equal(o1.numpy(), oracle.run("Add", x1, y1, "float32")[0], "float32")
+    assert_bits_equal(o2.numpy(), oracle.run("Mul", x2, y2, "float32")[0], "float32")
+
+
 def test_launch_count_and_binary_helper():
     x = torch.randn(4, 8, 32, 32, device="cuda")
     bias = torch.randn(8, 1, 1, device="cuda")
