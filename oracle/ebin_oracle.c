@@ -19,7 +19,8 @@
  *  - 0verkilll/onnx "ops" package docs -- BatchNormalizationOp (inference
  *    formula, channel axis 1), PReluOp (x >= 0 ? x : slope*x, slope broadcast
  *    to the data), ClipOp (optional min/max bounds), Add/Sub/Mul.
- *  - ncnn operators.md -- batchnorm, bias, binaryop, clip.
+ *  - ncnn operators.md -- batchnorm, bias, binaryop (operation types MAX,
+ *    MIN, RSUB, RDIV; with_scalar), clip.
  * Where the pages are silent the plain reading is taken (IEEE-754 binary32
  * round-to-nearest-even arithmetic without contraction, two's-complement wrap
  * for integers, C99 pow/fmod semantics, ONNX type lists).
@@ -45,6 +46,7 @@ enum {
     OR_BITWISE_AND, OR_BITWISE_OR, OR_BITWISE_XOR,
     OR_BITSHIFT, OR_PRELU,
     OR_BATCHNORM, OR_CLIP,
+    OR_MAX, OR_MIN, OR_RSUB, OR_RDIV,
     OR_NUM_OPS
 };
 enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL, OT_NUM };
@@ -200,7 +202,7 @@ int oracle_type_allowed(int op, int t)
     switch (op) {
     case OR_ADD: case OR_SUB: case OR_MUL: case OR_DIV: case OR_MOD:
     case OR_LESS: case OR_GREATER: case OR_LESS_EQUAL: case OR_GREATER_EQUAL:
-    case OR_CLIP:
+    case OR_CLIP: case OR_MAX: case OR_MIN: case OR_RSUB: case OR_RDIV:
         return t != OT_BOOL && t >= 0 && t < OT_NUM;
     case OR_POW:
         return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64;
@@ -260,9 +262,32 @@ static float float_mod(float a, float b, int fmod_flag)
     return r;
 }
 
+/*
+ * ncnn binaryop MAX / MIN (operation types 4 and 5).  The page names the
+ * operations only; read as IEEE 754-2019 maximum / minimum: a NaN operand
+ * gives NaN, and +0 counts as larger than -0.
+ */
+static float float_max(float a, float b)
+{
+    if (isnan(a) || isnan(b)) return a + b;            /* a NaN */
+    if (a == b) return signbit(a) ? b : a;             /* equal, or +0 / -0 */
+    return a > b ? a : b;
+}
+
+static float float_min(float a, float b)
+{
+    if (isnan(a) || isnan(b)) return a + b;
+    if (a == b) return signbit(a) ? a : b;
+    return a < b ? a : b;
+}
+
 static float float_op(int op, float a, float b, int fmod_flag)
 {
     switch (op) {
+    case OR_MAX: return float_max(a, b);
+    case OR_MIN: return float_min(a, b);
+    case OR_RSUB: return b - a;                         /* ncnn RSUB: B - A */
+    case OR_RDIV: return b / a;                         /* ncnn RDIV: B / A */
     case OR_ADD: return a + b;
     case OR_SUB: return a - b;
     case OR_MUL: return a * b;
@@ -347,6 +372,13 @@ static uint64_t int_op(int op, int t, int64_t a, int64_t b, int fmod_flag, int d
     }
     case OR_PRELU:                                             /* x >= 0 ? x : slope * x */
         return (!sgn || as_signed(ua, w) >= 0) ? ua : ub * ua;
+    case OR_MAX: return a > b ? ua : ub;                      /* values, not bit patterns */
+    case OR_MIN: return a < b ? ua : ub;
+    case OR_RSUB: return ub - ua;
+    case OR_RDIV:                                              /* B / A, truncated */
+        if (a == 0) { *status |= OR_ST_DIV_BY_ZERO; return 0; }
+        if (sgn && a == -1) return 0ull - ub;
+        return (uint64_t)(b / a);
     }
     return 0;
 }

@@ -400,6 +400,99 @@ def test_int_arith_matches_python_integers(dtype):
                 assert st == (0 if nz.all() else oracle.STATUS_DIV_BY_ZERO)
 
 
+# --------------------------------------------------------------------------- ncnn binaryop extras
+# ncnn operators.md, binaryop: operation types 4 = MAX, 5 = MIN, 7 = RSUB, 8 = RDIV.
+
+def _no_zero_pairs(a, b):
+    """Drop pairs where both are zeros: numpy's maximum/minimum do not order -0 and +0."""
+    keep = ~((a == 0) & (b == 0))
+    return a[keep], b[keep]
+
+
+@pytest.mark.parametrize("dtype", ["float32", "float16"])
+def test_max_min_match_numpy(dtype):
+    """numpy.maximum / numpy.minimum also return NaN for a NaN operand."""
+    if dtype == "float32":
+        a, b = float_corpus(20000, 21), np.roll(float_corpus(20000, 22), 5)
+    else:
+        a = np.concatenate([datagen.raw_u32(23, 0, 30000).astype(np.uint16).view(np.float16),
+                            datagen.make("normal", "float16", (30000,), 23, 1)])
+        b = np.concatenate([datagen.raw_u32(23, 2, 30000).astype(np.uint16).view(np.float16),
+                            datagen.make("normal", "float16", (30000,), 23, 3)])
+    b[::11] = a[::11]                                        # equal pairs
+    a, b = _no_zero_pairs(a, b)
+    for op, fn in (("Max", np.maximum), ("Min", np.minimum)):
+        got, st = oracle.run(op, a, b, dtype)
+        assert st == 0
+        assert_bits_equal(got, fn(a, b), dtype, op)
+
+
+def test_max_min_match_torch_bf16():
+    a = np.concatenate([datagen.raw_u32(24, 0, 30000).astype(np.uint16),
+                        datagen.make("normal", "bfloat16", (30000,), 24, 1)])
+    b = np.concatenate([datagen.raw_u32(24, 2, 30000).astype(np.uint16),
+                        datagen.make("normal", "bfloat16", (30000,), 24, 3)])
+    ta = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    tb = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+    keep = (~((ta == 0) & (tb == 0))).numpy()
+    a, b, ta, tb = a[keep], b[keep], ta[keep], tb[keep]
+    for op, fn in (("Max", torch.maximum), ("Min", torch.minimum)):
+        got, _ = oracle.run(op, a, b, "bfloat16")
+        want = fn(ta, tb).view(torch.int16).numpy().view(np.uint16)
+        assert_bits_equal(got, want, "bfloat16", op)
+
+
+def test_max_min_signed_zero_and_nan():
+    """Closed forms of the reading (IEEE 754-2019 maximum / minimum): +0 counts as
+    larger than -0, and a NaN operand on either side gives NaN."""
+    a = f32(0.0, -0.0, -0.0, 0.0, np.nan, 1.0, -np.inf, np.inf, 3.0)
+    b = f32(-0.0, 0.0, -0.0, 0.0, 1.0, np.nan, 5.0, 5.0, 3.0)
+    got, _ = oracle.run("Max", a, b, "float32")
+    assert_bits_equal(got, f32(0.0, 0.0, -0.0, 0.0, np.nan, np.nan, 5.0, np.inf, 3.0), "float32")
+    got, _ = oracle.run("Min", a, b, "float32")
+    assert_bits_equal(got, f32(-0.0, -0.0, -0.0, 0.0, np.nan, np.nan, -np.inf, 5.0, 3.0),
+                      "float32")
+
+
+@pytest.mark.parametrize("dtype", ["int32", "int64", "uint8", "uint32"])
+def test_int_max_min_rsub_rdiv_match_python_integers(dtype):
+    a, b = int_pairs(dtype)
+    st_t = datagen.STORAGE[dtype]
+    A = np.array([int(x) for x in a], dtype=object).astype(st_t)
+    B = np.array([int(x) for x in b], dtype=object).astype(st_t)
+    for op in ("Max", "Min", "RSub", "RDiv"):
+        got, st = oracle.run(op, A, B, dtype)
+        want = []
+        for x, y in zip(a, b):
+            x, y = int(x), int(y)
+            if op == "Max": v = max(x, y)
+            elif op == "Min": v = min(x, y)
+            elif op == "RSub": v = y - x
+            else: v = trunc_div(y, x) if x else 0
+            want.append(wrap(v, dtype))
+        want = np.array(want, dtype=object).astype(st_t)
+        assert (got == want).all(), (op, dtype)
+        if op == "RDiv":
+            assert st == (oracle.STATUS_DIV_BY_ZERO if (a == 0).any() else 0)
+        else:
+            assert st == 0
+
+
+@pytest.mark.parametrize("op,fn", [("RSub", np.subtract), ("RDiv", np.divide)])
+@pytest.mark.parametrize("dtype", ["float32", "float16"])
+def test_rsub_rdiv_are_numpy_with_operands_reversed(op, fn, dtype):
+    if dtype == "float32":
+        a, b = float_corpus(20000, 25), np.roll(float_corpus(20000, 26), 3)
+    else:
+        a = datagen.raw_u32(27, 0, 30000).astype(np.uint16).view(np.float16)
+        b = datagen.raw_u32(27, 1, 30000).astype(np.uint16).view(np.float16)
+    got, st = oracle.run(op, a, b, dtype)
+    with np.errstate(all="ignore"):
+        want = fn(b, a)
+    assert st == 0
+    assert_bits_equal(got, want, dtype, op)
+
+
 def test_int_division_by_zero_sets_status():
     a = np.array([5, 7, -9], np.int32)
     _, st = oracle.run("Div", a, np.array([1, 0, 2], np.int32), "int32")
