@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libebin.so")
@@ -30,7 +31,8 @@ OPS = {"Add": 0, "Sub": 1, "Mul": 2, "Div": 3, "Mod": 4, "Pow": 5,
        "Equal": 6, "Less": 7, "Greater": 8, "LessOrEqual": 9, "GreaterOrEqual": 10,
        "And": 11, "Or": 12, "Xor": 13,
        "BitwiseAnd": 14, "BitwiseOr": 15, "BitwiseXor": 16,
-       "BitShift": 17, "PRelu": 18, "BatchNormalization": 19, "Clip": 20}
+       "BitShift": 17, "PRelu": 18, "BatchNormalization": 19, "Clip": 20,
+       "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24}
 DTYPES = {"float32": 1, "uint8": 2, "int32": 6, "int64": 7, "bool": 9, "float16": 10,
           "uint32": 12, "bfloat16": 16}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
@@ -60,7 +62,8 @@ class EbinError(RuntimeError):
 class ebin_attrs(ctypes.Structure):
     _fields_ = [("fmod", ctypes.c_int32), ("direction", ctypes.c_int32),
                 ("epsilon", ctypes.c_float), ("clip_has_min", ctypes.c_int32),
-                ("clip_has_max", ctypes.c_int32)]
+                ("clip_has_max", ctypes.c_int32), ("with_scalar", ctypes.c_int32),
+                ("scalar_b", ctypes.c_float)]
 
 
 def _load():
@@ -287,11 +290,15 @@ class Descriptor:
     """Owns an ebin descriptor (operator, opset, attributes, element type)."""
 
     def __init__(self, op: str, dtype, *, opset: int = 28, fmod: int = 0, direction: int = 0,
-                 epsilon: float = 1e-5, has_min: bool = True, has_max: bool = True):
+                 epsilon: float = 1e-5, has_min: bool = True, has_max: bool = True,
+                 scalar_b: float | None = None):
+        """``scalar_b`` given: ncnn binaryop's with_scalar, B is that value."""
         self.op = op
         self.dtype = DTYPE_NAMES[_dtype_code(dtype)]
+        self.with_scalar = scalar_b is not None
         attrs = ebin_attrs(int(fmod), int(direction), float(epsilon), int(bool(has_min)),
-                           int(bool(has_max)))
+                           int(bool(has_max)), int(self.with_scalar),
+                           float(scalar_b) if self.with_scalar else 0.0)
         code = _dtype_code(dtype)
         self.handle = ebin_descriptor_create(OPS[op], int(opset), attrs, code, code)
         self.out_dtype = DTYPE_NAMES[ebin_descriptor_output_dtype(self.handle)]
@@ -352,9 +359,15 @@ def get_device_status(stream=None) -> int:
 _descriptors: dict = {}
 
 
+def _attr_key(v):
+    """Cache key of an attribute value: floats by bit pattern (-0.0 is not 0.0,
+    and a NaN matches itself)."""
+    return ("f", struct.pack("<d", v)) if isinstance(v, float) else v
+
+
 def descriptor(op: str, dtype, **attrs) -> Descriptor:
     """A process-wide Descriptor per (op, dtype, attributes), so plans stay cached."""
-    key = (op, _dtype_code(dtype), tuple(sorted(attrs.items())))
+    key = (op, _dtype_code(dtype), tuple(sorted((k, _attr_key(v)) for k, v in attrs.items())))
     d = _descriptors.get(key)
     if d is None:
         d = _descriptors[key] = Descriptor(op, dtype, **attrs)

@@ -64,6 +64,7 @@ bool type_legal(int op, ebin_dtype t) {
     case EBIN_OP_ADD: case EBIN_OP_SUB: case EBIN_OP_MUL: case EBIN_OP_DIV: case EBIN_OP_MOD:
     case EBIN_OP_LESS: case EBIN_OP_GREATER: case EBIN_OP_LESS_OR_EQUAL:
     case EBIN_OP_GREATER_OR_EQUAL: case EBIN_OP_CLIP:
+    case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV:
         return is_float(t) || is_int(t);
     case EBIN_OP_POW: return is_float(t) || is_signed_int(t);
     case EBIN_OP_EQUAL: return true;
@@ -82,9 +83,20 @@ ebin_dtype output_type(int op, ebin_dtype t) {
 
 // Operators whose kernels can meet invalid elements and report them.
 bool validates(int op, ebin_dtype t) {
-    if ((op == EBIN_OP_DIV || op == EBIN_OP_MOD) && is_int(t)) return true;
+    if ((op == EBIN_OP_DIV || op == EBIN_OP_MOD || op == EBIN_OP_RDIV) && is_int(t)) return true;
     if (op == EBIN_OP_POW && is_signed_int(t)) return true;
     return op == EBIN_OP_BITSHIFT;
+}
+
+// Operators that accept ncnn binaryop's with_scalar (operators.md, binaryop:
+// operation types ADD, SUB, MUL, DIV, MAX, MIN, POW, RSUB, RDIV).
+bool scalar_attr_op(int op) {
+    switch (op) {
+    case EBIN_OP_ADD: case EBIN_OP_SUB: case EBIN_OP_MUL: case EBIN_OP_DIV: case EBIN_OP_POW:
+    case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV:
+        return true;
+    }
+    return false;
 }
 
 // B is an ordinary broadcast tensor (not the BN parameter block or Clip bounds).
@@ -117,7 +129,7 @@ extern "C" ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_
     if (!out) return EBIN_ERR_INVALID_ARG;
     *out = nullptr;
     if ((int)op < 0 || (int)op >= EBIN_OP_COUNT) return EBIN_ERR_UNSUPPORTED_OP;
-    ebin_attrs a{0, 0, EBIN_DEFAULT_EPSILON, 1, 1};
+    ebin_attrs a{0, 0, EBIN_DEFAULT_EPSILON, 1, 1, 0, 0.0f};
     if (attrs) a = *attrs;
     if (dtype_a != dtype_b || !type_legal(op, dtype_a)) return EBIN_ERR_UNSUPPORTED_TYPE;
     if (op == EBIN_OP_MOD) {
@@ -129,6 +141,9 @@ extern "C" ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_
     }
     if (op == EBIN_OP_BITSHIFT && a.direction != 0 && a.direction != 1)
         return EBIN_ERR_INVALID_ATTR;
+    if (a.with_scalar != 0 && a.with_scalar != 1) return EBIN_ERR_INVALID_ATTR;
+    if (a.with_scalar && (!scalar_attr_op(op) || !is_float(dtype_a))) return EBIN_ERR_INVALID_ATTR;
+    if (!a.with_scalar) a.scalar_b = 0.0f;
     auto *d = new ebin_descriptor_s;
     d->id = g_next_id.fetch_add(1);
     d->op = op;
@@ -227,6 +242,8 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     } else if (d.op == EBIN_OP_CLIP) {
         if (rb != 1 || sb[0] != 2) return EBIN_ERR_INCOMPATIBLE_SHAPES;
         rlb = 0;
+    } else if (d.attrs.with_scalar) {
+        rlb = 0;               // B is the attribute value: a scalar
     } else {
         for (int i = 0; i < rb; ++i) lb[i] = sb[i];
     }
@@ -263,7 +280,7 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     for (int i = 0; i < r; ++i) p->shape_out[i] = so[i];
     p->numel = product(so, r);
     p->numel_a = product(sa, ra);
-    p->numel_b = product(sb, rb);
+    p->numel_b = d.attrs.with_scalar ? 0 : product(sb, rb);
     p->plane = plane;
 
     // 2. dense strides, zero on broadcast dims
@@ -301,9 +318,14 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     g.rank = k;
     p->g = g;
 
-    // 5. loop family
+    // 5. loop family (a with_scalar plan runs its own family or the general one)
     bool ok = true;
     p->family = family_of(*p, forced, &ok);
+    if (ok && d.attrs.with_scalar && forced != EBIN_FAMILY_AUTO &&
+        forced != EBIN_FAMILY_GENERAL_STRIDED) {
+        bool nat_ok = true;
+        ok = forced == family_of(*p, EBIN_FAMILY_AUTO, &nat_ok);
+    }
     if (!ok) {
         delete p;
         return EBIN_ERR_FAMILY;
@@ -356,6 +378,7 @@ extern "C" ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *s
                                         ebin_plan_t *out) {
     if (!desc || !out) return EBIN_ERR_INVALID_ARG;
     *out = nullptr;
+    if (desc->attrs.with_scalar) rank_b = 0;   // shape B is not read
     if (rank_a < 0 || rank_b < 0) return EBIN_ERR_INVALID_ARG;
     if (rank_a > kMaxRank || rank_b > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
     if ((rank_a > 0 && !shape_a) || (rank_b > 0 && !shape_b)) return EBIN_ERR_INVALID_ARG;
@@ -396,6 +419,7 @@ extern "C" ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int
                                                ebin_family family, ebin_plan_t *out) {
     if (!desc || !out) return EBIN_ERR_INVALID_ARG;
     *out = nullptr;
+    if (desc->attrs.with_scalar) rank_b = 0;
     ebin_plan_s *p = nullptr;
     const ebin_status st = build_plan(*desc, shape_a, rank_a, shape_b, rank_b, (int)family, &p);
     if (st != EBIN_OK) return st;
@@ -518,6 +542,7 @@ cudaError_t ebin::launch(const Launch &L) {
     case EBIN_OP_AND: case EBIN_OP_OR: case EBIN_OP_XOR: case EBIN_OP_BITWISE_AND:
     case EBIN_OP_BITWISE_OR: case EBIN_OP_BITWISE_XOR: case EBIN_OP_BITSHIFT: EBIN_PICK(logic)
     case EBIN_OP_PRELU: case EBIN_OP_BATCHNORM: case EBIN_OP_CLIP: EBIN_PICK(chan)
+    case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV: EBIN_PICK(ext)
     default: return cudaErrorInvalidValue;
     }
 #undef EBIN_PICK
@@ -529,8 +554,10 @@ namespace {
 // buffer, alias and alignment rules of ebin_execute, and the status word.
 ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, void *out,
                            cudaStream_t s, ebin::Launch &L) {
-    const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max);
+    const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max) &&
+                          !p.attrs.with_scalar;
     if (!A || !out || (b_needed && !B)) return EBIN_ERR_INVALID_ARG;
+    if (p.attrs.with_scalar) B = nullptr;   // never read
 
     // Aliasing: an input may share storage with out only as the identical
     // buffer of the output's type and element count; a broadcast input or a
@@ -562,6 +589,8 @@ ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, v
     L.args.has_min = p.attrs.clip_has_min;
     L.args.has_max = p.attrs.clip_has_max;
     L.args.plane = p.plane;
+    L.args.with_scalar = p.attrs.with_scalar;
+    L.args.scalar_b = p.attrs.scalar_b;
     L.stream = s;
     L.num_sms = sm_count(dev);
     L.status = nullptr;

@@ -666,12 +666,36 @@ cudaError_t run_general(const Launch &L) {
     return run_rows_kernel<Op, 1, 2, 2, false, 2, false>(L);
 }
 
+// Operators that accept a scalar B given as an attribute (Op::kScalarAttr).
+template <class Op, class = void> struct HasScalarAttr : std::false_type {};
+template <class Op>
+struct HasScalarAttr<Op, std::void_t<decltype(Op::kScalarAttr)>>
+    : std::bool_constant<Op::kScalarAttr> {};
+
+// A plan whose B is the attribute value: A is dense, so the right-scalar kernel
+// runs it (a single element plans as contiguous), or the general kernel when
+// pointers are off the 16-byte alignment.
+template <class Op>
+cudaError_t launch_with_scalar(const Launch &L) {
+    using W = WithScalar<Op>;
+    switch (L.family) {
+    case FAM_CONTIGUOUS:
+    case FAM_RIGHT_SCALAR: return run_scalar<W, false>(L);
+    case FAM_GENERAL_STRIDED: return run_general<W>(L);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 // Launch the kernel of L.family for operator functor Op.
 template <class Op>
 cudaError_t launch_op(const Launch &L) {
     if constexpr (!Op::kLegal) {
         return cudaErrorInvalidValue;
     } else {
+        if (L.args.with_scalar) {
+            if constexpr (HasScalarAttr<Op>::value) return launch_with_scalar<Op>(L);
+            else return cudaErrorInvalidValue;
+        }
         switch (L.family) {
         case FAM_CONTIGUOUS: return run_contiguous<Op>(L);
         case FAM_RIGHT_SCALAR: return run_scalar<Op, false>(L);

@@ -88,8 +88,10 @@ extern "C" ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, con
     if (status_bits) *status_bits = 0;
     if (p.numel == 0) return EBIN_OK;
     const bool plain_b = p.op != EBIN_OP_BATCHNORM && p.op != EBIN_OP_CLIP;
-    const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max);
+    const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max) &&
+                          !p.attrs.with_scalar;
     if (!A || !out || (b_needed && !B)) return EBIN_ERR_INVALID_ARG;
+    if (p.attrs.with_scalar) B = nullptr;   // B is the attribute value, never read
 
     // same aliasing rule as ebin_execute
     const int64_t isz = (int64_t)ebin_dtype_size(p.dt);
@@ -127,6 +129,8 @@ extern "C" ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, con
     L.args.has_min = p.attrs.clip_has_min;
     L.args.has_max = p.attrs.clip_has_max;
     L.args.plane = p.plane;
+    L.args.with_scalar = p.attrs.with_scalar;
+    L.args.scalar_b = p.attrs.scalar_b;
     L.stream = s;
     L.num_sms = setup.num_sms;
     L.status = word;  // only the validating operators' kernels write it

@@ -132,13 +132,19 @@ __device__ __forceinline__ float mod_float(float a, float b, int fmod_flag) {
 }
 
 // ---------------------------------------------------------------- arithmetic
-enum ArithK { K_ADD = 0, K_SUB = 1, K_MUL = 2, K_DIV = 3 };
+// K_RSUB and K_RDIV are ncnn binaryop's RSUB (B - A) and RDIV (B / A)
+// (ncnn operators.md, binaryop, operation types 7 and 8).
+enum ArithK { K_ADD = 0, K_SUB = 1, K_MUL = 2, K_DIV = 3, K_RSUB = 4, K_RDIV = 5 };
 
 template <class T, int K> struct OpArith : PlainB<T, T> {
     static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
-    static constexpr bool kValidates = (K == K_DIV) && is_int_v<T>;
+    static constexpr bool kValidates = (K == K_DIV || K == K_RDIV) && is_int_v<T>;
+    static constexpr bool kScalarAttr = is_float_v<T>;     // ncnn binaryop with_scalar
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
-        if constexpr (is_float_v<T>) {
+        if constexpr (K == K_RSUB || K == K_RDIV) {
+            // the same operation with the operands exchanged
+            return OpArith<T, K == K_RSUB ? K_SUB : K_DIV>::apply(b, a, OpArgs{}, err);
+        } else if constexpr (is_float_v<T>) {
             const float x = Tr<T>::in(a), y = Tr<T>::in(b);
             float r;
             if constexpr (K == K_ADD) r = __fadd_rn(x, y);
@@ -159,6 +165,39 @@ template <class T, int K> struct OpArith : PlainB<T, T> {
                 return (T)(a / b);                               // truncates toward zero
             }
         }
+    }
+};
+
+// ncnn binaryop MAX / MIN (operators.md, binaryop, operation types 4 and 5),
+// read as IEEE 754-2019 maximum / minimum: a NaN operand gives NaN and +0
+// counts as larger than -0.  Half and bfloat16 results are one of the two
+// widened inputs, so narrowing them back is exact.
+template <class T, bool kMax> struct OpMinMax : PlainB<T, T> {
+    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kValidates = false;
+    static constexpr bool kScalarAttr = is_float_v<T>;
+    __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &) {
+        if constexpr (is_float_v<T>) {
+            const float x = Tr<T>::in(a), y = Tr<T>::in(b);
+            float r;
+            if (isnan(x) || isnan(y)) r = __fadd_rn(x, y);                 // a NaN
+            else if (x == y) r = (signbit(x) == kMax) ? y : x;             // +0 vs -0
+            else r = kMax ? (x > y ? x : y) : (x < y ? x : y);
+            return Tr<T>::out(r);
+        } else {
+            return kMax ? (a > b ? a : b) : (a < b ? a : b);
+        }
+    }
+};
+
+// ncnn binaryop with_scalar: the operator with B replaced by the attribute
+// value, rounded to the element type (the same value a 0-d B tensor would
+// hold).  No B pointer is read.
+template <class Op> struct WithScalar : Op {
+    using In = typename Op::In;
+    __device__ __forceinline__ static typename Op::BV loadB(const In *, int64_t,
+                                                            const OpArgs &p) {
+        return Tr<In>::out(p.scalar_b);
     }
 };
 
@@ -340,6 +379,7 @@ template <class T> struct OpMod : PlainB<T, T> {
 template <class T> struct OpPow : PlainB<T, T> {
     static constexpr bool kLegal = is_float_v<T> || is_signed_int_v<T>;
     static constexpr bool kValidates = is_signed_int_v<T>;
+    static constexpr bool kScalarAttr = is_float_v<T>;     // ncnn binaryop POW with_scalar
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
         if constexpr (is_float_v<T>) {
             // C pow semantics evaluated in binary64, rounded once to binary32

@@ -78,7 +78,13 @@ typedef enum ebin_op {
     EBIN_OP_PRELU = 18,           /* B = slope, broadcast one way to A */
     EBIN_OP_BATCHNORM = 19,       /* inference; B = [4, C]: scale, bias, mean, var rows */
     EBIN_OP_CLIP = 20,            /* B = [2]: {min, max}; attrs.clip_has_min/max */
-    EBIN_OP_COUNT = 21
+    /* ncnn operators.md, binaryop operation types 4, 5, 7, 8 (0-3 are ADD..DIV
+     * above, 6 = POW is EBIN_OP_POW): */
+    EBIN_OP_MAX = 21,             /* IEEE 754-2019 maximum: NaN if either is NaN, +0 > -0 */
+    EBIN_OP_MIN = 22,             /* IEEE 754-2019 minimum: NaN if either is NaN, -0 < +0 */
+    EBIN_OP_RSUB = 23,            /* B - A */
+    EBIN_OP_RDIV = 24,            /* B / A; integer A == 0 raises EBIN_DEVICE_DIV_BY_ZERO */
+    EBIN_OP_COUNT = 25
 } ebin_op;
 
 /* Element types, numbered as ONNX TensorProto.DataType. */
@@ -115,7 +121,8 @@ typedef enum ebin_family {
 
 /*
  * Operator attributes.  Pass NULL to ebin_descriptor_create for the defaults
- * (fmod 0, direction LEFT, epsilon 1e-5, both Clip bounds present).
+ * (fmod 0, direction LEFT, epsilon 1e-5, both Clip bounds present, no
+ * with_scalar).
  *   fmod          Mod only: 0 = floor remainder (result and exact zeros take
  *                 the divisor's sign), 1 = truncated remainder (the dividend's
  *                 sign, including a signed zero).  Floating Mod with fmod 0
@@ -125,6 +132,14 @@ typedef enum ebin_family {
  *   epsilon       BatchNormalization only.
  *   clip_has_min  Clip only: nonzero if B[0] is a lower bound.
  *   clip_has_max  Clip only: nonzero if B[1] is an upper bound.
+ *   with_scalar   ncnn binaryop's with_scalar (operators.md, binaryop): 1 = B
+ *                 is not a tensor but the value scalar_b.  Allowed for Add,
+ *                 Sub, Mul, Div, Pow, Max, Min, RSub, RDiv on floating types
+ *                 (the page gives b as a float); B is then b rounded to the
+ *                 element type (round to nearest even), exactly as a 0-d B
+ *                 tensor holding that value.  Plans ignore shape B and read
+ *                 no B pointer.  Default 0.
+ *   scalar_b      the value b when with_scalar = 1.
  */
 typedef struct ebin_attrs {
     int32_t fmod;
@@ -132,6 +147,8 @@ typedef struct ebin_attrs {
     float epsilon;
     int32_t clip_has_min;
     int32_t clip_has_max;
+    int32_t with_scalar;
+    float scalar_b;
 } ebin_attrs;
 
 typedef struct ebin_descriptor_s *ebin_descriptor_t;
@@ -201,7 +218,8 @@ ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *shape_a, int
  * As ebin_plan_create, but force a loop family (for testing every kernel on
  * the same inputs).  Forced plans bypass the cache.  GENERAL_STRIDED can run
  * every plan; the others only geometries they can traverse (else FAMILY).
- * With zero output elements the family is always EMPTY.
+ * A with_scalar plan runs only its own family or GENERAL_STRIDED.  With zero
+ * output elements the family is always EMPTY.
  */
 ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape_a, int rank_a,
                                     const int64_t *shape_b, int rank_b, ebin_family family,

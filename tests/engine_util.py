@@ -22,6 +22,7 @@ MANIFEST = {
     "PRelu": FLOATS + ("int32", "int64", "uint32"),
     "BatchNormalization": FLOATS,
     "Clip": FLOATS + INTS,
+    "Max": FLOATS + INTS, "Min": FLOATS + INTS, "RSub": FLOATS + INTS, "RDiv": FLOATS + INTS,
 }
 ONE_WAY = ("PRelu", "BatchNormalization", "Clip")
 
@@ -106,11 +107,16 @@ def inputs_for(op, dtype, shape_a, shape_b, seed=0, attrs=None):
         else:
             a = mk("normal", dtype, shape_a, seed, 0)
             b = mk("normal", dtype, shape_b, seed, 1)
-            if op in ("Equal", "Less", "Greater", "LessOrEqual", "GreaterOrEqual"):
+            if op in ("Equal", "Less", "Greater", "LessOrEqual", "GreaterOrEqual", "Max", "Min"):
                 if a.shape == b.shape and a.size > 4:
                     b.reshape(-1)[::5] = a.reshape(-1)[::5]
             _sprinkle(a, specials(dtype))
             _sprinkle(b, specials(dtype)[::-1])
+            if op in ("Max", "Min") and a.size > 1 and b.size > 1:
+                # (+0, -0) and (-0, +0) as the first two elements of the two operands
+                z = datagen.float_to(np.array([0.0, -0.0], np.float32), dtype)
+                a.reshape(-1)[:2] = z
+                b.reshape(-1)[:2] = z[::-1]
         return a, b
     # integers
     st = datagen.STORAGE[dtype]
@@ -134,13 +140,23 @@ def inputs_for(op, dtype, shape_a, shape_b, seed=0, attrs=None):
         if a.size > 2 and dtype in ("int32", "int64"):
             a.reshape(-1)[0] = np.iinfo(st).min
         return a, b
+    if op == "RDiv":                                           # B / A: A is the divisor
+        lo = 0 if dtype.startswith("u") else -1000
+        a = mk("int_range", dtype, shape_a, seed, 0, lo=lo, hi=1000, skip_zero=True)
+        if dtype.startswith("u"):
+            a[a == 0] = 1
+        b = mk("bits", dtype, shape_b, seed, 1)
+        if a.size > 0 and b.size > 0 and dtype in ("int32", "int64"):
+            a.reshape(-1)[0] = -1                              # INT_MIN / -1 at output 0
+            b.reshape(-1)[0] = np.iinfo(st).min
+        return a, b
     if op == "PRelu":
         a = mk("bits", dtype, shape_a, seed, 0)
         b = mk("int_range", dtype, shape_b, seed, 1, lo=0, hi=5)
         return a, b
     a = mk("bits", dtype, shape_a, seed, 0)
     b = mk("bits", dtype, shape_b, seed, 1)
-    if op in ("Equal", "Less", "Greater", "LessOrEqual", "GreaterOrEqual"):
+    if op in ("Equal", "Less", "Greater", "LessOrEqual", "GreaterOrEqual", "Max", "Min"):
         if a.shape == b.shape and a.size > 4:
             b.reshape(-1)[::4] = a.reshape(-1)[::4]
     return a, b

@@ -174,6 +174,58 @@ def test_execute_host_pipelined_status_and_ordering():
     assert_bits_equal(o2.numpy(), oracle.run("Mul", x2, y2, "float32")[0], "float32")
 
 
+@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
+def test_with_scalar_matches_a_scalar_tensor(dtype):
+    """ncnn binaryop with_scalar: B is the attribute value rounded to the element
+    type, so the result equals the oracle's with a 0-d B holding that value.
+    Runs the right-scalar kernel, the general kernel (unaligned A), a single
+    element, and the host-buffer pipeline."""
+    from test_gpu_parity import compare
+    for op in ("Add", "Sub", "Mul", "Div", "Pow", "Max", "Min", "RSub", "RDiv"):
+        for v in (0.37, -2.5, 0.0, -0.0, float("inf"), float("nan"), 1e-8, 70000.0):
+            a, _ = inputs_for(op, dtype, (100003,), (), seed=90)
+            bq = datagen.float_to(np.array([v], np.float32), dtype).reshape(())
+            want, _ = oracle.run(op, a, bq, dtype)
+            desc = eb.descriptor(op, dtype, scalar_b=v)
+            for shape, offset in (((100003,), 0), ((100003,), 1), ((), 0)):
+                aa = a if shape else a[:1].reshape(())
+                ww = want if shape else want[:1].reshape(())
+                plan = eb.Plan(desc, aa.shape, ())
+                isz = eb.ITEMSIZE[dtype]
+                buf = to_device(np.concatenate([np.zeros(offset, aa.dtype), aa.reshape(-1)]))
+                out = torch.empty(max(plan.numel, 1) * isz + 16, dtype=torch.uint8,
+                                  device="cuda")
+                eb.execute(plan, buf.data_ptr() + offset * isz, None, out.data_ptr() + offset * isz)
+                got = out.cpu().numpy()[offset * isz: (offset + plan.numel) * isz] \
+                    .view(datagen.STORAGE[dtype]).reshape(ww.shape)
+                compare(op, dtype, got, ww, "%s %s b=%r shape=%s offset=%d" %
+                        (op, dtype, v, shape, offset))
+    # through the host-buffer pipeline (2^21 elements: chunked)
+    n = 1 << 21
+    a = datagen.make("normal", dtype, (n,), 91, 0)
+    bq = datagen.float_to(np.array([0.75], np.float32), dtype).reshape(())
+    want, _ = oracle.run("RDiv", a, bq, dtype)
+    p = eb.Plan(eb.descriptor("RDiv", dtype, scalar_b=0.75), (n,), ())
+    view = np.int16 if dtype != "float32" else np.int32
+    ha = torch.from_numpy(a.reshape(-1).view(view).copy()).pin_memory()
+    ho = torch.empty_like(ha).pin_memory()
+    da, do = torch.empty_like(ha, device="cuda"), torch.empty_like(ha, device="cuda")
+    s = torch.cuda.current_stream()
+    eb.ebin_execute_host(p.handle, ha.data_ptr(), None, ho.data_ptr(), da.data_ptr(), None,
+                         do.data_ptr(), s.cuda_stream)
+    s.synchronize()
+    assert_bits_equal(ho.numpy().view(datagen.STORAGE[dtype]), want, dtype, "RDiv host")
+
+
+def test_int_rdiv_validates_a():
+    a = np.array([3, 0, -1, 7] * 1000, np.int32)
+    b = np.array([10, 5, -2147483648, -21] * 1000, np.int32)
+    got, bits, _ = run_engine("RDiv", "int32", a, b)
+    want, wbits = oracle.run("RDiv", a, b, "int32")
+    assert bits == wbits == eb.DEVICE_DIV_BY_ZERO
+    assert (got == want).all()
+
+
 def test_launch_count_and_binary_helper():
     x = torch.randn(4, 8, 32, 32, device="cuda")
     bias = torch.randn(8, 1, 1, device="cuda")

@@ -185,6 +185,47 @@ def test_forced_families():
     assert eb.Plan(d, (0, 4), (4,), family="contiguous").family == "empty"
 
 
+SCALAR_ATTR_OPS = ("Add", "Sub", "Mul", "Div", "Pow", "Max", "Min", "RSub", "RDiv")
+
+
+def test_with_scalar_descriptor_rules():
+    """ncnn binaryop's with_scalar (operators.md, binaryop): the nine operation
+    types, on floating types only (the page gives b as a float)."""
+    for op in eb.OPS:
+        for dt in ALL_DTYPES:
+            legal = oracle.type_allowed(op, dt)
+            try:
+                eb.Descriptor(op, dt, scalar_b=0.5).close()
+                got = "ok"
+            except eb.EbinError as e:
+                got = e.code
+            if not legal:
+                assert got == "unsupported_type", (op, dt, got)
+            elif op in SCALAR_ATTR_OPS and dt in ("float32", "float16", "bfloat16"):
+                assert got == "ok", (op, dt, got)
+            else:
+                assert got == "invalid_attr", (op, dt, got)
+    bad = eb.ebin_attrs(0, 0, 1e-5, 1, 1, 2, 0.0)
+    with pytest.raises(eb.EbinError) as e:
+        eb.ebin_descriptor_create(eb.OPS["Add"], 28, bad, 1, 1)
+    assert e.value.code == "invalid_attr"
+
+
+def test_with_scalar_plans_ignore_shape_b():
+    d = eb.Descriptor("Mul", "float32", scalar_b=3.0)
+    p1 = eb.Plan(d, (64, 1000), (7, 1, 3))                 # any shape B: not read
+    p2 = eb.Plan(d, (64, 1000), ())
+    assert p1.handle == p2.handle                          # one cached plan
+    assert p1.output_shape == (64, 1000) and p1.family == "right_scalar"
+    assert eb.Plan(d, (), ()).numel == 1
+    assert eb.Plan(d, (64, 1000), (), family="general_strided").family == "general_strided"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (64, 1000), (), family="inner_vector_outer")
+    assert e.value.code == "family"
+    # B may be NULL: an empty execute checks nothing else
+    assert eb.Plan(d, (0, 5), ()).family == "empty"
+
+
 def test_plan_cache_is_an_8_entry_lru():
     eb.ebin_plan_cache_clear()
     d = eb.Descriptor("Sub", "int32")
