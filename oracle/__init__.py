@@ -33,7 +33,7 @@ OPS = ["Add", "Sub", "Mul", "Div", "Mod", "Pow",
        "BitwiseAnd", "BitwiseOr", "BitwiseXor",
        "BitShift", "PRelu",
        "BatchNormalization", "Clip",
-       "Max", "Min", "RSub", "RDiv"]
+       "Max", "Min", "RSub", "RDiv", "BiasPRelu"]
 DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool"]
 STORAGE = {"float32": np.float32, "float16": np.float16, "bfloat16": np.uint16,
            "int32": np.int32, "int64": np.int64, "uint8": np.uint8, "uint32": np.uint32,

@@ -18,7 +18,9 @@
  *    integer division, modulo and shifts; one byte per BOOL.
  *  - 0verkilll/onnx "ops" package docs -- BatchNormalizationOp (inference
  *    formula, channel axis 1), PReluOp (x >= 0 ? x : slope*x, slope broadcast
- *    to the data), ClipOp (optional min/max bounds), Add/Sub/Mul.
+ *    to the data), ClipOp (optional min/max bounds), Add/Sub/Mul,
+ *    ConvPReluOp (the per-output-channel bias add and PReLU fused into one
+ *    pass: here without the convolution, as BiasPRelu).
  *  - ncnn operators.md -- batchnorm, bias, binaryop (operation types MAX,
  *    MIN, RSUB, RDIV; with_scalar), clip.
  * Where the pages are silent the plain reading is taken (IEEE-754 binary32
@@ -47,6 +49,7 @@ enum {
     OR_BITSHIFT, OR_PRELU,
     OR_BATCHNORM, OR_CLIP,
     OR_MAX, OR_MIN, OR_RSUB, OR_RDIV,
+    OR_BIAS_PRELU,
     OR_NUM_OPS
 };
 enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL, OT_NUM };
@@ -217,7 +220,7 @@ int oracle_type_allowed(int op, int t)
     case OR_PRELU:
         return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64 ||
                t == OT_U32;
-    case OR_BATCHNORM:
+    case OR_BATCHNORM: case OR_BIAS_PRELU:
         return is_float_type(t);
     }
     return 0;
@@ -478,14 +481,18 @@ int oracle_offsets(const int64_t *sa, int ra, const int64_t *sb, int rb, const i
  *    order written, y = (x - mean) / sqrt(var + eps) * scale + bias;
  *  - Clip: B = [2] holding {min, max}; has_min / has_max say which bound
  *    applies; y = x, then raised to min if below it, then lowered to max if
- *    above it.
+ *    above it;
+ *  - BiasPRelu: A = x [N, C, ...] (rank >= 2), B = [2, C] holding bias and
+ *    slope rows; t = x + bias, then y = t when t >= 0 else slope * t, in
+ *    binary32, rounded once to x's type.
  * Out shape: see oracle_output_shape.
  */
 int oracle_output_shape(int op, const int64_t *sa, int ra, const int64_t *sb, int rb,
                         int64_t *so, int *ro)
 {
-    if (op == OR_BATCHNORM) {
-        if (ra < 2 || rb != 2 || sb[0] != 4 || sb[1] != sa[1]) return OR_SHAPES;
+    if (op == OR_BATCHNORM || op == OR_BIAS_PRELU) {
+        const int64_t rows = op == OR_BATCHNORM ? 4 : 2;
+        if (ra < 2 || rb != 2 || sb[0] != rows || sb[1] != sa[1]) return OR_SHAPES;
         for (int d = 0; d < ra; ++d) so[d] = sa[d];
         *ro = ra;
         return OR_OK;
@@ -522,8 +529,10 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
     int64_t count = idx ? n_idx : total;
     int to = oracle_output_type(op, t);
     aligned_strides(sa, ra, r, sta);
-    if (op != OR_BATCHNORM && op != OR_CLIP) aligned_strides(sb, rb, r, stb);
-    else for (int d = 0; d < r; ++d) stb[d] = 0;
+    if (op != OR_BATCHNORM && op != OR_CLIP && op != OR_BIAS_PRELU)
+        aligned_strides(sb, rb, r, stb);
+    else
+        for (int d = 0; d < r; ++d) stb[d] = 0;
 
     for (int64_t k = 0; k < count; ++k) {
         int64_t f = idx ? idx[k] : k;
@@ -539,6 +548,15 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             float mean = load_float(B, t, 2 * C + c);
             float var = load_float(B, t, 3 * C + c);
             float y = (x - mean) / sqrtf(var + eps) * scale + bias;
+            store_float(out, t, k, y);
+            continue;
+        }
+        if (op == OR_BIAS_PRELU) {
+            /* y = x + bias[c]; y >= 0 ? y : slope[c] * y; binary32 steps, one
+               rounding to x's type at the end */
+            int64_t C = sb[1], c = channel_of(f, so, r);
+            float y = load_float(A, t, oa) + load_float(B, t, c);
+            if (!(y >= 0.0f)) y = load_float(B, t, C + c) * y;
             store_float(out, t, k, y);
             continue;
         }

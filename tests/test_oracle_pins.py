@@ -702,6 +702,41 @@ def test_batchnorm_within_float64_bound():
     assert (err <= 8 * 2.0 ** -24 * scale + 1e-30).all()
 
 
+@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
+def test_bias_prelu_matches_float32_numpy_chain(dtype):
+    """BiasPRelu (0verkilll/onnx ops, ConvPReluOp: per-channel bias add then
+    per-channel PReLU in one pass): t = x + bias[c], y = t >= 0 ? t : slope[c]*t,
+    each step a binary32 operation, rounded once to x's type."""
+    C = 6
+    x = datagen.make("normal", dtype, (3, C, 5, 7), 31, 0)
+    x.reshape(-1)[:SPECIALS.size] = datagen.float_to(SPECIALS, dtype)
+    params = np.concatenate([datagen.normal(31, 1, C), datagen.uniform(31, 2, C, -0.5, 0.5)])
+    B = datagen.float_to(params.astype(np.float32), dtype).reshape(2, C)
+    got, st = oracle.run("BiasPRelu", x, B, dtype)
+    assert st == 0
+    if dtype == "bfloat16":
+        to32 = lambda v: torch.from_numpy(v.view(np.int16).copy()).view(torch.bfloat16).float()
+        xf, bf = to32(x), to32(B)
+        t = xf + bf[0].view(1, C, 1, 1)
+        y = torch.where(t >= 0, t, bf[1].view(1, C, 1, 1) * t)
+        want = y.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    else:
+        xf, bf = x.astype(np.float32), B.astype(np.float32)
+        with np.errstate(all="ignore"):
+            t = xf + bf[0].reshape(1, C, 1, 1)
+            y = np.where(t >= 0, t, bf[1].reshape(1, C, 1, 1) * t).astype(np.float32)
+        want = y.astype(x.dtype)
+    assert_bits_equal(got, want, dtype, "BiasPRelu")
+
+
+def test_bias_prelu_shapes():
+    x = np.zeros((2, 3, 4), np.float32)
+    assert oracle.run("BiasPRelu", x, np.zeros((2, 3), np.float32), "float32")[0].shape == x.shape
+    for bad in [(2, 4), (3, 3), (4, 3), (3,)]:
+        with pytest.raises(Exception):
+            oracle.run("BiasPRelu", x, np.zeros(bad, np.float32), "float32")
+
+
 def test_clip_matches_numpy_and_bounds_are_optional():
     x = float_corpus(5000, 48)
     lohi = f32(-2.5, 3.0)
