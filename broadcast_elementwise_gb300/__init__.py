@@ -32,7 +32,7 @@ OPS = {"Add": 0, "Sub": 1, "Mul": 2, "Div": 3, "Mod": 4, "Pow": 5,
        "And": 11, "Or": 12, "Xor": 13,
        "BitwiseAnd": 14, "BitwiseOr": 15, "BitwiseXor": 16,
        "BitShift": 17, "PRelu": 18, "BatchNormalization": 19, "Clip": 20,
-       "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24}
+       "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24, "BiasPRelu": 25}
 DTYPES = {"float32": 1, "uint8": 2, "int32": 6, "int64": 7, "bool": 9, "float16": 10,
           "uint32": 12, "bfloat16": 16}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}

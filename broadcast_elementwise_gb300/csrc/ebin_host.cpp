@@ -72,7 +72,7 @@ bool type_legal(int op, ebin_dtype t) {
     case EBIN_OP_BITWISE_AND: case EBIN_OP_BITWISE_OR: case EBIN_OP_BITWISE_XOR: return is_int(t);
     case EBIN_OP_BITSHIFT: return t == EBIN_UINT8 || t == EBIN_UINT32;
     case EBIN_OP_PRELU: return is_float(t) || is_signed_int(t) || t == EBIN_UINT32;
-    case EBIN_OP_BATCHNORM: return is_float(t);
+    case EBIN_OP_BATCHNORM: case EBIN_OP_BIAS_PRELU: return is_float(t);
     }
     return false;
 }
@@ -100,11 +100,14 @@ bool scalar_attr_op(int op) {
 }
 
 // B is an ordinary broadcast tensor (not the BN parameter block or Clip bounds).
-bool plain_b(int op) { return op != EBIN_OP_BATCHNORM && op != EBIN_OP_CLIP; }
+bool plain_b(int op) {
+    return op != EBIN_OP_BATCHNORM && op != EBIN_OP_CLIP && op != EBIN_OP_BIAS_PRELU;
+}
 
 // Output keeps A's shape: B broadcasts one way.
 bool one_way(int op) {
-    return op == EBIN_OP_PRELU || op == EBIN_OP_BATCHNORM || op == EBIN_OP_CLIP;
+    return op == EBIN_OP_PRELU || op == EBIN_OP_BATCHNORM || op == EBIN_OP_CLIP ||
+           op == EBIN_OP_BIAS_PRELU;
 }
 
 std::atomic<uint64_t> g_next_id{1};
@@ -234,8 +237,11 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     int64_t lb[kMaxRank];
     int rlb = rb;
     int64_t plane = 0;
-    if (d.op == EBIN_OP_BATCHNORM) {
-        if (ra < 2 || rb != 2 || sb[0] != 4 || sb[1] != sa[1]) return EBIN_ERR_INCOMPATIBLE_SHAPES;
+    if (d.op == EBIN_OP_BATCHNORM || d.op == EBIN_OP_BIAS_PRELU) {
+        // parameter rows of C: BN scale, bias, mean, var; BiasPRelu bias, slope
+        const int64_t rows = d.op == EBIN_OP_BATCHNORM ? 4 : 2;
+        if (ra < 2 || rb != 2 || sb[0] != rows || sb[1] != sa[1])
+            return EBIN_ERR_INCOMPATIBLE_SHAPES;
         rlb = ra;
         for (int i = 0; i < ra; ++i) lb[i] = (i == 1) ? sa[1] : 1;
         plane = sa[1];
@@ -541,7 +547,8 @@ cudaError_t ebin::launch(const Launch &L) {
     case EBIN_OP_GREATER_OR_EQUAL: EBIN_PICK(cmp)
     case EBIN_OP_AND: case EBIN_OP_OR: case EBIN_OP_XOR: case EBIN_OP_BITWISE_AND:
     case EBIN_OP_BITWISE_OR: case EBIN_OP_BITWISE_XOR: case EBIN_OP_BITSHIFT: EBIN_PICK(logic)
-    case EBIN_OP_PRELU: case EBIN_OP_BATCHNORM: case EBIN_OP_CLIP: EBIN_PICK(chan)
+    case EBIN_OP_PRELU: case EBIN_OP_BATCHNORM: case EBIN_OP_CLIP: case EBIN_OP_BIAS_PRELU:
+        EBIN_PICK(chan)
     case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV: EBIN_PICK(ext)
     default: return cudaErrorInvalidValue;
     }

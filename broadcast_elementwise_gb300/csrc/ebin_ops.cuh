@@ -524,6 +524,30 @@ template <class T> struct OpPRelu : PlainB<T, T> {
     }
 };
 
+// BiasPRelu (0verkilll/onnx ops, ConvPReluOp: the per-output-channel bias add
+// and PReLU fused into one pass, here as an elementwise operator): t = x + bias,
+// y = t when t >= 0 else slope * t, binary32 steps rounded once to x's type.
+// B holds two rows (bias, slope) of `plane` elements, read once per row.
+struct BiasSlope {
+    float bias, slope;
+};
+
+template <class T> struct OpBiasPRelu {
+    using In = T;
+    using Out = T;
+    using BV = BiasSlope;
+    static constexpr bool kPlainB = false;
+    static constexpr bool kLegal = is_float_v<T>;
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
+        return BiasSlope{Tr<T>::in(B[off]), Tr<T>::in(B[off + p.plane])};
+    }
+    __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
+        const float t = __fadd_rn(Tr<T>::in(a), q.bias);
+        return Tr<T>::out(t >= 0.0f ? t : __fmul_rn(q.slope, t));
+    }
+};
+
 // Inference BatchNormalization: y = (x - mean) / sqrt(var + eps) * scale + bias,
 // each step rounded in binary32 in the order written.  B holds four rows
 // (scale, bias, mean, var) of `plane` elements; the per-channel sqrt is formed

@@ -1,5 +1,5 @@
-// PRelu, inference BatchNormalization and Clip for one element class
-// (EBIN_DT): the per-channel and scalar broadcasts of the engine.
+// PRelu, inference BatchNormalization, Clip and BiasPRelu for one element
+// class (EBIN_DT): the per-channel and scalar broadcasts of the engine.
 #include "ebin_kernels.cuh"
 
 namespace ebin {
@@ -10,6 +10,7 @@ cudaError_t EBIN_GROUP_FN(chan)(const Launch &L) {
     case 18: return launch_op<OpPRelu<T>>(L);
     case 19: return launch_op<OpBN<T>>(L);
     case 20: return launch_op<OpClip<T>>(L);
+    case 25: return launch_op<OpBiasPRelu<T>>(L);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -8,7 +8,8 @@ operand j of a workload uses stream seed*16 + j.
   2  Mul fp32, A and B [2^28] ~ N(0,1); Div with B = |N(0,1)| + 0.5       seed 1
   3  bf16 x[8,64,256,256] ~ N(0,1): Add b[64,1,1] ~ U(-0.5,0.5),
      PRelu slope[64,1,1] ~ U(0,0.3), BatchNormalization with scale, bias,
-     mean ~ N(0,1), var ~ U(0.1,2), eps 1e-5 (parameters stored in bf16)  seed 2
+     mean ~ N(0,1), var ~ U(0.1,2), eps 1e-5 (parameters stored in bf16);
+     and the fused BiasPRelu with bias ~ N(0,1), slope ~ U(0,0.3)         seed 2
   4  Mod opset 28, A[4096,4096] against a scalar B and against B[4096,1]:
      fp32 fmod 0 and 1 with A ~ U(-100,100) holding 1% exact +-0 and
      B ~ U(-7,7) without |B| < 0.01; int32 fmod 0 with A ~ U[-2^31,2^31)
@@ -79,6 +80,12 @@ def cases(scale_log2: int = 0) -> list[Case]:
                     lambda: make("normal", "bfloat16", x, 2, 0),
                     lambda: _bn_params(2, 64, "bfloat16"),
                     "inner_vector_outer", 3))
+    out.append(Case("biasprelu_bf16_per_channel", "BiasPRelu", "bfloat16", {}, x, (2, 64),
+                    lambda: make("normal", "bfloat16", x, 2, 0),
+                    lambda: float_to(np.concatenate([normal(2, 1, 64),
+                                                     uniform(2, 2, 64, 0.0, 0.3)])
+                                     .astype(np.float32), "bfloat16").reshape(2, 64),
+                    "inner_vector_outer", 3, ["fused"]))
     m = (4096, 4096)
     for fm in (0, 1):
         out.append(Case("mod_f32_fmod%d_scalar" % fm, "Mod", "float32", {"fmod": fm}, m, (),

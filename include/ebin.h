@@ -84,7 +84,13 @@ typedef enum ebin_op {
     EBIN_OP_MIN = 22,             /* IEEE 754-2019 minimum: NaN if either is NaN, -0 < +0 */
     EBIN_OP_RSUB = 23,            /* B - A */
     EBIN_OP_RDIV = 24,            /* B / A; integer A == 0 raises EBIN_DEVICE_DIV_BY_ZERO */
-    EBIN_OP_COUNT = 25
+    /* 0verkilll/onnx ops, ConvPReluOp: the per-output-channel bias add and
+     * PReLU of the fused Conv -> PReLU epilogue, as one elementwise pass.
+     * B = [2, C]: bias and slope rows, channel axis 1 of A (rank >= 2);
+     * y = t >= 0 ? t : slope * t with t = x + bias, binary32 steps rounded
+     * once to A's type; floating types only. */
+    EBIN_OP_BIAS_PRELU = 25,
+    EBIN_OP_COUNT = 26
 } ebin_op;
 
 /* Element types, numbered as ONNX TensorProto.DataType. */

@@ -46,6 +46,7 @@ BN_CASES = [
     ("contiguous", (1, 64), (4, 64)),
     ("empty", (0, 16, 4), (4, 16)),
 ]
+BIAS_PRELU_CASES = [(fam, sa, (2, sb[1])) for fam, sa, sb in BN_CASES]
 CLIP_CASES = [
     ("right_scalar", (300007,), (2,)),
     ("right_scalar", (40, 77), (2,)),
@@ -58,6 +59,8 @@ def cases_for(op):
         return PRELU_CASES
     if op == "BatchNormalization":
         return BN_CASES
+    if op == "BiasPRelu":
+        return BIAS_PRELU_CASES
     if op == "Clip":
         return CLIP_CASES
     return TWO_WAY_CASES
