@@ -33,7 +33,7 @@ OPS = ["Add", "Sub", "Mul", "Div", "Mod", "Pow",
        "BitwiseAnd", "BitwiseOr", "BitwiseXor",
        "BitShift", "PRelu",
        "BatchNormalization", "Clip",
-       "Max", "Min", "RSub", "RDiv", "BiasPRelu"]
+       "Max", "Min", "RSub", "RDiv", "BiasPRelu", "MulAdd"]
 DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool"]
 STORAGE = {"float32": np.float32, "float16": np.float16, "bfloat16": np.uint16,
            "int32": np.int32, "int64": np.int64, "uint8": np.uint8, "uint32": np.uint32,
@@ -81,6 +81,10 @@ def _load():
             lib.oracle_eval.restype = i32
             lib.oracle_output_shape.argtypes = [i32, p, i32, p, i32, p, p]
             lib.oracle_output_shape.restype = i32
+            lib.oracle_eval3.argtypes = [i32, i32, p, i32, p, i32, p, i32, p, p, p, p, p, i64]
+            lib.oracle_eval3.restype = i32
+            lib.oracle_output_shape3.argtypes = [p, i32, p, i32, p, i32, p, p]
+            lib.oracle_output_shape3.restype = i32
             lib.oracle_broadcast_shape.argtypes = [p, i32, p, i32, p, p]
             lib.oracle_broadcast_shape.restype = i32
             lib.oracle_offsets.argtypes = [p, i32, p, i32, p, i64, p, p]
@@ -187,6 +191,50 @@ def run(op: str, a: np.ndarray, b: np.ndarray | None, dtype: str, *, shape_a=Non
     if rc:
         raise ValueError(RC[rc])
     return out, int(status.value)
+
+
+def output_shape3(shape_a, shape_b, shape_c) -> tuple:
+    """broadcast(broadcast(A, B), C)."""
+    sa, ra = _shape_arr(shape_a)
+    sb, rb = _shape_arr(shape_b)
+    sc, rc = _shape_arr(shape_c)
+    so = np.zeros(8, np.int64)
+    ro = ctypes.c_int(0)
+    rcode = _load().oracle_output_shape3(sa.ctypes.data, ra, sb.ctypes.data, rb, sc.ctypes.data,
+                                         rc, so.ctypes.data, ctypes.byref(ro))
+    if rcode:
+        raise ValueError(RC[rcode])
+    return tuple(int(v) for v in so[: ro.value])
+
+
+def run3(op: str, a: np.ndarray, b: np.ndarray, c: np.ndarray, dtype: str, *, idx=None):
+    """Evaluate the three-input ``op`` (MulAdd) on host arrays in ``dtype``'s storage.
+
+    Returns the output (output shape, or one element per flat index in ``idx``).
+    """
+    lib = _load()
+    arrs = [np.ascontiguousarray(x) for x in (a, b, c)]
+    for x in arrs:
+        if x.dtype != STORAGE[dtype]:
+            raise TypeError("storage %s does not match %s" % (x.dtype, dtype))
+    shapes = [_shape_arr(tuple(x.shape)) for x in arrs]
+    oshape = output_shape3(*(tuple(x.shape) for x in arrs))
+    if idx is None:
+        out = np.empty(oshape, STORAGE[dtype])
+        idx_p, n_idx = None, 0
+    else:
+        idx = np.ascontiguousarray(idx, dtype=np.int64)
+        out = np.empty(idx.size, STORAGE[dtype])
+        idx_p, n_idx = idx.ctypes.data, idx.size
+    rcode = lib.oracle_eval3(OPS.index(op), DTYPES.index(dtype),
+                             shapes[0][0].ctypes.data, shapes[0][1],
+                             shapes[1][0].ctypes.data, shapes[1][1],
+                             shapes[2][0].ctypes.data, shapes[2][1],
+                             arrs[0].ctypes.data, arrs[1].ctypes.data, arrs[2].ctypes.data,
+                             out.ctypes.data, idx_p, n_idx)
+    if rcode:
+        raise ValueError(RC[rcode])
+    return out
 
 
 def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:

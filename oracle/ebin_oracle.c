@@ -20,7 +20,8 @@
  *    formula, channel axis 1), PReluOp (x >= 0 ? x : slope*x, slope broadcast
  *    to the data), ClipOp (optional min/max bounds), Add/Sub/Mul,
  *    ConvPReluOp (the per-output-channel bias add and PReLU fused into one
- *    pass: here without the convolution, as BiasPRelu).
+ *    pass: here without the convolution, as BiasPRelu), MulAddOp (y = a*b + c
+ *    over three inputs broadcast together).
  *  - ncnn operators.md -- batchnorm, bias, binaryop (operation types MAX,
  *    MIN, RSUB, RDIV; with_scalar), clip.
  * Where the pages are silent the plain reading is taken (IEEE-754 binary32
@@ -49,7 +50,7 @@ enum {
     OR_BITSHIFT, OR_PRELU,
     OR_BATCHNORM, OR_CLIP,
     OR_MAX, OR_MIN, OR_RSUB, OR_RDIV,
-    OR_BIAS_PRELU,
+    OR_BIAS_PRELU, OR_MULADD,
     OR_NUM_OPS
 };
 enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL, OT_NUM };
@@ -205,7 +206,7 @@ int oracle_type_allowed(int op, int t)
     switch (op) {
     case OR_ADD: case OR_SUB: case OR_MUL: case OR_DIV: case OR_MOD:
     case OR_LESS: case OR_GREATER: case OR_LESS_EQUAL: case OR_GREATER_EQUAL:
-    case OR_CLIP: case OR_MAX: case OR_MIN: case OR_RSUB: case OR_RDIV:
+    case OR_CLIP: case OR_MAX: case OR_MIN: case OR_RSUB: case OR_RDIV: case OR_MULADD:
         return t != OT_BOOL && t >= 0 && t < OT_NUM;
     case OR_POW:
         return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64;
@@ -523,6 +524,7 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
     int r;
     *status = 0;
     if (op < 0 || op >= OR_NUM_OPS || !oracle_type_allowed(op, t)) return OR_TYPE;
+    if (op == OR_MULADD) return OR_ARGS;              /* three inputs: oracle_eval3 */
     int rc = oracle_output_shape(op, sa, ra, sb, rb, so, &r);
     if (rc) return rc;
     int64_t total = numel(so, r);
@@ -599,6 +601,61 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
         }
     }
     return OR_OK;
+}
+
+/*
+ * MulAdd (0verkilll/onnx ops, MulAddOp): y = (a * b) + c.  The shapes follow
+ * the unfused pair: the product has shape broadcast(A, B) and the output
+ * broadcast(broadcast(A, B), C).  Each output element is computed from its full
+ * multi-index: a binary32 product and a binary32 sum, each rounded on its own,
+ * then one rounding to a 16-bit type; integers wrap.  Elements at the flat
+ * indices idx[0..n) (all when idx == NULL) are stored densely in out.
+ */
+int oracle_eval3(int op, int t, const int64_t *sa, int ra, const int64_t *sb, int rb,
+                 const int64_t *sc, int rc, const void *A, const void *B, const void *C,
+                 void *out, const int64_t *idx, int64_t n_idx)
+{
+    int64_t sab[OR_MAX_RANK], so[OR_MAX_RANK];
+    int64_t sta[OR_MAX_RANK], stb[OR_MAX_RANK], stc[OR_MAX_RANK];
+    int rab, r;
+    if (op != OR_MULADD || !oracle_type_allowed(op, t)) return OR_TYPE;
+    int rcode = oracle_broadcast_shape(sa, ra, sb, rb, sab, &rab);
+    if (rcode) return rcode;
+    rcode = oracle_broadcast_shape(sab, rab, sc, rc, so, &r);
+    if (rcode) return rcode;
+    aligned_strides(sa, ra, r, sta);
+    aligned_strides(sb, rb, r, stb);
+    aligned_strides(sc, rc, r, stc);
+    int64_t total = numel(so, r);
+    int64_t count = idx ? n_idx : total;
+    for (int64_t k = 0; k < count; ++k) {
+        int64_t f = idx ? idx[k] : k;
+        if (f < 0 || f >= total) return OR_ARGS;
+        int64_t oa, ob, oc, unused;
+        offsets_of(f, so, r, sta, stb, &oa, &ob);
+        offsets_of(f, so, r, stc, stc, &oc, &unused);
+        if (is_float_type(t)) {
+            float p = load_float(A, t, oa) * load_float(B, t, ob);
+            float y = p + load_float(C, t, oc);
+            store_float(out, t, k, y);
+        } else {
+            uint64_t y = (uint64_t)load_int(A, t, oa) * (uint64_t)load_int(B, t, ob) +
+                         (uint64_t)load_int(C, t, oc);
+            store_int(out, t, k, y);
+        }
+    }
+    return OR_OK;
+}
+
+/* output shape of a three-input operator: broadcast(broadcast(A, B), C) */
+int oracle_output_shape3(const int64_t *sa, int ra, const int64_t *sb, int rb,
+                         const int64_t *sc, int rc, int64_t *so, int *ro)
+{
+    int64_t sab[OR_MAX_RANK];
+    int rab;
+    int rcode = oracle_broadcast_shape(sa, ra, sb, rb, sab, &rab);
+    if (rcode) return rcode;
+    return oracle_broadcast_shape(sab, rab, sc, rc, so, ro);
 }
 
 /* bulk forms of the conversions above, for the pin tests */

@@ -6,6 +6,7 @@ arithmetic with ``fractions``, arbitrary precision ``mpmath``), a closed form
 or worked table under ``tests/golden/`` (each with its citation), an identity,
 or brute force over tiny shapes.
 """
+import itertools
 import math
 import os
 from fractions import Fraction
@@ -735,6 +736,65 @@ def test_bias_prelu_shapes():
     for bad in [(2, 4), (3, 3), (4, 3), (3,)]:
         with pytest.raises(Exception):
             oracle.run("BiasPRelu", x, np.zeros(bad, np.float32), "float32")
+
+
+# --------------------------------------------------------------------------- MulAdd
+# 0verkilll/onnx ops, MulAddOp: y = (a * b) + c, shapes as the unfused Mul + Add.
+
+def _muladd_inputs(dtype, shapes, seed):
+    return [datagen.make("normal" if dtype in ("float32", "float16", "bfloat16") else "bits",
+                         dtype, sh, seed, k) for k, sh in enumerate(shapes)]
+
+
+@pytest.mark.parametrize("shapes", [((4, 8, 5, 6), (1, 8, 1, 1), (4, 8, 5, 6)),
+                                    ((1,), (3, 7, 11), (3, 7, 11)),
+                                    ((2, 1, 5), (1, 4, 1), (4, 5))])
+@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
+def test_muladd_matches_float32_chain(dtype, shapes):
+    a, b, c = _muladd_inputs(dtype, shapes, 41)
+    for x in (a, b, c):
+        x.reshape(-1)[: min(x.size, 5)] = datagen.float_to(SPECIALS[:5], dtype)[: min(x.size, 5)]
+    got = oracle.run3("MulAdd", a, b, c, dtype)
+    if dtype == "bfloat16":
+        t = [torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).float() for x in (a, b, c)]
+        want = (t[0] * t[1] + t[2]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    else:
+        f = [x.astype(np.float32) for x in (a, b, c)]
+        with np.errstate(all="ignore"):
+            prod = np.multiply(f[0], f[1], dtype=np.float32)       # rounded product
+            want = np.add(prod, f[2], dtype=np.float32).astype(a.dtype)
+    assert got.shape == np.broadcast_shapes(*shapes)
+    assert_bits_equal(got, want, dtype, "MulAdd")
+
+
+@pytest.mark.parametrize("dtype", ["int32", "int64", "uint8", "uint32"])
+def test_muladd_int_wraps_like_python_integers(dtype):
+    a, b, c = _muladd_inputs(dtype, [(3, 1, 40), (1, 5, 40), (40,)], 42)
+    got = oracle.run3("MulAdd", a, b, c, dtype)
+    lo, hi = INT_LIMITS[dtype]
+    A, B, C = np.broadcast_arrays(a.astype(object), b.astype(object), c.astype(object))
+    want = np.vectorize(lambda x, y, z: wrap(int(x) * int(y) + int(z), dtype), otypes=[object])(
+        A, B, C).astype(datagen.STORAGE[dtype])
+    assert (got == want).all()
+
+
+def test_muladd_broadcast_brute_force():
+    """Index mapping of three-way broadcasting against numpy's, with small integer
+    values so that every result is exact."""
+    rng = np.random.default_rng(43)
+    dims = [()] + [s for r in (1, 2, 3) for s in itertools.product((1, 2, 3), repeat=r)]
+    for _ in range(1500):
+        sh = [dims[i] for i in rng.integers(0, len(dims), 3)]
+        try:
+            want_shape = np.broadcast_shapes(*sh)
+        except ValueError:
+            with pytest.raises(ValueError):
+                oracle.run3("MulAdd", *[np.zeros(s, np.float32) for s in sh], "float32")
+            continue
+        a, b, c = [rng.integers(-8, 9, s).astype(np.float32) for s in sh]
+        got = oracle.run3("MulAdd", a, b, c, "float32")
+        assert got.shape == want_shape
+        assert (got == a * b + c).all(), sh
 
 
 def test_clip_matches_numpy_and_bounds_are_optional():
