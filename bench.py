@@ -189,26 +189,41 @@ def upload(arr):
     return torch.from_numpy(flat).to("cuda", non_blocking=False)
 
 
+def _case_plan(eb, c):
+    """(descriptor, plan, host inputs) of a workload case of two or three inputs."""
+    desc = eb.descriptor(c.op, c.dtype, **c.attrs)
+    if c.make_c is not None:
+        plan = eb.Plan3(desc, c.shape_a, c.shape_b, c.shape_c)
+        return desc, plan, [c.make_a(), c.make_b(), c.make_c()]
+    return desc, eb.Plan(desc, c.shape_a, c.shape_b), [c.make_a(), c.make_b()]
+
+
+def _case_run(eb, plan, bufs, stream):
+    """One launch of a case's plan on device buffers [inputs..., out]."""
+    if len(bufs) == 4:
+        eb.execute3(plan, *bufs, stream=stream)
+    else:
+        eb.execute(plan, *bufs, stream=stream)
+
+
 def time_family_table(eb, torch, cases, l2_bytes, peak):
     """Per-workload GB/s with enough rotating buffer sets to defeat L2."""
     rows = {}
     stream = torch.cuda.current_stream()
     for c in cases:
-        a, b = c.make_a(), c.make_b()
-        desc = eb.descriptor(c.op, c.dtype, **c.attrs)
-        plan = eb.Plan(desc, c.shape_a, c.shape_b)
+        desc, plan, host = _case_plan(eb, c)
         osz = eb.ITEMSIZE[desc.out_dtype]
         isz = eb.ITEMSIZE[c.dtype]
-        nbytes = a.size * isz + b.size * isz + plan.numel * osz
+        nbytes = sum(x.size for x in host) * isz + plan.numel * osz
         nrot = max(1, math.ceil(4 * l2_bytes / max(nbytes, 1)))
         nrot = min(nrot, 64)
         sets = []
-        da, db = upload(a), upload(b)
+        dev = [upload(x) for x in host]
         for i in range(nrot):
-            sets.append((da.clone() if i else da, db.clone() if i else db,
-                         torch.empty(plan.numel * osz, dtype=torch.uint8, device="cuda")))
+            sets.append([d.clone() if i else d for d in dev] +
+                        [torch.empty(plan.numel * osz, dtype=torch.uint8, device="cuda")])
         for i in range(3):
-            eb.execute(plan, *sets[i % nrot], stream=stream)
+            _case_run(eb, plan, sets[i % nrot], stream)
         # back-to-back launches between two events (the per-launch cost of a
         # pipeline), rotating buffer sets so that each launch reads from HBM
         reps = max(32, 2 * nrot)
@@ -218,7 +233,7 @@ def time_family_table(eb, torch, cases, l2_bytes, peak):
             torch.cuda.synchronize()
             e0.record(stream)
             for i in range(reps):
-                eb.execute(plan, *sets[i % nrot], stream=stream)
+                _case_run(eb, plan, sets[i % nrot], stream)
             e1.record(stream)
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1) * 1e-3 / reps)
@@ -232,7 +247,7 @@ def time_family_table(eb, torch, cases, l2_bytes, peak):
                         "frac_of_measured": round(gbs / peak, 4),
                         "frac_of_8tbs": round(gbs / HBM_NOMINAL_GBS, 4),
                         "rotating_sets": nrot, "timing": "%d back-to-back launches" % reps}
-        del sets, da, db
+        del sets, dev
         torch.cuda.empty_cache()
     return rows
 
@@ -469,27 +484,25 @@ def run_one_case(args):
     from datagen import workloads
 
     c = workloads.by_name(args.only, scale_log2=args.scale_log2)
-    a, b = c.make_a(), c.make_b()
-    desc = eb.descriptor(c.op, c.dtype, **c.attrs)
-    plan = eb.Plan(desc, c.shape_a, c.shape_b)
-    da, db = upload(a), upload(b)
+    desc, plan, host = _case_plan(eb, c)
     osz = eb.ITEMSIZE[desc.out_dtype]
-    out = torch.empty(plan.numel * osz, dtype=torch.uint8, device="cuda")
+    bufs = [upload(x) for x in host] + \
+        [torch.empty(plan.numel * osz, dtype=torch.uint8, device="cuda")]
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        eb.execute(plan, da, db, out, stream=stream)
+        _case_run(eb, plan, bufs, stream)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     torch.cuda.synchronize()
     for s0, s1 in evs:
         s0.record(stream)
-        eb.execute(plan, da, db, out, stream=stream)
+        _case_run(eb, plan, bufs, stream)
         s1.record(stream)
     torch.cuda.synchronize()
     if eb.get_device_status(stream) != 0:
         raise RuntimeError("device status set")
     ts = [x.elapsed_time(y) * 1e-3 for x, y in evs]
-    nbytes = a.size * eb.ITEMSIZE[c.dtype] + b.size * eb.ITEMSIZE[c.dtype] + plan.numel * osz
+    nbytes = sum(x.size for x in host) * eb.ITEMSIZE[c.dtype] + plan.numel * osz
     med = statistics.median(ts)
     print(json.dumps({"case": c.name, "family": plan.family, "numel": plan.numel,
                       "bytes": nbytes, "us_median": round(med * 1e6, 2),

@@ -32,7 +32,7 @@ OPS = {"Add": 0, "Sub": 1, "Mul": 2, "Div": 3, "Mod": 4, "Pow": 5,
        "And": 11, "Or": 12, "Xor": 13,
        "BitwiseAnd": 14, "BitwiseOr": 15, "BitwiseXor": 16,
        "BitShift": 17, "PRelu": 18, "BatchNormalization": 19, "Clip": 20,
-       "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24, "BiasPRelu": 25}
+       "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24, "BiasPRelu": 25, "MulAdd": 26}
 DTYPES = {"float32": 1, "uint8": 2, "int32": 6, "int64": 7, "bool": 9, "float16": 10,
           "uint32": 12, "bfloat16": 16}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
@@ -81,6 +81,10 @@ def _load():
         "ebin_descriptor_destroy": (None, [vp]),
         "ebin_plan_create": (i32, [vp, p_i64, i32, p_i64, i32, ctypes.POINTER(vp)]),
         "ebin_plan_create_forced": (i32, [vp, p_i64, i32, p_i64, i32, i32, ctypes.POINTER(vp)]),
+        "ebin_plan_create3": (i32, [vp, p_i64, i32, p_i64, i32, p_i64, i32, ctypes.POINTER(vp)]),
+        "ebin_plan_create3_forced": (i32, [vp, p_i64, i32, p_i64, i32, p_i64, i32, i32,
+                                           ctypes.POINTER(vp)]),
+        "ebin_execute3": (i32, [vp, vp, vp, vp, vp, vp]),
         "ebin_plan_output_shape": (i32, [vp, p_i64, ctypes.POINTER(ctypes.c_int)]),
         "ebin_plan_numel": (i32, [vp, p_i64]),
         "ebin_plan_family": (i32, [vp, ctypes.POINTER(ctypes.c_int)]),
@@ -180,6 +184,21 @@ def ebin_plan_create_forced(desc, shape_a, shape_b, family) -> int:
     return out.value
 
 
+def ebin_plan_create3(desc, shape_a, shape_b, shape_c, family=None) -> int:
+    """Marshal ebin_plan_create3 (family None) or ebin_plan_create3_forced."""
+    sa, ra = _shape(shape_a)
+    sb, rb = _shape(shape_b)
+    sc, rc = _shape(shape_c)
+    out = ctypes.c_void_p()
+    if family is None:
+        _check(lib.ebin_plan_create3(desc, sa, ra, sb, rb, sc, rc, ctypes.byref(out)),
+               "ebin_plan_create3")
+    else:
+        _check(lib.ebin_plan_create3_forced(desc, sa, ra, sb, rb, sc, rc, family,
+                                            ctypes.byref(out)), "ebin_plan_create3_forced")
+    return out.value
+
+
 def ebin_plan_output_shape(plan) -> tuple:
     shape = (ctypes.c_int64 * MAX_RANK)()
     rank = ctypes.c_int()
@@ -224,6 +243,10 @@ def ebin_plan_cache_clear() -> None:
 
 def ebin_execute(plan, A, B, out, stream) -> None:
     _check(lib.ebin_execute(plan, A, B, out, stream), "ebin_execute")
+
+
+def ebin_execute3(plan, A, B, C, out, stream) -> None:
+    _check(lib.ebin_execute3(plan, A, B, C, out, stream), "ebin_execute3")
 
 
 def ebin_execute_host(plan, host_a, host_b, host_out, dev_a, dev_b, dev_out, stream) -> None:
@@ -345,6 +368,26 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+class Plan3(Plan):
+    """Holds one three-input plan reference (MulAdd) for (descriptor, shapes A, B, C)."""
+
+    def __init__(self, desc: Descriptor, shape_a, shape_b, shape_c, family: str | None = None):
+        self.desc = desc
+        self.shape_a = tuple(int(d) for d in shape_a)
+        self.shape_b = tuple(int(d) for d in shape_b)
+        self.shape_c = tuple(int(d) for d in shape_c)
+        self.handle = ebin_plan_create3(desc.handle, self.shape_a, self.shape_b, self.shape_c,
+                                        None if family is None else FAMILIES[family])
+        self.output_shape = ebin_plan_output_shape(self.handle)
+        self.numel = ebin_plan_numel(self.handle)
+        self.family = FAMILY_NAMES[ebin_plan_family(self.handle)]
+
+
+def execute3(plan: Plan3, A, B, C, out, stream=None) -> None:
+    """Enqueue a three-input plan on device buffers (torch tensors or int addresses)."""
+    ebin_execute3(plan.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(out), _stream(stream))
 
 
 def execute(plan: Plan, A, B, out, stream=None) -> None:

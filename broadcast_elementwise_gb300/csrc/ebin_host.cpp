@@ -65,6 +65,7 @@ bool type_legal(int op, ebin_dtype t) {
     case EBIN_OP_LESS: case EBIN_OP_GREATER: case EBIN_OP_LESS_OR_EQUAL:
     case EBIN_OP_GREATER_OR_EQUAL: case EBIN_OP_CLIP:
     case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV:
+    case EBIN_OP_MULADD:
         return is_float(t) || is_int(t);
     case EBIN_OP_POW: return is_float(t) || is_signed_int(t);
     case EBIN_OP_EQUAL: return true;
@@ -103,6 +104,9 @@ bool scalar_attr_op(int op) {
 bool plain_b(int op) {
     return op != EBIN_OP_BATCHNORM && op != EBIN_OP_CLIP && op != EBIN_OP_BIAS_PRELU;
 }
+
+// Operators with three inputs (planned by ebin_plan_create3).
+bool ternary(int op) { return op == EBIN_OP_MULADD; }
 
 // Output keeps A's shape: B broadcasts one way.
 bool one_way(int op) {
@@ -340,6 +344,118 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     return EBIN_OK;
 }
 
+// Loop family of a three-input plan: one row traversal for inner strides in
+// {0, 1}, labelled by its shape; else the general kernel.
+int family_of3(const ebin_plan_s &p, int forced, bool *ok) {
+    *ok = true;
+    if (p.numel == 0) return ebin::FAM_EMPTY;
+    const Geom &g = p.g;
+    const int r = g.rank;
+    const int64_t G = 16 / (int64_t)ebin_dtype_size(p.dt);
+    const int64_t inner = g.n[r - 1];
+    const int64_t ia = g.sa[r - 1], ib = g.sb[r - 1], ic = g.sc[r - 1];
+    auto unit = [](int64_t v) { return v == 0 || v == 1; };
+    const bool vec = inner % G == 0 && unit(ia) && unit(ib) && unit(ic) &&
+                     (ia == 1 || ib == 1 || ic == 1) && (r == 1 || inner >= 64);
+    const int natural = !vec ? ebin::FAM_GENERAL_STRIDED
+                        : r > 1 ? ebin::FAM_INNER_VECTOR_OUTER
+                        : (ia == 1 && ib == 1 && ic == 1) ? ebin::FAM_CONTIGUOUS
+                                                          : ebin::FAM_RIGHT_SCALAR;
+    if (forced == EBIN_FAMILY_AUTO) return natural;
+    if (forced == EBIN_FAMILY_GENERAL_STRIDED) return forced;
+    *ok = forced == natural;
+    return forced;
+}
+
+ebin_status build_plan3(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
+                        int rb, const int64_t *sc, int rc, int forced, ebin_plan_s **out) {
+    if (ra < 0 || rb < 0 || rc < 0) return EBIN_ERR_INVALID_ARG;
+    if (ra > kMaxRank || rb > kMaxRank || rc > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
+    if ((ra > 0 && !sa) || (rb > 0 && !sb) || (rc > 0 && !sc)) return EBIN_ERR_INVALID_ARG;
+    const int64_t *shp[3] = {sa, sb, sc};
+    const int rk[3] = {ra, rb, rc};
+    for (int k = 0; k < 3; ++k)
+        for (int i = 0; i < rk[k]; ++i)
+            if (shp[k][i] < 0) return EBIN_ERR_INVALID_ARG;
+
+    // 1. right-align and broadcast all three (NumPy rules)
+    const int r = std::max(ra, std::max(rb, rc));
+    int64_t so[kMaxRank], x[3][kMaxRank];
+    for (int i = 0; i < r; ++i) {
+        int64_t o = 1;
+        for (int k = 0; k < 3; ++k) {
+            const int j = i - (r - rk[k]);
+            x[k][i] = j >= 0 ? shp[k][j] : 1;
+            if (x[k][i] == o || x[k][i] == 1) continue;
+            if (o != 1) return EBIN_ERR_INCOMPATIBLE_SHAPES;
+            o = x[k][i];
+        }
+        so[i] = o;
+    }
+
+    auto *p = new ebin_plan_s;
+    p->desc_id = d.id;
+    p->dt = d.dt;
+    p->rank_a = ra;
+    p->rank_b = rb;
+    p->rank_c = rc;
+    for (int i = 0; i < ra; ++i) p->shape_a[i] = sa[i];
+    for (int i = 0; i < rb; ++i) p->shape_b[i] = sb[i];
+    for (int i = 0; i < rc; ++i) p->shape_c[i] = sc[i];
+    p->op = d.op;
+    p->attrs = d.attrs;
+    p->out_dt = d.out_dt;
+    p->rank_out = r;
+    for (int i = 0; i < r; ++i) p->shape_out[i] = so[i];
+    p->numel = product(so, r);
+    p->numel_a = product(sa, ra);
+    p->numel_b = product(sb, rb);
+    p->numel_c = product(sc, rc);
+
+    // 2. dense strides, zero on broadcast dims;  3. drop unit dims;  4. merge
+    int64_t st[3][kMaxRank];
+    for (int k = 0; k < 3; ++k) {
+        int64_t acc = 1;
+        for (int i = r - 1; i >= 0; --i) {
+            st[k][i] = x[k][i] == 1 ? 0 : acc;
+            acc *= x[k][i];
+        }
+    }
+    Geom g{};
+    int n = 0;
+    for (int i = 0; i < r; ++i) {
+        if (so[i] == 1) continue;
+        if (n > 0 && g.sa[n - 1] == st[0][i] * so[i] && g.sb[n - 1] == st[1][i] * so[i] &&
+            g.sc[n - 1] == st[2][i] * so[i]) {
+            g.n[n - 1] *= so[i];
+            g.sa[n - 1] = st[0][i];
+            g.sb[n - 1] = st[1][i];
+            g.sc[n - 1] = st[2][i];
+            continue;
+        }
+        g.n[n] = so[i];
+        g.sa[n] = st[0][i];
+        g.sb[n] = st[1][i];
+        g.sc[n] = st[2][i];
+        ++n;
+    }
+    if (n == 0) {  // a single element
+        g.n[0] = 1;
+        g.sa[0] = g.sb[0] = g.sc[0] = 1;
+        n = 1;
+    }
+    g.rank = n;
+    p->g = g;
+    bool ok = true;
+    p->family = family_of3(*p, forced, &ok);
+    if (!ok) {
+        delete p;
+        return EBIN_ERR_FAMILY;
+    }
+    *out = p;
+    return EBIN_OK;
+}
+
 // ------------------------------------------------------------------ plan cache
 std::mutex g_cache_mu;
 std::list<ebin_plan_s *> g_cache;  // most recently used first
@@ -350,12 +466,14 @@ void plan_unref(ebin_plan_s *p) {
 }
 
 bool key_equal(const ebin_plan_s &p, uint64_t id, const int64_t *sa, int ra, const int64_t *sb,
-               int rb) {
-    if (p.desc_id != id || p.rank_a != ra || p.rank_b != rb) return false;
+               int rb, const int64_t *sc = nullptr, int rc = -1) {
+    if (p.desc_id != id || p.rank_a != ra || p.rank_b != rb || p.rank_c != rc) return false;
     for (int i = 0; i < ra; ++i)
         if (p.shape_a[i] != sa[i]) return false;
     for (int i = 0; i < rb; ++i)
         if (p.shape_b[i] != sb[i]) return false;
+    for (int i = 0; i < rc; ++i)
+        if (p.shape_c[i] != sc[i]) return false;
     return true;
 }
 
@@ -379,19 +497,15 @@ extern "C" void ebin_descriptor_destroy(ebin_descriptor_t desc) {
     delete desc;
 }
 
-extern "C" ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *shape_a,
-                                        int rank_a, const int64_t *shape_b, int rank_b,
-                                        ebin_plan_t *out) {
-    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
-    *out = nullptr;
-    if (desc->attrs.with_scalar) rank_b = 0;   // shape B is not read
-    if (rank_a < 0 || rank_b < 0) return EBIN_ERR_INVALID_ARG;
-    if (rank_a > kMaxRank || rank_b > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
-    if ((rank_a > 0 && !shape_a) || (rank_b > 0 && !shape_b)) return EBIN_ERR_INVALID_ARG;
+namespace {
+
+// LRU lookup, or build and insert (two-input plans: rc = -1).
+ebin_status cached_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
+                        int rb, const int64_t *sc, int rc, ebin_plan_t *out) {
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
         for (auto it = g_cache.begin(); it != g_cache.end(); ++it) {
-            if (key_equal(**it, desc->id, shape_a, rank_a, shape_b, rank_b)) {
+            if (key_equal(**it, d.id, sa, ra, sb, rb, sc, rc)) {
                 ebin_plan_s *p = *it;
                 g_cache.splice(g_cache.begin(), g_cache, it);
                 p->refs.fetch_add(1);
@@ -403,7 +517,9 @@ extern "C" ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *s
         ++g_misses;
     }
     ebin_plan_s *p = nullptr;
-    const ebin_status st = build_plan(*desc, shape_a, rank_a, shape_b, rank_b, EBIN_FAMILY_AUTO, &p);
+    const ebin_status st = rc < 0
+        ? build_plan(d, sa, ra, sb, rb, EBIN_FAMILY_AUTO, &p)
+        : build_plan3(d, sa, ra, sb, rb, sc, rc, EBIN_FAMILY_AUTO, &p);
     if (st != EBIN_OK) return st;
     ebin_plan_s *evicted = nullptr;
     {
@@ -420,14 +536,58 @@ extern "C" ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *s
     return EBIN_OK;
 }
 
+}  // namespace
+
+extern "C" ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *shape_a,
+                                        int rank_a, const int64_t *shape_b, int rank_b,
+                                        ebin_plan_t *out) {
+    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (ternary(desc->op)) return EBIN_ERR_INVALID_ARG;   // three inputs: ebin_plan_create3
+    if (desc->attrs.with_scalar) rank_b = 0;   // shape B is not read
+    if (rank_a < 0 || rank_b < 0) return EBIN_ERR_INVALID_ARG;
+    if (rank_a > kMaxRank || rank_b > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
+    if ((rank_a > 0 && !shape_a) || (rank_b > 0 && !shape_b)) return EBIN_ERR_INVALID_ARG;
+    return cached_plan(*desc, shape_a, rank_a, shape_b, rank_b, nullptr, -1, out);
+}
+
 extern "C" ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape_a,
                                                int rank_a, const int64_t *shape_b, int rank_b,
                                                ebin_family family, ebin_plan_t *out) {
     if (!desc || !out) return EBIN_ERR_INVALID_ARG;
     *out = nullptr;
+    if (ternary(desc->op)) return EBIN_ERR_INVALID_ARG;
     if (desc->attrs.with_scalar) rank_b = 0;
     ebin_plan_s *p = nullptr;
     const ebin_status st = build_plan(*desc, shape_a, rank_a, shape_b, rank_b, (int)family, &p);
+    if (st != EBIN_OK) return st;
+    *out = p;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_plan_create3(ebin_descriptor_t desc, const int64_t *shape_a,
+                                         int rank_a, const int64_t *shape_b, int rank_b,
+                                         const int64_t *shape_c, int rank_c, ebin_plan_t *out) {
+    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!ternary(desc->op)) return EBIN_ERR_INVALID_ARG;
+    if (rank_a < 0 || rank_b < 0 || rank_c < 0) return EBIN_ERR_INVALID_ARG;
+    if (rank_a > kMaxRank || rank_b > kMaxRank || rank_c > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
+    if ((rank_a > 0 && !shape_a) || (rank_b > 0 && !shape_b) || (rank_c > 0 && !shape_c))
+        return EBIN_ERR_INVALID_ARG;
+    return cached_plan(*desc, shape_a, rank_a, shape_b, rank_b, shape_c, rank_c, out);
+}
+
+extern "C" ebin_status ebin_plan_create3_forced(ebin_descriptor_t desc, const int64_t *shape_a,
+                                                int rank_a, const int64_t *shape_b, int rank_b,
+                                                const int64_t *shape_c, int rank_c,
+                                                ebin_family family, ebin_plan_t *out) {
+    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!ternary(desc->op)) return EBIN_ERR_INVALID_ARG;
+    ebin_plan_s *p = nullptr;
+    const ebin_status st =
+        build_plan3(*desc, shape_a, rank_a, shape_b, rank_b, shape_c, rank_c, (int)family, &p);
     if (st != EBIN_OK) return st;
     *out = p;
     return EBIN_OK;
@@ -550,6 +710,7 @@ cudaError_t ebin::launch(const Launch &L) {
     case EBIN_OP_PRELU: case EBIN_OP_BATCHNORM: case EBIN_OP_CLIP: case EBIN_OP_BIAS_PRELU:
         EBIN_PICK(chan)
     case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV: EBIN_PICK(ext)
+    case EBIN_OP_MULADD: EBIN_PICK(tern)
     default: return cudaErrorInvalidValue;
     }
 #undef EBIN_PICK
@@ -627,12 +788,50 @@ ebin_status launch_counted(const ebin::Launch &L) {
 
 extern "C" ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
                                     void *stream) {
-    if (!plan) return EBIN_ERR_INVALID_ARG;
+    if (!plan || plan->rank_c >= 0) return EBIN_ERR_INVALID_ARG;
     const ebin_plan_s &p = *plan;
     if (p.numel == 0) return EBIN_OK;  // empty dims: no work, nothing read
     ebin::Launch L;
     const ebin_status st = prepare_launch(p, A, B, out, static_cast<cudaStream_t>(stream), L);
     if (st != EBIN_OK) return st;
+    return launch_counted(L);
+}
+
+extern "C" ebin_status ebin_execute3(ebin_plan_t plan, const void *A, const void *B,
+                                     const void *C, void *out, void *stream) {
+    if (!plan || plan->rank_c < 0) return EBIN_ERR_INVALID_ARG;
+    const ebin_plan_s &p = *plan;
+    if (p.numel == 0) return EBIN_OK;
+    if (!A || !B || !C || !out) return EBIN_ERR_INVALID_ARG;
+    // an input may be out only as the identical buffer of the output's size
+    const int64_t isz = (int64_t)ebin_dtype_size(p.dt);
+    const int64_t out_bytes = p.numel * (int64_t)ebin_dtype_size(p.out_dt);
+    const void *in[3] = {A, B, C};
+    const int64_t cnt[3] = {p.numel_a, p.numel_b, p.numel_c};
+    for (int k = 0; k < 3; ++k)
+        if (overlaps(in[k], cnt[k] * isz, out, out_bytes) &&
+            !(in[k] == out && cnt[k] == p.numel && p.dt == p.out_dt))
+            return EBIN_ERR_ALIAS;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EBIN_ERR_CUDA;
+    ebin::Launch L{};
+    L.op = p.op;
+    L.dt = dt_class(p.dt);
+    L.family = p.family;
+    L.g = p.g;
+    L.numel = p.numel;
+    L.A = A;
+    L.B = B;
+    L.C = C;
+    L.out = out;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.num_sms = sm_count(dev);
+    L.status = nullptr;
+    if (L.family != ebin::FAM_GENERAL_STRIDED) {
+        bool aligned = (uintptr_t)out % 16 == 0;
+        for (int k = 0; k < 3; ++k) aligned = aligned && (uintptr_t)in[k] % 16 == 0;
+        if (!aligned) L.family = ebin::FAM_GENERAL_STRIDED;
+    }
     return launch_counted(L);
 }
 
@@ -697,7 +896,7 @@ ebin_status host_serial(const ebin_plan_s &p, const ebin::Launch &L, const void 
 extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, const void *host_b,
                                          void *host_out, void *dev_a, void *dev_b, void *dev_out,
                                          void *stream) {
-    if (!plan) return EBIN_ERR_INVALID_ARG;
+    if (!plan || plan->rank_c >= 0) return EBIN_ERR_INVALID_ARG;
     const ebin_plan_s &p = *plan;
     if (p.numel == 0) return EBIN_OK;
     if (!host_a || !host_out || !dev_a || !dev_out) return EBIN_ERR_INVALID_ARG;

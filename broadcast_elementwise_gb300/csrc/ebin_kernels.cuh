@@ -162,6 +162,7 @@ __device__ __forceinline__ void compute_group(const typename Op::In *a, const ty
 struct KArgs {
     const void *A;
     const void *B;
+    const void *C;       // three-input kernels only
     void *out;
     int64_t numel;
     OpArgs args;
@@ -325,6 +326,7 @@ struct RowArgs {
     int64_t M;            // extent of the run dim (1 for rank-1 plans)
     int64_t smA, smB;     // A and B strides along the run dim
     int64_t ia, ib;       // inner element strides (general kernel)
+    int64_t smC, ic;      // the same for a third input (three-input kernels)
     int32_t tpr;          // threads per row
     int32_t rs;           // rows in parallel (threads = tpr * rs)
     int32_t kr;           // rows per thread per tile
@@ -336,6 +338,7 @@ struct RowArgs {
     int64_t pn[kMaxRank];
     int64_t psa[kMaxRank];
     int64_t psb[kMaxRank];
+    int64_t psc[kMaxRank];
     FastDiv f_cc, f_runs, f_tpr, f_rs;
     FastDiv f_pn[kMaxRank];
 };
@@ -493,6 +496,171 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     flush_err<Op>(p.status, err);
 }
 
+// ---------------------------------------------------------------- three inputs
+//
+// The row traversal of k_rows for an operator of three inputs (Op::apply3):
+// the same tile (prefix index, run of rows, column chunk), V column groups a
+// row-width apart per thread, kr rows walked with constant pointer steps.
+// IA / IB / IC: 1 = the input advances along the row (16-byte packs when
+// G > 1), 0 = one value per row, 2 = any inner stride (G == 1).
+template <class In, int G, int I> struct RowOperand {
+    static constexpr bool kVec = I == 1 && G > 1;
+    using P = std::conditional_t<kVec, Pack<In, G>, Pack<In, 1>>;
+    __device__ __forceinline__ static P load(const In *q) {
+        P x;
+        if constexpr (kVec) x = ld_stream<In, G>(q);
+        else x.v[0] = *q;
+        return x;
+    }
+    __device__ __forceinline__ static In at(const P &x, int k) {
+        if constexpr (kVec) return x.v[k];
+        else return x.v[0];
+    }
+    // element distance between column groups cstep apart, and to the first group
+    __device__ __forceinline__ static int64_t step(int64_t cstep, int64_t inner) {
+        return I == 1 ? cstep * G : I == 2 ? cstep * inner : 0;
+    }
+};
+
+template <class Op, int G, int IA, int IB, int IC, int V>
+__global__ void __launch_bounds__(kThreads) k_rows3(KArgs p, RowArgs r) {
+    pdl_enter();
+    using In = typename Op::In;
+    using Out = typename Op::Out;
+    static_assert(G == 1 || (IA != 2 && IB != 2 && IC != 2), "runtime strides need G == 1");
+    using OA = RowOperand<In, G, IA>;
+    using OB = RowOperand<In, G, IB>;
+    using OC = RowOperand<In, G, IC>;
+
+    const int t = threadIdx.x;
+    if (t >= r.tpr * r.rs) return;
+    const bool wide = r.wide != 0;
+    const int64_t tile = blockIdx.x;
+    const int64_t q1 = udiv(tile, r.cc, r.f_cc, wide);
+    const int64_t ci = tile - q1 * r.cc;
+    const int64_t pi = udiv(q1, r.runs, r.f_runs, wide);
+    const int64_t ri = q1 - pi * r.runs;
+    const int rsub = r.rs == 1 ? 0 : (int)fastdiv((uint32_t)t, r.f_tpr);
+    const int64_t lane = ci * (int64_t)r.tpr + (t - rsub * r.tpr);
+    const int64_t c0 = lane + (ci * (int64_t)r.tpr) * (V - 1);
+    const int64_t cstep = r.tpr;
+    if (c0 >= r.cols) return;
+    const int64_t m0 = ri * (int64_t)(r.rs * r.kr) + rsub;
+    if (m0 >= r.M) return;
+    bool ok[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) ok[v] = c0 + v * cstep < r.cols;
+
+    int64_t baseA = 0, baseB = 0, baseC = 0;
+    int64_t rem = pi;
+#pragma unroll
+    for (int d = kMaxRank - 1; d >= 0; --d) {
+        if (d < r.nprefix) {
+            const int64_t q = udiv(rem, r.pn[d], r.f_pn[d], wide);
+            const int64_t digit = rem - q * r.pn[d];
+            rem = q;
+            baseA += digit * r.psa[d];
+            baseB += digit * r.psb[d];
+            baseC += digit * r.psc[d];
+        }
+    }
+    const int64_t vsA = OA::step(cstep, r.ia), vsB = OB::step(cstep, r.ib),
+                  vsC = OC::step(cstep, r.ic);
+    const In *pa = static_cast<const In *>(p.A) + baseA + m0 * r.smA + OA::step(c0, r.ia);
+    const In *pb = static_cast<const In *>(p.B) + baseB + m0 * r.smB + OB::step(c0, r.ib);
+    const In *pc = static_cast<const In *>(p.C) + baseC + m0 * r.smC + OC::step(c0, r.ic);
+    Out *po = static_cast<Out *>(p.out) + (pi * r.M + m0) * r.L + c0 * G;
+    const int64_t stepA = (int64_t)r.rs * r.smA, stepB = (int64_t)r.rs * r.smB,
+                  stepC = (int64_t)r.rs * r.smC, stepO = (int64_t)r.rs * r.L;
+    const int64_t rows_left = r.M - m0 + r.rs - 1;
+    const int64_t left = wide ? rows_left / r.rs : (int64_t)fastdiv((uint32_t)rows_left, r.f_rs);
+    const int n = (int)(left < r.kr ? left : r.kr);
+
+    // an input constant along the row is one value for all v
+    constexpr int VA = IA == 0 ? 1 : V, VB = IB == 0 ? 1 : V, VC = IC == 0 ? 1 : V;
+    typename OA::P a[VA];
+    typename OB::P b[VB];
+    typename OC::P c[VC];
+#pragma unroll 1
+    for (int j = 0; j < n; ++j) {
+        if (j == 0 || stepA != 0) {
+#pragma unroll
+            for (int v = 0; v < VA; ++v)
+                if (ok[v]) a[v] = OA::load(pa + v * vsA);
+        }
+        if (j == 0 || stepB != 0) {
+#pragma unroll
+            for (int v = 0; v < VB; ++v)
+                if (ok[v]) b[v] = OB::load(pb + v * vsB);
+        }
+        if (j == 0 || stepC != 0) {
+#pragma unroll
+            for (int v = 0; v < VC; ++v)
+                if (ok[v]) c[v] = OC::load(pc + v * vsC);
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            if (ok[v]) {
+                Pack<Out, G> o;
+#pragma unroll
+                for (int k = 0; k < G; ++k)
+                    o.v[k] = Op::apply3(OA::at(a[IA == 0 ? 0 : v], k),
+                                        OB::at(b[IB == 0 ? 0 : v], k),
+                                        OC::at(c[IC == 0 ? 0 : v], k));
+                if constexpr (G > 1) st_stream<Out, G>(po + v * cstep * G, o);
+                else po[v * cstep] = o.v[0];
+            }
+        }
+        pa += stepA;
+        pb += stepB;
+        pc += stepC;
+        po += stepO;
+    }
+}
+
+// Three inputs at rank 1: each dense (I = 1, 16-byte packs) or one value (I = 0,
+// read once per thread), one tile of kThreads x U groups per CTA as in
+// k_contiguous; a ragged tail of numel % G elements element by element.
+template <class Op, int IA, int IB, int IC, int U>
+__global__ void __launch_bounds__(kThreads) k_flat3(KArgs p) {
+    pdl_enter();
+    using In = typename Op::In;
+    using Out = typename Op::Out;
+    constexpr int G = 16 / sizeof(In);
+    const In *A = static_cast<const In *>(p.A);
+    const In *B = static_cast<const In *>(p.B);
+    const In *C = static_cast<const In *>(p.C);
+    Out *O = static_cast<Out *>(p.out);
+    const In sa = IA == 0 ? A[0] : In{}, sb = IB == 0 ? B[0] : In{}, sc = IC == 0 ? C[0] : In{};
+    const int64_t ng = p.numel / G;
+    const int64_t base = (int64_t)blockIdx.x * (kThreads * U) + threadIdx.x;
+    Pack<In, G> a[IA ? U : 1], b[IB ? U : 1], c[IC ? U : 1];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t g = base + (int64_t)u * kThreads;
+        if (g < ng) {
+            if constexpr (IA) a[u] = ld_stream<In, G>(A + g * G);
+            if constexpr (IB) b[u] = ld_stream<In, G>(B + g * G);
+            if constexpr (IC) c[u] = ld_stream<In, G>(C + g * G);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t g = base + (int64_t)u * kThreads;
+        if (g < ng) {
+            Pack<Out, G> o;
+#pragma unroll
+            for (int k = 0; k < G; ++k)
+                o.v[k] = Op::apply3(IA ? a[IA ? u : 0].v[k] : sa, IB ? b[IB ? u : 0].v[k] : sb,
+                                    IC ? c[IC ? u : 0].v[k] : sc);
+            st_stream<Out, G>(O + g * G, o);
+        }
+    }
+    for (int64_t e = ng * G + (int64_t)blockIdx.x * kThreads + threadIdx.x; e < p.numel;
+         e += (int64_t)gridDim.x * kThreads)
+        O[e] = Op::apply3(IA ? A[e] : sa, IB ? B[e] : sb, IC ? C[e] : sc);
+}
+
 // ---------------------------------------------------------------- launch helpers
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -501,6 +669,7 @@ KArgs kargs(const Launch &L) {
     KArgs k;
     k.A = L.A;
     k.B = L.B;
+    k.C = L.C;
     k.out = L.out;
     k.numel = L.numel;
     k.args = L.args;
@@ -556,14 +725,17 @@ inline RowArgs row_args(const Geom &g, int G, int V, int num_sms) {
     r.cols = r.L / G;
     r.ia = g.sa[rank - 1];
     r.ib = g.sb[rank - 1];
+    r.ic = g.sc[rank - 1];
     if (rank >= 2) {
         r.M = g.n[rank - 2];
         r.smA = g.sa[rank - 2];
         r.smB = g.sb[rank - 2];
+        r.smC = g.sc[rank - 2];
     } else {
         r.M = 1;
         r.smA = 0;
         r.smB = 0;
+        r.smC = 0;
     }
     r.nprefix = rank >= 2 ? rank - 2 : 0;
     int64_t P = 1;
@@ -571,6 +743,7 @@ inline RowArgs row_args(const Geom &g, int G, int V, int num_sms) {
         r.pn[i] = g.n[i];
         r.psa[i] = g.sa[i];
         r.psb[i] = g.sb[i];
+        r.psc[i] = g.sc[i];
         r.f_pn[i] = make_fastdiv((uint64_t)g.n[i]);
         P *= g.n[i];
     }
@@ -707,6 +880,66 @@ cudaError_t launch_op(const Launch &L) {
             return run_rows_vector<Op, false>(L);
         case FAM_INNER_VECTOR_OUTER: return run_rows_vector<Op, false>(L);
         case FAM_GENERAL_STRIDED: return run_general<Op>(L);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+}
+
+// Three-input operators: the row kernel for inner strides in {0, 1}, else the
+// element-by-element form.
+template <class Op, int G, int IA, int IB, int IC, int V>
+cudaError_t run_rows3_kernel(const Launch &L) {
+    const RowArgs r = row_args(L.g, G, V, L.num_sms);
+    const int64_t tiles = row_tiles(r);
+    if (tiles > kMaxGrid) return cudaErrorInvalidConfiguration;
+    return launch_pdl(k_rows3<Op, G, IA, IB, IC, V>, tiles, r.tpr * r.rs, L.stream,
+                      kargs<Op>(L), r);
+}
+
+template <class Op, int IA, int IB, int IC>
+cudaError_t run_flat3(const Launch &L) {
+    constexpr int G = 16 / sizeof(typename Op::In);
+    const int64_t ng = L.numel / G;
+    int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
+    grid = std::min<int64_t>(grid, kMaxGrid);
+    return launch_pdl(k_flat3<Op, IA, IB, IC, kUnrollFlat>, grid, kThreads, L.stream,
+                      kargs<Op>(L));
+}
+
+template <class Op>
+cudaError_t launch_op3(const Launch &L) {
+    if constexpr (!Op::kLegal) {
+        return cudaErrorInvalidValue;
+    } else {
+        constexpr int G = 16 / sizeof(typename Op::In);
+        // one column group per thread and row: two or three dense inputs hold
+        // enough bytes in flight (MulAdd bf16 x[8,64,256,256] * [1,64,1,1] + y:
+        // 32.9 us, against 37.7 with two groups)
+        constexpr int V = 1;
+        if (L.family == FAM_GENERAL_STRIDED) return run_rows3_kernel<Op, 1, 2, 2, 2, 2>(L);
+        if (L.family == FAM_EMPTY) return cudaSuccess;
+        const int r = L.g.rank;
+        const int code = (int)(L.g.sa[r - 1] * 4 + L.g.sb[r - 1] * 2 + L.g.sc[r - 1]);
+        if (r == 1) {   // streaming: one tile per CTA
+            switch (code) {
+            case 7: return run_flat3<Op, 1, 1, 1>(L);
+            case 6: return run_flat3<Op, 1, 1, 0>(L);
+            case 5: return run_flat3<Op, 1, 0, 1>(L);
+            case 4: return run_flat3<Op, 1, 0, 0>(L);
+            case 3: return run_flat3<Op, 0, 1, 1>(L);
+            case 2: return run_flat3<Op, 0, 1, 0>(L);
+            case 1: return run_flat3<Op, 0, 0, 1>(L);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+        switch (code) {
+        case 7: return run_rows3_kernel<Op, G, 1, 1, 1, V>(L);
+        case 6: return run_rows3_kernel<Op, G, 1, 1, 0, V>(L);
+        case 5: return run_rows3_kernel<Op, G, 1, 0, 1, V>(L);
+        case 4: return run_rows3_kernel<Op, G, 1, 0, 0, V>(L);
+        case 3: return run_rows3_kernel<Op, G, 0, 1, 1, V>(L);
+        case 2: return run_rows3_kernel<Op, G, 0, 1, 0, V>(L);
+        case 1: return run_rows3_kernel<Op, G, 0, 0, 1, V>(L);
         default: return cudaErrorInvalidValue;
         }
     }

@@ -43,6 +43,7 @@ struct Geom {
     int64_t n[kMaxRank];
     int64_t sa[kMaxRank];
     int64_t sb[kMaxRank];
+    int64_t sc[kMaxRank];   // third input (three-input operators), else 0
 };
 
 struct Launch {
@@ -53,6 +54,7 @@ struct Launch {
     int64_t numel;
     const void *A;
     const void *B;
+    const void *C;       // third input (three-input operators), else nullptr
     void *out;
     OpArgs args;
     uint32_t *status;    // device status word, or nullptr for operators that never flag
@@ -82,6 +84,7 @@ EBIN_DECLARE_GROUP(cmp)     // Equal Less Greater LessOrEqual GreaterOrEqual
 EBIN_DECLARE_GROUP(logic)   // And Or Xor BitwiseAnd/Or/Xor BitShift
 EBIN_DECLARE_GROUP(chan)    // PRelu BatchNormalization Clip BiasPRelu
 EBIN_DECLARE_GROUP(ext)     // Max Min RSub RDiv
+EBIN_DECLARE_GROUP(tern)    // MulAdd (three inputs)
 #undef EBIN_DECLARE_GROUP
 
 }  // namespace ebin

@@ -82,7 +82,7 @@ bool overlaps(const void *p, int64_t pb, const void *q, int64_t qb) {
 extern "C" ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, const void *B,
                                             void *out, void *stream, int status_slot,
                                             uint32_t *status_bits) {
-    if (!plan) return EBIN_ERR_INVALID_ARG;
+    if (!plan || plan->rank_c >= 0) return EBIN_ERR_INVALID_ARG;   // two-input plans only
     if (status_slot < 0 || status_slot >= EBIN_NOALLOC_STATUS_SLOTS) return EBIN_ERR_INVALID_ARG;
     const ebin_plan_s &p = *plan;
     if (status_bits) *status_bits = 0;

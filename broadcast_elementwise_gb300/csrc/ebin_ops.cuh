@@ -548,6 +548,24 @@ template <class T> struct OpBiasPRelu {
     }
 };
 
+// MulAdd (0verkilll/onnx ops, MulAddOp): y = (a * b) + c, a binary32 product
+// and sum each rounded on their own (never one FMA) and one rounding to a
+// 16-bit type; integers wrap.  A three-input operator (apply3).
+template <class T> struct OpMulAdd {
+    using In = T;
+    using Out = T;
+    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    __device__ __forceinline__ static T apply3(T a, T b, T c) {
+        if constexpr (is_float_v<T>) {
+            return Tr<T>::out(
+                __fadd_rn(__fmul_rn(Tr<T>::in(a), Tr<T>::in(b)), Tr<T>::in(c)));
+        } else {
+            using U = typename Tr<T>::UT;
+            return (T)((U)((U)a * (U)b) + (U)c);
+        }
+    }
+};
+
 // Inference BatchNormalization: y = (x - mean) / sqrt(var + eps) * scale + bias,
 // each step rounded in binary32 in the order written.  B holds four rows
 // (scale, bias, mean, var) of `plane` elements; the per-channel sqrt is formed

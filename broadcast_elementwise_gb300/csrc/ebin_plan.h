@@ -14,15 +14,17 @@ struct ebin_plan_s {
     uint64_t desc_id = 0;
     ebin_dtype dt = EBIN_FLOAT32;
     int rank_a = 0, rank_b = 0;
+    int rank_c = -1;                       // three-input plans only (else -1)
     int64_t shape_a[ebin::kMaxRank] = {};
     int64_t shape_b[ebin::kMaxRank] = {};
+    int64_t shape_c[ebin::kMaxRank] = {};
     // what execution needs (copied: a plan may outlive its descriptor)
     int op = 0;
     ebin_attrs attrs{};
     ebin_dtype out_dt = EBIN_FLOAT32;
     int rank_out = 0;
     int64_t shape_out[ebin::kMaxRank] = {};
-    int64_t numel = 0, numel_a = 0, numel_b = 0;
+    int64_t numel = 0, numel_a = 0, numel_b = 0, numel_c = 0;
     ebin::Geom g{};
     int family = ebin::FAM_EMPTY;
     int64_t plane = 0;

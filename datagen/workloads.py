@@ -9,7 +9,9 @@ operand j of a workload uses stream seed*16 + j.
   3  bf16 x[8,64,256,256] ~ N(0,1): Add b[64,1,1] ~ U(-0.5,0.5),
      PRelu slope[64,1,1] ~ U(0,0.3), BatchNormalization with scale, bias,
      mean ~ N(0,1), var ~ U(0.1,2), eps 1e-5 (parameters stored in bf16);
-     and the fused BiasPRelu with bias ~ N(0,1), slope ~ U(0,0.3)         seed 2
+     the fused BiasPRelu with bias ~ N(0,1), slope ~ U(0,0.3); and the
+     fused MulAdd x * s + y (residual scaling) with y ~ N(0,1) and s a
+     scalar or per-channel [1,64,1,1] ~ U(0,0.3)                          seed 2
   4  Mod opset 28, A[4096,4096] against a scalar B and against B[4096,1]:
      fp32 fmod 0 and 1 with A ~ U(-100,100) holding 1% exact +-0 and
      B ~ U(-7,7) without |B| < 0.01; int32 fmod 0 with A ~ U[-2^31,2^31)
@@ -41,6 +43,8 @@ class Case:
     family: str
     workload: int
     tags: list = field(default_factory=list)
+    shape_c: tuple | None = None                 # three-input operators (MulAdd)
+    make_c: Callable[[], np.ndarray] | None = None
 
 
 def _bn_params(seed: int, C: int, dtype: str) -> np.ndarray:
@@ -86,6 +90,13 @@ def cases(scale_log2: int = 0) -> list[Case]:
                                                      uniform(2, 2, 64, 0.0, 0.3)])
                                      .astype(np.float32), "bfloat16").reshape(2, 64),
                     "inner_vector_outer", 3, ["fused"]))
+    for name, sb, fam in (("muladd_bf16_residual_scale", (1,), "right_scalar"),
+                          ("muladd_bf16_per_channel", (1, 64, 1, 1), "inner_vector_outer")):
+        out.append(Case(name, "MulAdd", "bfloat16", {}, x, sb,
+                        lambda: make("normal", "bfloat16", x, 2, 0),
+                        (lambda sb=sb: make("uniform", "bfloat16", sb, 2, 3, lo=0.0, hi=0.3)),
+                        fam, 3, ["fused"], shape_c=x,
+                        make_c=lambda: make("normal", "bfloat16", x, 2, 4)))
     m = (4096, 4096)
     for fm in (0, 1):
         out.append(Case("mod_f32_fmod%d_scalar" % fm, "Mod", "float32", {"fmod": fm}, m, (),

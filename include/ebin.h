@@ -90,7 +90,13 @@ typedef enum ebin_op {
      * y = t >= 0 ? t : slope * t with t = x + bias, binary32 steps rounded
      * once to A's type; floating types only. */
     EBIN_OP_BIAS_PRELU = 25,
-    EBIN_OP_COUNT = 26
+    /* 0verkilll/onnx ops, MulAddOp: y = (a * b) + c over three inputs, shapes as
+     * the unfused Mul + Add (out = broadcast(broadcast(A, B), C)); binary32
+     * product and sum each rounded on their own (no FMA), one rounding to a
+     * 16-bit type; integers wrap.  The only three-input operator: plans come
+     * from ebin_plan_create3 and run with ebin_execute3. */
+    EBIN_OP_MULADD = 26,
+    EBIN_OP_COUNT = 27
 } ebin_op;
 
 /* Element types, numbered as ONNX TensorProto.DataType. */
@@ -231,6 +237,28 @@ ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape
                                     const int64_t *shape_b, int rank_b, ebin_family family,
                                     ebin_plan_t *out);
 
+/*
+ * Plan a three-input operator (MulAdd): the three shapes broadcast together
+ * (NumPy rules, right-aligned; the output is broadcast(broadcast(A, B), C)),
+ * unit dims are dropped and adjacent dims merged where all three stride sets
+ * allow.  Loop family: a row traversal (reported as CONTIGUOUS at rank 1 with
+ * three dense inputs, RIGHT_SCALAR at rank 1 otherwise, INNER_VECTOR_OUTER at
+ * rank >= 2) when every input moves along the innermost dim with stride 0 or
+ * 1, that dim is a multiple of 16 bytes of elements and, at rank >= 2, at
+ * least 64 long; else GENERAL_STRIDED.  Plans are cached like two-input plans,
+ * keyed on all three shapes.  The _forced form accepts AUTO, GENERAL_STRIDED or
+ * the family the plan would pick, and bypasses the cache.
+ * Errors: INVALID_ARG (also for a two-input descriptor), RANK_TOO_LARGE,
+ * INCOMPATIBLE_SHAPES, FAMILY.  ebin_plan_create refuses three-input
+ * descriptors with INVALID_ARG.
+ */
+ebin_status ebin_plan_create3(ebin_descriptor_t desc, const int64_t *shape_a, int rank_a,
+                              const int64_t *shape_b, int rank_b, const int64_t *shape_c,
+                              int rank_c, ebin_plan_t *out);
+ebin_status ebin_plan_create3_forced(ebin_descriptor_t desc, const int64_t *shape_a, int rank_a,
+                                     const int64_t *shape_b, int rank_b, const int64_t *shape_c,
+                                     int rank_c, ebin_family family, ebin_plan_t *out);
+
 /* Output shape: `shape` must hold EBIN_MAX_RANK entries; *rank receives its rank. */
 ebin_status ebin_plan_output_shape(ebin_plan_t plan, int64_t *shape, int *rank);
 
@@ -273,6 +301,17 @@ void ebin_plan_cache_clear(void);
  */
 ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
                          void *stream);
+
+/*
+ * Run a three-input plan: out = op(A, B, C) on device buffers, enqueued on
+ * `stream`.  A, B, C are dense in their own shapes; each may be `out` only as
+ * the identical buffer with the output's element count (anything else
+ * overlapping out is ALIAS).  Pointers off 16-byte alignment run the general
+ * kernel.  A two-input plan, or NULL buffers with work to do, give INVALID_ARG.
+ * Errors: INVALID_ARG, ALIAS, CUDA.
+ */
+ebin_status ebin_execute3(ebin_plan_t plan, const void *A, const void *B, const void *C,
+                          void *out, void *stream);
 
 /*
  * End-to-end form of ebin_execute for callers whose data lives in host

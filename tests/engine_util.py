@@ -56,6 +56,24 @@ def run_engine(op, dtype, a, b, *, shape_a=None, shape_b=None, family=None, attr
     return host.reshape(plan.output_shape), bits, plan.family
 
 
+def run_engine3(op, dtype, a, b, c, *, family=None, offset=0):
+    """Run one three-input plan on the GPU (offset: elements by which every
+    buffer is shifted off 16-byte alignment); returns (out, family)."""
+    import torch
+    import broadcast_elementwise_gb300 as eb
+    desc = eb.descriptor(op, dtype)
+    plan = eb.Plan3(desc, a.shape, b.shape, c.shape, family=family)
+    isz = eb.ITEMSIZE[dtype]
+    bufs = [to_device(np.concatenate([np.zeros(offset, x.dtype), x.reshape(-1)]))
+            for x in (a, b, c)]
+    out = torch.full(((max(plan.numel, 1) + offset) * isz + 16,), 0xAB, dtype=torch.uint8,
+                     device="cuda")
+    ptrs = [x.data_ptr() + offset * isz for x in bufs]
+    eb.execute3(plan, *ptrs, out.data_ptr() + offset * isz)
+    host = out.cpu().numpy()[offset * isz: (offset + plan.numel) * isz]
+    return host.view(datagen.STORAGE[dtype]).reshape(plan.output_shape), plan.family
+
+
 def specials(dtype):
     v = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 0.5, -2.5, 65504.0, 1e-7,
                   3.0, -7.0, 1e30, -1e-30], np.float32)

@@ -37,6 +37,18 @@ NAMES = [c.name for c in workloads.cases()]
 def test_workload_parity(name):
     c = workloads.by_name(name)
     a, b = c.make_a(), c.make_b()
+    if c.make_c is not None:                       # three inputs (MulAdd)
+        from engine_util import run_engine3
+        cc = c.make_c()
+        got, fam = run_engine3(c.op, c.dtype, a, b, cc)
+        assert fam == c.family
+        rng = np.random.default_rng(12345)
+        numel = got.size
+        idx = np.unique(np.concatenate([np.arange(1 << 16), np.arange(numel - (1 << 16), numel),
+                                        rng.integers(0, numel, 1 << 21)]))
+        want = oracle.run3(c.op, a, b, cc, c.dtype, idx=idx)
+        assert_bits_equal(got.reshape(-1)[idx], want, c.dtype, name + " (sampled)")
+        return
     got, bits, fam = run_engine(c.op, c.dtype, a, b, attrs=c.attrs)
     assert fam == c.family
     otype = "bool" if c.op == "Greater" else c.dtype

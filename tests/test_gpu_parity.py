@@ -9,6 +9,7 @@ bits), except floating Pow, which must be within 2 ulp of the oracle.
 import numpy as np
 import pytest
 
+import datagen
 import oracle
 from conftest import assert_bits_equal, ulp_distance
 from engine_util import FLOATS, MANIFEST, ONE_WAY, inputs_for, run_engine
@@ -142,3 +143,41 @@ def test_packed_compare_rows_with_ragged_ends(op, dtype, inner):
         got, _, fam = run_engine(op, dtype, a, b)
         assert fam in ("inner_vector_outer", "repeated_block"), fam
         compare(op, dtype, got, want, "%s %s %s x %s" % (op, dtype, sa, sb))
+
+
+MULADD_CASES = [
+    ("contiguous", (300016,), (300016,), (300016,)),
+    ("right_scalar", (300016,), (1,), (300016,)),
+    ("right_scalar", (), (300016,), ()),
+    ("inner_vector_outer", (4, 16, 8, 64), (1, 16, 1, 1), (4, 16, 8, 64)),
+    ("inner_vector_outer", (1, 16, 1, 1), (4, 16, 8, 64), (4, 16, 8, 64)),
+    ("inner_vector_outer", (6, 256), (256,), (6, 1)),
+    ("general_strided", (3, 1, 5), (1, 4, 1), (4, 5)),
+    ("general_strided", (7, 1, 93), (1, 5, 93), (93,)),
+    ("empty", (0, 4), (4,), (1, 4)),
+]
+
+
+@pytest.mark.parametrize("dtype", FLOATS + ("int32", "int64", "uint8", "uint32"))
+def test_muladd_parity_all_families(dtype):
+    """MulAdd (0verkilll/onnx ops, MulAddOp) through ebin_execute3: the pages'
+    fast paths (a scalar or per-channel multiplier, c shaped like the other
+    operand), general three-way broadcasts, natural and forced-general, and
+    buffers off 16-byte alignment."""
+    from engine_util import run_engine3
+    for i, (fam, sa, sb, sc) in enumerate(MULADD_CASES):
+        kind = "normal" if dtype in FLOATS else "bits"
+        a, b, c = [datagen.make(kind, dtype, s, 50 + i, k) for k, s in enumerate((sa, sb, sc))]
+        if dtype in FLOATS:
+            for x in (a, b, c):
+                sp = datagen.float_to(np.array([0.0, -0.0, np.inf, np.nan, -1.5], np.float32),
+                                      dtype)
+                x.reshape(-1)[: min(x.size, 5)] = sp[: min(x.size, 5)]
+        want = oracle.run3("MulAdd", a, b, c, dtype)
+        for forced, offset in ((None, 0), ("general_strided", 0), (None, 1)):
+            got, family = run_engine3("MulAdd", dtype, a, b, c, family=forced, offset=offset)
+            if forced is None and offset == 0:
+                assert family == fam, (sa, sb, sc, family)
+            assert_bits_equal(got, want, dtype, "MulAdd %s %s %s %s forced=%s offset=%d" %
+                              (dtype, sa, sb, sc, forced, offset))
+

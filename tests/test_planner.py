@@ -226,6 +226,57 @@ def test_with_scalar_plans_ignore_shape_b():
     assert eb.Plan(d, (0, 5), ()).family == "empty"
 
 
+def test_three_input_plans():
+    """MulAdd plans: broadcast(broadcast(A, B), C) against the oracle, the row
+    family for the pages' scalar and per-channel patterns, the shape-C cache key
+    and the separation from two-input entry points."""
+    d = eb.Descriptor("MulAdd", "float32")
+    rng = np.random.default_rng(5)
+    dims = [()] + [s for r in (1, 2, 3) for s in itertools.product((0, 1, 2, 3), repeat=r)]
+    for _ in range(400):
+        sh = [dims[i] for i in rng.integers(0, len(dims), 3)]
+        try:
+            want = oracle.output_shape3(*sh)
+        except ValueError:
+            with pytest.raises(eb.EbinError) as e:
+                eb.Plan3(d, *sh)
+            assert e.value.code == "incompatible_shapes"
+            continue
+        p = eb.Plan3(d, *sh)
+        assert p.output_shape == want and p.numel == int(np.prod(want))
+    x = (8, 64, 256, 256)
+    assert eb.Plan3(d, x, (1,), x).family == "right_scalar"
+    assert eb.Plan3(d, x, (1, 64, 1, 1), x).family == "inner_vector_outer"
+    assert eb.Plan3(d, (4096,), (4096,), (4096,)).family == "contiguous"
+    assert eb.Plan3(d, (3, 1, 5), (1, 4, 1), (4, 5)).family == "general_strided"
+    p1, p2 = eb.Plan3(d, (64, 64), (64,), (64, 64)), eb.Plan3(d, (64, 64), (64,), (64, 1))
+    assert p1.handle != p2.handle                          # shape C is part of the key
+    assert eb.Plan3(d, (64, 64), (64,), (64, 64)).handle == p1.handle
+    assert eb.Plan3(d, x, (1,), x, family="general_strided").family == "general_strided"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan3(d, x, (1,), x, family="inner_vector_outer")
+    assert e.value.code == "family"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (4,), (4,))                             # three inputs need plan_create3
+    assert e.value.code == "invalid_arg"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan3(eb.Descriptor("Add", "float32"), (4,), (4,), (4,))
+    assert e.value.code == "invalid_arg"
+    pe = eb.Plan3(d, (0, 4), (4,), (4,))
+    assert pe.family == "empty"
+    # (stream 0: no CUDA call is reached on these paths)
+    eb.ebin_execute3(pe.handle, None, None, None, None, None)   # nothing to do, nothing read
+    with pytest.raises(eb.EbinError) as e:
+        eb.ebin_execute(p1.handle, 16, 16, 16, None)       # a three-input plan
+    assert e.value.code == "invalid_arg"
+    with pytest.raises(eb.EbinError) as e:
+        eb.ebin_execute3(p1.handle, 16, None, 16, 4096, None)
+    assert e.value.code == "invalid_arg"
+    with pytest.raises(eb.EbinError) as e:                 # C overlaps out, not identical
+        eb.ebin_execute3(p1.handle, 1 << 20, 2 << 20, 3 << 20, (3 << 20) + 64, None)
+    assert e.value.code == "alias"
+
+
 def test_plan_cache_is_an_8_entry_lru():
     eb.ebin_plan_cache_clear()
     d = eb.Descriptor("Sub", "int32")
