@@ -82,6 +82,8 @@ def _load():
         "ebin_plan_create": (i32, [vp, p_i64, i32, p_i64, i32, ctypes.POINTER(vp)]),
         "ebin_plan_create_forced": (i32, [vp, p_i64, i32, p_i64, i32, i32, ctypes.POINTER(vp)]),
         "ebin_plan_create3": (i32, [vp, p_i64, i32, p_i64, i32, p_i64, i32, ctypes.POINTER(vp)]),
+        "ebin_plan_create_strided": (i32, [vp, p_i64, p_i64, i32, p_i64, p_i64, i32, i32,
+                                           ctypes.POINTER(vp)]),
         "ebin_plan_create3_forced": (i32, [vp, p_i64, i32, p_i64, i32, p_i64, i32, i32,
                                            ctypes.POINTER(vp)]),
         "ebin_execute3": (i32, [vp, vp, vp, vp, vp, vp]),
@@ -181,6 +183,18 @@ def ebin_plan_create_forced(desc, shape_a, shape_b, family) -> int:
     out = ctypes.c_void_p()
     _check(lib.ebin_plan_create_forced(desc, sa, ra, sb, rb, family, ctypes.byref(out)),
            "ebin_plan_create_forced")
+    return out.value
+
+
+def ebin_plan_create_strided(desc, shape_a, strides_a, shape_b, strides_b, family=-1) -> int:
+    """Marshal ebin_plan_create_strided (strides None = dense)."""
+    sa, ra = _shape(shape_a)
+    sb, rb = _shape(shape_b)
+    ta = _shape(strides_a)[0] if strides_a is not None else None
+    tb = _shape(strides_b)[0] if strides_b is not None else None
+    out = ctypes.c_void_p()
+    _check(lib.ebin_plan_create_strided(desc, sa, ta, ra, sb, tb, rb, family, ctypes.byref(out)),
+           "ebin_plan_create_strided")
     return out.value
 
 
@@ -342,11 +356,17 @@ class Descriptor:
 class Plan:
     """Holds one plan reference for (descriptor, shape_a, shape_b)."""
 
-    def __init__(self, desc: Descriptor, shape_a, shape_b, family: str | None = None):
+    def __init__(self, desc: Descriptor, shape_a, shape_b, family: str | None = None,
+                 strides_a=None, strides_b=None):
+        """strides_a / strides_b: element strides of strided input views (None = dense)."""
         self.desc = desc
         self.shape_a = tuple(int(d) for d in shape_a)
         self.shape_b = tuple(int(d) for d in shape_b)
-        if family is None:
+        if strides_a is not None or strides_b is not None:
+            self.handle = ebin_plan_create_strided(
+                desc.handle, self.shape_a, strides_a, self.shape_b, strides_b,
+                -1 if family is None else FAMILIES[family])
+        elif family is None:
             self.handle = ebin_plan_create(desc.handle, self.shape_a, self.shape_b)
         else:
             self.handle = ebin_plan_create_forced(desc.handle, self.shape_a, self.shape_b,
@@ -420,14 +440,18 @@ def descriptor(op: str, dtype, **attrs) -> Descriptor:
 def binary(op: str, a, b, out=None, *, stream=None, **attrs):
     """One-shot call on torch CUDA tensors: returns ``out`` (allocated if None).
 
-    Inputs that are not contiguous are copied first (on the current stream).
+    Inputs that are not contiguous run as strided views (no copy), except a
+    BatchNormalization / Clip / BiasPRelu parameter block, which is copied.
     """
     import torch
     desc = descriptor(op, a.dtype, **attrs)
-    plan = Plan(desc, a.shape, b.shape if b is not None else (2,))
+    plain_b = op not in ("BatchNormalization", "Clip", "BiasPRelu")
+    if b is not None and not plain_b:
+        b = b.contiguous()
+    ta = None if a.is_contiguous() else tuple(a.stride())
+    tb = None if (b is None or b.is_contiguous()) else tuple(b.stride())
+    plan = Plan(desc, a.shape, b.shape if b is not None else (2,), strides_a=ta, strides_b=tb)
     if out is None:
         out = torch.empty(plan.output_shape, dtype=torch_dtype(desc.out_dtype), device=a.device)
-    a_c = a.contiguous()
-    b_c = b.contiguous() if b is not None else None
-    execute(plan, a_c, b_c, out, stream)
+    execute(plan, a, b, out, stream)
     return out

@@ -195,8 +195,16 @@ int family_of(const ebin_plan_s &p, int forced, bool *ok) {
     const bool contig = r == 1 && g.sa[0] == 1 && g.sb[0] == 1;
     const bool left = r == 1 && g.sa[0] == 0 && g.sb[0] == 1 && plain_b(p.op);
     const bool right = r == 1 && g.sa[0] == 1 && g.sb[0] == 0;
+    const int64_t ia = g.sa[r - 1], ib = g.sb[r - 1];
+    // an input read in 16-byte packs along the rows needs every row to start on
+    // a pack boundary: its outer strides are multiples of G (always true of
+    // dense inputs; strided views may break it)
+    bool rows_aligned = true;
+    for (int i = 0; i + 1 < r; ++i)
+        rows_aligned = rows_aligned && (ia != 1 || g.sa[i] % G == 0) &&
+                       (ib != 1 || g.sb[i] % G == 0);
     bool block = false;
-    if (r == 2 && inner % G == 0) {
+    if (r == 2 && inner % G == 0 && rows_aligned) {
         const bool a_dense = g.sa[0] == inner && g.sa[1] == 1;
         const bool b_dense = g.sb[0] == inner && g.sb[1] == 1;
         auto bcast = [](const int64_t *s) {
@@ -204,9 +212,8 @@ int family_of(const ebin_plan_s &p, int forced, bool *ok) {
         };
         block = (a_dense && bcast(g.sb)) || (b_dense && bcast(g.sa) && plain_b(p.op));
     }
-    const int64_t ia = g.sa[r - 1], ib = g.sb[r - 1];
     const bool inner_ok = inner % G == 0 && (ia == 0 || ia == 1) && (ib == 0 || ib == 1) &&
-                          (ia == 1 || ib == 1) && (ia == 1 || plain_b(p.op));
+                          (ia == 1 || ib == 1) && (ia == 1 || plain_b(p.op)) && rows_aligned;
     switch (forced) {
     case EBIN_FAMILY_AUTO:
         if (contig) return ebin::FAM_CONTIGUOUS;
@@ -225,8 +232,34 @@ int family_of(const ebin_plan_s &p, int forced, bool *ok) {
     }
 }
 
+// Element strides of a view, or nullptr when they are the dense row-major ones
+// (dims of extent 1 or 0 place no constraint).  Negative strides: *bad.
+const int64_t *view_strides(const int64_t *shape, const int64_t *st, int rank, bool *bad) {
+    *bad = false;
+    if (!st) return nullptr;
+    bool dense = true;
+    int64_t acc = 1;
+    for (int i = rank - 1; i >= 0; --i) {
+        if (st[i] < 0) *bad = true;
+        if (shape[i] > 1 && st[i] != acc) dense = false;
+        acc *= shape[i];
+    }
+    return dense ? nullptr : st;
+}
+
+// Storage extent of a view in elements: largest offset + 1 (0 when empty).
+int64_t view_span(const int64_t *shape, const int64_t *st, int rank) {
+    int64_t span = 1;
+    for (int i = 0; i < rank; ++i) {
+        if (shape[i] == 0) return 0;
+        span += (shape[i] - 1) * st[i];
+    }
+    return span;
+}
+
 ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
-                       int rb, int forced, ebin_plan_s **out) {
+                       int rb, int forced, ebin_plan_s **out, const int64_t *ta = nullptr,
+                       const int64_t *tb = nullptr) {
     if (ra < 0 || rb < 0) return EBIN_ERR_INVALID_ARG;
     if (ra > kMaxRank || rb > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
     if ((ra > 0 && !sa) || (rb > 0 && !sb)) return EBIN_ERR_INVALID_ARG;
@@ -234,6 +267,11 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
         if (sa[i] < 0) return EBIN_ERR_INVALID_ARG;
     for (int i = 0; i < rb; ++i)
         if (sb[i] < 0) return EBIN_ERR_INVALID_ARG;
+    // strided views: A always; B only where it is an ordinary tensor
+    bool bad_a = false, bad_b = false;
+    ta = view_strides(sa, ta, ra, &bad_a);
+    tb = d.attrs.with_scalar ? nullptr : view_strides(sb, tb, rb, &bad_b);
+    if (bad_a || bad_b || (tb && !plain_b(d.op))) return EBIN_ERR_INVALID_ARG;
 
     // The logical shape B broadcasts with.  BatchNormalization: B = [4, C]
     // holds four parameter rows of C and broadcasts as [1, C, 1, ...] along
@@ -291,14 +329,21 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     p->numel = product(so, r);
     p->numel_a = product(sa, ra);
     p->numel_b = d.attrs.with_scalar ? 0 : product(sb, rb);
+    p->strided_a = ta != nullptr;
+    p->strided_b = tb != nullptr;
+    for (int i = 0; ta && i < ra; ++i) p->strides_a[i] = ta[i];
+    for (int i = 0; tb && i < rb; ++i) p->strides_b[i] = tb[i];
+    p->span_a = ta ? view_span(sa, ta, ra) : p->numel_a;
+    p->span_b = tb ? view_span(sb, tb, rb) : p->numel_b;
     p->plane = plane;
 
-    // 2. dense strides, zero on broadcast dims
+    // 2. element strides (dense, or the view's), zero on broadcast dims
     int64_t st_a[kMaxRank], st_b[kMaxRank];
     int64_t acc_a = 1, acc_b = 1;
     for (int i = r - 1; i >= 0; --i) {
-        st_a[i] = xa[i] == 1 ? 0 : acc_a;
-        st_b[i] = xb[i] == 1 ? 0 : acc_b;
+        const int ja = i - (r - ra), jb = i - (r - rlb);
+        st_a[i] = xa[i] == 1 ? 0 : (ta ? ta[ja] : acc_a);
+        st_b[i] = xb[i] == 1 ? 0 : (tb ? tb[jb] : acc_b);
         acc_a *= xa[i];
         acc_b *= xb[i];
     }
@@ -411,6 +456,8 @@ ebin_status build_plan3(const ebin_descriptor_s &d, const int64_t *sa, int ra, c
     p->numel_a = product(sa, ra);
     p->numel_b = product(sb, rb);
     p->numel_c = product(sc, rc);
+    p->span_a = p->numel_a;
+    p->span_b = p->numel_b;
 
     // 2. dense strides, zero on broadcast dims;  3. drop unit dims;  4. merge
     int64_t st[3][kMaxRank];
@@ -465,13 +512,16 @@ void plan_unref(ebin_plan_s *p) {
     if (p && p->refs.fetch_sub(1) == 1) delete p;
 }
 
+// ta / tb: the view strides as normalised by view_strides (nullptr = dense).
 bool key_equal(const ebin_plan_s &p, uint64_t id, const int64_t *sa, int ra, const int64_t *sb,
-               int rb, const int64_t *sc = nullptr, int rc = -1) {
+               int rb, const int64_t *sc = nullptr, int rc = -1, const int64_t *ta = nullptr,
+               const int64_t *tb = nullptr) {
     if (p.desc_id != id || p.rank_a != ra || p.rank_b != rb || p.rank_c != rc) return false;
+    if (p.strided_a != (ta != nullptr) || p.strided_b != (tb != nullptr)) return false;
     for (int i = 0; i < ra; ++i)
-        if (p.shape_a[i] != sa[i]) return false;
+        if (p.shape_a[i] != sa[i] || (ta && p.strides_a[i] != ta[i])) return false;
     for (int i = 0; i < rb; ++i)
-        if (p.shape_b[i] != sb[i]) return false;
+        if (p.shape_b[i] != sb[i] || (tb && p.strides_b[i] != tb[i])) return false;
     for (int i = 0; i < rc; ++i)
         if (p.shape_c[i] != sc[i]) return false;
     return true;
@@ -501,11 +551,16 @@ namespace {
 
 // LRU lookup, or build and insert (two-input plans: rc = -1).
 ebin_status cached_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
-                        int rb, const int64_t *sc, int rc, ebin_plan_t *out) {
+                        int rb, const int64_t *sc, int rc, ebin_plan_t *out,
+                        const int64_t *ta = nullptr, const int64_t *tb = nullptr) {
+    // the key holds the normalised strides (dense views share the dense plans)
+    bool bad = false;
+    const int64_t *ka = view_strides(sa, ta, ra, &bad);
+    const int64_t *kb = d.attrs.with_scalar ? nullptr : view_strides(sb, tb, rb, &bad);
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
-        for (auto it = g_cache.begin(); it != g_cache.end(); ++it) {
-            if (key_equal(**it, d.id, sa, ra, sb, rb, sc, rc)) {
+        for (auto it = g_cache.begin(); !bad && it != g_cache.end(); ++it) {
+            if (key_equal(**it, d.id, sa, ra, sb, rb, sc, rc, ka, kb)) {
                 ebin_plan_s *p = *it;
                 g_cache.splice(g_cache.begin(), g_cache, it);
                 p->refs.fetch_add(1);
@@ -518,7 +573,7 @@ ebin_status cached_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, c
     }
     ebin_plan_s *p = nullptr;
     const ebin_status st = rc < 0
-        ? build_plan(d, sa, ra, sb, rb, EBIN_FAMILY_AUTO, &p)
+        ? build_plan(d, sa, ra, sb, rb, EBIN_FAMILY_AUTO, &p, ta, tb)
         : build_plan3(d, sa, ra, sb, rb, sc, rc, EBIN_FAMILY_AUTO, &p);
     if (st != EBIN_OK) return st;
     ebin_plan_s *evicted = nullptr;
@@ -560,6 +615,32 @@ extern "C" ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int
     if (desc->attrs.with_scalar) rank_b = 0;
     ebin_plan_s *p = nullptr;
     const ebin_status st = build_plan(*desc, shape_a, rank_a, shape_b, rank_b, (int)family, &p);
+    if (st != EBIN_OK) return st;
+    *out = p;
+    return EBIN_OK;
+}
+
+extern "C" ebin_status ebin_plan_create_strided(ebin_descriptor_t desc, const int64_t *shape_a,
+                                                const int64_t *strides_a, int rank_a,
+                                                const int64_t *shape_b, const int64_t *strides_b,
+                                                int rank_b, ebin_family family,
+                                                ebin_plan_t *out) {
+    if (!desc || !out) return EBIN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (ternary(desc->op)) return EBIN_ERR_INVALID_ARG;
+    if (desc->attrs.with_scalar) {
+        rank_b = 0;
+        strides_b = nullptr;
+    }
+    if (rank_a < 0 || rank_b < 0) return EBIN_ERR_INVALID_ARG;
+    if (rank_a > kMaxRank || rank_b > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
+    if ((rank_a > 0 && !shape_a) || (rank_b > 0 && !shape_b)) return EBIN_ERR_INVALID_ARG;
+    if (family == EBIN_FAMILY_AUTO)
+        return cached_plan(*desc, shape_a, rank_a, shape_b, rank_b, nullptr, -1, out, strides_a,
+                           strides_b);
+    ebin_plan_s *p = nullptr;
+    const ebin_status st = build_plan(*desc, shape_a, rank_a, shape_b, rank_b, (int)family, &p,
+                                      strides_a, strides_b);
     if (st != EBIN_OK) return st;
     *out = p;
     return EBIN_OK;
@@ -730,13 +811,17 @@ ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, v
     // Aliasing: an input may share storage with out only as the identical
     // buffer of the output's type and element count; a broadcast input or a
     // parameter block is never overwritten in place.
+    // (a strided view may be in place only where its layout is the output's:
+    // never, so any overlap with out is ALIAS)
     const int64_t isz = (int64_t)ebin_dtype_size(p.dt);
     const int64_t out_bytes = p.numel * (int64_t)ebin_dtype_size(p.out_dt);
-    if (overlaps(A, p.numel_a * isz, out, out_bytes)) {
-        if (!(A == out && p.numel_a == p.numel && p.dt == p.out_dt)) return EBIN_ERR_ALIAS;
+    if (overlaps(A, p.span_a * isz, out, out_bytes)) {
+        if (!(A == out && !p.strided_a && p.numel_a == p.numel && p.dt == p.out_dt))
+            return EBIN_ERR_ALIAS;
     }
-    if (B && overlaps(B, p.numel_b * isz, out, out_bytes)) {
-        if (!(plain_b(p.op) && B == out && p.numel_b == p.numel && p.dt == p.out_dt))
+    if (B && overlaps(B, p.span_b * isz, out, out_bytes)) {
+        if (!(plain_b(p.op) && B == out && !p.strided_b && p.numel_b == p.numel &&
+              p.dt == p.out_dt))
             return EBIN_ERR_ALIAS;
     }
 
@@ -875,11 +960,12 @@ ebin_status host_serial(const ebin_plan_s &p, const ebin::Launch &L, const void 
                         const void *host_b, void *host_out, void *dev_a, void *dev_b,
                         void *dev_out, cudaStream_t s) {
     const size_t isz = ebin_dtype_size(p.dt);
-    if (cudaMemcpyAsync(dev_a, host_a, (size_t)p.numel_a * isz, cudaMemcpyHostToDevice, s) !=
+    // the inputs' whole storage extents (a strided view's span)
+    if (cudaMemcpyAsync(dev_a, host_a, (size_t)p.span_a * isz, cudaMemcpyHostToDevice, s) !=
         cudaSuccess)
         return EBIN_ERR_CUDA;
-    if (host_b && dev_b && p.numel_b > 0) {
-        if (cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz, cudaMemcpyHostToDevice, s) !=
+    if (host_b && dev_b && p.span_b > 0) {
+        if (cudaMemcpyAsync(dev_b, host_b, (size_t)p.span_b * isz, cudaMemcpyHostToDevice, s) !=
             cudaSuccess)
             return EBIN_ERR_CUDA;
     }
@@ -910,9 +996,10 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
     // of each dense operand (and all of a scalar one) run as a pipeline of
     // chunks: chunk c+1 is copied in while chunk c computes and chunk c-1 is
     // copied out, on two copy streams beside the caller's.
-    const bool streaming = L.family == ebin::FAM_CONTIGUOUS ||
-                           L.family == ebin::FAM_LEFT_SCALAR ||
-                           L.family == ebin::FAM_RIGHT_SCALAR;
+    const bool streaming = (L.family == ebin::FAM_CONTIGUOUS ||
+                            L.family == ebin::FAM_LEFT_SCALAR ||
+                            L.family == ebin::FAM_RIGHT_SCALAR) &&
+                           !p.strided_a && !p.strided_b;
     int dev = 0;
     HostPipe *hp = nullptr;
     if (streaming && p.numel >= 2 * kPipeMinChunk && cudaGetDevice(&dev) == cudaSuccess)

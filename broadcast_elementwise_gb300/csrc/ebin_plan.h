@@ -18,6 +18,11 @@ struct ebin_plan_s {
     int64_t shape_a[ebin::kMaxRank] = {};
     int64_t shape_b[ebin::kMaxRank] = {};
     int64_t shape_c[ebin::kMaxRank] = {};
+    // strided input views (ebin_plan_create_strided): element strides given for
+    // A / B when they differ from the dense ones (part of the cache key)
+    bool strided_a = false, strided_b = false;
+    int64_t strides_a[ebin::kMaxRank] = {};
+    int64_t strides_b[ebin::kMaxRank] = {};
     // what execution needs (copied: a plan may outlive its descriptor)
     int op = 0;
     ebin_attrs attrs{};
@@ -25,6 +30,7 @@ struct ebin_plan_s {
     int rank_out = 0;
     int64_t shape_out[ebin::kMaxRank] = {};
     int64_t numel = 0, numel_a = 0, numel_b = 0, numel_c = 0;
+    int64_t span_a = 0, span_b = 0;        // storage extent of A / B in elements
     ebin::Geom g{};
     int family = ebin::FAM_EMPTY;
     int64_t plane = 0;

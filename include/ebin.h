@@ -238,6 +238,28 @@ ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape
                                     ebin_plan_t *out);
 
 /*
+ * Plan for strided input views: inputs need not be dense.
+ * strides_a / strides_b give each input's element strides in its own rank
+ * (non-negative; NULL = dense row-major); strides equal to the dense ones are
+ * the dense plan.  The planner uses the view's strides in place of the dense
+ * ones, then drops unit dims and merges dims exactly as for dense inputs.  The
+ * vector families additionally need every row of a packed input to start on a
+ * 16-byte boundary (its outer strides multiples of 16 bytes of elements), else
+ * the plan is GENERAL_STRIDED.  B strides are refused (INVALID_ARG) for the
+ * parameter blocks of BatchNormalization, Clip and BiasPRelu, and ignored with
+ * with_scalar.  family: EBIN_FAMILY_AUTO (the plan is cached, keyed with the
+ * strides) or a forced family as ebin_plan_create_forced (not cached).
+ * A strided input is never executed in place: any overlap with out is ALIAS.
+ * ebin_execute_host copies each input's whole storage extent (largest offset
+ * + 1 elements) and runs strided plans without the chunked pipeline.
+ * Errors: as ebin_plan_create, and FAMILY for a forced family.
+ */
+ebin_status ebin_plan_create_strided(ebin_descriptor_t desc, const int64_t *shape_a,
+                                     const int64_t *strides_a, int rank_a,
+                                     const int64_t *shape_b, const int64_t *strides_b, int rank_b,
+                                     ebin_family family, ebin_plan_t *out);
+
+/*
  * Plan a three-input operator (MulAdd): the three shapes broadcast together
  * (NumPy rules, right-aligned; the output is broadcast(broadcast(A, B), C)),
  * unit dims are dropped and adjacent dims merged where all three stride sets

@@ -226,6 +226,20 @@ def test_int_rdiv_validates_a():
     assert (got == want).all()
 
 
+def test_binary_helper_reads_strided_tensors_in_place():
+    """Non-contiguous torch tensors (a transpose, a step slice) go to the engine
+    as strided views, without a copy."""
+    x = torch.randn(64, 48, device="cuda").t()             # (48, 64), strides (1, 48)
+    y = torch.randn(200, 64, device="cuda")[::4]           # (50, 64) ... broadcast below
+    before = eb.ebin_launch_count()
+    z = eb.binary("Mul", x, y[:48])
+    torch.cuda.synchronize()
+    assert eb.ebin_launch_count() == before + 1            # one kernel, no copy kernels
+    want, _ = oracle.run("Mul", x.contiguous().cpu().numpy(), y[:48].contiguous().cpu().numpy(),
+                         "float32")
+    assert_bits_equal(z.cpu().numpy(), want, "float32")
+
+
 def test_launch_count_and_binary_helper():
     x = torch.randn(4, 8, 32, 32, device="cuda")
     bias = torch.randn(8, 1, 1, device="cuda")

@@ -12,7 +12,9 @@ import pytest
 import datagen
 import oracle
 from conftest import assert_bits_equal, ulp_distance
-from engine_util import FLOATS, MANIFEST, ONE_WAY, inputs_for, run_engine
+from engine_util import FLOATS, MANIFEST, ONE_WAY, inputs_for, run_engine, to_device
+
+eb = pytest.importorskip("broadcast_elementwise_gb300")
 
 pytestmark = pytest.mark.gpu
 
@@ -180,4 +182,40 @@ def test_muladd_parity_all_families(dtype):
                 assert family == fam, (sa, sb, sc, family)
             assert_bits_equal(got, want, dtype, "MulAdd %s %s %s %s forced=%s offset=%d" %
                               (dtype, sa, sb, sc, forced, offset))
+
+
+STRIDED_VIEWS = [  # (base length, shape, element strides) of A, shape of B
+    (64 * 48, (48, 64), (1, 48), (64,)),
+    (200 * 9, (100, 3), (18, 3), (100, 1)),
+    (64, (7, 64), (0, 1), (7, 64)),
+    (64 * 1008, (64, 1000), (1008, 1), (1000,)),
+    (64 * 1001, (64, 1000), (1001, 1), (64, 1)),
+    (5 * 6 * 7 * 3, (5, 6, 7), (126, 21, 3), (6, 1)),
+]
+
+
+@pytest.mark.parametrize("op,dtype", [("Add", "float32"), ("Mul", "bfloat16"),
+                                      ("Greater", "float16"), ("Mod", "int32"),
+                                      ("Sub", "uint8"), ("PRelu", "float32")])
+def test_strided_input_views(op, dtype):
+    """Strided A views (transposed, sliced with steps, expanded, padded rows,
+    inner stride 3) read in place: the result equals the oracle on the view's
+    contiguous copy, in the natural family and forced through the general one."""
+    import torch
+    for i, (base_n, shape, strides, shape_b) in enumerate(STRIDED_VIEWS):
+        if op == "PRelu":
+            shape_b = (shape[-1],) if len(shape) else ()
+        base, b = inputs_for(op, dtype, (base_n,), shape_b, seed=70 + i)
+        view = np.lib.stride_tricks.as_strided(base, shape, [x * base.itemsize for x in strides])
+        want, _ = oracle.run(op, np.ascontiguousarray(view), b, dtype)
+        desc = eb.descriptor(op, dtype)
+        dA, dB = to_device(base), to_device(b)
+        for forced in (None, "general_strided"):
+            plan = eb.Plan(desc, shape, shape_b, family=forced, strides_a=strides)
+            osz = eb.ITEMSIZE[desc.out_dtype]
+            out = torch.empty(plan.numel * osz, dtype=torch.uint8, device="cuda")
+            eb.execute(plan, dA, dB, out)
+            got = out.cpu().numpy().view(datagen.STORAGE[desc.out_dtype]).reshape(want.shape)
+            compare(op, dtype, got, want, "%s %s view %s/%s forced=%s family=%s" %
+                    (op, dtype, shape, strides, forced, plan.family))
 

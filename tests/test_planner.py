@@ -277,6 +277,73 @@ def test_three_input_plans():
     assert e.value.code == "alias"
 
 
+def _geometry_offsets(plan, numel):
+    """Element offsets of A and B for every output index, from the plan's
+    coalesced geometry (extents n, strides sa, sb)."""
+    n, sa, sb = plan.geometry()
+    f = np.arange(numel, dtype=np.int64)
+    oa = np.zeros(numel, np.int64)
+    ob = np.zeros(numel, np.int64)
+    for d in range(len(n) - 1, -1, -1):
+        digit = f % n[d]
+        f //= n[d]
+        oa += digit * sa[d]
+        ob += digit * sb[d]
+    return oa, ob
+
+
+VIEWS = [  # (base length, shape, element strides) of A; B dense of the given shape
+    (64 * 48, (48, 64), (1, 48), (64,)),               # transpose
+    (200 * 9, (100, 3), (18, 3), (100, 1)),             # every other row, every third column
+    (64, (7, 64), (0, 1), (7, 64)),                     # expanded rows
+    (64 * 1008, (64, 1000), (1008, 1), (1000,)),         # padded rows, 16-byte aligned
+    (64 * 1001, (64, 1000), (1001, 1), (64, 1)),         # padded rows, not aligned
+    (5 * 6 * 7 * 3, (5, 6, 7), (126, 21, 3), (6, 1)),    # inner stride 3
+]
+
+
+def test_strided_views_map_every_element():
+    """Each view is built over arange(base) so that its values are its storage
+    offsets: the geometry must address exactly numpy's broadcast of the view."""
+    d = eb.Descriptor("Add", "float32")
+    for base, shape, strides, shape_b in VIEWS:
+        view = np.lib.stride_tricks.as_strided(np.arange(base, dtype=np.int64), shape,
+                                               [x * 8 for x in strides])
+        p = eb.Plan(d, shape, shape_b, strides_a=strides)
+        out_shape = np.broadcast_shapes(shape, shape_b)
+        assert p.output_shape == out_shape
+        oa, ob = _geometry_offsets(p, p.numel)
+        want_a = np.broadcast_to(view, out_shape).reshape(-1)
+        want_b = np.broadcast_to(np.arange(int(np.prod(shape_b))).reshape(shape_b),
+                                 out_shape).reshape(-1)
+        assert (oa == want_a).all() and (ob == want_b).all(), (shape, strides)
+
+
+def test_strided_view_rules():
+    d = eb.Descriptor("Add", "float32")
+    dense = eb.Plan(d, (64, 1000), (1000,))
+    assert eb.Plan(d, (64, 1000), (1000,), strides_a=(1000, 1)).handle == dense.handle
+    # padded rows: not dense, so the inner-vector traversal (any aligned run stride)
+    assert eb.Plan(d, (64, 1000), (1000,), strides_a=(1008, 1)).family == "inner_vector_outer"
+    assert eb.Plan(d, (64, 1000), (1000,), strides_a=(1001, 1)).family == "general_strided"
+    assert eb.Plan(d, (64, 1000), (1000,), strides_a=(1008, 1),
+                   family="general_strided").family == "general_strided"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (64, 1000), (1000,), strides_a=(-1000, 1))
+    assert e.value.code == "invalid_arg"
+    bn = eb.Descriptor("BatchNormalization", "float32")
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(bn, (2, 4, 8), (4, 4), strides_b=(8, 2))
+    assert e.value.code == "invalid_arg"
+    assert eb.Plan(bn, (2, 4, 8), (4, 4), strides_a=(64, 16, 2)).family in (
+        "general_strided", "inner_vector_outer")
+    # a strided A is never in place: the identical buffer is ALIAS too
+    p = eb.Plan(d, (48, 64), (64,), strides_a=(1, 48))
+    with pytest.raises(eb.EbinError) as e:
+        eb.ebin_execute(p.handle, 1 << 20, 4 << 20, 1 << 20, None)
+    assert e.value.code == "alias"
+
+
 def test_plan_cache_is_an_8_entry_lru():
     eb.ebin_plan_cache_clear()
     d = eb.Descriptor("Sub", "int32")
