@@ -81,6 +81,8 @@ def _load():
             lib.oracle_eval.restype = i32
             lib.oracle_output_shape.argtypes = [i32, p, i32, p, i32, p, p]
             lib.oracle_output_shape.restype = i32
+            lib.oracle_eval_pow_mixed.argtypes = [i32, i32, p, i32, p, i32, p, p, p, p, i64, p]
+            lib.oracle_eval_pow_mixed.restype = i32
             lib.oracle_eval3.argtypes = [i32, i32, p, i32, p, i32, p, i32, p, p, p, p, p, i64]
             lib.oracle_eval3.restype = i32
             lib.oracle_output_shape3.argtypes = [p, i32, p, i32, p, i32, p, p]
@@ -188,6 +190,31 @@ def run(op: str, a: np.ndarray, b: np.ndarray | None, dtype: str, *, shape_a=Non
                          sa.ctypes.data, ra, sb.ctypes.data, rb,
                          a.ctypes.data, None if b is None else b.ctypes.data, out.ctypes.data,
                          idx_p, n_idx, ctypes.byref(status))
+    if rc:
+        raise ValueError(RC[rc])
+    return out, int(status.value)
+
+
+def run_pow_mixed(a: np.ndarray, b: np.ndarray, dtype_a: str, dtype_b: str, *, idx=None):
+    """Pow with base type dtype_a and exponent type dtype_b; returns (out, status)."""
+    lib = _load()
+    a, b = np.ascontiguousarray(a), np.ascontiguousarray(b)
+    if a.dtype != STORAGE[dtype_a] or b.dtype != STORAGE[dtype_b]:
+        raise TypeError("storage does not match the types")
+    oshape = tuple(np.broadcast_shapes(a.shape, b.shape))
+    sa, ra = _shape_arr(tuple(a.shape))
+    sb, rb = _shape_arr(tuple(b.shape))
+    if idx is None:
+        out = np.empty(oshape, STORAGE[dtype_a])
+        idx_p, n_idx = None, 0
+    else:
+        idx = np.ascontiguousarray(idx, dtype=np.int64)
+        out = np.empty(idx.size, STORAGE[dtype_a])
+        idx_p, n_idx = idx.ctypes.data, idx.size
+    status = ctypes.c_uint32(0)
+    rc = lib.oracle_eval_pow_mixed(DTYPES.index(dtype_a), DTYPES.index(dtype_b), sa.ctypes.data,
+                                   ra, sb.ctypes.data, rb, a.ctypes.data, b.ctypes.data,
+                                   out.ctypes.data, idx_p, n_idx, ctypes.byref(status))
     if rc:
         raise ValueError(RC[rc])
     return out, int(status.value)

@@ -604,6 +604,66 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
 }
 
 /*
+ * Pow with an exponent of another type ("Binary Kernel Design", Compute,
+ * scheduling, and safety: legal signatures other than the same-type ones run
+ * through typed scalar adapters; ONNX Pow takes base T and exponent T1).
+ * Base types: the Pow types; exponent types: every non-BOOL type.  Reading:
+ *  - floating base: the same-type floating Pow with the exponent converted to
+ *    binary64 (exact for the 16- and 32-bit types; int64 above 2^53 rounds);
+ *  - integer base, integer exponent: the same-type integer Pow (exponent as a
+ *    64-bit value);
+ *  - integer base, floating exponent: pow in binary64, truncated toward zero
+ *    into the base type, saturating at its bounds; NaN gives 0; no status.
+ * Output type: the base's.  Same broadcasting and element-by-element
+ * evaluation as oracle_eval.
+ */
+static double exponent_as_double(const void *B, int tb, int64_t i)
+{
+    if (is_float_type(tb)) return (double)load_float(B, tb, i);
+    return (double)load_int(B, tb, i);
+}
+
+int oracle_eval_pow_mixed(int ta, int tb, const int64_t *sa, int ra, const int64_t *sb, int rb,
+                          const void *A, const void *B, void *out, const int64_t *idx,
+                          int64_t n_idx, uint32_t *status)
+{
+    int64_t so[OR_MAX_RANK], sta[OR_MAX_RANK], stb[OR_MAX_RANK];
+    int r;
+    *status = 0;
+    if (!oracle_type_allowed(OR_POW, ta) || tb == OT_BOOL || tb < 0 || tb >= OT_NUM)
+        return OR_TYPE;
+    int rc = oracle_broadcast_shape(sa, ra, sb, rb, so, &r);
+    if (rc) return rc;
+    aligned_strides(sa, ra, r, sta);
+    aligned_strides(sb, rb, r, stb);
+    int64_t total = numel(so, r);
+    int64_t count = idx ? n_idx : total;
+    for (int64_t k = 0; k < count; ++k) {
+        int64_t f = idx ? idx[k] : k;
+        if (f < 0 || f >= total) return OR_ARGS;
+        int64_t oa, ob;
+        offsets_of(f, so, r, sta, stb, &oa, &ob);
+        if (is_float_type(ta)) {
+            double x = (double)load_float(A, ta, oa);
+            store_float(out, ta, k, (float)pow(x, exponent_as_double(B, tb, ob)));
+        } else if (!is_float_type(tb)) {
+            store_int(out, ta, k, int_op(OR_POW, ta, load_int(A, ta, oa), load_int(B, tb, ob),
+                                         0, 0, status));
+        } else {
+            double y = pow((double)load_int(A, ta, oa), exponent_as_double(B, tb, ob));
+            int64_t v;
+            if (isnan(y)) v = 0;
+            else if (ta == OT_I32) v = y >= 2147483647.0 ? 2147483647 :
+                                       y <= -2147483648.0 ? -2147483647 - 1 : (int64_t)y;
+            else v = y >= 9223372036854775807.0 ? INT64_MAX :
+                     y <= -9223372036854775808.0 ? INT64_MIN : (int64_t)y;
+            store_int(out, ta, k, (uint64_t)v);
+        }
+    }
+    return OR_OK;
+}
+
+/*
  * MulAdd (0verkilll/onnx ops, MulAddOp): y = (a * b) + c.  The shapes follow
  * the unfused pair: the product has shape broadcast(A, B) and the output
  * broadcast(broadcast(A, B), C).  Each output element is computed from its full

@@ -565,6 +565,92 @@ def test_f32_pow_within_half_ulp_of_mpmath():
     assert (d == 0).mean() > 0.999
 
 
+# --------------------------------------------------------------------------- mixed-type Pow
+MIXED_EXP = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32"]
+
+
+def _exponents(dtype, n, seed):
+    if dtype in ("float32", "float16", "bfloat16"):
+        e = datagen.uniform(seed, 0, n, -4.0, 4.0)
+        e[::3] = np.round(e[::3])
+        return datagen.float_to(e.astype(np.float32), dtype)
+    lo = 0 if dtype.startswith("u") else -3
+    return datagen.make("int_range", dtype, (n,), seed, 1, lo=lo, hi=9)
+
+
+def _as_f64(x, dtype):
+    if dtype == "bfloat16":
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+@pytest.mark.parametrize("ta", ["float32", "float16", "bfloat16"])
+@pytest.mark.parametrize("tb", MIXED_EXP)
+def test_pow_mixed_float_base_matches_numpy_float64(ta, tb):
+    """ONNX Pow base T / exponent T1 (typed scalar adapters): a floating base
+    takes pow in binary64 on the exponent's exact value, rounded to binary32,
+    then to the base type."""
+    if ta == tb:
+        pytest.skip("same type")
+    n = 4000
+    a = datagen.float_to(datagen.uniform(61, 0, n, 0.0, 6.0).astype(np.float32), ta)
+    b = _exponents(tb, n, 62)
+    got, st = oracle.run_pow_mixed(a, b, ta, tb)
+    with np.errstate(all="ignore"):
+        y = np.power(_as_f64(a, ta), _as_f64(b, tb)).astype(np.float32)
+    want = datagen.float_to(y, ta) if ta != "float32" else y
+    assert st == 0
+    assert_bits_equal(got, want, ta, "Pow %s^%s" % (ta, tb))
+
+
+@pytest.mark.parametrize("ta", ["int32", "int64"])
+@pytest.mark.parametrize("tb", ["int32", "int64", "uint8", "uint32"])
+def test_pow_mixed_int_base_int_exponent_matches_python(ta, tb):
+    if ta == tb:
+        pytest.skip("same type")
+    a = np.array([v for v in range(-5, 6) for _ in range(12)], datagen.STORAGE[ta])
+    lo = 0 if tb.startswith("u") else -3
+    b = np.array(list(range(lo, lo + 12)) * 11, datagen.STORAGE[tb])
+    got, st = oracle.run_pow_mixed(a, b, ta, tb)
+    want = []
+    for x, e in zip(a.tolist(), b.tolist()):
+        if e >= 0:
+            want.append(wrap(x ** e, ta))
+        else:                                    # the same-type reading: 1/x^|e| truncated
+            want.append(1 if x == 1 else (1 if e % 2 == 0 else -1) if x == -1 else 0)
+    assert (got == np.array(want, dtype=object).astype(datagen.STORAGE[ta])).all()
+    assert st == (oracle.STATUS_DIV_BY_ZERO if ((a == 0) & (b < 0)).any() else 0)
+
+
+@pytest.mark.parametrize("ta", ["int32", "int64"])
+@pytest.mark.parametrize("tb", ["float32", "float16", "bfloat16"])
+def test_pow_mixed_int_base_float_exponent(ta, tb):
+    """pow in binary64, truncated toward zero, saturated at the type's bounds,
+    NaN to 0, no status."""
+    n = 3000
+    a = datagen.make("int_range", ta, (n,), 63, 0, lo=-20, hi=40)
+    b = _exponents(tb, n, 64)
+    a[:6] = [2, -8, 0, 10, 7, 3]
+    b[:6] = datagen.float_to(np.array([0.5, 1 / 3, -1.0, 20.0, np.nan, 2.0], np.float32), tb)
+    got, st = oracle.run_pow_mixed(a, b, ta, tb)
+    info = np.iinfo(datagen.STORAGE[ta])
+    with np.errstate(all="ignore"):
+        y = np.power(a.astype(np.float64), _as_f64(b, tb))
+    want = []
+    for v in y.tolist():
+        if math.isnan(v):
+            want.append(0)
+        elif v >= info.max:
+            want.append(info.max)
+        elif v <= info.min:
+            want.append(info.min)
+        else:
+            want.append(int(math.trunc(v)))
+    assert (got == np.array(want, dtype=object).astype(datagen.STORAGE[ta])).all()
+    assert list(got[:6]) == [1, 0, info.max, info.max, 0, 9]    # 10^20 saturates both
+    assert st == 0
+
+
 def test_pow_special_values():
     for x, y, want in read_golden("pow_special_values.txt"):
         got, _ = oracle.run("Pow", f32(float(x)), f32(float(y)), "float32")
