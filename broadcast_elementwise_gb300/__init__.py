@@ -328,16 +328,19 @@ class Descriptor:
 
     def __init__(self, op: str, dtype, *, opset: int = 28, fmod: int = 0, direction: int = 0,
                  epsilon: float = 1e-5, has_min: bool = True, has_max: bool = True,
-                 scalar_b: float | None = None):
-        """``scalar_b`` given: ncnn binaryop's with_scalar, B is that value."""
+                 scalar_b: float | None = None, dtype_b=None):
+        """``scalar_b`` given: ncnn binaryop's with_scalar, B is that value.
+        ``dtype_b``: B's type where it may differ from A's (Pow's exponent)."""
         self.op = op
         self.dtype = DTYPE_NAMES[_dtype_code(dtype)]
+        self.dtype_b = self.dtype if dtype_b is None else DTYPE_NAMES[_dtype_code(dtype_b)]
         self.with_scalar = scalar_b is not None
         attrs = ebin_attrs(int(fmod), int(direction), float(epsilon), int(bool(has_min)),
                            int(bool(has_max)), int(self.with_scalar),
                            float(scalar_b) if self.with_scalar else 0.0)
         code = _dtype_code(dtype)
-        self.handle = ebin_descriptor_create(OPS[op], int(opset), attrs, code, code)
+        code_b = code if dtype_b is None else _dtype_code(dtype_b)
+        self.handle = ebin_descriptor_create(OPS[op], int(opset), attrs, code, code_b)
         self.out_dtype = DTYPE_NAMES[ebin_descriptor_output_dtype(self.handle)]
         self.id = ebin_descriptor_id(self.handle)
 

@@ -21,7 +21,7 @@ OBJDIR = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(PKG, "libebin.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-GROUPS = ["arith", "mod", "pow", "cmp", "logic", "chan", "ext", "tern"]
+GROUPS = ["arith", "mod", "pow", "cmp", "logic", "chan", "ext", "tern", "powmix"]
 N_DT = 8
 # -fmad=false: no multiply-add contraction anywhere; the kernels also use the
 # _rn intrinsics explicitly.  No fast-math.

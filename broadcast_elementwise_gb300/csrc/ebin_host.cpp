@@ -125,6 +125,7 @@ struct ebin_descriptor_s {
     int opset;
     ebin_attrs attrs;
     ebin_dtype dt;
+    ebin_dtype dt_b;       // B's type: dt, except for Pow with another exponent type
     ebin_dtype out_dt;
 };
 
@@ -138,7 +139,12 @@ extern "C" ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_
     if ((int)op < 0 || (int)op >= EBIN_OP_COUNT) return EBIN_ERR_UNSUPPORTED_OP;
     ebin_attrs a{0, 0, EBIN_DEFAULT_EPSILON, 1, 1, 0, 0.0f};
     if (attrs) a = *attrs;
-    if (dtype_a != dtype_b || !type_legal(op, dtype_a)) return EBIN_ERR_UNSUPPORTED_TYPE;
+    // A and B share a type, except Pow's exponent, which may be any non-BOOL
+    // type ("typed scalar adapters" for the other legal signatures)
+    if (!type_legal(op, dtype_a)) return EBIN_ERR_UNSUPPORTED_TYPE;
+    if (dtype_a != dtype_b &&
+        !(op == EBIN_OP_POW && dt_class(dtype_b) >= 0 && dtype_b != EBIN_BOOL))
+        return EBIN_ERR_UNSUPPORTED_TYPE;
     if (op == EBIN_OP_MOD) {
         // "Mod tracks schema version 28 while retaining minimum opset 10";
         // floating fmod=0 (floor remainder) only from opset 28.
@@ -157,6 +163,7 @@ extern "C" ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_
     d->opset = opset;
     d->attrs = a;
     d->dt = dtype_a;
+    d->dt_b = dtype_b;
     d->out_dt = output_type(op, dtype_a);
     *out = d;
     return EBIN_OK;
@@ -324,6 +331,7 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     p->op = d.op;
     p->attrs = d.attrs;
     p->out_dt = d.out_dt;
+    p->dt_b = d.dt_b;
     p->rank_out = r;
     for (int i = 0; i < r; ++i) p->shape_out[i] = so[i];
     p->numel = product(so, r);
@@ -373,9 +381,14 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     g.rank = k;
     p->g = g;
 
-    // 5. loop family (a with_scalar plan runs its own family or the general one)
+    // 5. loop family (a with_scalar plan runs its own family or the general one;
+    // a mixed-type Pow only the general one)
     bool ok = true;
     p->family = family_of(*p, forced, &ok);
+    if (ok && p->dt_b != p->dt && p->numel > 0) {
+        ok = forced == EBIN_FAMILY_AUTO || forced == EBIN_FAMILY_GENERAL_STRIDED;
+        p->family = ebin::FAM_GENERAL_STRIDED;
+    }
     if (ok && d.attrs.with_scalar && forced != EBIN_FAMILY_AUTO &&
         forced != EBIN_FAMILY_GENERAL_STRIDED) {
         bool nat_ok = true;
@@ -441,6 +454,7 @@ ebin_status build_plan3(const ebin_descriptor_s &d, const int64_t *sa, int ra, c
     auto *p = new ebin_plan_s;
     p->desc_id = d.id;
     p->dt = d.dt;
+    p->dt_b = d.dt_b;
     p->rank_a = ra;
     p->rank_b = rb;
     p->rank_c = rc;
@@ -783,7 +797,9 @@ cudaError_t ebin::launch(const Launch &L) {
     switch (L.op) {
     case EBIN_OP_ADD: case EBIN_OP_SUB: case EBIN_OP_MUL: case EBIN_OP_DIV: EBIN_PICK(arith)
     case EBIN_OP_MOD: EBIN_PICK(mod)
-    case EBIN_OP_POW: EBIN_PICK(pow)
+    case EBIN_OP_POW:
+        if (L.dt_b != L.dt) EBIN_PICK(powmix)
+        EBIN_PICK(pow)
     case EBIN_OP_EQUAL: case EBIN_OP_LESS: case EBIN_OP_GREATER: case EBIN_OP_LESS_OR_EQUAL:
     case EBIN_OP_GREATER_OR_EQUAL: EBIN_PICK(cmp)
     case EBIN_OP_AND: case EBIN_OP_OR: case EBIN_OP_XOR: case EBIN_OP_BITWISE_AND:
@@ -814,14 +830,15 @@ ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, v
     // (a strided view may be in place only where its layout is the output's:
     // never, so any overlap with out is ALIAS)
     const int64_t isz = (int64_t)ebin_dtype_size(p.dt);
+    const int64_t isz_b = (int64_t)ebin_dtype_size(p.dt_b);
     const int64_t out_bytes = p.numel * (int64_t)ebin_dtype_size(p.out_dt);
     if (overlaps(A, p.span_a * isz, out, out_bytes)) {
         if (!(A == out && !p.strided_a && p.numel_a == p.numel && p.dt == p.out_dt))
             return EBIN_ERR_ALIAS;
     }
-    if (B && overlaps(B, p.span_b * isz, out, out_bytes)) {
+    if (B && overlaps(B, p.span_b * isz_b, out, out_bytes)) {
         if (!(plain_b(p.op) && B == out && !p.strided_b && p.numel_b == p.numel &&
-              p.dt == p.out_dt))
+              p.dt_b == p.out_dt))
             return EBIN_ERR_ALIAS;
     }
 
@@ -830,6 +847,7 @@ ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, v
     L = ebin::Launch{};
     L.op = p.op;
     L.dt = dt_class(p.dt);
+    L.dt_b = dt_class(p.dt_b);
     L.family = p.family;
     L.g = p.g;
     L.numel = p.numel;
@@ -902,6 +920,7 @@ extern "C" ebin_status ebin_execute3(ebin_plan_t plan, const void *A, const void
     ebin::Launch L{};
     L.op = p.op;
     L.dt = dt_class(p.dt);
+    L.dt_b = L.dt;
     L.family = p.family;
     L.g = p.g;
     L.numel = p.numel;
@@ -965,7 +984,8 @@ ebin_status host_serial(const ebin_plan_s &p, const ebin::Launch &L, const void 
         cudaSuccess)
         return EBIN_ERR_CUDA;
     if (host_b && dev_b && p.span_b > 0) {
-        if (cudaMemcpyAsync(dev_b, host_b, (size_t)p.span_b * isz, cudaMemcpyHostToDevice, s) !=
+        if (cudaMemcpyAsync(dev_b, host_b, (size_t)p.span_b * ebin_dtype_size(p.dt_b),
+                            cudaMemcpyHostToDevice, s) !=
             cudaSuccess)
             return EBIN_ERR_CUDA;
     }

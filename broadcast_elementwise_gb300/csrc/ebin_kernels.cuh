@@ -131,6 +131,14 @@ struct PrepNone {
     using PB = int;
 };
 
+// B's element type: Op::BIn where it differs from A's (mixed-type Pow), else In.
+template <class Op, class = void> struct BInOf {
+    using type = typename Op::In;
+};
+template <class Op> struct BInOf<Op, std::void_t<typename Op::BIn>> {
+    using type = typename Op::BIn;
+};
+
 // o[k] = op(a[k], b[k]) for one group of G elements.  SA / SB: the operand is
 // one value for the whole group (a[0] / b[0]), not G values.
 template <class Op, int G, bool SA = false, bool SB = false>
@@ -403,8 +411,9 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     const int64_t vstepO = cstep * G;
     const In *pa = static_cast<const In *>(p.A) + baseA + m0 * r.smA +
                    (IA == 1 ? c0 * G : IA == 2 ? c0 * r.ia : 0);
-    const In *pb = static_cast<const In *>(p.B) + baseB + m0 * r.smB +
-                   (IB == 1 ? c0 * G : IB == 2 ? c0 * r.ib : 0);
+    using BIn = typename BInOf<Op>::type;
+    const BIn *pb = static_cast<const BIn *>(p.B) + baseB + m0 * r.smB +
+                    (IB == 1 ? c0 * G : IB == 2 ? c0 * r.ib : 0);
     Out *po = static_cast<Out *>(p.out) + (pi * r.M + m0) * r.L + c0 * G;
     const int64_t stepA = (int64_t)r.rs * r.smA;
     const int64_t stepB = (int64_t)r.rs * r.smB;
@@ -427,7 +436,7 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
         else x.v[0] = *q;
         return x;
     };
-    auto load_b = [&](const In *q) {
+    auto load_b = [&](const BIn *q) {
         BPack x;
         if constexpr (kVecB && Op::kPlainB) {
             x = ld_stream<In, G>(q);

@@ -49,6 +49,7 @@ struct Geom {
 struct Launch {
     int op;              // public ebin_op code
     int dt;              // input element class (Dt)
+    int dt_b;            // B's element class (differs from dt for mixed-type Pow)
     int family;          // Fam (after the alignment fallback)
     Geom g;
     int64_t numel;
@@ -85,6 +86,7 @@ EBIN_DECLARE_GROUP(logic)   // And Or Xor BitwiseAnd/Or/Xor BitShift
 EBIN_DECLARE_GROUP(chan)    // PRelu BatchNormalization Clip BiasPRelu
 EBIN_DECLARE_GROUP(ext)     // Max Min RSub RDiv
 EBIN_DECLARE_GROUP(tern)    // MulAdd (three inputs)
+EBIN_DECLARE_GROUP(powmix)  // Pow with an exponent of another type
 #undef EBIN_DECLARE_GROUP
 
 }  // namespace ebin

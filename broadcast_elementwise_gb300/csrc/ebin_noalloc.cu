@@ -96,12 +96,13 @@ extern "C" ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, con
 
     // same aliasing rule as ebin_execute
     const int64_t isz = (int64_t)ebin_dtype_size(p.dt);
+    const int64_t isz_b = (int64_t)ebin_dtype_size(p.dt_b);
     const int64_t out_bytes = p.numel * (int64_t)ebin_dtype_size(p.out_dt);
     if (overlaps(A, p.span_a * isz, out, out_bytes) &&
         !(A == out && !p.strided_a && p.numel_a == p.numel && p.dt == p.out_dt))
         return EBIN_ERR_ALIAS;
-    if (B && overlaps(B, p.span_b * isz, out, out_bytes) &&
-        !(plain_b && B == out && !p.strided_b && p.numel_b == p.numel && p.dt == p.out_dt))
+    if (B && overlaps(B, p.span_b * isz_b, out, out_bytes) &&
+        !(plain_b && B == out && !p.strided_b && p.numel_b == p.numel && p.dt_b == p.out_dt))
         return EBIN_ERR_ALIAS;
 
     int dev = 0;
@@ -118,6 +119,7 @@ extern "C" ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, con
     ebin::Launch L{};
     L.op = p.op;
     L.dt = dt_class(p.dt);
+    L.dt_b = dt_class(p.dt_b);
     L.family = p.family;
     L.g = p.g;
     L.numel = p.numel;

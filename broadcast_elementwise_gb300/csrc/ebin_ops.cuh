@@ -376,30 +376,81 @@ template <class T> struct OpMod : PlainB<T, T> {
     }
 };
 
+// Integer a^e with wrap: square and multiply; a negative e gives
+// trunc(1 / a^|e|) (+-1 for a = +-1, else 0) and a = 0 raises DIV_BY_ZERO.
+template <class T>
+__device__ __forceinline__ T int_pow(T a, int64_t e, uint32_t &err) {
+    using U = typename Tr<T>::UT;
+    if (e < 0) {
+        if (a == 0) { err |= kErrDivByZero; return (T)0; }
+        if (a == 1) return (T)1;
+        if (a == (T)-1) return (e & 1) ? (T)-1 : (T)1;
+        return (T)0;
+    }
+    U result = 1, base = (U)a;
+    uint64_t k = (uint64_t)e;
+    while (k) {
+        if (k & 1u) result *= base;
+        base *= base;
+        k >>= 1;
+    }
+    return (T)result;
+}
+
+// Floating a^e: C pow semantics evaluated in binary64, rounded once to
+// binary32 (then to a 16-bit type).
+template <class T>
+__device__ __forceinline__ T float_pow(T a, double e) {
+    return Tr<T>::out(__double2float_rn(pow((double)Tr<T>::in(a), e)));
+}
+
 template <class T> struct OpPow : PlainB<T, T> {
     static constexpr bool kLegal = is_float_v<T> || is_signed_int_v<T>;
     static constexpr bool kValidates = is_signed_int_v<T>;
     static constexpr bool kScalarAttr = is_float_v<T>;     // ncnn binaryop POW with_scalar
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
-        if constexpr (is_float_v<T>) {
-            // C pow semantics evaluated in binary64, rounded once to binary32
-            const double r = pow((double)Tr<T>::in(a), (double)Tr<T>::in(b));
-            return Tr<T>::out(__double2float_rn(r));
+        if constexpr (is_float_v<T>) return float_pow(a, (double)Tr<T>::in(b));
+        else return int_pow(a, (int64_t)b, err);
+    }
+};
+
+// Pow with an exponent of another type ("Binary Kernel Design", Compute,
+// scheduling, and safety: signatures other than the same-type ones run
+// through typed scalar adapters; ONNX Pow takes base T, exponent T1).
+//  - floating base: float_pow on the exponent's value as binary64;
+//  - integer base, integer exponent: int_pow with the exponent as 64 bits;
+//  - integer base, floating exponent: pow in binary64, truncated toward zero,
+//    saturated at the base type's bounds, NaN to 0 (no status).
+// Only the general (element by element) kernel runs it.
+template <class TA, class TB> struct OpPowMixed {
+    using In = TA;
+    using Out = TA;
+    using BV = TB;
+    using BIn = TB;                  // B's element type differs from A's
+    static constexpr bool kPlainB = false;
+    static constexpr bool kLegal = (is_float_v<TA> || is_signed_int_v<TA>) && !is_bool_v<TB>;
+    static constexpr bool kValidates = is_signed_int_v<TA> && !is_float_v<TB>;
+    __device__ __forceinline__ static BV loadB(const TB *B, int64_t off, const OpArgs &) {
+        return B[off];
+    }
+    __device__ __forceinline__ static double as_double(TB e) {
+        if constexpr (is_float_v<TB>) return (double)Tr<TB>::in(e);
+        else return (double)e;
+    }
+    __device__ __forceinline__ static TA apply(TA a, TB b, const OpArgs &, uint32_t &err) {
+        if constexpr (is_float_v<TA>) {
+            return float_pow(a, as_double(b));
+        } else if constexpr (!is_float_v<TB>) {
+            return int_pow(a, (int64_t)b, err);
         } else {
-            using U = typename Tr<T>::UT;
-            if (b < 0) {
-                if (a == 0) { err |= kErrDivByZero; return (T)0; }
-                if (a == 1) return (T)1;
-                if (a == (T)-1) return (b & 1) ? (T)-1 : (T)1;
-                return (T)0;                                     // trunc(1 / a^|b|)
-            }
-            U result = 1, base = (U)a, e = (U)b;
-            while (e) {                                          // square and multiply, wrapping
-                if (e & 1u) result *= base;
-                base *= base;
-                e >>= 1;
-            }
-            return (T)result;
+            const double y = pow((double)a, as_double(b));
+            constexpr bool k32 = std::is_same_v<TA, int32_t>;
+            constexpr TA tmin = k32 ? (TA)INT32_MIN : (TA)INT64_MIN;
+            constexpr TA tmax = k32 ? (TA)INT32_MAX : (TA)INT64_MAX;
+            if (isnan(y)) return (TA)0;
+            if (y >= (double)tmax) return tmax;
+            if (y <= (double)tmin) return tmin;
+            return (TA)y;                                        // truncates toward zero
         }
     }
 };

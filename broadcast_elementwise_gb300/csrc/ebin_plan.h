@@ -27,6 +27,7 @@ struct ebin_plan_s {
     int op = 0;
     ebin_attrs attrs{};
     ebin_dtype out_dt = EBIN_FLOAT32;
+    ebin_dtype dt_b = EBIN_FLOAT32;        // B's type (mixed-type Pow), else dt
     int rank_out = 0;
     int64_t shape_out[ebin::kMaxRank] = {};
     int64_t numel = 0, numel_a = 0, numel_b = 0, numel_c = 0;

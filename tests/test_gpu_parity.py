@@ -219,3 +219,50 @@ def test_strided_input_views(op, dtype):
             compare(op, dtype, got, want, "%s %s view %s/%s forced=%s family=%s" %
                     (op, dtype, shape, strides, forced, plan.family))
 
+
+MIXED_POW = [(ta, tb) for ta in ("float32", "float16", "bfloat16", "int32", "int64")
+             for tb in ("float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32")
+             if ta != tb]
+
+
+@pytest.mark.parametrize("ta,tb", MIXED_POW, ids=["%s^%s" % p for p in MIXED_POW])
+def test_pow_with_exponent_of_another_type(ta, tb):
+    """Pow base T / exponent T1 through the typed-adapter (general) kernel
+    against the oracle: floating bases within 2 ulp, integer bases exactly,
+    status bits equal."""
+    import torch
+    rng_a = {"float32": (0.0, 6.0), "float16": (0.0, 4.0), "bfloat16": (0.0, 6.0)}
+    for i, (sa, sb) in enumerate([((3000,), (3000,)), ((40, 75), (75,)), ((6, 1, 50), (1, 7, 1))]):
+        na, nb = int(np.prod(sa)), int(np.prod(sb))
+        if ta in FLOATS:
+            lo, hi = rng_a[ta]
+            a = datagen.float_to(datagen.uniform(80 + i, 0, na, lo, hi), ta).reshape(sa)
+        else:
+            a = datagen.make("int_range", ta, sa, 80 + i, 0, lo=-6, hi=6)
+        if tb in FLOATS:
+            e = datagen.uniform(80 + i, 1, nb, -3.0, 3.0)
+            e[::4] = np.round(e[::4])
+            b = datagen.float_to(e, tb).reshape(sb)
+        else:
+            lo = 0 if tb.startswith("u") else -2
+            b = datagen.make("int_range", tb, sb, 80 + i, 1, lo=lo, hi=12)
+        want, wbits = oracle.run_pow_mixed(a, b, ta, tb)
+        got, bits, fam = run_engine("Pow", ta, a, b, attrs={"dtype_b": tb})
+        assert fam == "general_strided"
+        assert bits == wbits
+        if ta in FLOATS:
+            d = ulp_distance(got, want, ta)
+            assert d.max(initial=0) <= 2, ("Pow %s^%s" % (ta, tb), d.max())
+        elif tb in FLOATS:
+            # pow in binary64 is within 2 ulp on the device; where the power lies
+            # within 4 ulp of an integer, truncation may land one unit apart
+            bf = b.astype(np.float64) if tb != "bfloat16" else \
+                (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            with np.errstate(all="ignore"):
+                y = np.broadcast_to(np.power(a.astype(np.float64), bf), want.shape)
+                near = np.abs(y - np.round(y)) <= 4 * np.spacing(np.abs(y))
+            diff = np.abs(got.astype(np.int64) - want.astype(np.int64))
+            assert ((diff == 0) | (near & (diff == 1))).all(), ("Pow %s^%s" % (ta, tb))
+        else:
+            assert (got == want).all(), ("Pow %s^%s" % (ta, tb))
+

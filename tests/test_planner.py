@@ -344,6 +344,31 @@ def test_strided_view_rules():
     assert e.value.code == "alias"
 
 
+def test_mixed_type_pow_rules():
+    """Pow's exponent may have any non-BOOL type (typed scalar adapters); every
+    other operator needs equal types.  Mixed plans run the general kernel."""
+    for op in eb.OPS:
+        for ta in ALL_DTYPES:
+            for tb in ALL_DTYPES:
+                if ta == tb:
+                    continue
+                legal = op == "Pow" and oracle.type_allowed("Pow", ta) and tb != "bool"
+                try:
+                    eb.Descriptor(op, ta, dtype_b=tb).close()
+                    got = True
+                except eb.EbinError as e:
+                    assert e.code == "unsupported_type"
+                    got = False
+                assert got == legal, (op, ta, tb)
+    d = eb.Descriptor("Pow", "bfloat16", dtype_b="uint8")
+    assert d.out_dtype == "bfloat16"
+    assert eb.Plan(d, (300, 256), (256,)).family == "general_strided"
+    assert eb.Plan(d, (0, 256), (256,)).family == "empty"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (300, 256), (256,), family="repeated_block")
+    assert e.value.code == "family"
+
+
 def test_plan_cache_is_an_8_entry_lru():
     eb.ebin_plan_cache_clear()
     d = eb.Descriptor("Sub", "int32")
