@@ -36,6 +36,10 @@ STORAGE = {
     "uint8": np.uint8,
     "uint32": np.uint32,
     "bool": np.uint8,
+    "int8": np.int8,
+    "int16": np.int16,
+    "uint16": np.uint16,
+    "uint64": np.uint64,
 }
 
 

@@ -53,7 +53,8 @@ enum {
     OR_BIAS_PRELU, OR_MULADD,
     OR_NUM_OPS
 };
-enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL, OT_NUM };
+enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL,
+       OT_I8, OT_I16, OT_U16, OT_U64, OT_NUM };
 
 /* return codes */
 enum { OR_OK = 0, OR_SHAPES = 1, OR_ARGS = 2, OR_TYPE = 3, OR_ATTR = 4 };
@@ -66,9 +67,9 @@ static int size_of(int t)
 {
     switch (t) {
     case OT_F32: case OT_I32: case OT_U32: return 4;
-    case OT_F16: case OT_BF16: return 2;
-    case OT_I64: return 8;
-    case OT_U8: case OT_BOOL: return 1;
+    case OT_F16: case OT_BF16: case OT_I16: case OT_U16: return 2;
+    case OT_I64: case OT_U64: return 8;
+    case OT_U8: case OT_BOOL: case OT_I8: return 1;
     }
     return 0;
 }
@@ -147,8 +148,14 @@ uint16_t oracle_float_to_bf16(float f)
 /* element access                                                            */
 /* ------------------------------------------------------------------------ */
 static int is_float_type(int t) { return t == OT_F32 || t == OT_F16 || t == OT_BF16; }
-static int is_signed_int(int t) { return t == OT_I32 || t == OT_I64; }
-static int is_int_type(int t) { return t == OT_I32 || t == OT_I64 || t == OT_U8 || t == OT_U32; }
+static int is_signed_int(int t)
+{
+    return t == OT_I32 || t == OT_I64 || t == OT_I8 || t == OT_I16;
+}
+static int is_int_type(int t)
+{
+    return is_signed_int(t) || t == OT_U8 || t == OT_U16 || t == OT_U32 || t == OT_U64;
+}
 
 static float load_float(const void *p, int t, int64_t i)
 {
@@ -164,7 +171,9 @@ static void store_float(void *p, int t, int64_t i, float v)
     else ((uint16_t *)p)[i] = oracle_float_to_bf16(v);
 }
 
-/* integers travel as their value in int64 (uint32 fits), wrapped on store */
+/* integers travel as their value in int64 (every unsigned type up to 32 bits
+   fits); uint64 travels as its bit pattern and is compared and divided
+   unsigned (see int_cmp and int_op); wrapped on store */
 static int64_t load_int(const void *p, int t, int64_t i)
 {
     switch (t) {
@@ -172,6 +181,10 @@ static int64_t load_int(const void *p, int t, int64_t i)
     case OT_I64: return ((const int64_t *)p)[i];
     case OT_U8: case OT_BOOL: return ((const uint8_t *)p)[i];
     case OT_U32: return ((const uint32_t *)p)[i];
+    case OT_I8: return ((const int8_t *)p)[i];
+    case OT_I16: return ((const int16_t *)p)[i];
+    case OT_U16: return ((const uint16_t *)p)[i];
+    case OT_U64: return (int64_t)((const uint64_t *)p)[i];
     }
     return 0;
 }
@@ -183,7 +196,16 @@ static void store_int(void *p, int t, int64_t i, uint64_t v)
     case OT_I64: ((uint64_t *)p)[i] = v; break;
     case OT_U8: case OT_BOOL: ((uint8_t *)p)[i] = (uint8_t)v; break;
     case OT_U32: ((uint32_t *)p)[i] = (uint32_t)v; break;
+    case OT_I8: ((uint8_t *)p)[i] = (uint8_t)v; break;
+    case OT_I16: case OT_U16: ((uint16_t *)p)[i] = (uint16_t)v; break;
+    case OT_U64: ((uint64_t *)p)[i] = v; break;
     }
+}
+
+/* a < b on values of type t */
+static int int_less(int t, int64_t a, int64_t b)
+{
+    return t == OT_U64 ? (uint64_t)a < (uint64_t)b : a < b;
 }
 
 static int bits_of(int t) { return 8 * size_of(t); }
@@ -217,10 +239,10 @@ int oracle_type_allowed(int op, int t)
     case OR_BITWISE_AND: case OR_BITWISE_OR: case OR_BITWISE_XOR:
         return is_int_type(t);
     case OR_BITSHIFT:
-        return t == OT_U8 || t == OT_U32;
+        return t == OT_U8 || t == OT_U16 || t == OT_U32 || t == OT_U64;
     case OR_PRELU:
         return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64 ||
-               t == OT_U32;
+               t == OT_U32 || t == OT_U64;
     case OR_BATCHNORM: case OR_BIAS_PRELU:
         return is_float_type(t);
     }
@@ -315,14 +337,14 @@ static int float_cmp(int op, float a, float b)
     return 0;
 }
 
-static int int_cmp(int op, int64_t a, int64_t b)
+static int int_cmp(int op, int t, int64_t a, int64_t b)
 {
     switch (op) {
     case OR_EQUAL: return a == b;
-    case OR_LESS: return a < b;
-    case OR_GREATER: return a > b;
-    case OR_LESS_EQUAL: return a <= b;
-    case OR_GREATER_EQUAL: return a >= b;
+    case OR_LESS: return int_less(t, a, b);
+    case OR_GREATER: return int_less(t, b, a);
+    case OR_LESS_EQUAL: return !int_less(t, b, a);
+    case OR_GREATER_EQUAL: return !int_less(t, a, b);
     }
     return 0;
 }
@@ -340,11 +362,13 @@ static uint64_t int_op(int op, int t, int64_t a, int64_t b, int fmod_flag, int d
     case OR_MUL: return ua * ub;
     case OR_DIV:
         if (b == 0) { *status |= OR_ST_DIV_BY_ZERO; return 0; }
-        if (sgn && b == -1) return 0ull - ua;                 /* INT_MIN / -1 wraps */
+        if (!sgn) return ua / ub;                              /* unsigned (uint64 too) */
+        if (b == -1) return 0ull - ua;                         /* INT_MIN / -1 wraps */
         return (uint64_t)(a / b);                              /* C truncation */
     case OR_MOD: {
         if (b == 0) { *status |= OR_ST_DIV_BY_ZERO; return 0; }
-        if (sgn && b == -1) return 0;
+        if (!sgn) return ua % ub;
+        if (b == -1) return 0;
         int64_t r = a % b;                                     /* truncated, sign of a */
         if (!fmod_flag && r != 0 && ((r < 0) != (b < 0))) r += b;   /* floor: sign of b */
         return (uint64_t)r;
@@ -376,12 +400,13 @@ static uint64_t int_op(int op, int t, int64_t a, int64_t b, int fmod_flag, int d
     }
     case OR_PRELU:                                             /* x >= 0 ? x : slope * x */
         return (!sgn || as_signed(ua, w) >= 0) ? ua : ub * ua;
-    case OR_MAX: return a > b ? ua : ub;                      /* values, not bit patterns */
-    case OR_MIN: return a < b ? ua : ub;
+    case OR_MAX: return int_less(t, b, a) ? ua : ub;          /* values, not bit patterns */
+    case OR_MIN: return int_less(t, a, b) ? ua : ub;
     case OR_RSUB: return ub - ua;
     case OR_RDIV:                                              /* B / A, truncated */
         if (a == 0) { *status |= OR_ST_DIV_BY_ZERO; return 0; }
-        if (sgn && a == -1) return 0ull - ub;
+        if (!sgn) return ub / ua;
+        if (a == -1) return 0ull - ub;
         return (uint64_t)(b / a);
     }
     return 0;
@@ -570,8 +595,8 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
                 store_float(out, t, k, y);
             } else {
                 int64_t y = load_int(A, t, oa);
-                if (has_min) { int64_t lo = load_int(B, t, 0); if (y < lo) y = lo; }
-                if (has_max) { int64_t hi = load_int(B, t, 1); if (y > hi) y = hi; }
+                if (has_min) { int64_t lo = load_int(B, t, 0); if (int_less(t, y, lo)) y = lo; }
+                if (has_max) { int64_t hi = load_int(B, t, 1); if (int_less(t, hi, y)) y = hi; }
                 store_int(out, t, k, (uint64_t)y);
             }
             continue;
@@ -584,9 +609,9 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             } else if (is_float_type(t)) {
                 v = float_cmp(op, load_float(A, t, oa), load_float(B, t, ob));
             } else if (t == OT_BOOL) {
-                v = int_cmp(op, load_int(A, t, oa) != 0, load_int(B, t, ob) != 0);
+                v = int_cmp(op, t, load_int(A, t, oa) != 0, load_int(B, t, ob) != 0);
             } else {
-                v = int_cmp(op, load_int(A, t, oa), load_int(B, t, ob));
+                v = int_cmp(op, t, load_int(A, t, oa), load_int(B, t, ob));
             }
             ((uint8_t *)out)[k] = (uint8_t)(v ? 1 : 0);
             continue;
@@ -620,6 +645,7 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
 static double exponent_as_double(const void *B, int tb, int64_t i)
 {
     if (is_float_type(tb)) return (double)load_float(B, tb, i);
+    if (tb == OT_U64) return (double)(uint64_t)load_int(B, tb, i);
     return (double)load_int(B, tb, i);
 }
 
@@ -647,8 +673,18 @@ int oracle_eval_pow_mixed(int ta, int tb, const int64_t *sa, int ra, const int64
             double x = (double)load_float(A, ta, oa);
             store_float(out, ta, k, (float)pow(x, exponent_as_double(B, tb, ob)));
         } else if (!is_float_type(tb)) {
-            store_int(out, ta, k, int_op(OR_POW, ta, load_int(A, ta, oa), load_int(B, tb, ob),
-                                         0, 0, status));
+            int64_t e = load_int(B, tb, ob);
+            if (tb == OT_U64 && e < 0) {                       /* an exponent of 2^63 or more */
+                uint64_t result = 1, base = (uint64_t)load_int(A, ta, oa), k2 = (uint64_t)e;
+                while (k2) {
+                    if (k2 & 1u) result *= base;
+                    base *= base;
+                    k2 >>= 1;
+                }
+                store_int(out, ta, k, result);
+            } else {
+                store_int(out, ta, k, int_op(OR_POW, ta, load_int(A, ta, oa), e, 0, 0, status));
+            }
         } else {
             double y = pow((double)load_int(A, ta, oa), exponent_as_double(B, tb, ob));
             int64_t v;

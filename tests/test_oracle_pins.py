@@ -345,7 +345,10 @@ def test_mod_specials():
 # --------------------------------------------------------------------------- integers
 
 INT_LIMITS = {"int32": (-(1 << 31), (1 << 31) - 1), "int64": (-(1 << 63), (1 << 63) - 1),
-              "uint8": (0, 255), "uint32": (0, (1 << 32) - 1)}
+              "uint8": (0, 255), "uint32": (0, (1 << 32) - 1),
+              "int8": (-128, 127), "int16": (-(1 << 15), (1 << 15) - 1),
+              "uint16": (0, (1 << 16) - 1), "uint64": (0, (1 << 64) - 1)}
+ALL_INTS = ["int32", "int64", "uint8", "uint32", "int8", "int16", "uint16", "uint64"]
 
 
 def wrap(v, dtype):
@@ -369,7 +372,7 @@ def trunc_div(a, b):
     return q if (a >= 0) == (b >= 0) else -q
 
 
-@pytest.mark.parametrize("dtype", ["int32", "int64", "uint8", "uint32"])
+@pytest.mark.parametrize("dtype", ALL_INTS)
 def test_int_arith_matches_python_integers(dtype):
     a, b = int_pairs(dtype)
     st_t = datagen.STORAGE[dtype]
@@ -455,7 +458,7 @@ def test_max_min_signed_zero_and_nan():
                       "float32")
 
 
-@pytest.mark.parametrize("dtype", ["int32", "int64", "uint8", "uint32"])
+@pytest.mark.parametrize("dtype", ALL_INTS)
 def test_int_max_min_rsub_rdiv_match_python_integers(dtype):
     a, b = int_pairs(dtype)
     st_t = datagen.STORAGE[dtype]
@@ -502,7 +505,7 @@ def test_int_division_by_zero_sets_status():
     assert st == 0
 
 
-@pytest.mark.parametrize("dtype", ["uint8", "uint32"])
+@pytest.mark.parametrize("dtype", ["uint8", "uint16", "uint32", "uint64"])
 def test_bitshift_matches_numpy(dtype):
     w = 8 * np.dtype(datagen.STORAGE[dtype]).itemsize
     a = datagen.make("bits", dtype, (4096,), 5, 0)
@@ -566,7 +569,8 @@ def test_f32_pow_within_half_ulp_of_mpmath():
 
 
 # --------------------------------------------------------------------------- mixed-type Pow
-MIXED_EXP = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32"]
+MIXED_EXP = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "int8",
+             "int16", "uint16", "uint64"]
 
 
 def _exponents(dtype, n, seed):
@@ -604,7 +608,8 @@ def test_pow_mixed_float_base_matches_numpy_float64(ta, tb):
 
 
 @pytest.mark.parametrize("ta", ["int32", "int64"])
-@pytest.mark.parametrize("tb", ["int32", "int64", "uint8", "uint32"])
+@pytest.mark.parametrize("tb", ["int32", "int64", "uint8", "uint32", "int8", "int16", "uint16",
+                                "uint64"])
 def test_pow_mixed_int_base_int_exponent_matches_python(ta, tb):
     if ta == tb:
         pytest.skip("same type")
@@ -681,7 +686,7 @@ def test_comparisons_match_numpy(op, fn):
     bf_a, bf_b = bf16_bits(a), bf16_bits(b)
     got, _ = oracle.run(op, bf_a, bf_b, "bfloat16")
     assert (got == fn(bf16_to_f32(bf_a), bf16_to_f32(bf_b)).astype(np.uint8)).all()
-    for dtype in ("int32", "int64", "uint8", "uint32"):
+    for dtype in ALL_INTS:
         ia = datagen.make("bits", dtype, (3000,), 42, 0)
         ib = datagen.make("bits", dtype, (3000,), 42, 1)
         ib[::4] = ia[::4]
@@ -853,7 +858,7 @@ def test_muladd_matches_float32_chain(dtype, shapes):
     assert_bits_equal(got, want, dtype, "MulAdd")
 
 
-@pytest.mark.parametrize("dtype", ["int32", "int64", "uint8", "uint32"])
+@pytest.mark.parametrize("dtype", ALL_INTS)
 def test_muladd_int_wraps_like_python_integers(dtype):
     a, b, c = _muladd_inputs(dtype, [(3, 1, 40), (1, 5, 40), (40,)], 42)
     got = oracle.run3("MulAdd", a, b, c, dtype)
