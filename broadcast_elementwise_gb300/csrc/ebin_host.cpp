@@ -45,6 +45,10 @@ int dt_class(ebin_dtype t) {
     case EBIN_UINT8: return ebin::DT_U8;
     case EBIN_UINT32: return ebin::DT_U32;
     case EBIN_BOOL: return ebin::DT_BOOL;
+    case EBIN_INT8: return ebin::DT_I8;
+    case EBIN_INT16: return ebin::DT_I16;
+    case EBIN_UINT16: return ebin::DT_U16;
+    case EBIN_UINT64: return ebin::DT_U64;
     }
     return -1;
 }
@@ -53,9 +57,12 @@ bool is_float(ebin_dtype t) {
     return t == EBIN_FLOAT32 || t == EBIN_FLOAT16 || t == EBIN_BFLOAT16;
 }
 bool is_int(ebin_dtype t) {
-    return t == EBIN_INT32 || t == EBIN_INT64 || t == EBIN_UINT8 || t == EBIN_UINT32;
+    return t == EBIN_INT32 || t == EBIN_INT64 || t == EBIN_UINT8 || t == EBIN_UINT32 ||
+           t == EBIN_INT8 || t == EBIN_INT16 || t == EBIN_UINT16 || t == EBIN_UINT64;
 }
-bool is_signed_int(ebin_dtype t) { return t == EBIN_INT32 || t == EBIN_INT64; }
+bool is_signed_int(ebin_dtype t) {
+    return t == EBIN_INT32 || t == EBIN_INT64 || t == EBIN_INT8 || t == EBIN_INT16;
+}
 
 // Type manifest: which element type each operator accepts (A and B share it).
 bool type_legal(int op, ebin_dtype t) {
@@ -67,12 +74,15 @@ bool type_legal(int op, ebin_dtype t) {
     case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV:
     case EBIN_OP_MULADD:
         return is_float(t) || is_int(t);
-    case EBIN_OP_POW: return is_float(t) || is_signed_int(t);
+    case EBIN_OP_POW: return is_float(t) || t == EBIN_INT32 || t == EBIN_INT64;  // ONNX Pow T
     case EBIN_OP_EQUAL: return true;
     case EBIN_OP_AND: case EBIN_OP_OR: case EBIN_OP_XOR: return t == EBIN_BOOL;
     case EBIN_OP_BITWISE_AND: case EBIN_OP_BITWISE_OR: case EBIN_OP_BITWISE_XOR: return is_int(t);
-    case EBIN_OP_BITSHIFT: return t == EBIN_UINT8 || t == EBIN_UINT32;
-    case EBIN_OP_PRELU: return is_float(t) || is_signed_int(t) || t == EBIN_UINT32;
+    case EBIN_OP_BITSHIFT:
+        return t == EBIN_UINT8 || t == EBIN_UINT16 || t == EBIN_UINT32 || t == EBIN_UINT64;
+    case EBIN_OP_PRELU:   // ONNX PRelu T
+        return is_float(t) || t == EBIN_INT32 || t == EBIN_INT64 || t == EBIN_UINT32 ||
+               t == EBIN_UINT64;
     case EBIN_OP_BATCHNORM: case EBIN_OP_BIAS_PRELU: return is_float(t);
     }
     return false;
@@ -85,7 +95,7 @@ ebin_dtype output_type(int op, ebin_dtype t) {
 // Operators whose kernels can meet invalid elements and report them.
 bool validates(int op, ebin_dtype t) {
     if ((op == EBIN_OP_DIV || op == EBIN_OP_MOD || op == EBIN_OP_RDIV) && is_int(t)) return true;
-    if (op == EBIN_OP_POW && is_signed_int(t)) return true;
+    if (op == EBIN_OP_POW && (t == EBIN_INT32 || t == EBIN_INT64)) return true;
     return op == EBIN_OP_BITSHIFT;
 }
 
@@ -792,6 +802,10 @@ cudaError_t ebin::launch(const Launch &L) {
     case 5: return launch_##g##_5(L);                                                     \
     case 6: return launch_##g##_6(L);                                                     \
     case 7: return launch_##g##_7(L);                                                     \
+    case 8: return launch_##g##_8(L);                                                     \
+    case 9: return launch_##g##_9(L);                                                     \
+    case 10: return launch_##g##_10(L);                                                   \
+    case 11: return launch_##g##_11(L);                                                   \
     default: return cudaErrorInvalidValue;                                                \
     }
     switch (L.op) {
@@ -1103,9 +1117,9 @@ void ebin::count_launch() { g_launches.fetch_add(1); }
 extern "C" size_t ebin_dtype_size(ebin_dtype t) {
     switch (t) {
     case EBIN_FLOAT32: case EBIN_INT32: case EBIN_UINT32: return 4;
-    case EBIN_FLOAT16: case EBIN_BFLOAT16: return 2;
-    case EBIN_INT64: return 8;
-    case EBIN_UINT8: case EBIN_BOOL: return 1;
+    case EBIN_FLOAT16: case EBIN_BFLOAT16: case EBIN_INT16: case EBIN_UINT16: return 2;
+    case EBIN_INT64: case EBIN_UINT64: return 8;
+    case EBIN_UINT8: case EBIN_BOOL: case EBIN_INT8: return 1;
     }
     return 0;
 }

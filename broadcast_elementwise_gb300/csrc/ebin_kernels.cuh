@@ -964,6 +964,10 @@ template <> struct DtType<DT_I64> { using type = int64_t; };
 template <> struct DtType<DT_U8> { using type = uint8_t; };
 template <> struct DtType<DT_U32> { using type = uint32_t; };
 template <> struct DtType<DT_BOOL> { using type = Bool8; };
+template <> struct DtType<DT_I8> { using type = int8_t; };
+template <> struct DtType<DT_I16> { using type = int16_t; };
+template <> struct DtType<DT_U16> { using type = uint16_t; };
+template <> struct DtType<DT_U64> { using type = uint64_t; };
 
 }  // namespace ebin
 

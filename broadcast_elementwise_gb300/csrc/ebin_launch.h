@@ -11,7 +11,10 @@ namespace ebin {
 constexpr int kMaxRank = 8;
 
 // Internal element-type classes, one kernel set each.
-enum Dt : int { DT_F32 = 0, DT_F16, DT_BF16, DT_I32, DT_I64, DT_U8, DT_U32, DT_BOOL, DT_COUNT };
+enum Dt : int {
+    DT_F32 = 0, DT_F16, DT_BF16, DT_I32, DT_I64, DT_U8, DT_U32, DT_BOOL,
+    DT_I8, DT_I16, DT_U16, DT_U64, DT_COUNT
+};
 
 // Loop families (same numbering as the public ebin_family).
 enum Fam : int {
@@ -77,7 +80,11 @@ cudaError_t launch(const Launch &L);
     cudaError_t launch_##g##_4(const Launch &);                                       \
     cudaError_t launch_##g##_5(const Launch &);                                       \
     cudaError_t launch_##g##_6(const Launch &);                                       \
-    cudaError_t launch_##g##_7(const Launch &);
+    cudaError_t launch_##g##_7(const Launch &);                                       \
+    cudaError_t launch_##g##_8(const Launch &);                                       \
+    cudaError_t launch_##g##_9(const Launch &);                                       \
+    cudaError_t launch_##g##_10(const Launch &);                                      \
+    cudaError_t launch_##g##_11(const Launch &);
 EBIN_DECLARE_GROUP(arith)   // Add Sub Mul Div
 EBIN_DECLARE_GROUP(mod)     // Mod
 EBIN_DECLARE_GROUP(pow)     // Pow

@@ -68,6 +68,10 @@ int dt_class(ebin_dtype t) {
     case EBIN_UINT8: return ebin::DT_U8;
     case EBIN_UINT32: return ebin::DT_U32;
     case EBIN_BOOL: return ebin::DT_BOOL;
+    case EBIN_INT8: return ebin::DT_I8;
+    case EBIN_INT16: return ebin::DT_I16;
+    case EBIN_UINT16: return ebin::DT_U16;
+    case EBIN_UINT64: return ebin::DT_U64;
     }
     return -1;
 }

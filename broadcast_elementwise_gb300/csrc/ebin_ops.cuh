@@ -68,6 +68,10 @@ template <> struct Tr<int32_t> : IntTr<int32_t, uint32_t, true> {};
 template <> struct Tr<int64_t> : IntTr<int64_t, uint64_t, true> {};
 template <> struct Tr<uint8_t> : IntTr<uint8_t, uint8_t, false> {};
 template <> struct Tr<uint32_t> : IntTr<uint32_t, uint32_t, false> {};
+template <> struct Tr<int8_t> : IntTr<int8_t, uint8_t, true> {};
+template <> struct Tr<int16_t> : IntTr<int16_t, uint16_t, true> {};
+template <> struct Tr<uint16_t> : IntTr<uint16_t, uint16_t, false> {};
+template <> struct Tr<uint64_t> : IntTr<uint64_t, uint64_t, false> {};
 template <> struct Tr<Bool8> {
     using C = bool;
     static constexpr bool kFloat = false;
@@ -80,10 +84,19 @@ template <class T> constexpr bool is_float_v = std::is_same_v<T, float> ||
 template <class T> constexpr bool is_int_v = std::is_same_v<T, int32_t> ||
                                              std::is_same_v<T, int64_t> ||
                                              std::is_same_v<T, uint8_t> ||
-                                             std::is_same_v<T, uint32_t>;
+                                             std::is_same_v<T, uint32_t> ||
+                                             std::is_same_v<T, int8_t> ||
+                                             std::is_same_v<T, int16_t> ||
+                                             std::is_same_v<T, uint16_t> ||
+                                             std::is_same_v<T, uint64_t>;
 template <class T> constexpr bool is_bool_v = std::is_same_v<T, Bool8>;
 template <class T> constexpr bool is_signed_int_v = std::is_same_v<T, int32_t> ||
-                                                    std::is_same_v<T, int64_t>;
+                                                    std::is_same_v<T, int64_t> ||
+                                                    std::is_same_v<T, int8_t> ||
+                                                    std::is_same_v<T, int16_t>;
+// ONNX Pow's integer base types
+template <class T> constexpr bool is_pow_int_v = std::is_same_v<T, int32_t> ||
+                                                 std::is_same_v<T, int64_t>;
 
 // Common shape of an operator functor whose B operand is an ordinary
 // broadcast tensor of the input type.
@@ -378,17 +391,19 @@ template <class T> struct OpMod : PlainB<T, T> {
 
 // Integer a^e with wrap: square and multiply; a negative e gives
 // trunc(1 / a^|e|) (+-1 for a = +-1, else 0) and a = 0 raises DIV_BY_ZERO.
+// (e is given as its sign and its magnitude: unsigned 64-bit exponents reach
+// 2^64 - 1)
 template <class T>
-__device__ __forceinline__ T int_pow(T a, int64_t e, uint32_t &err) {
+__device__ __forceinline__ T int_pow(T a, bool neg, uint64_t mag, uint32_t &err) {
     using U = typename Tr<T>::UT;
-    if (e < 0) {
+    if (neg) {
         if (a == 0) { err |= kErrDivByZero; return (T)0; }
         if (a == 1) return (T)1;
-        if (a == (T)-1) return (e & 1) ? (T)-1 : (T)1;
+        if (a == (T)-1) return (mag & 1) ? (T)-1 : (T)1;
         return (T)0;
     }
     U result = 1, base = (U)a;
-    uint64_t k = (uint64_t)e;
+    uint64_t k = mag;
     while (k) {
         if (k & 1u) result *= base;
         base *= base;
@@ -405,12 +420,12 @@ __device__ __forceinline__ T float_pow(T a, double e) {
 }
 
 template <class T> struct OpPow : PlainB<T, T> {
-    static constexpr bool kLegal = is_float_v<T> || is_signed_int_v<T>;
-    static constexpr bool kValidates = is_signed_int_v<T>;
+    static constexpr bool kLegal = is_float_v<T> || is_pow_int_v<T>;
+    static constexpr bool kValidates = is_pow_int_v<T>;
     static constexpr bool kScalarAttr = is_float_v<T>;     // ncnn binaryop POW with_scalar
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
         if constexpr (is_float_v<T>) return float_pow(a, (double)Tr<T>::in(b));
-        else return int_pow(a, (int64_t)b, err);
+        else return int_pow(a, b < 0, b < 0 ? 0 - (uint64_t)b : (uint64_t)b, err);
     }
 };
 
@@ -428,8 +443,8 @@ template <class TA, class TB> struct OpPowMixed {
     using BV = TB;
     using BIn = TB;                  // B's element type differs from A's
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = (is_float_v<TA> || is_signed_int_v<TA>) && !is_bool_v<TB>;
-    static constexpr bool kValidates = is_signed_int_v<TA> && !is_float_v<TB>;
+    static constexpr bool kLegal = (is_float_v<TA> || is_pow_int_v<TA>) && !is_bool_v<TB>;
+    static constexpr bool kValidates = is_pow_int_v<TA> && !is_float_v<TB>;
     __device__ __forceinline__ static BV loadB(const TB *B, int64_t off, const OpArgs &) {
         return B[off];
     }
@@ -441,7 +456,10 @@ template <class TA, class TB> struct OpPowMixed {
         if constexpr (is_float_v<TA>) {
             return float_pow(a, as_double(b));
         } else if constexpr (!is_float_v<TB>) {
-            return int_pow(a, (int64_t)b, err);
+            if constexpr (is_signed_int_v<TB>)
+                return int_pow(a, b < 0, b < 0 ? 0 - (uint64_t)(int64_t)b : (uint64_t)b, err);
+            else
+                return int_pow(a, false, (uint64_t)b, err);
         } else {
             const double y = pow((double)a, as_double(b));
             constexpr bool k32 = std::is_same_v<TA, int32_t>;
@@ -542,14 +560,16 @@ template <class T, int K> struct OpBitwise : PlainB<T, T> {
 };
 
 template <class T> struct OpShift : PlainB<T, T> {
-    static constexpr bool kLegal = std::is_same_v<T, uint8_t> || std::is_same_v<T, uint32_t>;
+    static constexpr bool kLegal = std::is_same_v<T, uint8_t> || std::is_same_v<T, uint16_t> ||
+                                   std::is_same_v<T, uint32_t> || std::is_same_v<T, uint64_t>;
     static constexpr bool kValidates = true;
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &p, uint32_t &err) {
         if constexpr (kLegal) {
-            constexpr uint32_t w = 8 * sizeof(T);
-            const uint32_t s = (uint32_t)b;
-            if (s >= w) { err |= kErrShiftRange; return (T)0; }
-            return p.direction == 0 ? (T)((uint32_t)a << s) : (T)((uint32_t)a >> s);
+            // the count compared in the element's own width; narrow types shift in 32 bits
+            using U = std::conditional_t<(sizeof(T) < 4), uint32_t, T>;
+            constexpr T w = (T)(8 * sizeof(T));
+            if (b >= w) { err |= kErrShiftRange; return (T)0; }
+            return p.direction == 0 ? (T)((U)a << (U)b) : (T)((U)a >> (U)b);
         } else {
             return a;
         }
@@ -558,8 +578,8 @@ template <class T> struct OpShift : PlainB<T, T> {
 
 // ---------------------------------------------------------------- per-channel operators
 template <class T> struct OpPRelu : PlainB<T, T> {
-    static constexpr bool kLegal = is_float_v<T> || is_signed_int_v<T> ||
-                                   std::is_same_v<T, uint32_t>;
+    static constexpr bool kLegal = is_float_v<T> || is_pow_int_v<T> ||   // ONNX PRelu T
+                                   std::is_same_v<T, uint32_t> || std::is_same_v<T, uint64_t>;
     static constexpr bool kValidates = false;
     __device__ __forceinline__ static T apply(T a, T slope, const OpArgs &, uint32_t &) {
         if constexpr (is_float_v<T>) {

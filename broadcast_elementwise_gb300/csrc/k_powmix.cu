@@ -26,6 +26,10 @@ cudaError_t EBIN_GROUP_FN(powmix)(const Launch &L) {
     case DT_I64: return launch_mixed<OpPowMixed<TA, int64_t>>(L);
     case DT_U8: return launch_mixed<OpPowMixed<TA, uint8_t>>(L);
     case DT_U32: return launch_mixed<OpPowMixed<TA, uint32_t>>(L);
+    case DT_I8: return launch_mixed<OpPowMixed<TA, int8_t>>(L);
+    case DT_I16: return launch_mixed<OpPowMixed<TA, int16_t>>(L);
+    case DT_U16: return launch_mixed<OpPowMixed<TA, uint16_t>>(L);
+    case DT_U64: return launch_mixed<OpPowMixed<TA, uint64_t>>(L);
     default: return cudaErrorInvalidValue;
     }
 }

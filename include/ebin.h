@@ -103,11 +103,15 @@ typedef enum ebin_op {
 typedef enum ebin_dtype {
     EBIN_FLOAT32 = 1,
     EBIN_UINT8 = 2,
+    EBIN_INT8 = 3,
+    EBIN_UINT16 = 4,
+    EBIN_INT16 = 5,
     EBIN_INT32 = 6,
     EBIN_INT64 = 7,
     EBIN_BOOL = 9,                /* one byte per element */
     EBIN_FLOAT16 = 10,
     EBIN_UINT32 = 12,
+    EBIN_UINT64 = 13,
     EBIN_BFLOAT16 = 16
 } ebin_dtype;
 

@@ -7,7 +7,7 @@ import numpy as np
 import datagen
 
 FLOATS = ("float32", "float16", "bfloat16")
-INTS = ("int32", "int64", "uint8", "uint32")
+INTS = ("int32", "int64", "uint8", "uint32", "int8", "int16", "uint16", "uint64")
 ALL_DTYPES = FLOATS + INTS + ("bool",)
 
 # operator -> element types (the engine's manifest; the oracle's agrees, see test_planner)
@@ -18,8 +18,8 @@ MANIFEST = {
     "LessOrEqual": FLOATS + INTS, "GreaterOrEqual": FLOATS + INTS,
     "And": ("bool",), "Or": ("bool",), "Xor": ("bool",),
     "BitwiseAnd": INTS, "BitwiseOr": INTS, "BitwiseXor": INTS,
-    "BitShift": ("uint8", "uint32"),
-    "PRelu": FLOATS + ("int32", "int64", "uint32"),
+    "BitShift": ("uint8", "uint16", "uint32", "uint64"),
+    "PRelu": FLOATS + ("int32", "int64", "uint32", "uint64"),
     "BatchNormalization": FLOATS,
     "Clip": FLOATS + INTS,
     "Max": FLOATS + INTS, "Min": FLOATS + INTS, "RSub": FLOATS + INTS, "RDiv": FLOATS + INTS,
@@ -105,10 +105,10 @@ def inputs_for(op, dtype, shape_a, shape_b, seed=0, attrs=None):
             b = datagen.float_to(np.array([-1.0, 1.5], np.float32), dtype)
         else:
             a = mk("bits", dtype, shape_a, seed, 0)
-            lo, hi = (20, 200) if dtype == "uint8" else (-1000000, 2000000000)
-            if dtype == "uint32":
-                lo, hi = 1000, 3000000000
-            b = np.array([lo, hi]).astype(datagen.STORAGE[dtype])
+            lo, hi = {"uint8": (20, 200), "uint32": (1000, 3000000000), "int8": (-50, 60),
+                      "int16": (-1000, 20000), "uint16": (1000, 50000),
+                      "uint64": (1000, (1 << 63) + 5)}.get(dtype, (-1000000, 2000000000))
+            b = np.array([lo, hi], dtype=object).astype(datagen.STORAGE[dtype])
         return a, b
     if dtype == "bool":
         return mk("bool", dtype, shape_a, seed, 0), mk("bool", dtype, shape_b, seed, 1)
@@ -155,10 +155,11 @@ def inputs_for(op, dtype, shape_a, shape_b, seed=0, attrs=None):
         a = mk("int_range", dtype, shape_a, seed, 0, lo=-9, hi=9)
         b = mk("int_range", dtype, shape_b, seed, 1, lo=-2, hi=40)
         return a, b
+    small = {"int8": 100, "uint8": 200}.get(dtype, 1000)       # divisors within the type
     if op in ("Div", "Mod"):
         a = mk("bits", dtype, shape_a, seed, 0)
-        lo = 0 if dtype.startswith("u") else -1000
-        b = mk("int_range", dtype, shape_b, seed, 1, lo=lo, hi=1000, skip_zero=True)
+        lo = 0 if dtype.startswith("u") else -small
+        b = mk("int_range", dtype, shape_b, seed, 1, lo=lo, hi=small, skip_zero=True)
         if dtype.startswith("u"):
             b[b == 0] = 1
         if b.size > 2 and dtype in ("int32", "int64"):
@@ -167,8 +168,8 @@ def inputs_for(op, dtype, shape_a, shape_b, seed=0, attrs=None):
             a.reshape(-1)[0] = np.iinfo(st).min
         return a, b
     if op == "RDiv":                                           # B / A: A is the divisor
-        lo = 0 if dtype.startswith("u") else -1000
-        a = mk("int_range", dtype, shape_a, seed, 0, lo=lo, hi=1000, skip_zero=True)
+        lo = 0 if dtype.startswith("u") else -small
+        a = mk("int_range", dtype, shape_a, seed, 0, lo=lo, hi=small, skip_zero=True)
         if dtype.startswith("u"):
             a[a == 0] = 1
         b = mk("bits", dtype, shape_b, seed, 1)

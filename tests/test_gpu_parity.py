@@ -221,7 +221,8 @@ def test_strided_input_views(op, dtype):
 
 
 MIXED_POW = [(ta, tb) for ta in ("float32", "float16", "bfloat16", "int32", "int64")
-             for tb in ("float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32")
+             for tb in ("float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32",
+                        "int8", "int16", "uint16", "uint64")
              if ta != tb]
 
 

@@ -15,7 +15,8 @@ import oracle
 eb = pytest.importorskip("broadcast_elementwise_gb300")
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-ALL_DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool"]
+ALL_DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool",
+              "int8", "int16", "uint16", "uint64"]
 
 
 def header_functions():
