@@ -40,6 +40,7 @@ STORAGE = {
     "int16": np.int16,
     "uint16": np.uint16,
     "uint64": np.uint64,
+    "float64": np.float64,
 }
 
 
@@ -161,6 +162,8 @@ def float_to(values: np.ndarray, dtype: str) -> np.ndarray:
     values = np.ascontiguousarray(values, dtype=np.float32)
     if dtype == "float32":
         return values
+    if dtype == "float64":
+        return values.astype(np.float64)
     if dtype == "float16":
         return values.astype(np.float16)
     if dtype == "bfloat16":
@@ -191,7 +194,7 @@ def make(kind: str, dtype: str, shape, seed: int, operand: int, **kw) -> np.ndar
     n = int(np.prod(shape, dtype=np.int64)) if shape else 1
     if kind == "uniform":
         v = float_to(uniform(seed, operand, n, kw.get("lo", -1.0), kw.get("hi", 1.0)), dtype) \
-            if dtype in ("float32", "float16", "bfloat16") else None
+            if dtype in ("float32", "float16", "bfloat16", "float64") else None
     elif kind == "normal":
         v = float_to(normal(seed, operand, n), dtype)
     elif kind == "absnormal":

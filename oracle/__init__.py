@@ -35,11 +35,11 @@ OPS = ["Add", "Sub", "Mul", "Div", "Mod", "Pow",
        "BatchNormalization", "Clip",
        "Max", "Min", "RSub", "RDiv", "BiasPRelu", "MulAdd"]
 DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool",
-          "int8", "int16", "uint16", "uint64"]
+          "int8", "int16", "uint16", "uint64", "float64"]
 STORAGE = {"float32": np.float32, "float16": np.float16, "bfloat16": np.uint16,
            "int32": np.int32, "int64": np.int64, "uint8": np.uint8, "uint32": np.uint32,
            "bool": np.uint8, "int8": np.int8, "int16": np.int16, "uint16": np.uint16,
-           "uint64": np.uint64}
+           "uint64": np.uint64, "float64": np.float64}
 RC = {0: "ok", 1: "incompatible_shapes", 2: "invalid_arg", 3: "unsupported_type", 4: "invalid_attr"}
 STATUS_DIV_BY_ZERO = 1
 STATUS_SHIFT_RANGE = 2

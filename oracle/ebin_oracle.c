@@ -54,7 +54,7 @@ enum {
     OR_NUM_OPS
 };
 enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL,
-       OT_I8, OT_I16, OT_U16, OT_U64, OT_NUM };
+       OT_I8, OT_I16, OT_U16, OT_U64, OT_F64, OT_NUM };
 
 /* return codes */
 enum { OR_OK = 0, OR_SHAPES = 1, OR_ARGS = 2, OR_TYPE = 3, OR_ATTR = 4 };
@@ -68,7 +68,7 @@ static int size_of(int t)
     switch (t) {
     case OT_F32: case OT_I32: case OT_U32: return 4;
     case OT_F16: case OT_BF16: case OT_I16: case OT_U16: return 2;
-    case OT_I64: case OT_U64: return 8;
+    case OT_I64: case OT_U64: case OT_F64: return 8;
     case OT_U8: case OT_BOOL: case OT_I8: return 1;
     }
     return 0;
@@ -147,7 +147,12 @@ uint16_t oracle_float_to_bf16(float f)
 /* ------------------------------------------------------------------------ */
 /* element access                                                            */
 /* ------------------------------------------------------------------------ */
+/* binary32 and the 16-bit types computed through it; binary64 is separate */
 static int is_float_type(int t) { return t == OT_F32 || t == OT_F16 || t == OT_BF16; }
+static int is_fp(int t) { return is_float_type(t) || t == OT_F64; }
+
+static double load_double(const void *p, int64_t i) { return ((const double *)p)[i]; }
+static void store_double(void *p, int64_t i, double v) { ((double *)p)[i] = v; }
 static int is_signed_int(int t)
 {
     return t == OT_I32 || t == OT_I64 || t == OT_I8 || t == OT_I16;
@@ -231,7 +236,7 @@ int oracle_type_allowed(int op, int t)
     case OR_CLIP: case OR_MAX: case OR_MIN: case OR_RSUB: case OR_RDIV: case OR_MULADD:
         return t != OT_BOOL && t >= 0 && t < OT_NUM;
     case OR_POW:
-        return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64;
+        return is_fp(t) || t == OT_I32 || t == OT_I64;
     case OR_EQUAL:
         return t >= 0 && t < OT_NUM;
     case OR_AND: case OR_OR: case OR_XOR:
@@ -241,10 +246,9 @@ int oracle_type_allowed(int op, int t)
     case OR_BITSHIFT:
         return t == OT_U8 || t == OT_U16 || t == OT_U32 || t == OT_U64;
     case OR_PRELU:
-        return t == OT_F32 || t == OT_F16 || t == OT_BF16 || t == OT_I32 || t == OT_I64 ||
-               t == OT_U32 || t == OT_U64;
+        return is_fp(t) || t == OT_I32 || t == OT_I64 || t == OT_U32 || t == OT_U64;
     case OR_BATCHNORM: case OR_BIAS_PRELU:
-        return is_float_type(t);
+        return is_fp(t);
     }
     return 0;
 }
@@ -268,7 +272,7 @@ int oracle_check_descriptor(int op, int opset, int fmod, int direction, int ta, 
     if (op == OR_MOD) {
         if (opset < 10 || opset > 28) return OR_ATTR;
         if (fmod != 0 && fmod != 1) return OR_ATTR;
-        if (is_float_type(ta) && fmod == 0 && opset < 28) return OR_ATTR;
+        if (is_fp(ta) && fmod == 0 && opset < 28) return OR_ATTR;
     }
     if (op == OR_BITSHIFT && direction != 0 && direction != 1) return OR_ATTR;
     return OR_OK;
@@ -323,6 +327,58 @@ static float float_op(int op, float a, float b, int fmod_flag)
     case OR_PRELU: return (a >= 0.0f) ? a : b * a;      /* slope * x below zero */
     }
     return 0.0f;
+}
+
+/* binary64 (DOUBLE): the same operators natively in binary64, each rounded
+   on its own; Pow is C pow in binary64 */
+static double double_max(double a, double b)
+{
+    if (isnan(a) || isnan(b)) return a + b;
+    if (a == b) return signbit(a) ? b : a;
+    return a > b ? a : b;
+}
+
+static double double_min(double a, double b)
+{
+    if (isnan(a) || isnan(b)) return a + b;
+    if (a == b) return signbit(a) ? a : b;
+    return a < b ? a : b;
+}
+
+static double double_op(int op, double a, double b, int fmod_flag)
+{
+    switch (op) {
+    case OR_ADD: return a + b;
+    case OR_SUB: return a - b;
+    case OR_MUL: return a * b;
+    case OR_DIV: return a / b;
+    case OR_MOD: {
+        double r = fmod(a, b);
+        if (fmod_flag) return r;
+        if (r == 0.0) return copysign(0.0, b);
+        if (signbit(r) != signbit(b)) r = r + b;
+        return r;
+    }
+    case OR_POW: return pow(a, b);
+    case OR_PRELU: return (a >= 0.0) ? a : b * a;
+    case OR_MAX: return double_max(a, b);
+    case OR_MIN: return double_min(a, b);
+    case OR_RSUB: return b - a;
+    case OR_RDIV: return b / a;
+    }
+    return 0.0;
+}
+
+static int double_cmp(int op, double a, double b)
+{
+    switch (op) {
+    case OR_EQUAL: return a == b;
+    case OR_LESS: return a < b;
+    case OR_GREATER: return a > b;
+    case OR_LESS_EQUAL: return a <= b;
+    case OR_GREATER_EQUAL: return a >= b;
+    }
+    return 0;
 }
 
 static int float_cmp(int op, float a, float b)
@@ -567,6 +623,28 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
         int64_t oa, ob;
         offsets_of(f, so, r, sta, stb, &oa, &ob);
 
+        if (op == OR_BATCHNORM && t == OT_F64) {     /* the same formula in binary64 */
+            int64_t C = sb[1], c = channel_of(f, so, r);
+            double x = load_double(A, oa);
+            double scale = load_double(B, 0 * C + c), bias = load_double(B, 1 * C + c);
+            double mean = load_double(B, 2 * C + c), var = load_double(B, 3 * C + c);
+            store_double(out, k, (x - mean) / sqrt(var + (double)eps) * scale + bias);
+            continue;
+        }
+        if (op == OR_BIAS_PRELU && t == OT_F64) {
+            int64_t C = sb[1], c = channel_of(f, so, r);
+            double y = load_double(A, oa) + load_double(B, c);
+            if (!(y >= 0.0)) y = load_double(B, C + c) * y;
+            store_double(out, k, y);
+            continue;
+        }
+        if (op == OR_CLIP && t == OT_F64) {
+            double y = load_double(A, oa);
+            if (has_min) { double lo = load_double(B, 0); if (y < lo) y = lo; }
+            if (has_max) { double hi = load_double(B, 1); if (y > hi) y = hi; }
+            store_double(out, k, y);
+            continue;
+        }
         if (op == OR_BATCHNORM) {
             int64_t C = sb[1], c = channel_of(f, so, r);
             float x = load_float(A, t, oa);
@@ -606,6 +684,8 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             if (op == OR_AND || op == OR_OR || op == OR_XOR) {
                 int x = load_int(A, t, oa) != 0, y = load_int(B, t, ob) != 0;
                 v = op == OR_AND ? (x && y) : op == OR_OR ? (x || y) : (x != y);
+            } else if (t == OT_F64) {
+                v = double_cmp(op, load_double(A, oa), load_double(B, ob));
             } else if (is_float_type(t)) {
                 v = float_cmp(op, load_float(A, t, oa), load_float(B, t, ob));
             } else if (t == OT_BOOL) {
@@ -616,7 +696,9 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             ((uint8_t *)out)[k] = (uint8_t)(v ? 1 : 0);
             continue;
         }
-        if (is_float_type(t)) {
+        if (t == OT_F64) {
+            store_double(out, k, double_op(op, load_double(A, oa), load_double(B, ob), fmod_flag));
+        } else if (is_float_type(t)) {
             float y = float_op(op, load_float(A, t, oa), load_float(B, t, ob), fmod_flag);
             store_float(out, t, k, y);
         } else {
@@ -644,6 +726,7 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
  */
 static double exponent_as_double(const void *B, int tb, int64_t i)
 {
+    if (tb == OT_F64) return load_double(B, i);
     if (is_float_type(tb)) return (double)load_float(B, tb, i);
     if (tb == OT_U64) return (double)(uint64_t)load_int(B, tb, i);
     return (double)load_int(B, tb, i);
@@ -669,10 +752,12 @@ int oracle_eval_pow_mixed(int ta, int tb, const int64_t *sa, int ra, const int64
         if (f < 0 || f >= total) return OR_ARGS;
         int64_t oa, ob;
         offsets_of(f, so, r, sta, stb, &oa, &ob);
-        if (is_float_type(ta)) {
+        if (ta == OT_F64) {
+            store_double(out, k, pow(load_double(A, oa), exponent_as_double(B, tb, ob)));
+        } else if (is_float_type(ta)) {
             double x = (double)load_float(A, ta, oa);
             store_float(out, ta, k, (float)pow(x, exponent_as_double(B, tb, ob)));
-        } else if (!is_float_type(tb)) {
+        } else if (!is_fp(tb)) {
             int64_t e = load_int(B, tb, ob);
             if (tb == OT_U64 && e < 0) {                       /* an exponent of 2^63 or more */
                 uint64_t result = 1, base = (uint64_t)load_int(A, ta, oa), k2 = (uint64_t)e;
@@ -730,7 +815,10 @@ int oracle_eval3(int op, int t, const int64_t *sa, int ra, const int64_t *sb, in
         int64_t oa, ob, oc, unused;
         offsets_of(f, so, r, sta, stb, &oa, &ob);
         offsets_of(f, so, r, stc, stc, &oc, &unused);
-        if (is_float_type(t)) {
+        if (t == OT_F64) {
+            double p = load_double(A, oa) * load_double(B, ob);
+            store_double(out, k, p + load_double(C, oc));
+        } else if (is_float_type(t)) {
             float p = load_float(A, t, oa) * load_float(B, t, ob);
             float y = p + load_float(C, t, oc);
             store_float(out, t, k, y);

@@ -888,6 +888,89 @@ def test_muladd_broadcast_brute_force():
         assert (got == a * b + c).all(), sh
 
 
+# --------------------------------------------------------------------------- float64
+# DOUBLE computes natively in binary64, each operation rounded on its own.
+
+def f64_corpus(n, seed):
+    bits = datagen.make("bits", "float64", (n,), seed, 0)
+    mid = datagen.normal(seed, 1, n).astype(np.float64) * 100.0 + \
+        datagen.normal(seed, 2, n).astype(np.float64) * 1e-6
+    sp = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 5e-324, -5e-324,
+                   2.2250738585072014e-308, 1.7976931348623157e308, 3.0, -7.0], np.float64)
+    return np.concatenate([bits, mid, sp])
+
+
+@pytest.mark.parametrize("op,fn", [("Add", np.add), ("Sub", np.subtract), ("Mul", np.multiply),
+                                   ("Div", np.divide), ("RSub", lambda a, b: b - a),
+                                   ("RDiv", lambda a, b: b / a)])
+def test_f64_arith_matches_numpy(op, fn):
+    a, b = f64_corpus(20000, 91), np.roll(f64_corpus(20000, 92), 5)
+    got, st = oracle.run(op, a, b, "float64")
+    with np.errstate(all="ignore"):
+        want = fn(a, b)
+    assert st == 0
+    assert_bits_equal(got, want, "float64", op)
+
+
+def test_f64_mod_matches_numpy_remainder_and_fmod():
+    """fmod=0: numpy's floating remainder takes the divisor's sign by the same
+    rule (one rounded add, zeros copysigned); fmod=1: C fmod."""
+    a = f64_corpus(20000, 93)
+    b = np.roll(f64_corpus(20000, 94), 3)
+    with np.errstate(all="ignore"):
+        got0, _ = oracle.run("Mod", a, b, "float64", fmod=0)
+        got1, _ = oracle.run("Mod", a, b, "float64", fmod=1)
+        assert_bits_equal(got1, np.fmod(a, b), "float64", "fmod=1")
+        fin = np.isfinite(a) & np.isfinite(b) & (b != 0)
+        assert_bits_equal(got0[fin], np.remainder(a[fin], b[fin]), "float64", "fmod=0")
+
+
+def test_f64_pow_within_one_ulp_of_mpmath():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.prec = 120
+    a = np.abs(datagen.normal(95, 0, 3000).astype(np.float64)) * 3 + 1e-3
+    b = datagen.uniform(95, 1, 3000, -6.0, 6.0).astype(np.float64)
+    got, _ = oracle.run("Pow", a, b, "float64")
+    for x, y, g in zip(a.tolist(), b.tolist(), got.tolist()):
+        exact = mpmath.power(mpmath.mpf(x), mpmath.mpf(y))
+        assert abs(mpmath.mpf(g) - exact) <= mpmath.mpf(np.spacing(abs(g))), (x, y, g)
+
+
+def test_f64_compare_max_min_clip_match_numpy():
+    a, b = f64_corpus(20000, 96), np.roll(f64_corpus(20000, 97), 7)
+    b[::9] = a[::9]
+    for op, fn in CMP:
+        got, _ = oracle.run(op, a, b, "float64")
+        with np.errstate(all="ignore"):
+            assert (got == fn(a, b).astype(np.uint8)).all(), op
+    a2, b2 = _no_zero_pairs(a, b)
+    for op, fn in (("Max", np.maximum), ("Min", np.minimum)):
+        got, _ = oracle.run(op, a2, b2, "float64")
+        assert_bits_equal(got, fn(a2, b2), "float64", op)
+    got, _ = oracle.run("Max", np.array([-0.0, 0.0]), np.array([0.0, -0.0]), "float64")
+    assert_bits_equal(got, np.array([0.0, 0.0]), "float64", "Max zeros")
+    fin = a[np.isfinite(a)]
+    got, _ = oracle.run("Clip", fin, np.array([-50.0, 75.5]), "float64")
+    assert_bits_equal(got, np.clip(fin, -50.0, 75.5), "float64", "Clip")
+
+
+def test_f64_channel_ops_and_muladd_match_numpy():
+    C = 5
+    x = datagen.normal(98, 0, 4 * C * 6).astype(np.float64).reshape(4, C, 6) * 3
+    p = np.stack([datagen.normal(98, k, C).astype(np.float64) for k in (1, 2, 3)] +
+                 [datagen.uniform(98, 4, C, 0.1, 2.0).astype(np.float64)])
+    got, _ = oracle.run("BatchNormalization", x, p, "float64", eps=1e-5)
+    rs = lambda v: v.reshape(1, C, 1)
+    want = (x - rs(p[2])) / np.sqrt(rs(p[3]) + np.float64(np.float32(1e-5))) * rs(p[0]) + rs(p[1])
+    assert_bits_equal(got, want, "float64", "BN")
+    bs = p[:2].copy()
+    got, _ = oracle.run("BiasPRelu", x, bs, "float64")
+    t = x + rs(bs[0])
+    assert_bits_equal(got, np.where(t >= 0, t, rs(bs[1]) * t), "float64", "BiasPRelu")
+    a, b, c = x, p[0].reshape(1, C, 1), np.roll(x, 1)
+    assert_bits_equal(oracle.run3("MulAdd", a, b, c, "float64"), a * b + c, "float64", "MulAdd")
+
+
 def test_clip_matches_numpy_and_bounds_are_optional():
     x = float_corpus(5000, 48)
     lohi = f32(-2.5, 3.0)
