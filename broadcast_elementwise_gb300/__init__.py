@@ -34,10 +34,11 @@ OPS = {"Add": 0, "Sub": 1, "Mul": 2, "Div": 3, "Mod": 4, "Pow": 5,
        "BitShift": 17, "PRelu": 18, "BatchNormalization": 19, "Clip": 20,
        "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24, "BiasPRelu": 25, "MulAdd": 26}
 DTYPES = {"float32": 1, "uint8": 2, "int8": 3, "uint16": 4, "int16": 5, "int32": 6, "int64": 7,
-          "bool": 9, "float16": 10, "uint32": 12, "uint64": 13, "bfloat16": 16}
+          "bool": 9, "float16": 10, "float64": 11, "uint32": 12, "uint64": 13, "bfloat16": 16}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
 ITEMSIZE = {"float32": 4, "uint8": 1, "int32": 4, "int64": 8, "bool": 1, "float16": 2,
-            "uint32": 4, "bfloat16": 2, "int8": 1, "int16": 2, "uint16": 2, "uint64": 8}
+            "uint32": 4, "bfloat16": 2, "int8": 1, "int16": 2, "uint16": 2, "uint64": 8,
+            "float64": 8}
 FAMILIES = {"auto": -1, "empty": 0, "contiguous": 1, "left_scalar": 2, "right_scalar": 3,
             "repeated_block": 4, "inner_vector_outer": 5, "general_strided": 6}
 FAMILY_NAMES = {v: k for k, v in FAMILIES.items()}
@@ -313,7 +314,8 @@ def torch_dtype_name(t) -> str:
     table = {torch.float32: "float32", torch.float16: "float16", torch.bfloat16: "bfloat16",
              torch.int32: "int32", torch.int64: "int64", torch.uint8: "uint8",
              torch.bool: "bool", torch.uint32: "uint32", torch.int8: "int8",
-             torch.int16: "int16", torch.uint16: "uint16", torch.uint64: "uint64"}
+             torch.int16: "int16", torch.uint16: "uint16", torch.uint64: "uint64",
+             torch.float64: "float64"}
     return table[t]
 
 
@@ -322,7 +324,8 @@ def torch_dtype(name: str):
     return {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16,
             "int32": torch.int32, "int64": torch.int64, "uint8": torch.uint8,
             "bool": torch.bool, "uint32": torch.uint32, "int8": torch.int8,
-            "int16": torch.int16, "uint16": torch.uint16, "uint64": torch.uint64}[name]
+            "int16": torch.int16, "uint16": torch.uint16, "uint64": torch.uint64,
+            "float64": torch.float64}[name]
 
 
 class Descriptor:

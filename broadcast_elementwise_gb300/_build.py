@@ -1,7 +1,7 @@
 """Build libebin.so (the C-ABI engine) in-tree for sm_103a.
 
 Every kernel translation unit is compiled once per element class
-(-DEBIN_DT=0..11) so the objects build in parallel; only objects older
+(-DEBIN_DT=0..12) so the objects build in parallel; only objects older
 than their sources are rebuilt.  No cmake, one -gencode.
 """
 from __future__ import annotations
@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libebin.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 GROUPS = ["arith", "mod", "pow", "cmp", "logic", "chan", "ext", "tern", "powmix"]
-N_DT = 12
+N_DT = 13
 # -fmad=false: no multiply-add contraction anywhere; the kernels also use the
 # _rn intrinsics explicitly.  No fast-math.
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",

@@ -49,12 +49,14 @@ int dt_class(ebin_dtype t) {
     case EBIN_INT16: return ebin::DT_I16;
     case EBIN_UINT16: return ebin::DT_U16;
     case EBIN_UINT64: return ebin::DT_U64;
+    case EBIN_DOUBLE: return ebin::DT_F64;
     }
     return -1;
 }
 
+// floating types (binary32 and the 16-bit types computed through it, and binary64)
 bool is_float(ebin_dtype t) {
-    return t == EBIN_FLOAT32 || t == EBIN_FLOAT16 || t == EBIN_BFLOAT16;
+    return t == EBIN_FLOAT32 || t == EBIN_FLOAT16 || t == EBIN_BFLOAT16 || t == EBIN_DOUBLE;
 }
 bool is_int(ebin_dtype t) {
     return t == EBIN_INT32 || t == EBIN_INT64 || t == EBIN_UINT8 || t == EBIN_UINT32 ||
@@ -806,6 +808,7 @@ cudaError_t ebin::launch(const Launch &L) {
     case 9: return launch_##g##_9(L);                                                     \
     case 10: return launch_##g##_10(L);                                                   \
     case 11: return launch_##g##_11(L);                                                   \
+    case 12: return launch_##g##_12(L);                                                   \
     default: return cudaErrorInvalidValue;                                                \
     }
     switch (L.op) {
@@ -1118,7 +1121,7 @@ extern "C" size_t ebin_dtype_size(ebin_dtype t) {
     switch (t) {
     case EBIN_FLOAT32: case EBIN_INT32: case EBIN_UINT32: return 4;
     case EBIN_FLOAT16: case EBIN_BFLOAT16: case EBIN_INT16: case EBIN_UINT16: return 2;
-    case EBIN_INT64: case EBIN_UINT64: return 8;
+    case EBIN_INT64: case EBIN_UINT64: case EBIN_DOUBLE: return 8;
     case EBIN_UINT8: case EBIN_BOOL: case EBIN_INT8: return 1;
     }
     return 0;

@@ -968,6 +968,7 @@ template <> struct DtType<DT_I8> { using type = int8_t; };
 template <> struct DtType<DT_I16> { using type = int16_t; };
 template <> struct DtType<DT_U16> { using type = uint16_t; };
 template <> struct DtType<DT_U64> { using type = uint64_t; };
+template <> struct DtType<DT_F64> { using type = double; };
 
 }  // namespace ebin
 

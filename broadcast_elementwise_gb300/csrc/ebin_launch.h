@@ -13,7 +13,7 @@ constexpr int kMaxRank = 8;
 // Internal element-type classes, one kernel set each.
 enum Dt : int {
     DT_F32 = 0, DT_F16, DT_BF16, DT_I32, DT_I64, DT_U8, DT_U32, DT_BOOL,
-    DT_I8, DT_I16, DT_U16, DT_U64, DT_COUNT
+    DT_I8, DT_I16, DT_U16, DT_U64, DT_F64, DT_COUNT
 };
 
 // Loop families (same numbering as the public ebin_family).
@@ -84,7 +84,8 @@ cudaError_t launch(const Launch &L);
     cudaError_t launch_##g##_8(const Launch &);                                       \
     cudaError_t launch_##g##_9(const Launch &);                                       \
     cudaError_t launch_##g##_10(const Launch &);                                      \
-    cudaError_t launch_##g##_11(const Launch &);
+    cudaError_t launch_##g##_11(const Launch &);                                      \
+    cudaError_t launch_##g##_12(const Launch &);
 EBIN_DECLARE_GROUP(arith)   // Add Sub Mul Div
 EBIN_DECLARE_GROUP(mod)     // Mod
 EBIN_DECLARE_GROUP(pow)     // Pow

@@ -72,6 +72,7 @@ int dt_class(ebin_dtype t) {
     case EBIN_INT16: return ebin::DT_I16;
     case EBIN_UINT16: return ebin::DT_U16;
     case EBIN_UINT64: return ebin::DT_U64;
+    case EBIN_DOUBLE: return ebin::DT_F64;
     }
     return -1;
 }

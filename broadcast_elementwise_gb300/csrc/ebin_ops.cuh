@@ -49,6 +49,12 @@ template <> struct Tr<__half> {
     __device__ __forceinline__ static float in(__half x) { return __half2float(x); }
     __device__ __forceinline__ static __half out(float v) { return __float2half_rn(v); }
 };
+template <> struct Tr<double> {
+    using C = double;
+    static constexpr bool kFloat = true;
+    __device__ __forceinline__ static double in(double x) { return x; }
+    __device__ __forceinline__ static double out(double v) { return v; }
+};
 template <> struct Tr<__nv_bfloat16> {
     using C = float;
     static constexpr bool kFloat = true;
@@ -78,9 +84,13 @@ template <> struct Tr<Bool8> {
     __device__ __forceinline__ static bool in(Bool8 x) { return x.v != 0; }
 };
 
+// binary32 and the 16-bit types computed through it
 template <class T> constexpr bool is_float_v = std::is_same_v<T, float> ||
                                                std::is_same_v<T, __half> ||
                                                std::is_same_v<T, __nv_bfloat16>;
+// binary64 (DOUBLE), computed natively
+template <class T> constexpr bool is_double_v = std::is_same_v<T, double>;
+template <class T> constexpr bool is_fp_v = is_float_v<T> || is_double_v<T>;
 template <class T> constexpr bool is_int_v = std::is_same_v<T, int32_t> ||
                                              std::is_same_v<T, int64_t> ||
                                              std::is_same_v<T, uint8_t> ||
@@ -150,13 +160,18 @@ __device__ __forceinline__ float mod_float(float a, float b, int fmod_flag) {
 enum ArithK { K_ADD = 0, K_SUB = 1, K_MUL = 2, K_DIV = 3, K_RSUB = 4, K_RDIV = 5 };
 
 template <class T, int K> struct OpArith : PlainB<T, T> {
-    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> || is_int_v<T>;
     static constexpr bool kValidates = (K == K_DIV || K == K_RDIV) && is_int_v<T>;
-    static constexpr bool kScalarAttr = is_float_v<T>;     // ncnn binaryop with_scalar
+    static constexpr bool kScalarAttr = is_fp_v<T>;        // ncnn binaryop with_scalar
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
         if constexpr (K == K_RSUB || K == K_RDIV) {
             // the same operation with the operands exchanged
             return OpArith<T, K == K_RSUB ? K_SUB : K_DIV>::apply(b, a, OpArgs{}, err);
+        } else if constexpr (is_double_v<T>) {
+            if constexpr (K == K_ADD) return __dadd_rn(a, b);
+            else if constexpr (K == K_SUB) return __dsub_rn(a, b);
+            else if constexpr (K == K_MUL) return __dmul_rn(a, b);
+            else return __ddiv_rn(a, b);
         } else if constexpr (is_float_v<T>) {
             const float x = Tr<T>::in(a), y = Tr<T>::in(b);
             float r;
@@ -186,14 +201,15 @@ template <class T, int K> struct OpArith : PlainB<T, T> {
 // counts as larger than -0.  Half and bfloat16 results are one of the two
 // widened inputs, so narrowing them back is exact.
 template <class T, bool kMax> struct OpMinMax : PlainB<T, T> {
-    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> || is_int_v<T>;
     static constexpr bool kValidates = false;
-    static constexpr bool kScalarAttr = is_float_v<T>;
+    static constexpr bool kScalarAttr = is_fp_v<T>;
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &) {
-        if constexpr (is_float_v<T>) {
-            const float x = Tr<T>::in(a), y = Tr<T>::in(b);
-            float r;
-            if (isnan(x) || isnan(y)) r = __fadd_rn(x, y);                 // a NaN
+        if constexpr (is_fp_v<T>) {
+            using C = typename Tr<T>::C;
+            const C x = Tr<T>::in(a), y = Tr<T>::in(b);
+            C r;
+            if (isnan(x) || isnan(y)) r = x + y;                            // a NaN
             else if (x == y) r = (signbit(x) == kMax) ? y : x;             // +0 vs -0
             else r = kMax ? (x > y ? x : y) : (x < y ? x : y);
             return Tr<T>::out(r);
@@ -309,10 +325,17 @@ __device__ __forceinline__ int32_t imod_floor_neg(int32_t a, const IModPrep &p) 
 }
 
 template <class T> struct OpMod : PlainB<T, T> {
-    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> || is_int_v<T>;
     static constexpr bool kValidates = is_int_v<T>;
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &p, uint32_t &err) {
-        if constexpr (is_float_v<T>) {
+        if constexpr (is_double_v<T>) {
+            // binary64: C fmod (exact), then the same floor rule in binary64
+            double r = fmod(a, b);
+            if (p.fmod) return r;
+            if (r == 0.0) return copysign(0.0, b);
+            if (signbit(r) != signbit(b)) r = __dadd_rn(r, b);
+            return r;
+        } else if constexpr (is_float_v<T>) {
             return Tr<T>::out(mod_float(Tr<T>::in(a), Tr<T>::in(b), p.fmod));
         } else {
             if (b == 0) { err |= kErrDivByZero; return (T)0; }
@@ -420,11 +443,12 @@ __device__ __forceinline__ T float_pow(T a, double e) {
 }
 
 template <class T> struct OpPow : PlainB<T, T> {
-    static constexpr bool kLegal = is_float_v<T> || is_pow_int_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> || is_pow_int_v<T>;
     static constexpr bool kValidates = is_pow_int_v<T>;
-    static constexpr bool kScalarAttr = is_float_v<T>;     // ncnn binaryop POW with_scalar
+    static constexpr bool kScalarAttr = is_fp_v<T>;        // ncnn binaryop POW with_scalar
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
-        if constexpr (is_float_v<T>) return float_pow(a, (double)Tr<T>::in(b));
+        if constexpr (is_double_v<T>) return pow(a, b);          // C pow in binary64
+        else if constexpr (is_float_v<T>) return float_pow(a, (double)Tr<T>::in(b));
         else return int_pow(a, b < 0, b < 0 ? 0 - (uint64_t)b : (uint64_t)b, err);
     }
 };
@@ -443,19 +467,21 @@ template <class TA, class TB> struct OpPowMixed {
     using BV = TB;
     using BIn = TB;                  // B's element type differs from A's
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = (is_float_v<TA> || is_pow_int_v<TA>) && !is_bool_v<TB>;
-    static constexpr bool kValidates = is_pow_int_v<TA> && !is_float_v<TB>;
+    static constexpr bool kLegal = (is_fp_v<TA> || is_pow_int_v<TA>) && !is_bool_v<TB>;
+    static constexpr bool kValidates = is_pow_int_v<TA> && !is_fp_v<TB>;
     __device__ __forceinline__ static BV loadB(const TB *B, int64_t off, const OpArgs &) {
         return B[off];
     }
     __device__ __forceinline__ static double as_double(TB e) {
-        if constexpr (is_float_v<TB>) return (double)Tr<TB>::in(e);
+        if constexpr (is_fp_v<TB>) return (double)Tr<TB>::in(e);
         else return (double)e;
     }
     __device__ __forceinline__ static TA apply(TA a, TB b, const OpArgs &, uint32_t &err) {
-        if constexpr (is_float_v<TA>) {
+        if constexpr (is_double_v<TA>) {
+            return pow(a, as_double(b));
+        } else if constexpr (is_float_v<TA>) {
             return float_pow(a, as_double(b));
-        } else if constexpr (!is_float_v<TB>) {
+        } else if constexpr (!is_fp_v<TB>) {
             if constexpr (is_signed_int_v<TB>)
                 return int_pow(a, b < 0, b < 0 ? 0 - (uint64_t)(int64_t)b : (uint64_t)b, err);
             else
@@ -498,7 +524,7 @@ __device__ __forceinline__ unsigned cmp_mask2(T2 a, T2 b) {
 }
 
 template <class T, int K> struct OpCmp : PlainB<T, Bool8> {
-    static constexpr bool kLegal = is_float_v<T> || is_int_v<T> || (K == K_EQ && is_bool_v<T>);
+    static constexpr bool kLegal = is_fp_v<T> || is_int_v<T> || (K == K_EQ && is_bool_v<T>);
     static constexpr bool kValidates = false;
     // half and bfloat16 compare exactly in their own format, two lanes per
     // instruction; the comparison of the exact float widenings is the same
@@ -577,15 +603,28 @@ template <class T> struct OpShift : PlainB<T, T> {
 };
 
 // ---------------------------------------------------------------- per-channel operators
+// Round-to-nearest arithmetic in the compute type (binary32 or binary64); the
+// _rn intrinsics are never contracted into a fused multiply-add.
+__device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
+__device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
+__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
+__device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
+__device__ __forceinline__ double div_rn(double a, double b) { return __ddiv_rn(a, b); }
+__device__ __forceinline__ float sqrt_rn(float a) { return __fsqrt_rn(a); }
+__device__ __forceinline__ double sqrt_rn(double a) { return __dsqrt_rn(a); }
+
 template <class T> struct OpPRelu : PlainB<T, T> {
-    static constexpr bool kLegal = is_float_v<T> || is_pow_int_v<T> ||   // ONNX PRelu T
+    static constexpr bool kLegal = is_fp_v<T> || is_pow_int_v<T> ||      // ONNX PRelu T
                                    std::is_same_v<T, uint32_t> || std::is_same_v<T, uint64_t>;
     static constexpr bool kValidates = false;
     __device__ __forceinline__ static T apply(T a, T slope, const OpArgs &, uint32_t &) {
-        if constexpr (is_float_v<T>) {
-            const float x = Tr<T>::in(a);
-            if (x >= 0.0f) return a;                             // keeps -0 and exact bits
-            return Tr<T>::out(__fmul_rn(Tr<T>::in(slope), x));
+        if constexpr (is_fp_v<T>) {
+            const auto x = Tr<T>::in(a);
+            if (x >= 0) return a;                                // keeps -0 and exact bits
+            return Tr<T>::out(mul_rn(Tr<T>::in(slope), x));
         } else if constexpr (Tr<T>::kSigned) {
             using U = typename Tr<T>::UT;
             return a >= 0 ? a : (T)((U)slope * (U)a);
@@ -597,25 +636,27 @@ template <class T> struct OpPRelu : PlainB<T, T> {
 
 // BiasPRelu (0verkilll/onnx ops, ConvPReluOp: the per-output-channel bias add
 // and PReLU fused into one pass, here as an elementwise operator): t = x + bias,
-// y = t when t >= 0 else slope * t, binary32 steps rounded once to x's type.
-// B holds two rows (bias, slope) of `plane` elements, read once per row.
-struct BiasSlope {
-    float bias, slope;
+// y = t when t >= 0 else slope * t, steps in the compute type (binary32, or
+// binary64 for DOUBLE) rounded once to x's type.  B holds two rows (bias,
+// slope) of `plane` elements, read once per row.
+template <class C> struct BiasSlope {
+    C bias, slope;
 };
 
 template <class T> struct OpBiasPRelu {
     using In = T;
     using Out = T;
-    using BV = BiasSlope;
+    using C = typename Tr<T>::C;
+    using BV = BiasSlope<C>;
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = is_float_v<T>;
+    static constexpr bool kLegal = is_fp_v<T>;
     static constexpr bool kValidates = false;
     __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
-        return BiasSlope{Tr<T>::in(B[off]), Tr<T>::in(B[off + p.plane])};
+        return BV{Tr<T>::in(B[off]), Tr<T>::in(B[off + p.plane])};
     }
     __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
-        const float t = __fadd_rn(Tr<T>::in(a), q.bias);
-        return Tr<T>::out(t >= 0.0f ? t : __fmul_rn(q.slope, t));
+        const C t = add_rn(Tr<T>::in(a), q.bias);
+        return Tr<T>::out(t >= 0 ? t : mul_rn(q.slope, t));
     }
 };
 
@@ -625,11 +666,10 @@ template <class T> struct OpBiasPRelu {
 template <class T> struct OpMulAdd {
     using In = T;
     using Out = T;
-    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> || is_int_v<T>;
     __device__ __forceinline__ static T apply3(T a, T b, T c) {
-        if constexpr (is_float_v<T>) {
-            return Tr<T>::out(
-                __fadd_rn(__fmul_rn(Tr<T>::in(a), Tr<T>::in(b)), Tr<T>::in(c)));
+        if constexpr (is_fp_v<T>) {
+            return Tr<T>::out(add_rn(mul_rn(Tr<T>::in(a), Tr<T>::in(b)), Tr<T>::in(c)));
         } else {
             using U = typename Tr<T>::UT;
             return (T)((U)((U)a * (U)b) + (U)c);
@@ -638,36 +678,37 @@ template <class T> struct OpMulAdd {
 };
 
 // Inference BatchNormalization: y = (x - mean) / sqrt(var + eps) * scale + bias,
-// each step rounded in binary32 in the order written.  B holds four rows
-// (scale, bias, mean, var) of `plane` elements; the per-channel sqrt is formed
-// when the parameters are loaded.  (A per-channel reciprocal with a
-// remainder-checked correction was measured slower than the IEEE divide on
-// GB300, so the divide stays.)
-struct BNParams {
-    float scale, bias, mean, d;
+// each step rounded in the compute type (binary32, or binary64 for DOUBLE) in
+// the order written.  B holds four rows (scale, bias, mean, var) of `plane`
+// elements; the per-channel sqrt is formed when the parameters are loaded.  (A
+// per-channel reciprocal with a remainder-checked correction was measured
+// slower than the IEEE divide on GB300, so the divide stays.)
+template <class C> struct BNParams {
+    C scale, bias, mean, d;
 };
 
 template <class T> struct OpBN {
     using In = T;
     using Out = T;
-    using BV = BNParams;
+    using C = typename Tr<T>::C;
+    using BV = BNParams<C>;
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = is_float_v<T>;
+    static constexpr bool kLegal = is_fp_v<T>;
     static constexpr bool kValidates = false;
     __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
-        BNParams r;
+        BV r;
         r.scale = Tr<T>::in(B[off]);
         r.bias = Tr<T>::in(B[off + p.plane]);
         r.mean = Tr<T>::in(B[off + 2 * p.plane]);
-        const float var = Tr<T>::in(B[off + 3 * p.plane]);
-        r.d = __fsqrt_rn(__fadd_rn(var, p.eps));
+        const C var = Tr<T>::in(B[off + 3 * p.plane]);
+        r.d = sqrt_rn(add_rn(var, (C)p.eps));
         return r;
     }
     __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
-        float t = __fsub_rn(Tr<T>::in(a), q.mean);
-        t = __fdiv_rn(t, q.d);
-        t = __fmul_rn(t, q.scale);
-        return Tr<T>::out(__fadd_rn(t, q.bias));
+        C t = sub_rn(Tr<T>::in(a), q.mean);
+        t = div_rn(t, q.d);
+        t = mul_rn(t, q.scale);
+        return Tr<T>::out(add_rn(t, q.bias));
     }
 };
 
@@ -683,7 +724,7 @@ template <class T> struct OpClip {
     using Out = T;
     using BV = ClipParams<T>;
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = is_float_v<T> || is_int_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> || is_int_v<T>;
     static constexpr bool kValidates = false;
     __device__ __forceinline__ static BV loadB(const T *B, int64_t, const OpArgs &p) {
         BV r{};

@@ -30,6 +30,7 @@ cudaError_t EBIN_GROUP_FN(powmix)(const Launch &L) {
     case DT_I16: return launch_mixed<OpPowMixed<TA, int16_t>>(L);
     case DT_U16: return launch_mixed<OpPowMixed<TA, uint16_t>>(L);
     case DT_U64: return launch_mixed<OpPowMixed<TA, uint64_t>>(L);
+    case DT_F64: return launch_mixed<OpPowMixed<TA, double>>(L);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -110,6 +110,7 @@ typedef enum ebin_dtype {
     EBIN_INT64 = 7,
     EBIN_BOOL = 9,                /* one byte per element */
     EBIN_FLOAT16 = 10,
+    EBIN_DOUBLE = 11,             /* computed natively in binary64 */
     EBIN_UINT32 = 12,
     EBIN_UINT64 = 13,
     EBIN_BFLOAT16 = 16

@@ -6,7 +6,7 @@ import numpy as np
 
 import datagen
 
-FLOATS = ("float32", "float16", "bfloat16")
+FLOATS = ("float32", "float16", "bfloat16", "float64")
 INTS = ("int32", "int64", "uint8", "uint32", "int8", "int16", "uint16", "uint64")
 ALL_DTYPES = FLOATS + INTS + ("bool",)
 

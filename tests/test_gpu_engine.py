@@ -174,7 +174,7 @@ def test_execute_host_pipelined_status_and_ordering():
     assert_bits_equal(o2.numpy(), oracle.run("Mul", x2, y2, "float32")[0], "float32")
 
 
-@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
+@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16", "float64"])
 def test_with_scalar_matches_a_scalar_tensor(dtype):
     """ncnn binaryop with_scalar: B is the attribute value rounded to the element
     type, so the result equals the oracle's with a 0-d B holding that value.
@@ -206,7 +206,7 @@ def test_with_scalar_matches_a_scalar_tensor(dtype):
     bq = datagen.float_to(np.array([0.75], np.float32), dtype).reshape(())
     want, _ = oracle.run("RDiv", a, bq, dtype)
     p = eb.Plan(eb.descriptor("RDiv", dtype, scalar_b=0.75), (n,), ())
-    view = np.int16 if dtype != "float32" else np.int32
+    view = {2: np.int16, 4: np.int32, 8: np.int64}[eb.ITEMSIZE[dtype]]
     ha = torch.from_numpy(a.reshape(-1).view(view).copy()).pin_memory()
     ho = torch.empty_like(ha).pin_memory()
     da, do = torch.empty_like(ha, device="cuda"), torch.empty_like(ha, device="cuda")

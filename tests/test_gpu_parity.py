@@ -220,9 +220,9 @@ def test_strided_input_views(op, dtype):
                     (op, dtype, shape, strides, forced, plan.family))
 
 
-MIXED_POW = [(ta, tb) for ta in ("float32", "float16", "bfloat16", "int32", "int64")
-             for tb in ("float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32",
-                        "int8", "int16", "uint16", "uint64")
+MIXED_POW = [(ta, tb) for ta in ("float32", "float16", "bfloat16", "float64", "int32", "int64")
+             for tb in ("float32", "float16", "bfloat16", "float64", "int32", "int64", "uint8",
+                        "uint32", "int8", "int16", "uint16", "uint64")
              if ta != tb]
 
 
@@ -232,7 +232,8 @@ def test_pow_with_exponent_of_another_type(ta, tb):
     against the oracle: floating bases within 2 ulp, integer bases exactly,
     status bits equal."""
     import torch
-    rng_a = {"float32": (0.0, 6.0), "float16": (0.0, 4.0), "bfloat16": (0.0, 6.0)}
+    rng_a = {"float32": (0.0, 6.0), "float16": (0.0, 4.0), "bfloat16": (0.0, 6.0),
+             "float64": (0.0, 6.0)}
     for i, (sa, sb) in enumerate([((3000,), (3000,)), ((40, 75), (75,)), ((6, 1, 50), (1, 7, 1))]):
         na, nb = int(np.prod(sa)), int(np.prod(sb))
         if ta in FLOATS:

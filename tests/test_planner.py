@@ -16,7 +16,7 @@ eb = pytest.importorskip("broadcast_elementwise_gb300")
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ALL_DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool",
-              "int8", "int16", "uint16", "uint64"]
+              "int8", "int16", "uint16", "uint64", "float64"]
 
 
 def header_functions():
@@ -202,7 +202,7 @@ def test_with_scalar_descriptor_rules():
                 got = e.code
             if not legal:
                 assert got == "unsupported_type", (op, dt, got)
-            elif op in SCALAR_ATTR_OPS and dt in ("float32", "float16", "bfloat16"):
+            elif op in SCALAR_ATTR_OPS and dt in ("float32", "float16", "bfloat16", "float64"):
                 assert got == "ok", (op, dt, got)
             else:
                 assert got == "invalid_attr", (op, dt, got)
