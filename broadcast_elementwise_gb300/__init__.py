@@ -99,6 +99,7 @@ def _load():
         "ebin_plan_cache_clear": (None, []),
         "ebin_execute": (i32, [vp, vp, vp, vp, vp]),
         "ebin_execute_host": (i32, [vp, vp, vp, vp, vp, vp, vp, vp]),
+        "ebin_execute_mapped": (i32, [vp, vp, vp, vp, vp]),
         "ebin_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ebin_execute_noalloc": (i32, [vp, vp, vp, vp, vp, i32, ctypes.POINTER(ctypes.c_uint32)]),
         "ebin_launch_count": (ctypes.c_uint64, []),
@@ -269,6 +270,10 @@ def ebin_execute_host(plan, host_a, host_b, host_out, dev_a, dev_b, dev_out, str
            "ebin_execute_host")
 
 
+def ebin_execute_mapped(plan, host_a, host_b, host_out, stream) -> None:
+    _check(lib.ebin_execute_mapped(plan, host_a, host_b, host_out, stream), "ebin_execute_mapped")
+
+
 def ebin_execute_noalloc(plan, A, B, out, stream, status_slot, want_status=True):
     """Marshal ebin_execute_noalloc; returns the status bits (0 when not requested)."""
     bits = ctypes.c_uint32(0)
@@ -421,6 +426,12 @@ def execute3(plan: Plan3, A, B, C, out, stream=None) -> None:
 def execute(plan: Plan, A, B, out, stream=None) -> None:
     """Enqueue the plan on device buffers (torch tensors or int addresses)."""
     ebin_execute(plan.handle, _ptr(A), _ptr(B), _ptr(out), _stream(stream))
+
+
+def execute_mapped(plan: Plan, A, B, out, stream=None) -> None:
+    """Enqueue the plan on pinned host buffers, read and written in place by the
+    kernel (torch pinned tensors or int addresses)."""
+    ebin_execute_mapped(plan.handle, _ptr(A), _ptr(B), _ptr(out), _stream(stream))
 
 
 def get_device_status(stream=None) -> int:

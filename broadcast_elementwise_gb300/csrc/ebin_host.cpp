@@ -22,6 +22,7 @@
 #include <mutex>
 #include <utility>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ebin.h"
@@ -1094,6 +1095,77 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
     if (!ok(cudaEventRecord(hp->done, hp->out)) || !ok(cudaStreamWaitEvent(s, hp->done, 0)))
         return EBIN_ERR_CUDA;
     return EBIN_OK;
+}
+
+namespace {
+
+// cuPointerGetAttribute, looked up through the runtime (no link against the
+// driver library), or null.
+using PointerAttrFn = CUresult (*)(void *, CUpointer_attribute, CUdeviceptr);
+
+PointerAttrFn pointer_attr_fn() {
+    static const PointerAttrFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return (PointerAttrFn) nullptr;
+        }
+        return reinterpret_cast<PointerAttrFn>(f);
+    }();
+    return fn;
+}
+
+// Device address of the host range [p, p + bytes) when all of it lies in one
+// pinned allocation mapped into the device's address space (first and last
+// byte in host memory, with the same allocation id and a contiguous device
+// mapping); else null.
+const void *mapped_range(const void *p, size_t bytes) {
+    if (!p || bytes == 0) return nullptr;
+    const char *first = static_cast<const char *>(p);
+    const char *last = first + (bytes - 1);
+    cudaPointerAttributes a0{}, a1{};
+    if (cudaPointerGetAttributes(&a0, first) != cudaSuccess ||
+        cudaPointerGetAttributes(&a1, last) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a0.type != cudaMemoryTypeHost || a1.type != cudaMemoryTypeHost || !a0.devicePointer ||
+        static_cast<const char *>(a1.devicePointer) !=
+            static_cast<const char *>(a0.devicePointer) + (bytes - 1))
+        return nullptr;
+    const PointerAttrFn fn = pointer_attr_fn();
+    unsigned long long id0 = 0, id1 = 0;
+    if (!fn || fn(&id0, CU_POINTER_ATTRIBUTE_BUFFER_ID, (CUdeviceptr)(uintptr_t)first) != CUDA_SUCCESS ||
+        fn(&id1, CU_POINTER_ATTRIBUTE_BUFFER_ID, (CUdeviceptr)(uintptr_t)last) != CUDA_SUCCESS ||
+        id0 != id1)
+        return nullptr;
+    return a0.devicePointer;
+}
+
+}  // namespace
+
+extern "C" ebin_status ebin_execute_mapped(ebin_plan_t plan, const void *host_a,
+                                           const void *host_b, void *host_out, void *stream) {
+    if (!plan || plan->rank_c >= 0) return EBIN_ERR_INVALID_ARG;
+    const ebin_plan_s &p = *plan;
+    if (p.numel == 0) return EBIN_OK;
+    if (!host_a || !host_out) return EBIN_ERR_INVALID_ARG;
+    const void *da = mapped_range(host_a, (size_t)p.span_a * ebin_dtype_size(p.dt));
+    const void *db = nullptr;
+    if (host_b && p.span_b > 0) {
+        db = mapped_range(host_b, (size_t)p.span_b * ebin_dtype_size(p.dt_b));
+        if (!db) return EBIN_ERR_INVALID_ARG;
+    }
+    void *dout = const_cast<void *>(
+        mapped_range(host_out, (size_t)p.numel * ebin_dtype_size(p.out_dt)));
+    if (!da || !dout) return EBIN_ERR_INVALID_ARG;
+    ebin::Launch L;
+    const ebin_status st = prepare_launch(p, da, db, dout, static_cast<cudaStream_t>(stream), L);
+    if (st != EBIN_OK) return st;
+    return launch_counted(L);
 }
 
 extern "C" ebin_status ebin_get_device_status(void *stream, uint32_t *bits) {

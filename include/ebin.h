@@ -365,6 +365,32 @@ ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, const void *
                               void *stream);
 
 /*
+ * End-to-end form without staging: the kernel reads host_a and host_b and
+ * writes host_out in place, over the host-device link.  On Grace-Blackwell
+ * this link is NVLink-C2C, and the kernel keeps it busy in both directions
+ * at once.  Same computation and results as ebin_execute.  No counterpart in
+ * the pages: they only speak of device buffers.
+ *
+ * Each host buffer must lie wholly inside one pinned allocation mapped into
+ * the device's address space: cudaHostAlloc / cudaMallocHost memory, or
+ * memory registered with cudaHostRegister, which on a unified-addressing
+ * system is mapped.  For each buffer, the first and last byte of its extent
+ * are checked: both must be host memory, carry the same allocation id and
+ * map contiguously.  A buffer that fails the check (pageable memory, a range
+ * past its allocation) gives INVALID_ARG before any device work, so the
+ * kernel never touches an unmapped address.  The extents are: A and B their
+ * storage extent in elements of their types; out the output's element count
+ * in the output type.  host_b is NULL where ebin_execute takes B = NULL.
+ *
+ * Enqueued on `stream`; does not synchronise.  host_out is valid once
+ * `stream` has completed, and the host must not touch the buffers before
+ * then.
+ * Errors: as ebin_execute, and INVALID_ARG for an unmapped buffer.
+ */
+ebin_status ebin_execute_mapped(ebin_plan_t plan, const void *host_a, const void *host_b,
+                                void *host_out, void *stream);
+
+/*
  * Read and clear the device status word of `stream` on the current device:
  * synchronises the stream, returns the OR of the EBIN_DEVICE_* bits raised
  * since the last call, then zeroes the word (stream-ordered).  A stream that

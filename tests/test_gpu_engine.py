@@ -389,3 +389,58 @@ def test_batchnorm_division_is_exact(dtype):
     got, _, _ = run_engine("BatchNormalization", dtype, x2, params, attrs={"epsilon": eps})
     want, _ = oracle.run("BatchNormalization", x2, params, dtype, eps=eps)
     assert_bits_equal(got, want, dtype, "BN rank-2")
+
+
+def _pinned(arr: np.ndarray, pin=True):
+    t = torch.from_numpy(np.ascontiguousarray(arr).reshape(-1).view(np.uint8).copy())
+    return t.pin_memory() if pin else t
+
+
+@pytest.mark.parametrize("op,dtype,sa,sb,fam", [
+    ("Mul", "float32", (3000017,), (3000017,), "contiguous"),
+    ("Add", "bfloat16", (1000003,), (), "right_scalar"),
+    ("PRelu", "bfloat16", (4, 64, 64, 64), (64, 1, 1), "inner_vector_outer"),
+    ("Greater", "float16", (16, 1, 512, 1), (1, 8, 1, 1024), "inner_vector_outer"),
+    ("Add", "float32", (2, 3, 4, 5), (3, 1, 5), "general_strided"),
+    ("Mod", "int32", (4096, 640), (4096, 1), "repeated_block"),
+])
+def test_execute_mapped_matches_the_oracle(op, dtype, sa, sb, fam):
+    """ebin_execute_mapped: the kernel reads and writes pinned host buffers in
+    place, with the results of ebin_execute."""
+    a, b = inputs_for(op, dtype, sa, sb, seed=91)
+    want, wbits = oracle.run(op, a, b, dtype)
+    p = eb.Plan(eb.descriptor(op, dtype), sa, sb)
+    assert p.family == fam
+    osz = eb.ITEMSIZE[eb.descriptor(op, dtype).out_dtype]
+    ha, hb = _pinned(a), _pinned(b)
+    ho = torch.full((p.numel * osz,), 0xAB, dtype=torch.uint8).pin_memory()
+    s = torch.cuda.current_stream()
+    before = eb.ebin_launch_count()
+    eb.execute_mapped(p, ha, hb, ho, s)
+    s.synchronize()
+    assert eb.ebin_launch_count() - before == 1
+    otype = "bool" if op == "Greater" else dtype
+    got = ho.numpy().view(datagen.STORAGE[otype]).reshape(want.shape)
+    assert_bits_equal(got, want, otype, op)
+    assert eb.get_device_status() == wbits
+
+
+def test_execute_mapped_refuses_unmapped_buffers():
+    """Pageable memory, or a pinned buffer shorter than the plan, is refused
+    with INVALID_ARG before any device work; the output is left alone."""
+    n = 1 << 20
+    a, b = inputs_for("Add", "float32", (n,), (n,), seed=92)
+    p = eb.Plan(eb.descriptor("Add", "float32"), (n,), (n,))
+    ha, hb = _pinned(a), _pinned(b)
+    ho = torch.full((4 * n,), 0x5A, dtype=torch.uint8).pin_memory()
+    pageable = _pinned(a, pin=False)
+    short = torch.zeros(4 * n // 2, dtype=torch.uint8).pin_memory()
+    before = eb.ebin_launch_count()
+    out_pageable = _pinned(np.zeros(4 * n, np.uint8), pin=False)
+    for args in ((pageable, hb, ho), (ha, pageable, ho), (ha, hb, out_pageable),
+                 (short, hb, ho), (ha, hb, short)):
+        with pytest.raises(eb.EbinError, match="invalid_arg"):
+            eb.execute_mapped(p, *args)
+    torch.cuda.synchronize()
+    assert eb.ebin_launch_count() == before
+    assert bool((ho == 0x5A).all()) and bool((short == 0).all())
