@@ -33,7 +33,7 @@ OPS = ["Add", "Sub", "Mul", "Div", "Mod", "Pow",
        "BitwiseAnd", "BitwiseOr", "BitwiseXor",
        "BitShift", "PRelu",
        "BatchNormalization", "Clip",
-       "Max", "Min", "RSub", "RDiv", "BiasPRelu", "MulAdd"]
+       "Max", "Min", "RSub", "RDiv", "BiasPRelu", "MulAdd", "BiasPReluBN"]
 DTYPES = ["float32", "float16", "bfloat16", "int32", "int64", "uint8", "uint32", "bool",
           "int8", "int16", "uint16", "uint64", "float64"]
 STORAGE = {"float32": np.float32, "float16": np.float16, "bfloat16": np.uint16,

@@ -21,7 +21,9 @@
  *    to the data), ClipOp (optional min/max bounds), Add/Sub/Mul,
  *    ConvPReluOp (the per-output-channel bias add and PReLU fused into one
  *    pass: here without the convolution, as BiasPRelu), MulAddOp (y = a*b + c
- *    over three inputs broadcast together).
+ *    over three inputs broadcast together).  The bias -> PReLU ->
+ *    BatchNormalization chain of one pass (BiasPReluBN) joins ConvPReluOp's
+ *    epilogue to BatchNormalizationOp's formula.
  *  - ncnn operators.md -- batchnorm, bias, binaryop (operation types MAX,
  *    MIN, RSUB, RDIV; with_scalar), clip.
  * Where the pages are silent the plain reading is taken (IEEE-754 binary32
@@ -50,7 +52,7 @@ enum {
     OR_BITSHIFT, OR_PRELU,
     OR_BATCHNORM, OR_CLIP,
     OR_MAX, OR_MIN, OR_RSUB, OR_RDIV,
-    OR_BIAS_PRELU, OR_MULADD,
+    OR_BIAS_PRELU, OR_MULADD, OR_BIAS_PRELU_BN,
     OR_NUM_OPS
 };
 enum { OT_F32 = 0, OT_F16, OT_BF16, OT_I32, OT_I64, OT_U8, OT_U32, OT_BOOL,
@@ -247,7 +249,7 @@ int oracle_type_allowed(int op, int t)
         return t == OT_U8 || t == OT_U16 || t == OT_U32 || t == OT_U64;
     case OR_PRELU:
         return is_fp(t) || t == OT_I32 || t == OT_I64 || t == OT_U32 || t == OT_U64;
-    case OR_BATCHNORM: case OR_BIAS_PRELU:
+    case OR_BATCHNORM: case OR_BIAS_PRELU: case OR_BIAS_PRELU_BN:
         return is_fp(t);
     }
     return 0;
@@ -566,14 +568,20 @@ int oracle_offsets(const int64_t *sa, int ra, const int64_t *sb, int rb, const i
  *    above it;
  *  - BiasPRelu: A = x [N, C, ...] (rank >= 2), B = [2, C] holding bias and
  *    slope rows; t = x + bias, then y = t when t >= 0 else slope * t, in
- *    binary32, rounded once to x's type.
+ *    binary32, rounded once to x's type;
+ *  - BiasPReluBN: the per-channel chain bias add -> PReLU -> inference
+ *    BatchNormalization in one pass.  A = x [N, C, ...] (rank >= 2), B = [6, C]
+ *    holding bias, slope, scale, bn_bias, mean, var rows; t = x + bias;
+ *    t = t >= 0 ? t : slope * t; y = (t - mean) / sqrt(var + eps) * scale +
+ *    bn_bias; every step in binary32 in the order written, one rounding to
+ *    x's type at the end (no rounding to x's type between the three).
  * Out shape: see oracle_output_shape.
  */
 int oracle_output_shape(int op, const int64_t *sa, int ra, const int64_t *sb, int rb,
                         int64_t *so, int *ro)
 {
-    if (op == OR_BATCHNORM || op == OR_BIAS_PRELU) {
-        const int64_t rows = op == OR_BATCHNORM ? 4 : 2;
+    if (op == OR_BATCHNORM || op == OR_BIAS_PRELU || op == OR_BIAS_PRELU_BN) {
+        const int64_t rows = op == OR_BATCHNORM ? 4 : op == OR_BIAS_PRELU ? 2 : 6;
         if (ra < 2 || rb != 2 || sb[0] != rows || sb[1] != sa[1]) return OR_SHAPES;
         for (int d = 0; d < ra; ++d) so[d] = sa[d];
         *ro = ra;
@@ -612,7 +620,7 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
     int64_t count = idx ? n_idx : total;
     int to = oracle_output_type(op, t);
     aligned_strides(sa, ra, r, sta);
-    if (op != OR_BATCHNORM && op != OR_CLIP && op != OR_BIAS_PRELU)
+    if (op != OR_BATCHNORM && op != OR_CLIP && op != OR_BIAS_PRELU && op != OR_BIAS_PRELU_BN)
         aligned_strides(sb, rb, r, stb);
     else
         for (int d = 0; d < r; ++d) stb[d] = 0;
@@ -636,6 +644,15 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             double y = load_double(A, oa) + load_double(B, c);
             if (!(y >= 0.0)) y = load_double(B, C + c) * y;
             store_double(out, k, y);
+            continue;
+        }
+        if (op == OR_BIAS_PRELU_BN && t == OT_F64) {
+            int64_t C = sb[1], c = channel_of(f, so, r);
+            double y = load_double(A, oa) + load_double(B, c);
+            if (!(y >= 0.0)) y = load_double(B, C + c) * y;
+            double scale = load_double(B, 2 * C + c), bn_bias = load_double(B, 3 * C + c);
+            double mean = load_double(B, 4 * C + c), var = load_double(B, 5 * C + c);
+            store_double(out, k, (y - mean) / sqrt(var + (double)eps) * scale + bn_bias);
             continue;
         }
         if (op == OR_CLIP && t == OT_F64) {
@@ -662,6 +679,20 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             int64_t C = sb[1], c = channel_of(f, so, r);
             float y = load_float(A, t, oa) + load_float(B, t, c);
             if (!(y >= 0.0f)) y = load_float(B, t, C + c) * y;
+            store_float(out, t, k, y);
+            continue;
+        }
+        if (op == OR_BIAS_PRELU_BN) {
+            /* bias add, PReLU, then the BatchNormalization formula, binary32
+               steps in the order written; one rounding to x's type */
+            int64_t C = sb[1], c = channel_of(f, so, r);
+            float y = load_float(A, t, oa) + load_float(B, t, c);
+            if (!(y >= 0.0f)) y = load_float(B, t, C + c) * y;
+            float scale = load_float(B, t, 2 * C + c);
+            float bn_bias = load_float(B, t, 3 * C + c);
+            float mean = load_float(B, t, 4 * C + c);
+            float var = load_float(B, t, 5 * C + c);
+            y = (y - mean) / sqrtf(var + eps) * scale + bn_bias;
             store_float(out, t, k, y);
             continue;
         }

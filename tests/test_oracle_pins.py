@@ -829,6 +829,87 @@ def test_bias_prelu_shapes():
             oracle.run("BiasPRelu", x, np.zeros(bad, np.float32), "float32")
 
 
+# --------------------------------------------------------------------------- BiasPReluBN
+def test_bias_prelu_bn_closed_forms():
+    for row in read_golden("bias_prelu_bn_closed_form.txt"):
+        x, bias, slope, mean, var, eps, scale, bnb, want = (float(v) for v in row)
+        xs = f32(x).reshape(1, 1)
+        params = f32(bias, slope, scale, bnb, mean, var).reshape(6, 1)
+        got, _ = oracle.run("BiasPReluBN", xs, params, "float32", eps=eps)
+        g = float(got[0, 0])
+        assert g == want and math.copysign(1, g) == math.copysign(1, want), (row, g)
+
+
+def _chain_params(dtype, C, seed):
+    p = np.concatenate([datagen.normal(seed, 1, C), datagen.uniform(seed, 2, C, -0.5, 0.5),
+                        datagen.normal(seed, 3, C), datagen.normal(seed, 4, C),
+                        datagen.normal(seed, 5, C), datagen.uniform(seed, 6, C, 0.1, 2.0)])
+    return datagen.float_to(p.astype(np.float32), dtype).reshape(6, C)
+
+
+@pytest.mark.parametrize("dtype", ["float32", "float16", "bfloat16"])
+def test_bias_prelu_bn_matches_float32_numpy_chain(dtype):
+    """BiasPReluBN: bias add, PReLU and inference BatchNormalization of one
+    channel in one pass, every step a binary32 operation in the order written,
+    rounded once to x's type (torch rounds float32 to bfloat16)."""
+    C = 6
+    x = datagen.make("normal", dtype, (3, C, 5, 7), 33, 0)
+    x.reshape(-1)[:SPECIALS.size] = datagen.float_to(SPECIALS, dtype)
+    B = _chain_params(dtype, C, 33)
+    eps = np.float32(1e-5)
+    got, st = oracle.run("BiasPReluBN", x, B, dtype, eps=float(eps))
+    assert st == 0
+    if dtype == "bfloat16":
+        to32 = lambda v: torch.from_numpy(v.view(np.int16).copy()).view(torch.bfloat16).float()
+        xf, bf = to32(x), to32(B)
+        col = lambda i: bf[i].view(1, C, 1, 1)
+        t = xf + col(0)
+        t = torch.where(t >= 0, t, col(1) * t)
+        y = (t - col(4)) / torch.sqrt(col(5) + torch.tensor(eps)) * col(2) + col(3)
+        want = y.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    else:
+        xf, bf = x.astype(np.float32), B.astype(np.float32)
+        col = lambda i: bf[i].reshape(1, C, 1, 1)
+        with np.errstate(all="ignore"):
+            t = xf + col(0)
+            t = np.where(t >= 0, t, col(1) * t).astype(np.float32)
+            y = ((t - col(4)) / np.sqrt(col(5) + eps) * col(2) + col(3)).astype(np.float32)
+        want = y.astype(x.dtype)
+    assert_bits_equal(got, want, dtype, "BiasPReluBN")
+
+
+def test_bias_prelu_bn_float32_is_the_unfused_chain():
+    """In binary32 the fused pass equals BiasPRelu followed by
+    BatchNormalization, each rounded to float32; channel by channel."""
+    C = 5
+    x = datagen.make("normal", "float32", (4, C, 9), 34, 0)
+    B = _chain_params("float32", C, 34)
+    got, _ = oracle.run("BiasPReluBN", x, B, "float32", eps=1e-3)
+    t, _ = oracle.run("BiasPRelu", x, B[:2].copy(), "float32")
+    want, _ = oracle.run("BatchNormalization", t, B[2:].copy(), "float32", eps=1e-3)
+    assert_bits_equal(got, want, "float32", "fused vs unfused")
+
+
+def test_bias_prelu_bn_float64_chain():
+    C = 4
+    x = datagen.make("normal", "float64", (2, C, 6), 35, 0)
+    B = _chain_params("float64", C, 35)
+    got, _ = oracle.run("BiasPReluBN", x, B, "float64", eps=1e-5)
+    col = lambda i: B[i].reshape(1, C, 1)
+    t = x + col(0)
+    t = np.where(t >= 0, t, col(1) * t)
+    want = (t - col(4)) / np.sqrt(col(5) + np.float64(np.float32(1e-5))) * col(2) + col(3)
+    assert_bits_equal(got, want, "float64", "BiasPReluBN float64")
+
+
+def test_bias_prelu_bn_shapes():
+    x = np.zeros((2, 3, 4), np.float32)
+    assert oracle.run("BiasPReluBN", x, np.zeros((6, 3), np.float32), "float32")[0].shape == x.shape
+    for bad in [(6, 4), (4, 3), (2, 3), (6,)]:
+        with pytest.raises(Exception):
+            oracle.run("BiasPReluBN", x, np.zeros(bad, np.float32), "float32")
+
+
 # --------------------------------------------------------------------------- MulAdd
 # 0verkilll/onnx ops, MulAddOp: y = (a * b) + c, shapes as the unfused Mul + Add.
 
