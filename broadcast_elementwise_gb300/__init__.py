@@ -32,7 +32,8 @@ OPS = {"Add": 0, "Sub": 1, "Mul": 2, "Div": 3, "Mod": 4, "Pow": 5,
        "And": 11, "Or": 12, "Xor": 13,
        "BitwiseAnd": 14, "BitwiseOr": 15, "BitwiseXor": 16,
        "BitShift": 17, "PRelu": 18, "BatchNormalization": 19, "Clip": 20,
-       "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24, "BiasPRelu": 25, "MulAdd": 26}
+       "Max": 21, "Min": 22, "RSub": 23, "RDiv": 24, "BiasPRelu": 25, "MulAdd": 26,
+       "BiasPReluBN": 27}
 DTYPES = {"float32": 1, "uint8": 2, "int8": 3, "uint16": 4, "int16": 5, "int32": 6, "int64": 7,
           "bool": 9, "float16": 10, "float64": 11, "uint32": 12, "uint64": 13, "bfloat16": 16}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
@@ -460,11 +461,11 @@ def binary(op: str, a, b, out=None, *, stream=None, **attrs):
     """One-shot call on torch CUDA tensors: returns ``out`` (allocated if None).
 
     Inputs that are not contiguous run as strided views (no copy), except a
-    BatchNormalization / Clip / BiasPRelu parameter block, which is copied.
+    BatchNormalization / Clip / BiasPRelu / BiasPReluBN parameter block, which is copied.
     """
     import torch
     desc = descriptor(op, a.dtype, **attrs)
-    plain_b = op not in ("BatchNormalization", "Clip", "BiasPRelu")
+    plain_b = op not in ("BatchNormalization", "Clip", "BiasPRelu", "BiasPReluBN")
     if b is not None and not plain_b:
         b = b.contiguous()
     ta = None if a.is_contiguous() else tuple(a.stride())

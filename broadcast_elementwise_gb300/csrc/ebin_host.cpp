@@ -86,7 +86,8 @@ bool type_legal(int op, ebin_dtype t) {
     case EBIN_OP_PRELU:   // ONNX PRelu T
         return is_float(t) || t == EBIN_INT32 || t == EBIN_INT64 || t == EBIN_UINT32 ||
                t == EBIN_UINT64;
-    case EBIN_OP_BATCHNORM: case EBIN_OP_BIAS_PRELU: return is_float(t);
+    case EBIN_OP_BATCHNORM: case EBIN_OP_BIAS_PRELU: case EBIN_OP_BIAS_PRELU_BN:
+        return is_float(t);
     }
     return false;
 }
@@ -115,7 +116,8 @@ bool scalar_attr_op(int op) {
 
 // B is an ordinary broadcast tensor (not the BN parameter block or Clip bounds).
 bool plain_b(int op) {
-    return op != EBIN_OP_BATCHNORM && op != EBIN_OP_CLIP && op != EBIN_OP_BIAS_PRELU;
+    return op != EBIN_OP_BATCHNORM && op != EBIN_OP_CLIP && op != EBIN_OP_BIAS_PRELU &&
+           op != EBIN_OP_BIAS_PRELU_BN;
 }
 
 // Operators with three inputs (planned by ebin_plan_create3).
@@ -124,7 +126,7 @@ bool ternary(int op) { return op == EBIN_OP_MULADD; }
 // Output keeps A's shape: B broadcasts one way.
 bool one_way(int op) {
     return op == EBIN_OP_PRELU || op == EBIN_OP_BATCHNORM || op == EBIN_OP_CLIP ||
-           op == EBIN_OP_BIAS_PRELU;
+           op == EBIN_OP_BIAS_PRELU || op == EBIN_OP_BIAS_PRELU_BN;
 }
 
 std::atomic<uint64_t> g_next_id{1};
@@ -299,9 +301,11 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     int64_t lb[kMaxRank];
     int rlb = rb;
     int64_t plane = 0;
-    if (d.op == EBIN_OP_BATCHNORM || d.op == EBIN_OP_BIAS_PRELU) {
-        // parameter rows of C: BN scale, bias, mean, var; BiasPRelu bias, slope
-        const int64_t rows = d.op == EBIN_OP_BATCHNORM ? 4 : 2;
+    if (d.op == EBIN_OP_BATCHNORM || d.op == EBIN_OP_BIAS_PRELU ||
+        d.op == EBIN_OP_BIAS_PRELU_BN) {
+        // parameter rows of C: BN scale, bias, mean, var; BiasPRelu bias,
+        // slope; BiasPReluBN bias, slope, scale, bn_bias, mean, var
+        const int64_t rows = d.op == EBIN_OP_BATCHNORM ? 4 : d.op == EBIN_OP_BIAS_PRELU ? 2 : 6;
         if (ra < 2 || rb != 2 || sb[0] != rows || sb[1] != sa[1])
             return EBIN_ERR_INCOMPATIBLE_SHAPES;
         rlb = ra;
@@ -823,6 +827,7 @@ cudaError_t ebin::launch(const Launch &L) {
     case EBIN_OP_AND: case EBIN_OP_OR: case EBIN_OP_XOR: case EBIN_OP_BITWISE_AND:
     case EBIN_OP_BITWISE_OR: case EBIN_OP_BITWISE_XOR: case EBIN_OP_BITSHIFT: EBIN_PICK(logic)
     case EBIN_OP_PRELU: case EBIN_OP_BATCHNORM: case EBIN_OP_CLIP: case EBIN_OP_BIAS_PRELU:
+    case EBIN_OP_BIAS_PRELU_BN:
         EBIN_PICK(chan)
     case EBIN_OP_MAX: case EBIN_OP_MIN: case EBIN_OP_RSUB: case EBIN_OP_RDIV: EBIN_PICK(ext)
     case EBIN_OP_MULADD: EBIN_PICK(tern)

@@ -34,7 +34,7 @@ struct OpArgs {
     float eps;           // BatchNormalization
     int32_t has_min;     // Clip
     int32_t has_max;     // Clip
-    int64_t plane;       // BatchNormalization, BiasPRelu: elements between parameter rows
+    int64_t plane;       // BatchNormalization, BiasPRelu(BN): elements between parameter rows
     int32_t with_scalar; // B is scalar_b, not a tensor (ncnn binaryop with_scalar)
     float scalar_b;
 };
@@ -91,7 +91,7 @@ EBIN_DECLARE_GROUP(mod)     // Mod
 EBIN_DECLARE_GROUP(pow)     // Pow
 EBIN_DECLARE_GROUP(cmp)     // Equal Less Greater LessOrEqual GreaterOrEqual
 EBIN_DECLARE_GROUP(logic)   // And Or Xor BitwiseAnd/Or/Xor BitShift
-EBIN_DECLARE_GROUP(chan)    // PRelu BatchNormalization Clip BiasPRelu
+EBIN_DECLARE_GROUP(chan)    // PRelu BatchNormalization Clip BiasPRelu BiasPReluBN
 EBIN_DECLARE_GROUP(ext)     // Max Min RSub RDiv
 EBIN_DECLARE_GROUP(tern)    // MulAdd (three inputs)
 EBIN_DECLARE_GROUP(powmix)  // Pow with an exponent of another type

@@ -93,7 +93,8 @@ extern "C" ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, con
     if (status_bits) *status_bits = 0;
     if (p.numel == 0) return EBIN_OK;
     const bool plain_b =
-        p.op != EBIN_OP_BATCHNORM && p.op != EBIN_OP_CLIP && p.op != EBIN_OP_BIAS_PRELU;
+        p.op != EBIN_OP_BATCHNORM && p.op != EBIN_OP_CLIP && p.op != EBIN_OP_BIAS_PRELU &&
+        p.op != EBIN_OP_BIAS_PRELU_BN;
     const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max) &&
                           !p.attrs.with_scalar;
     if (!A || !out || (b_needed && !B)) return EBIN_ERR_INVALID_ARG;

@@ -712,6 +712,43 @@ template <class T> struct OpBN {
     }
 };
 
+// BiasPReluBN: the per-channel chain bias add -> PReLU -> inference
+// BatchNormalization in one pass (0verkilll/onnx ops, ConvPReluOp's epilogue
+// followed by BatchNormalizationOp): t = x + bias; t = t >= 0 ? t : slope * t;
+// y = (t - mean) / sqrt(var + eps) * scale + bn_bias, every step rounded in the
+// compute type (binary32, or binary64 for DOUBLE) in the order written, one
+// rounding to x's type.  B holds six rows (bias, slope, scale, bn_bias, mean,
+// var) of `plane` elements, read once per row with the sqrt formed there.
+template <class C> struct ChainParams {
+    C bias, slope, scale, bn_bias, mean, d;
+};
+
+template <class T> struct OpBiasPReluBN {
+    using In = T;
+    using Out = T;
+    using C = typename Tr<T>::C;
+    using BV = ChainParams<C>;
+    static constexpr bool kPlainB = false;
+    static constexpr bool kLegal = is_fp_v<T>;
+    static constexpr bool kValidates = false;
+    __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
+        BV r;
+        r.bias = Tr<T>::in(B[off]);
+        r.slope = Tr<T>::in(B[off + p.plane]);
+        r.scale = Tr<T>::in(B[off + 2 * p.plane]);
+        r.bn_bias = Tr<T>::in(B[off + 3 * p.plane]);
+        r.mean = Tr<T>::in(B[off + 4 * p.plane]);
+        r.d = sqrt_rn(add_rn(Tr<T>::in(B[off + 5 * p.plane]), (C)p.eps));
+        return r;
+    }
+    __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
+        C t = add_rn(Tr<T>::in(a), q.bias);
+        if (!(t >= 0)) t = mul_rn(q.slope, t);
+        t = div_rn(sub_rn(t, q.mean), q.d);
+        return Tr<T>::out(add_rn(mul_rn(t, q.scale), q.bn_bias));
+    }
+};
+
 // Clip: y = x, raised to min when below it, then lowered to max when above it.
 // B = {min, max}; an absent bound is never applied.  The element offset is
 // ignored: the two bounds are shared by every element.

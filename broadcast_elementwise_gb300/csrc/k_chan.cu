@@ -1,4 +1,4 @@
-// PRelu, inference BatchNormalization, Clip and BiasPRelu for one element
+// PRelu, inference BatchNormalization, Clip, BiasPRelu and BiasPReluBN for one element
 // class (EBIN_DT): the per-channel and scalar broadcasts of the engine.
 #include "ebin_kernels.cuh"
 
@@ -11,6 +11,7 @@ cudaError_t EBIN_GROUP_FN(chan)(const Launch &L) {
     case 19: return launch_op<OpBN<T>>(L);
     case 20: return launch_op<OpClip<T>>(L);
     case 25: return launch_op<OpBiasPRelu<T>>(L);
+    case 27: return launch_op<OpBiasPReluBN<T>>(L);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -9,7 +9,8 @@ operand j of a workload uses stream seed*16 + j.
   3  bf16 x[8,64,256,256] ~ N(0,1): Add b[64,1,1] ~ U(-0.5,0.5),
      PRelu slope[64,1,1] ~ U(0,0.3), BatchNormalization with scale, bias,
      mean ~ N(0,1), var ~ U(0.1,2), eps 1e-5 (parameters stored in bf16);
-     the fused BiasPRelu with bias ~ N(0,1), slope ~ U(0,0.3); and the
+     the fused BiasPRelu with bias ~ N(0,1), slope ~ U(0,0.3); the chain
+     BiasPReluBN with the BiasPRelu then BatchNormalization parameters; the
      fused MulAdd x * s + y (residual scaling) with y ~ N(0,1) and s a
      scalar or per-channel [1,64,1,1] ~ U(0,0.3)                          seed 2
   4  Mod opset 28, A[4096,4096] against a scalar B and against B[4096,1]:
@@ -89,6 +90,16 @@ def cases(scale_log2: int = 0) -> list[Case]:
                     lambda: float_to(np.concatenate([normal(2, 1, 64),
                                                      uniform(2, 2, 64, 0.0, 0.3)])
                                      .astype(np.float32), "bfloat16").reshape(2, 64),
+                    "inner_vector_outer", 3, ["fused"]))
+    # the chain bias add -> PReLU -> BatchNormalization in one pass, with the
+    # parameters of the BiasPRelu and BatchNormalization cases above
+    out.append(Case("biasprelubn_bf16_per_channel", "BiasPReluBN", "bfloat16",
+                    {"epsilon": 1e-5}, x, (6, 64),
+                    lambda: make("normal", "bfloat16", x, 2, 0),
+                    lambda: np.concatenate([
+                        float_to(np.concatenate([normal(2, 1, 64), uniform(2, 2, 64, 0.0, 0.3)])
+                                 .astype(np.float32), "bfloat16").reshape(2, 64),
+                        _bn_params(2, 64, "bfloat16")]),
                     "inner_vector_outer", 3, ["fused"]))
     for name, sb, fam in (("muladd_bf16_residual_scale", (1,), "right_scalar"),
                           ("muladd_bf16_per_channel", (1, 64, 1, 1), "inner_vector_outer")):

@@ -96,7 +96,16 @@ typedef enum ebin_op {
      * 16-bit type; integers wrap.  The only three-input operator: plans come
      * from ebin_plan_create3 and run with ebin_execute3. */
     EBIN_OP_MULADD = 26,
-    EBIN_OP_COUNT = 27
+    /* The per-channel chain bias add -> PReLU -> inference BatchNormalization
+     * as one pass (ConvPReluOp's epilogue followed by BatchNormalizationOp).
+     * B = [6, C]: bias, slope, scale, bn_bias, mean, var rows, channel axis 1
+     * of A (rank >= 2; rank 2 [N, C] is per element); attrs.epsilon.
+     * t = x + bias; t = t >= 0 ? t : slope * t; y = (t - mean) /
+     * sqrt(var + eps) * scale + bn_bias: binary32 steps (binary64 for
+     * DOUBLE) in the order written, one rounding to A's type; floating types
+     * only. */
+    EBIN_OP_BIAS_PRELU_BN = 27,
+    EBIN_OP_COUNT = 28
 } ebin_op;
 
 /* Element types, numbered as ONNX TensorProto.DataType. */
@@ -146,7 +155,7 @@ typedef enum ebin_family {
  *                 needs opset 28 ("Binary Kernel Design", Operators and
  *                 traversal).
  *   direction     BitShift only: 0 = LEFT, 1 = RIGHT.
- *   epsilon       BatchNormalization only.
+ *   epsilon       BatchNormalization and BiasPReluBN only.
  *   clip_has_min  Clip only: nonzero if B[0] is a lower bound.
  *   clip_has_max  Clip only: nonzero if B[1] is an upper bound.
  *   with_scalar   ncnn binaryop's with_scalar (operators.md, binaryop): 1 = B
@@ -251,7 +260,7 @@ ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape
  * vector families additionally need every row of a packed input to start on a
  * 16-byte boundary (its outer strides multiples of 16 bytes of elements), else
  * the plan is GENERAL_STRIDED.  B strides are refused (INVALID_ARG) for the
- * parameter blocks of BatchNormalization, Clip and BiasPRelu, and ignored with
+ * parameter blocks of BatchNormalization, Clip, BiasPRelu and BiasPReluBN, and ignored with
  * with_scalar.  family: EBIN_FAMILY_AUTO (the plan is cached, keyed with the
  * strides) or a forced family as ebin_plan_create_forced (not cached).
  * A strided input is never executed in place: any overlap with out is ALIAS.

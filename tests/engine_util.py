@@ -23,9 +23,9 @@ MANIFEST = {
     "BatchNormalization": FLOATS,
     "Clip": FLOATS + INTS,
     "Max": FLOATS + INTS, "Min": FLOATS + INTS, "RSub": FLOATS + INTS, "RDiv": FLOATS + INTS,
-    "BiasPRelu": FLOATS,
+    "BiasPRelu": FLOATS, "BiasPReluBN": FLOATS,
 }
-ONE_WAY = ("PRelu", "BatchNormalization", "Clip", "BiasPRelu")
+ONE_WAY = ("PRelu", "BatchNormalization", "Clip", "BiasPRelu", "BiasPReluBN")
 
 
 def to_device(arr: np.ndarray):
@@ -97,6 +97,15 @@ def inputs_for(op, dtype, shape_a, shape_b, seed=0, attrs=None):
         _sprinkle(a, specials(dtype))
         params = np.concatenate([datagen.normal(seed, 1, C),
                                  datagen.uniform(seed, 2, C, -0.5, 0.5)]).astype(np.float32)
+        return a, datagen.float_to(params, dtype).reshape(shape_b)
+    if op == "BiasPReluBN":
+        C = shape_b[1]
+        a = mk("normal", dtype, shape_a, seed, 0)
+        _sprinkle(a, specials(dtype))
+        params = np.concatenate([
+            datagen.normal(seed, 1, C), datagen.uniform(seed, 2, C, -0.5, 0.5),
+            datagen.normal(seed, 3, C), datagen.normal(seed, 4, C), datagen.normal(seed, 5, C),
+            datagen.uniform(seed, 6, C, 0.1, 2.0)]).astype(np.float32)
         return a, datagen.float_to(params, dtype).reshape(shape_b)
     if op == "Clip":
         if dtype in FLOATS:

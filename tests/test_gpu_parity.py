@@ -50,6 +50,7 @@ BN_CASES = [
     ("empty", (0, 16, 4), (4, 16)),
 ]
 BIAS_PRELU_CASES = [(fam, sa, (2, sb[1])) for fam, sa, sb in BN_CASES]
+CHAIN_CASES = [(fam, sa, (6, sb[1])) for fam, sa, sb in BN_CASES]
 CLIP_CASES = [
     ("right_scalar", (300007,), (2,)),
     ("right_scalar", (40, 77), (2,)),
@@ -64,6 +65,8 @@ def cases_for(op):
         return BN_CASES
     if op == "BiasPRelu":
         return BIAS_PRELU_CASES
+    if op == "BiasPReluBN":
+        return CHAIN_CASES
     if op == "Clip":
         return CLIP_CASES
     return TWO_WAY_CASES
@@ -74,7 +77,7 @@ def attr_variants(op):
         return [{"fmod": 0}, {"fmod": 1}]
     if op == "BitShift":
         return [{"direction": 0}, {"direction": 1}]
-    if op == "BatchNormalization":
+    if op in ("BatchNormalization", "BiasPReluBN"):
         return [{"epsilon": 1e-5}]
     return [{}]
 
