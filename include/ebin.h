@@ -333,6 +333,12 @@ void ebin_plan_cache_clear(void);
  * Returns once the kernel is enqueued.  Invalid elements (integer division by
  * zero, shift counts out of range) do not stop the kernel: they write 0 and set
  * bits in the stream's status word, read with ebin_get_device_status.
+ * Stream capture: the launch path makes no allocation and no synchronising
+ * call, so executions can be captured into a CUDA graph and replayed.  The one
+ * exception is the first validating operator on a stream, which allocates that
+ * stream's status word; for validating operators in a graph, use
+ * ebin_execute_noalloc.  Launch the kernels once before the first capture,
+ * because a kernel's first launch loads its module.
  * Errors: INVALID_ARG, ALIAS, CUDA.
  */
 ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,

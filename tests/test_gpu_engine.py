@@ -444,3 +444,39 @@ def test_execute_mapped_refuses_unmapped_buffers():
     torch.cuda.synchronize()
     assert eb.ebin_launch_count() == before
     assert bool((ho == 0x5A).all()) and bool((short == 0).all())
+
+
+def test_cuda_graph_capture_and_replay():
+    """The launch path of a non-validating operator makes no allocation and no
+    synchronising call, so plans can be captured in a CUDA graph: a captured
+    per-channel BatchNormalization followed by a scalar Mul replays on fresh
+    inputs with the oracle's results."""
+    sa, C = (4, 16, 64, 64), 16
+    bn = eb.descriptor("BatchNormalization", "bfloat16", epsilon=1e-5)
+    mul = eb.descriptor("Mul", "bfloat16")
+    plan_bn = eb.Plan(bn, sa, (4, C))
+    plan_mul = eb.Plan(mul, sa, (1,))
+    x0, params = inputs_for("BatchNormalization", "bfloat16", sa, (4, C), seed=93)
+    s_val = datagen.float_to(np.array([0.75], np.float32), "bfloat16")
+    n = int(np.prod(sa))
+    dx, dp, ds = to_device(x0), to_device(params), to_device(s_val)
+    dmid = torch.empty(2 * n, dtype=torch.uint8, device="cuda")
+    dout = torch.empty(2 * n, dtype=torch.uint8, device="cuda")
+    eb.execute(plan_bn, dx, dp, dmid)          # first launches load the kernels
+    eb.execute(plan_mul, dmid, ds, dout)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    before = eb.ebin_launch_count()
+    with torch.cuda.graph(g):
+        eb.execute(plan_bn, dx, dp, dmid)
+        eb.execute(plan_mul, dmid, ds, dout)
+    assert eb.ebin_launch_count() - before == 2
+    for seed in (94, 95, 96):
+        x = datagen.make("normal", "bfloat16", sa, seed, 0)
+        dx.copy_(to_device(x))
+        g.replay()
+        torch.cuda.synchronize()
+        mid, _ = oracle.run("BatchNormalization", x, params, "bfloat16", eps=1e-5)
+        want, _ = oracle.run("Mul", mid, s_val, "bfloat16", shape_b=(1,))
+        got = dout.cpu().numpy().view(np.uint16).reshape(sa)
+        assert_bits_equal(got, want, "bfloat16", "graph replay %d" % seed)
