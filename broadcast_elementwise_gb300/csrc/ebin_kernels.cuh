@@ -109,6 +109,14 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The same split in two, for kernels with index arithmetic to do first: the
+// arithmetic between pdl_launch and pdl_wait reads kernel parameters only
+// and overlaps the tail of the grid this one depends on.
+__device__ __forceinline__ void pdl_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <class Op>
 __device__ __forceinline__ void flush_err(uint32_t *status, uint32_t err) {
     if constexpr (Op::kValidates) {
@@ -360,7 +368,7 @@ struct RowArgs {
 // Pointers advance by constant steps from row to row.
 template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, bool PACKED>
 __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
-    pdl_enter();
+    pdl_launch();
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
@@ -451,6 +459,7 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     APack a[VA];
     BPack b[VB];
     uint32_t err = 0;
+    pdl_wait();   // the index arithmetic above touched no global memory
     // Not unrolled: an unrolled row loop holds two rows' registers (64 against
     // 40 for bf16 Add), costing a third of the resident CTAs (per-channel bf16
     // Add 25.9 -> 22.6 us, Greater fp16 -> BOOL 149 -> 141 us on GB300).
@@ -533,7 +542,7 @@ template <class In, int G, int I> struct RowOperand {
 
 template <class Op, int G, int IA, int IB, int IC, int V>
 __global__ void __launch_bounds__(kThreads) k_rows3(KArgs p, RowArgs r) {
-    pdl_enter();
+    pdl_launch();
     using In = typename Op::In;
     using Out = typename Op::Out;
     static_assert(G == 1 || (IA != 2 && IB != 2 && IC != 2), "runtime strides need G == 1");
@@ -590,6 +599,7 @@ __global__ void __launch_bounds__(kThreads) k_rows3(KArgs p, RowArgs r) {
     typename OA::P a[VA];
     typename OB::P b[VB];
     typename OC::P c[VC];
+    pdl_wait();   // the index arithmetic above touched no global memory
 #pragma unroll 1
     for (int j = 0; j < n; ++j) {
         if (j == 0 || stepA != 0) {
