@@ -737,7 +737,9 @@ cudaError_t run_scalar(const Launch &L) {
 // Tile shape for a row traversal with rows of `cols` groups and V groups per
 // thread per row: threads per row, rows in parallel and rows per thread,
 // aiming at enough CTAs for several waves.
-inline RowArgs row_args(const Geom &g, int G, int V, int num_sms) {
+// min_kr: the fewest rows a thread walks (operators that prepare a divisor
+// per row amortise the thread's setup over at least two).
+inline RowArgs row_args(const Geom &g, int G, int V, int num_sms, int64_t min_kr = 1) {
     RowArgs r{};
     const int rank = g.rank;
     r.L = g.n[rank - 1];
@@ -781,7 +783,7 @@ inline RowArgs row_args(const Geom &g, int G, int V, int num_sms) {
     const int64_t groups = P * r.M * r.cols;
     const int64_t per_cta = (int64_t)r.tpr * r.rs * V;
     int64_t kr = groups / (per_cta * (int64_t)num_sms * 16);
-    kr = std::max<int64_t>(1, std::min<int64_t>(16, kr));
+    kr = std::max<int64_t>(min_kr, std::min<int64_t>(16, kr));
     kr = std::min<int64_t>(kr, ceil_div(r.M, r.rs));
     r.kr = (int32_t)kr;
     r.runs = ceil_div(r.M, (int64_t)r.rs * r.kr);
@@ -805,7 +807,9 @@ inline int64_t row_tiles(const RowArgs &r) {
 
 template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, bool PACKED>
 cudaError_t run_rows_kernel(const Launch &L) {
-    const RowArgs r = row_args(L.g, G, V, L.num_sms);
+    // Mod against per-row divisors: two rows per thread at least (fp32 rows
+    // [4096,4096] vs [4096,1]: 24.1 -> 23.4 us; int32: 22.6 -> 22.1 us)
+    const RowArgs r = row_args(L.g, G, V, L.num_sms, HasPrep<Op>::value ? 2 : 1);
     const int64_t tiles = row_tiles(r);
     if (tiles > kMaxGrid) return cudaErrorInvalidConfiguration;
     return launch_pdl(k_rows<Op, G, IA, IB, NOPREFIX, V, PACKED>, tiles, r.tpr * r.rs, L.stream,
