@@ -132,6 +132,12 @@ struct HasPack<Op, std::void_t<decltype(Op::kPack)>> : std::bool_constant<Op::kP
 // Operators that prepare a B shared by many elements (Op::kPrep, Op::prep,
 // Op::apply_prep_group) -- e.g. the reciprocal of a Mod divisor.
 template <class Op, class = void> struct HasPrep : std::false_type {};
+// The fewest rows a thread of the row kernel walks (Op::kMinRows, default 1):
+// operators with costly per-row parameters amortise the thread's setup.
+template <class Op, class = void> struct MinRowsOf : std::integral_constant<int, 1> {};
+template <class Op>
+struct MinRowsOf<Op, std::void_t<decltype(Op::kMinRows)>>
+    : std::integral_constant<int, Op::kMinRows> {};
 template <class Op>
 struct HasPrep<Op, std::void_t<decltype(Op::kPrep)>> : std::bool_constant<Op::kPrep> {};
 
@@ -807,9 +813,7 @@ inline int64_t row_tiles(const RowArgs &r) {
 
 template <class Op, int G, int IA, int IB, bool NOPREFIX, int V, bool PACKED>
 cudaError_t run_rows_kernel(const Launch &L) {
-    // Mod against per-row divisors: two rows per thread at least (fp32 rows
-    // [4096,4096] vs [4096,1]: 24.1 -> 23.4 us; int32: 22.6 -> 22.1 us)
-    const RowArgs r = row_args(L.g, G, V, L.num_sms, HasPrep<Op>::value ? 2 : 1);
+    const RowArgs r = row_args(L.g, G, V, L.num_sms, MinRowsOf<Op>::value);
     const int64_t tiles = row_tiles(r);
     if (tiles > kMaxGrid) return cudaErrorInvalidConfiguration;
     return launch_pdl(k_rows<Op, G, IA, IB, NOPREFIX, V, PACKED>, tiles, r.tpr * r.rs, L.stream,
