@@ -446,3 +446,23 @@ def test_dtype_sizes_and_strings():
     for name, code in eb.DTYPES.items():
         assert eb.ebin_dtype_size(code) == eb.ITEMSIZE[name]
     assert eb.ebin_status_string(7) == "input aliases the output"
+
+
+def test_execute_mapped_host_checks():
+    """ebin_execute_mapped refuses before any device work: NULL buffers, a
+    three-input plan, and host memory that is not pinned and mapped (here,
+    pageable numpy memory; the check runs without a GPU too)."""
+    import numpy as np
+    d = eb.descriptor("Add", "float32")
+    p = eb.Plan(d, (1024,), (1024,))
+    a = np.zeros(1024, np.float32)
+    o = np.zeros(1024, np.float32)
+    pe = eb.Plan(d, (0, 4), (4,))
+    eb.ebin_execute_mapped(pe.handle, None, None, None, None)       # nothing to do
+    for args in ((None, a.ctypes.data, o.ctypes.data), (a.ctypes.data, a.ctypes.data, None),
+                 (a.ctypes.data, a.ctypes.data, o.ctypes.data)):
+        with pytest.raises(eb.EbinError, match="invalid_arg"):
+            eb.ebin_execute_mapped(p.handle, *args, None)
+    p3 = eb.Plan3(eb.descriptor("MulAdd", "float32"), (8,), (8,), (8,))
+    with pytest.raises(eb.EbinError, match="invalid_arg"):
+        eb.ebin_execute_mapped(p3.handle, a.ctypes.data, a.ctypes.data, o.ctypes.data, None)
