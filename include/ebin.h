@@ -55,6 +55,8 @@ typedef enum ebin_status {
  * BatchNormalization and Clip reduce to (0verkilll/onnx "ops" docs,
  * BatchNormalizationOp and ClipOp; ncnn operators.md, batchnorm and clip).
  * Bias (ncnn operators.md, bias) is EBIN_OP_ADD with B shaped [C,1,1].
+ * Then ncnn binaryop's MAX, MIN, RSUB and RDIV, and three fused passes: bias
+ * + PReLU, bias + PReLU + BatchNormalization, and the three-input MulAdd.
  */
 typedef enum ebin_op {
     EBIN_OP_ADD = 0,
