@@ -458,14 +458,27 @@ def descriptor(op: str, dtype, **attrs) -> Descriptor:
 
 
 def binary(op: str, a, b, out=None, *, stream=None, **attrs):
-    """One-shot call on torch CUDA tensors: returns ``out`` (allocated if None).
+    """One-shot call: returns ``out`` (allocated if None).
 
-    Inputs that are not contiguous run as strided views (no copy), except a
-    BatchNormalization / Clip / BiasPRelu / BiasPReluBN parameter block, which is copied.
+    On torch CUDA tensors, inputs that are not contiguous run as strided views
+    (no copy), except a BatchNormalization / Clip / BiasPRelu / BiasPReluBN
+    parameter block, which is copied.  On pinned CPU tensors (contiguous),
+    the kernel reads and writes host memory in place (ebin_execute_mapped;
+    ``out`` is allocated pinned); synchronise ``stream`` before reading it.
     """
     import torch
     desc = descriptor(op, a.dtype, **attrs)
     plain_b = op not in ("BatchNormalization", "Clip", "BiasPRelu", "BiasPReluBN")
+    if not a.is_cuda:
+        if not a.is_pinned() or (b is not None and not b.is_pinned()):
+            raise ValueError("binary: CPU tensors must be pinned (tensor.pin_memory())")
+        if not a.is_contiguous() or (b is not None and not b.is_contiguous()):
+            raise ValueError("binary: pinned CPU tensors must be contiguous")
+        plan = Plan(desc, a.shape, b.shape if b is not None else (2,))
+        if out is None:
+            out = torch.empty(plan.output_shape, dtype=torch_dtype(desc.out_dtype)).pin_memory()
+        execute_mapped(plan, a, b, out, stream)
+        return out
     if b is not None and not plain_b:
         b = b.contiguous()
     ta = None if a.is_contiguous() else tuple(a.stride())

@@ -480,3 +480,16 @@ def test_cuda_graph_capture_and_replay():
         want, _ = oracle.run("Mul", mid, s_val, "bfloat16", shape_b=(1,))
         got = dout.cpu().numpy().view(np.uint16).reshape(sa)
         assert_bits_equal(got, want, "bfloat16", "graph replay %d" % seed)
+
+
+def test_binary_helper_on_pinned_host_tensors():
+    """binary() on pinned CPU tensors runs the kernel on host memory in place."""
+    a, b = inputs_for("Mul", "float32", (64, 1000), (1000,), seed=97)
+    want, _ = oracle.run("Mul", a, b, "float32")
+    ta, tb = torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory()
+    out = eb.binary("Mul", ta, tb)
+    torch.cuda.synchronize()
+    assert out.is_pinned() and not out.is_cuda
+    assert_bits_equal(out.numpy(), want, "float32", "binary on pinned host tensors")
+    with pytest.raises(ValueError, match="pinned"):
+        eb.binary("Mul", torch.from_numpy(a), tb)
