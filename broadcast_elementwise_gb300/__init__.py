@@ -101,6 +101,7 @@ def _load():
         "ebin_execute": (i32, [vp, vp, vp, vp, vp]),
         "ebin_execute_host": (i32, [vp, vp, vp, vp, vp, vp, vp, vp]),
         "ebin_execute_mapped": (i32, [vp, vp, vp, vp, vp]),
+        "ebin_execute3_mapped": (i32, [vp, vp, vp, vp, vp, vp]),
         "ebin_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ebin_execute_noalloc": (i32, [vp, vp, vp, vp, vp, i32, ctypes.POINTER(ctypes.c_uint32)]),
         "ebin_launch_count": (ctypes.c_uint64, []),
@@ -275,6 +276,11 @@ def ebin_execute_mapped(plan, host_a, host_b, host_out, stream) -> None:
     _check(lib.ebin_execute_mapped(plan, host_a, host_b, host_out, stream), "ebin_execute_mapped")
 
 
+def ebin_execute3_mapped(plan, host_a, host_b, host_c, host_out, stream) -> None:
+    _check(lib.ebin_execute3_mapped(plan, host_a, host_b, host_c, host_out, stream),
+           "ebin_execute3_mapped")
+
+
 def ebin_execute_noalloc(plan, A, B, out, stream, status_slot, want_status=True):
     """Marshal ebin_execute_noalloc; returns the status bits (0 when not requested)."""
     bits = ctypes.c_uint32(0)
@@ -433,6 +439,11 @@ def execute_mapped(plan: Plan, A, B, out, stream=None) -> None:
     """Enqueue the plan on pinned host buffers, read and written in place by the
     kernel (torch pinned tensors or int addresses)."""
     ebin_execute_mapped(plan.handle, _ptr(A), _ptr(B), _ptr(out), _stream(stream))
+
+
+def execute3_mapped(plan: Plan3, A, B, C, out, stream=None) -> None:
+    """Enqueue a three-input plan on pinned host buffers, in place."""
+    ebin_execute3_mapped(plan.handle, _ptr(A), _ptr(B), _ptr(C), _ptr(out), _stream(stream))
 
 
 def get_device_status(stream=None) -> int:

@@ -1173,6 +1173,23 @@ extern "C" ebin_status ebin_execute_mapped(ebin_plan_t plan, const void *host_a,
     return launch_counted(L);
 }
 
+extern "C" ebin_status ebin_execute3_mapped(ebin_plan_t plan, const void *host_a,
+                                            const void *host_b, const void *host_c,
+                                            void *host_out, void *stream) {
+    if (!plan || plan->rank_c < 0) return EBIN_ERR_INVALID_ARG;
+    const ebin_plan_s &p = *plan;
+    if (p.numel == 0) return EBIN_OK;
+    if (!host_a || !host_b || !host_c || !host_out) return EBIN_ERR_INVALID_ARG;
+    const size_t isz = ebin_dtype_size(p.dt);
+    const void *da = mapped_range(host_a, (size_t)p.numel_a * isz);
+    const void *db = mapped_range(host_b, (size_t)p.numel_b * isz);
+    const void *dc = mapped_range(host_c, (size_t)p.numel_c * isz);
+    void *dout = const_cast<void *>(
+        mapped_range(host_out, (size_t)p.numel * ebin_dtype_size(p.out_dt)));
+    if (!da || !db || !dc || !dout) return EBIN_ERR_INVALID_ARG;
+    return ebin_execute3(plan, da, db, dc, dout, stream);
+}
+
 extern "C" ebin_status ebin_get_device_status(void *stream, uint32_t *bits) {
     if (!bits) return EBIN_ERR_INVALID_ARG;
     *bits = 0;

@@ -408,6 +408,15 @@ ebin_status ebin_execute_mapped(ebin_plan_t plan, const void *host_a, const void
                                 void *host_out, void *stream);
 
 /*
+ * ebin_execute3 on host buffers, in place over the host-device link, with the
+ * checks of ebin_execute_mapped on all four buffers (each input's extent is
+ * its element count in the plan's type).  A two-input plan gives INVALID_ARG.
+ * Errors: as ebin_execute3, and INVALID_ARG for an unmapped buffer.
+ */
+ebin_status ebin_execute3_mapped(ebin_plan_t plan, const void *host_a, const void *host_b,
+                                 const void *host_c, void *host_out, void *stream);
+
+/*
  * Read and clear the device status word of `stream` on the current device:
  * synchronises the stream, returns the OR of the EBIN_DEVICE_* bits raised
  * since the last call, then zeroes the word (stream-ordered).  A stream that

@@ -493,3 +493,18 @@ def test_binary_helper_on_pinned_host_tensors():
     assert_bits_equal(out.numpy(), want, "float32", "binary on pinned host tensors")
     with pytest.raises(ValueError, match="pinned"):
         eb.binary("Mul", torch.from_numpy(a), tb)
+
+
+@pytest.mark.parametrize("sb", [(1,), (1, 16, 1, 1), (4, 16, 8, 33)])
+def test_execute3_mapped_matches_the_oracle(sb):
+    """ebin_execute3_mapped: MulAdd with all four buffers in pinned host memory."""
+    sa = (4, 16, 8, 33)
+    x = datagen.make("normal", "bfloat16", sa, 98, 0)
+    s = datagen.make("uniform", "bfloat16", sb, 98, 1, lo=0.0, hi=0.3)
+    y = datagen.make("normal", "bfloat16", sa, 98, 2)
+    want = oracle.run3("MulAdd", x, s, y, "bfloat16")
+    p = eb.Plan3(eb.descriptor("MulAdd", "bfloat16"), sa, sb, sa)
+    out = torch.zeros(2 * p.numel, dtype=torch.uint8).pin_memory()
+    eb.execute3_mapped(p, _pinned(x), _pinned(s), _pinned(y), out)
+    torch.cuda.synchronize()
+    assert_bits_equal(out.numpy().view(np.uint16).reshape(sa), want, "bfloat16", "MulAdd mapped")

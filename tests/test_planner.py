@@ -466,3 +466,8 @@ def test_execute_mapped_host_checks():
     p3 = eb.Plan3(eb.descriptor("MulAdd", "float32"), (8,), (8,), (8,))
     with pytest.raises(eb.EbinError, match="invalid_arg"):
         eb.ebin_execute_mapped(p3.handle, a.ctypes.data, a.ctypes.data, o.ctypes.data, None)
+    # the three-input form: pageable buffers and a two-input plan are refused too
+    for plan in (p3, p):
+        with pytest.raises(eb.EbinError, match="invalid_arg"):
+            eb.ebin_execute3_mapped(plan.handle, a.ctypes.data, a.ctypes.data, a.ctypes.data,
+                                    o.ctypes.data, None)
