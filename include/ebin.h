@@ -215,7 +215,8 @@ void ebin_descriptor_destroy(ebin_descriptor_t desc);
  * Operators and traversal; Prepared execution for the cache):
  *   1. right-align the shapes (a rank-0 shape is a scalar) and check that each
  *      dimension pair is equal or contains a 1 (0 pairs only with 0 or 1);
- *      PRelu, BatchNormalization and Clip broadcast one way: out == A's shape;
+ *      PRelu, BatchNormalization, Clip, BiasPRelu and BiasPReluBN broadcast
+ *      one way: out == A's shape;
  *   2. give broadcast dimensions zero strides;
  *   3. drop dimensions of output extent 1;
  *   4. merge adjacent dimensions i, i+1 when stride[i] == stride[i+1] * n[i+1]
@@ -235,7 +236,8 @@ void ebin_descriptor_destroy(ebin_descriptor_t desc);
  * a miss always builds and validates a fresh plan.
  *
  * Shapes: shape_a[rank_a], shape_b[rank_b], dims >= 0.  For BatchNormalization
- * B is [4, C] with C == shape_a[1] (rank_a >= 2); for Clip B is [2].
+ * B is [4, C], for BiasPRelu [2, C] and for BiasPReluBN [6, C], with
+ * C == shape_a[1] (rank_a >= 2); for Clip B is [2].
  *   out            receives a plan reference; release it with ebin_plan_release
  * Errors: INVALID_ARG, RANK_TOO_LARGE, INCOMPATIBLE_SHAPES.
  */
