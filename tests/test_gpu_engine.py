@@ -508,3 +508,23 @@ def test_execute3_mapped_matches_the_oracle(sb):
     eb.execute3_mapped(p, _pinned(x), _pinned(s), _pinned(y), out)
     torch.cuda.synchronize()
     assert_bits_equal(out.numpy().view(np.uint16).reshape(sa), want, "bfloat16", "MulAdd mapped")
+
+
+def test_execute_mapped_on_registered_host_memory():
+    """Memory pinned after the fact with cudaHostRegister is accepted too."""
+    n = (1 << 20) + 3
+    a, b = inputs_for("Add", "float32", (n,), (n,), seed=99)
+    a, b = np.ascontiguousarray(a), np.ascontiguousarray(b)
+    o = np.zeros(n, np.float32)
+    cr = torch.cuda.cudart()
+    for arr in (a, b, o):
+        assert cr.cudaHostRegister(arr.ctypes.data, arr.nbytes, 0) == cr.cudaError.success
+    try:
+        p = eb.Plan(eb.descriptor("Add", "float32"), (n,), (n,))
+        eb.execute_mapped(p, a.ctypes.data, b.ctypes.data, o.ctypes.data)
+        torch.cuda.synchronize()
+        want, _ = oracle.run("Add", a, b, "float32")
+        assert_bits_equal(o, want, "float32", "registered host memory")
+    finally:
+        for arr in (a, b, o):
+            cr.cudaHostUnregister(arr.ctypes.data)
