@@ -528,3 +528,42 @@ def test_execute_mapped_on_registered_host_memory():
     finally:
         for arr in (a, b, o):
             cr.cudaHostUnregister(arr.ctypes.data)
+
+
+def test_host_threads_on_their_own_streams():
+    """Four host threads, each on its own stream, run int32 Div plans at once;
+    only the threads whose divisors hold a zero see DIV_BY_ZERO on their
+    stream, and every output equals the oracle's."""
+    import threading
+    shape = (256, 1024)
+    results, errors = {}, []
+
+    def work(tid):
+        try:
+            stream = torch.cuda.Stream()
+            a, b = inputs_for("Div", "int32", shape, shape, seed=100 + tid)
+            b = b.copy()
+            b[b == 0] = 1
+            if tid % 2:
+                b[tid, 7] = 0
+            p = eb.Plan(eb.descriptor("Div", "int32"), shape, shape)
+            dA, dB = to_device(a), to_device(b)
+            out = torch.empty(4 * p.numel, dtype=torch.uint8, device="cuda")
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    eb.execute(p, dA, dB, out, stream)
+            bits = eb.get_device_status(stream)
+            results[tid] = (a, b, out.cpu().numpy().view(np.int32).reshape(shape), bits)
+        except Exception as e:          # reported below, in the main thread
+            errors.append((tid, repr(e)))
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for tid, (a, b, got, bits) in results.items():
+        want, wbits = oracle.run("Div", a, b, "int32")
+        assert_bits_equal(got, want, "int32", "thread %d" % tid)
+        assert bits == wbits == (eb.DEVICE_DIV_BY_ZERO if tid % 2 else 0), (tid, bits, wbits)

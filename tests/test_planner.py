@@ -471,3 +471,39 @@ def test_execute_mapped_host_checks():
         with pytest.raises(eb.EbinError, match="invalid_arg"):
             eb.ebin_execute3_mapped(plan.handle, a.ctypes.data, a.ctypes.data, a.ctypes.data,
                                     o.ctypes.data, None)
+
+
+def test_plans_and_descriptors_from_many_host_threads():
+    """The C ABI is thread-safe: eight host threads create descriptors and
+    plans (hits, misses and evictions of the shared 8-entry LRU) and release
+    them, concurrently (ctypes drops the GIL around each call)."""
+    import threading
+    import numpy as np
+    shapes = [((64, 32), (32,)), ((8, 16, 4), (16, 1)), ((5, 1, 7), (1, 6, 7)), ((3,), ()),
+              ((2, 3, 4, 5), (3, 1, 5)), ((100,), (100,)), ((9, 9), (9, 1)), ((4, 1), (1, 4)),
+              ((7, 2, 3), (2, 3)), ((1, 11), (11, 1))]
+    want = {(sa, sb): tuple(np.broadcast_shapes(sa, sb)) for sa, sb in shapes}
+    errors = []
+
+    def work(tid):
+        try:
+            for it in range(300):
+                sa, sb = shapes[(tid * 7 + it) % len(shapes)]
+                op = ("Add", "Mul", "Greater")[it % 3]
+                d = eb.ebin_descriptor_create(eb.OPS[op], 18, None, eb.DTYPES["float32"],
+                                              eb.DTYPES["float32"])
+                h = eb.ebin_plan_create(d, sa, sb)
+                assert eb.ebin_plan_output_shape(h) == want[(sa, sb)]
+                eb.ebin_plan_release(h)
+                eb.ebin_descriptor_destroy(d)
+        except Exception as e:          # reported below, in the main thread
+            errors.append((tid, repr(e)))
+
+    threads = [threading.Thread(target=work, args=(t,)) for t in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:3]
+    hits, misses, size = eb.ebin_plan_cache_stats()
+    assert size <= eb.PLAN_CACHE_CAPACITY
