@@ -225,8 +225,11 @@ int family_of(const ebin_plan_s &p, int forced, bool *ok) {
     for (int i = 0; i + 1 < r; ++i)
         rows_aligned = rows_aligned && (ia != 1 || g.sa[i] % G == 0) &&
                        (ib != 1 || g.sb[i] % G == 0);
+    // REPEATED_BLOCK: one input dense, the other a row block reused (0,1) or
+    // one value per row (1,0), any row length (rows that are not a whole
+    // number of 16-byte packs run the periodic flat kernel)
     bool block = false;
-    if (r == 2 && inner % G == 0 && rows_aligned) {
+    if (r == 2) {
         const bool a_dense = g.sa[0] == inner && g.sa[1] == 1;
         const bool b_dense = g.sb[0] == inner && g.sb[1] == 1;
         auto bcast = [](const int64_t *s) {

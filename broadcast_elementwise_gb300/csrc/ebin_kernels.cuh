@@ -520,6 +520,72 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
     flush_err<Op>(p.status, err);
 }
 
+// ---------------------------------------------------------------- short rows
+//
+// REPEATED_BLOCK whose rows are not a whole number of 16-byte packs (a
+// channels-last per-channel operand of 3 or 4 channels, rows of 13): the
+// dense input and the output are flat arrays, read and written in packs of G
+// as in k_scalar; the other input is X[e mod P] (a row block reused) or
+// X[e / P] (one value per row) for output element e, with P the row length.
+// The row position is decoded once per pack and stepped with selects.
+template <class Op, bool DENSE_A, bool PER_ROW, int U>
+__global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int64_t P, FastDiv fP,
+                                                       int32_t wide_i) {
+    pdl_launch();
+    using In = typename Op::In;
+    using Out = typename Op::Out;
+    using BIn = typename BInOf<Op>::type;
+    constexpr int G = 16 / sizeof(In);
+    const bool wide = wide_i != 0;
+    const In *A = static_cast<const In *>(p.A);
+    const BIn *B = static_cast<const BIn *>(p.B);
+    Out *O = static_cast<Out *>(p.out);
+    const In *D = DENSE_A ? A : reinterpret_cast<const In *>(B);
+    const int64_t ng = p.numel / G;
+    const int64_t step = (int64_t)gridDim.x * (kThreads * U);
+    uint32_t err = 0;
+    pdl_wait();
+    for (int64_t base = (int64_t)blockIdx.x * (kThreads * U) + threadIdx.x; base < ng;
+         base += step) {
+        Pack<In, G> d[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t g = base + (int64_t)u * kThreads;
+            if (g < ng) d[u] = ld_stream<In, G>(D + g * G);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t g = base + (int64_t)u * kThreads;
+            if (g < ng) {
+                const int64_t e0 = g * G;
+                int64_t q = udiv(e0, P, fP, wide);
+                int64_t r = e0 - q * P;
+                Pack<Out, G> o;
+#pragma unroll
+                for (int k = 0; k < G; ++k) {
+                    const int64_t xi = PER_ROW ? q : r;
+                    if constexpr (DENSE_A)
+                        o.v[k] = Op::apply(d[u].v[k], Op::loadB(B, xi, p.args), p.args, err);
+                    else
+                        o.v[k] = Op::apply(A[xi], d[u].v[k], p.args, err);
+                    const bool wrap = ++r == P;
+                    r = wrap ? 0 : r;
+                    q += wrap ? 1 : 0;
+                }
+                st_stream<Out, G>(O + e0, o);
+            }
+        }
+    }
+    for (int64_t e = ng * G + (int64_t)blockIdx.x * kThreads + threadIdx.x; e < p.numel;
+         e += (int64_t)gridDim.x * kThreads) {
+        const int64_t q = udiv(e, P, fP, wide);
+        const int64_t xi = PER_ROW ? q : e - q * P;
+        if constexpr (DENSE_A) O[e] = Op::apply(A[e], Op::loadB(B, xi, p.args), p.args, err);
+        else O[e] = Op::apply(A[xi], D[e], p.args, err);
+    }
+    flush_err<Op>(p.status, err);
+}
+
 // ---------------------------------------------------------------- three inputs
 //
 // The row traversal of k_rows for an operator of three inputs (Op::apply3):
@@ -866,6 +932,38 @@ cudaError_t run_general(const Launch &L) {
     return run_rows_kernel<Op, 1, 2, 2, false, 2, false>(L);
 }
 
+// REPEATED_BLOCK with rows off the pack width: rank 2, one input dense
+// (strides (P, 1)), the other (0, 1) or (1, 0).
+template <class Op>
+cudaError_t run_periodic(const Launch &L) {
+    constexpr int G = 16 / sizeof(typename Op::In);
+    const int64_t P = L.g.n[1];
+    const bool a_dense = L.g.sa[0] == P && L.g.sa[1] == 1;
+    const int64_t *xs = a_dense ? L.g.sb : L.g.sa;      // the broadcast input's strides
+    const bool per_row = xs[0] == 1 && xs[1] == 0;
+    const int32_t wide = (L.numel >= (1ll << 32) || P >= (1ll << 32)) ? 1 : 0;
+    const FastDiv fP = make_fastdiv((uint64_t)P);
+    const int64_t ng = L.numel / G;
+    int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
+    grid = std::min<int64_t>(grid, kMaxGrid);
+    if (a_dense) {
+        if (per_row)
+            return launch_pdl(k_periodic<Op, true, true, kUnrollFlat>, grid, kThreads, L.stream,
+                              kargs<Op>(L), P, fP, wide);
+        return launch_pdl(k_periodic<Op, true, false, kUnrollFlat>, grid, kThreads, L.stream,
+                          kargs<Op>(L), P, fP, wide);
+    }
+    if constexpr (Op::kPlainB) {
+        if (per_row)
+            return launch_pdl(k_periodic<Op, false, true, kUnrollFlat>, grid, kThreads, L.stream,
+                              kargs<Op>(L), P, fP, wide);
+        return launch_pdl(k_periodic<Op, false, false, kUnrollFlat>, grid, kThreads, L.stream,
+                          kargs<Op>(L), P, fP, wide);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+}
+
 // Operators that accept a scalar B given as an attribute (Op::kScalarAttr).
 template <class Op, class = void> struct HasScalarAttr : std::false_type {};
 template <class Op>
@@ -903,6 +1001,8 @@ cudaError_t launch_op(const Launch &L) {
             if constexpr (Op::kPlainB) return run_scalar<Op, true>(L);
             else return cudaErrorInvalidValue;
         case FAM_REPEATED_BLOCK:
+            if (L.g.rank == 2 && L.g.n[1] % (16 / (int64_t)sizeof(typename Op::In)) != 0)
+                return run_periodic<Op>(L);
             if (L.g.rank == 2) return run_rows_vector<Op, true>(L);
             return run_rows_vector<Op, false>(L);
         case FAM_INNER_VECTOR_OUTER: return run_rows_vector<Op, false>(L);

@@ -225,8 +225,8 @@ void ebin_descriptor_destroy(ebin_descriptor_t desc);
  *        numel == 0                                   -> EMPTY
  *        rank 1, strides (A,B) (1,1) / (0,1) / (1,0)  -> CONTIGUOUS / LEFT_ / RIGHT_SCALAR
  *        rank 2, one input dense and the other with strides (1,0) (one value
- *        per row) or (0,1) (one row block reused), row length a multiple of
- *        the vector width                              -> REPEATED_BLOCK
+ *        per row) or (0,1) (one row block reused), any row length
+ *                                                      -> REPEATED_BLOCK
  *        innermost extent >= 64 and a multiple of the vector width
  *                                                      -> INNER_VECTOR_OUTER
  *        otherwise                                     -> GENERAL_STRIDED

@@ -30,7 +30,13 @@ TWO_WAY_CASES = [
     ("inner_vector_outer", (6, 1, 5, 1), (1, 7, 1, 256)),
     ("general_strided", (2, 3, 4, 5), (3, 1, 5)),
     ("general_strided", (7, 1, 93), (1, 5, 93)),
-    ("general_strided", (33, 65), (33, 1)),
+    ("repeated_block", (33, 65), (33, 1)),
+    # rows off the 16-byte pack width: the periodic flat kernel
+    ("repeated_block", (1000, 3), (3,)),
+    ("repeated_block", (1000, 3), (1000, 1)),
+    ("repeated_block", (3,), (1000, 3)),
+    ("repeated_block", (1000, 1), (1000, 13)),
+    ("repeated_block", (257, 17), (17,)),
     ("empty", (0, 5), (5,)),
     ("contiguous", (), ()),
 ]
@@ -41,10 +47,12 @@ PRELU_CASES = [
     ("right_scalar", (300007,), (1,)),
     ("contiguous", (50001,), (50001,)),
     ("general_strided", (2, 3, 4, 5), (3, 1, 5)),
+    ("repeated_block", (300, 7), (7,)),
 ]
 BN_CASES = [
     ("inner_vector_outer", (4, 16, 8, 32), (4, 16)),
     ("repeated_block", (300, 64), (4, 64)),
+    ("repeated_block", (301, 6), (4, 6)),
     ("general_strided", (3, 16, 9, 11), (4, 16)),
     ("contiguous", (1, 64), (4, 64)),
     ("empty", (0, 16, 4), (4, 16)),
