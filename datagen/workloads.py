@@ -143,6 +143,13 @@ def cases(scale_log2: int = 0) -> list[Case]:
                     lambda: make("bits", "uint32", (n5,), 4, 2),
                     lambda: make("int_range", "uint32", (1,), 4, 3, lo=0, hi=31),
                     "right_scalar", 5))
+    # not from the pages: a channels-last per-channel broadcast (NHWC image
+    # data, 3 channels), whose rows are off the 16-byte pack width
+    nhwc = (1 << max(24 - scale_log2, 8), 3)
+    out.append(Case("add_f32_channels_last_c3", "Add", "float32", {}, nhwc, (3,),
+                    lambda: make("normal", "float32", nhwc, 5, 0),
+                    lambda: make("uniform", "float32", (3,), 5, 1, lo=-0.5, hi=0.5),
+                    "repeated_block", 6, ["extra"]))
     return out
 
 
