@@ -37,6 +37,9 @@ TWO_WAY_CASES = [
     ("repeated_block", (3,), (1000, 3)),
     ("repeated_block", (1000, 1), (1000, 13)),
     ("repeated_block", (257, 17), (17,)),
+    # a block length dividing the pack: the broadcast values are read once
+    ("repeated_block", (1000, 4), (4,)),
+    ("repeated_block", (2,), (999, 2)),
     ("empty", (0, 5), (5,)),
     ("contiguous", (), ()),
 ]
