@@ -148,6 +148,24 @@ def test_families_of_the_benchmark_workloads():
     assert family("Add", "float32", (0, 5), (5,))[0] == "empty"
     assert family("Clip", "float32", (30, 40), (2,))[0] == "right_scalar"
     assert family("BatchNormalization", "float32", (300, 64), (4, 64))[0] == "repeated_block"
+    assert family("Add", "float32", (1 << 24, 3), (3,))[0] == "repeated_block"
+
+
+def test_repeated_block_rule_for_any_row_length():
+    """Rank 2, one input dense and the other a reused row block (0,1) or one
+    value per row (1,0) is REPEATED_BLOCK whatever the row length; with both
+    inputs broadcast it stays GENERAL_STRIDED, and a one-way operator cannot
+    have a dense B with a broadcast A."""
+    for P in (2, 3, 5, 13, 17, 63, 64, 65):
+        for sa, sb in (((100, P), (P,)), ((100, P), (100, 1)), ((P,), (100, P)),
+                       ((100, 1), (100, P))):
+            f, (n, ga, gb) = family("Sub", "int16", sa, sb)
+            assert f == "repeated_block" and n == [100, P], (sa, sb, f, n)
+        # both broadcast: the outer-product row kernel when rows are long
+        # whole packs, else the general kernel -- never the block kernel
+        want = "inner_vector_outer" if P >= 64 and P % 4 == 0 else "general_strided"
+        assert family("Add", "float32", (100, 1), (1, P))[0] == want
+        assert family("PRelu", "float32", (100, P), (P,))[0] == "repeated_block"
 
 
 def test_one_way_broadcasts():
