@@ -130,7 +130,8 @@ typedef enum ebin_dtype {
 /*
  * Loop families ("Binary Kernel Design", section "Operators and traversal",
  * loop-family table).  Each has its own kernel; the selection rule is stated
- * at ebin_plan_create.
+ * at ebin_plan_create.  REPEATED_BLOCK has two: the row kernel when rows are a
+ * whole number of 16-byte packs, a flat periodic kernel otherwise.
  */
 typedef enum ebin_family {
     EBIN_FAMILY_AUTO = -1,            /* only as a request to ebin_plan_create_forced */
