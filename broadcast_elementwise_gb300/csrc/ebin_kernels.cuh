@@ -528,15 +528,15 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
 // as in k_scalar; the other input is X[e mod P] (a row block reused) or
 // X[e / P] (one value per row) for output element e, with P the row length.
 // The row position is decoded once per pack and stepped with selects.
+// Indices are 32-bit: the launcher sends plans of 2^31 elements or more to the
+// general kernel.
 template <class Op, bool DENSE_A, bool PER_ROW, int U>
-__global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int64_t P, FastDiv fP,
-                                                       int32_t wide_i) {
+__global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int32_t P, FastDiv fP) {
     pdl_launch();
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BIn = typename BInOf<Op>::type;
     constexpr int G = 16 / sizeof(In);
-    const bool wide = wide_i != 0;
     const In *A = static_cast<const In *>(p.A);
     const BIn *B = static_cast<const BIn *>(p.B);
     Out *O = static_cast<Out *>(p.out);
@@ -557,13 +557,13 @@ __global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int64_t P, FastD
         for (int u = 0; u < U; ++u) {
             const int64_t g = base + (int64_t)u * kThreads;
             if (g < ng) {
-                const int64_t e0 = g * G;
-                int64_t q = udiv(e0, P, fP, wide);
-                int64_t r = e0 - q * P;
+                const int32_t e0 = (int32_t)(g * G);
+                int32_t q = (int32_t)fastdiv((uint32_t)e0, fP);
+                int32_t r = e0 - q * P;
                 Pack<Out, G> o;
 #pragma unroll
                 for (int k = 0; k < G; ++k) {
-                    const int64_t xi = PER_ROW ? q : r;
+                    const int32_t xi = PER_ROW ? q : r;
                     if constexpr (DENSE_A)
                         o.v[k] = Op::apply(d[u].v[k], Op::loadB(B, xi, p.args), p.args, err);
                     else
@@ -578,8 +578,8 @@ __global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int64_t P, FastD
     }
     for (int64_t e = ng * G + (int64_t)blockIdx.x * kThreads + threadIdx.x; e < p.numel;
          e += (int64_t)gridDim.x * kThreads) {
-        const int64_t q = udiv(e, P, fP, wide);
-        const int64_t xi = PER_ROW ? q : e - q * P;
+        const int32_t q = (int32_t)fastdiv((uint32_t)e, fP);
+        const int32_t xi = PER_ROW ? q : (int32_t)e - q * P;
         if constexpr (DENSE_A) O[e] = Op::apply(A[e], Op::loadB(B, xi, p.args), p.args, err);
         else O[e] = Op::apply(A[xi], D[e], p.args, err);
     }
@@ -937,11 +937,11 @@ cudaError_t run_general(const Launch &L) {
 template <class Op>
 cudaError_t run_periodic(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    const int64_t P = L.g.n[1];
+    if (L.numel >= (1ll << 31)) return run_general<Op>(L);   // 32-bit indices below
+    const int32_t P = (int32_t)L.g.n[1];
     const bool a_dense = L.g.sa[0] == P && L.g.sa[1] == 1;
     const int64_t *xs = a_dense ? L.g.sb : L.g.sa;      // the broadcast input's strides
     const bool per_row = xs[0] == 1 && xs[1] == 0;
-    const int32_t wide = (L.numel >= (1ll << 32) || P >= (1ll << 32)) ? 1 : 0;
     const FastDiv fP = make_fastdiv((uint64_t)P);
     const int64_t ng = L.numel / G;
     int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
@@ -949,16 +949,16 @@ cudaError_t run_periodic(const Launch &L) {
     if (a_dense) {
         if (per_row)
             return launch_pdl(k_periodic<Op, true, true, kUnrollFlat>, grid, kThreads, L.stream,
-                              kargs<Op>(L), P, fP, wide);
+                              kargs<Op>(L), P, fP);
         return launch_pdl(k_periodic<Op, true, false, kUnrollFlat>, grid, kThreads, L.stream,
-                          kargs<Op>(L), P, fP, wide);
+                          kargs<Op>(L), P, fP);
     }
     if constexpr (Op::kPlainB) {
         if (per_row)
             return launch_pdl(k_periodic<Op, false, true, kUnrollFlat>, grid, kThreads, L.stream,
-                              kargs<Op>(L), P, fP, wide);
+                              kargs<Op>(L), P, fP);
         return launch_pdl(k_periodic<Op, false, false, kUnrollFlat>, grid, kThreads, L.stream,
-                          kargs<Op>(L), P, fP, wide);
+                          kargs<Op>(L), P, fP);
     } else {
         return cudaErrorInvalidValue;
     }
