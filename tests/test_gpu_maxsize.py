@@ -62,12 +62,17 @@ CASES = [
     ("Add", "uint8", ((1 << 32) + 7, 1), (1, 2), "general_strided"),
     ("Mul", "float32", (2, 64, (1 << 24) + 4), (1, 64, 1), "inner_vector_outer"),
     ("BitwiseXor", "int64", ((1 << 28) + 5, 4), (4,), "repeated_block"),
+    # rows off the pack width: the periodic kernel's 32-bit indices just below
+    # 2^31 elements, and the general kernel past it
+    ("Add", "uint8", (715827882, 3), (3,), "repeated_block"),
+    ("Sub", "uint8", ((1 << 31) + 3, 3), ((1 << 31) + 3, 1), "repeated_block"),
 ]
 
 
 @pytest.mark.parametrize("op,dtype,sa,sb,family", CASES,
                          ids=["xor_u8_2p32", "add_u8_scalar_2p32", "add_u8_general_wide",
-                              "mul_f32_channel_2p31", "xor_i64_rows_8GiB"])
+                              "mul_f32_channel_2p31", "xor_i64_rows_8GiB",
+                              "add_u8_block3_below_2p31", "sub_u8_rows3_past_2p31"])
 def test_past_32bit_indices(op, dtype, sa, sb, family):
     import broadcast_elementwise_gb300 as eb
     plan = eb.Plan(eb.descriptor(op, dtype), sa, sb)
