@@ -199,9 +199,19 @@ extern "C" ebin_status ebin_descriptor_id(ebin_descriptor_t desc, uint64_t *id) 
 // ------------------------------------------------------------------ planner
 namespace {
 
-int64_t product(const int64_t *s, int r) {
+// Element counts and view spans stay below 2^60, so that every element
+// offset, byte offset and byte size (elements of at most 8 bytes) fits in
+// int64_t; a larger shape is refused before any arithmetic on it.
+constexpr int64_t kMaxElems = EBIN_MAX_ELEMENTS;
+
+// Number of elements of a shape: 0 when an extent is 0 (whatever the others
+// are), -1 when the count reaches kMaxElems.
+int64_t elem_count(const int64_t *s, int r) {
+    for (int i = 0; i < r; ++i)
+        if (s[i] == 0) return 0;
     int64_t n = 1;
-    for (int i = 0; i < r; ++i) n *= s[i];
+    for (int i = 0; i < r; ++i)
+        if (__builtin_mul_overflow(n, s[i], &n) || n >= kMaxElems) return -1;
     return n;
 }
 
@@ -267,19 +277,75 @@ const int64_t *view_strides(const int64_t *shape, const int64_t *st, int rank, b
     for (int i = rank - 1; i >= 0; --i) {
         if (st[i] < 0) *bad = true;
         if (shape[i] > 1 && st[i] != acc) dense = false;
-        acc *= shape[i];
+        // saturates: a shape this large is refused by its element count
+        if (__builtin_mul_overflow(acc, shape[i], &acc)) acc = INT64_MAX;
     }
     return dense ? nullptr : st;
 }
 
-// Storage extent of a view in elements: largest offset + 1 (0 when empty).
+// Storage extent of a view in elements: largest offset + 1 (0 when empty, -1
+// when it reaches kMaxElems).
 int64_t view_span(const int64_t *shape, const int64_t *st, int rank) {
+    for (int i = 0; i < rank; ++i)
+        if (shape[i] == 0) return 0;
     int64_t span = 1;
     for (int i = 0; i < rank; ++i) {
-        if (shape[i] == 0) return 0;
-        span += (shape[i] - 1) * st[i];
+        int64_t t;
+        if (__builtin_mul_overflow(shape[i] - 1, st[i], &t) ||
+            __builtin_add_overflow(span, t, &span) || span >= kMaxElems)
+            return -1;
     }
     return span;
+}
+
+// The traversal of a plan without output elements: nothing is read, so no
+// stride is formed (an empty input's extents may overflow any product).
+Geom empty_geometry() {
+    Geom g{};
+    g.rank = 1;
+    return g;
+}
+
+// Steps 2-4 of planning a non-empty two-input broadcast: element strides
+// (dense, or the view's ta / tb), zero on broadcast dims; output dims of extent
+// 1 dropped; adjacent dims merged where both inputs continue across them.
+// so: output shape; xa / xb: each input right-aligned to rank r (rank ra / rb
+// before alignment).  Every product stays below the element-count bound.
+Geom coalesce2(const int64_t *so, const int64_t *xa, const int64_t *xb, int r, int ra, int rb,
+               const int64_t *ta, const int64_t *tb) {
+    int64_t st_a[kMaxRank], st_b[kMaxRank];
+    int64_t acc_a = 1, acc_b = 1;
+    for (int i = r - 1; i >= 0; --i) {
+        const int ja = i - (r - ra), jb = i - (r - rb);
+        st_a[i] = xa[i] == 1 ? 0 : (ta ? ta[ja] : acc_a);
+        st_b[i] = xb[i] == 1 ? 0 : (tb ? tb[jb] : acc_b);
+        acc_a *= xa[i];
+        acc_b *= xb[i];
+    }
+    Geom g{};
+    int k = 0;
+    for (int i = 0; i < r; ++i) {
+        if (so[i] == 1) continue;
+        if (k > 0 && g.sa[k - 1] == st_a[i] * so[i] && g.sb[k - 1] == st_b[i] * so[i]) {
+            // the previous (outer) dim continues this one: fold it in
+            g.n[k - 1] *= so[i];
+            g.sa[k - 1] = st_a[i];
+            g.sb[k - 1] = st_b[i];
+            continue;
+        }
+        g.n[k] = so[i];
+        g.sa[k] = st_a[i];
+        g.sb[k] = st_b[i];
+        ++k;
+    }
+    if (k == 0) {  // a single element
+        g.n[0] = 1;
+        g.sa[0] = 1;
+        g.sb[0] = 1;
+        k = 1;
+    }
+    g.rank = k;
+    return g;
 }
 
 ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
@@ -340,6 +406,12 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
         for (int i = 0; i < r; ++i)
             if (so[i] != sa[i]) return EBIN_ERR_INCOMPATIBLE_SHAPES;
     }
+    const int64_t numel = elem_count(so, r), numel_a = elem_count(sa, ra);
+    const int64_t numel_b = d.attrs.with_scalar ? 0 : elem_count(sb, rb);
+    const int64_t span_a = ta ? view_span(sa, ta, ra) : numel_a;
+    const int64_t span_b = tb ? view_span(sb, tb, rb) : numel_b;
+    if (numel < 0 || numel_a < 0 || numel_b < 0 || span_a < 0 || span_b < 0)
+        return EBIN_ERR_INVALID_ARG;
 
     auto *p = new ebin_plan_s;
     p->desc_id = d.id;
@@ -354,52 +426,18 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     p->dt_b = d.dt_b;
     p->rank_out = r;
     for (int i = 0; i < r; ++i) p->shape_out[i] = so[i];
-    p->numel = product(so, r);
-    p->numel_a = product(sa, ra);
-    p->numel_b = d.attrs.with_scalar ? 0 : product(sb, rb);
+    p->numel = numel;
+    p->numel_a = numel_a;
+    p->numel_b = numel_b;
     p->strided_a = ta != nullptr;
     p->strided_b = tb != nullptr;
     for (int i = 0; ta && i < ra; ++i) p->strides_a[i] = ta[i];
     for (int i = 0; tb && i < rb; ++i) p->strides_b[i] = tb[i];
-    p->span_a = ta ? view_span(sa, ta, ra) : p->numel_a;
-    p->span_b = tb ? view_span(sb, tb, rb) : p->numel_b;
+    p->span_a = span_a;
+    p->span_b = span_b;
     p->plane = plane;
-
-    // 2. element strides (dense, or the view's), zero on broadcast dims
-    int64_t st_a[kMaxRank], st_b[kMaxRank];
-    int64_t acc_a = 1, acc_b = 1;
-    for (int i = r - 1; i >= 0; --i) {
-        const int ja = i - (r - ra), jb = i - (r - rlb);
-        st_a[i] = xa[i] == 1 ? 0 : (ta ? ta[ja] : acc_a);
-        st_b[i] = xb[i] == 1 ? 0 : (tb ? tb[jb] : acc_b);
-        acc_a *= xa[i];
-        acc_b *= xb[i];
-    }
-    // 3. drop output dims of extent 1;  4. merge adjacent compatible dims
-    Geom g{};
-    int k = 0;
-    for (int i = 0; i < r; ++i) {
-        if (so[i] == 1) continue;
-        if (k > 0 && g.sa[k - 1] == st_a[i] * so[i] && g.sb[k - 1] == st_b[i] * so[i]) {
-            // the previous (outer) dim continues this one: fold it in
-            g.n[k - 1] *= so[i];
-            g.sa[k - 1] = st_a[i];
-            g.sb[k - 1] = st_b[i];
-            continue;
-        }
-        g.n[k] = so[i];
-        g.sa[k] = st_a[i];
-        g.sb[k] = st_b[i];
-        ++k;
-    }
-    if (k == 0) {  // a single element
-        g.n[0] = 1;
-        g.sa[0] = 1;
-        g.sb[0] = 1;
-        k = 1;
-    }
-    g.rank = k;
-    p->g = g;
+    p->g = empty_geometry();
+    if (numel > 0) p->g = coalesce2(so, xa, xb, r, ra, rlb, ta, tb);
 
     // 5. loop family (a with_scalar plan runs its own family or the general one;
     // a mixed-type Pow only the general one)
@@ -445,55 +483,11 @@ int family_of3(const ebin_plan_s &p, int forced, bool *ok) {
     return forced;
 }
 
-ebin_status build_plan3(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
-                        int rb, const int64_t *sc, int rc, int forced, ebin_plan_s **out) {
-    if (ra < 0 || rb < 0 || rc < 0) return EBIN_ERR_INVALID_ARG;
-    if (ra > kMaxRank || rb > kMaxRank || rc > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
-    if ((ra > 0 && !sa) || (rb > 0 && !sb) || (rc > 0 && !sc)) return EBIN_ERR_INVALID_ARG;
-    const int64_t *shp[3] = {sa, sb, sc};
-    const int rk[3] = {ra, rb, rc};
-    for (int k = 0; k < 3; ++k)
-        for (int i = 0; i < rk[k]; ++i)
-            if (shp[k][i] < 0) return EBIN_ERR_INVALID_ARG;
-
-    // 1. right-align and broadcast all three (NumPy rules)
-    const int r = std::max(ra, std::max(rb, rc));
-    int64_t so[kMaxRank], x[3][kMaxRank];
-    for (int i = 0; i < r; ++i) {
-        int64_t o = 1;
-        for (int k = 0; k < 3; ++k) {
-            const int j = i - (r - rk[k]);
-            x[k][i] = j >= 0 ? shp[k][j] : 1;
-            if (x[k][i] == o || x[k][i] == 1) continue;
-            if (o != 1) return EBIN_ERR_INCOMPATIBLE_SHAPES;
-            o = x[k][i];
-        }
-        so[i] = o;
-    }
-
-    auto *p = new ebin_plan_s;
-    p->desc_id = d.id;
-    p->dt = d.dt;
-    p->dt_b = d.dt_b;
-    p->rank_a = ra;
-    p->rank_b = rb;
-    p->rank_c = rc;
-    for (int i = 0; i < ra; ++i) p->shape_a[i] = sa[i];
-    for (int i = 0; i < rb; ++i) p->shape_b[i] = sb[i];
-    for (int i = 0; i < rc; ++i) p->shape_c[i] = sc[i];
-    p->op = d.op;
-    p->attrs = d.attrs;
-    p->out_dt = d.out_dt;
-    p->rank_out = r;
-    for (int i = 0; i < r; ++i) p->shape_out[i] = so[i];
-    p->numel = product(so, r);
-    p->numel_a = product(sa, ra);
-    p->numel_b = product(sb, rb);
-    p->numel_c = product(sc, rc);
-    p->span_a = p->numel_a;
-    p->span_b = p->numel_b;
-
-    // 2. dense strides, zero on broadcast dims;  3. drop unit dims;  4. merge
+// Steps 2-4 of planning a non-empty three-input broadcast: dense strides,
+// zero on broadcast dims; output dims of extent 1 dropped; adjacent dims
+// merged where all three inputs continue across them.  so: output shape;
+// x[k]: input k right-aligned to rank r.
+Geom coalesce3(const int64_t *so, const int64_t (*x)[kMaxRank], int r) {
     int64_t st[3][kMaxRank];
     for (int k = 0; k < 3; ++k) {
         int64_t acc = 1;
@@ -526,7 +520,62 @@ ebin_status build_plan3(const ebin_descriptor_s &d, const int64_t *sa, int ra, c
         n = 1;
     }
     g.rank = n;
-    p->g = g;
+    return g;
+}
+
+ebin_status build_plan3(const ebin_descriptor_s &d, const int64_t *sa, int ra, const int64_t *sb,
+                        int rb, const int64_t *sc, int rc, int forced, ebin_plan_s **out) {
+    if (ra < 0 || rb < 0 || rc < 0) return EBIN_ERR_INVALID_ARG;
+    if (ra > kMaxRank || rb > kMaxRank || rc > kMaxRank) return EBIN_ERR_RANK_TOO_LARGE;
+    if ((ra > 0 && !sa) || (rb > 0 && !sb) || (rc > 0 && !sc)) return EBIN_ERR_INVALID_ARG;
+    const int64_t *shp[3] = {sa, sb, sc};
+    const int rk[3] = {ra, rb, rc};
+    for (int k = 0; k < 3; ++k)
+        for (int i = 0; i < rk[k]; ++i)
+            if (shp[k][i] < 0) return EBIN_ERR_INVALID_ARG;
+
+    // 1. right-align and broadcast all three (NumPy rules)
+    const int r = std::max(ra, std::max(rb, rc));
+    int64_t so[kMaxRank], x[3][kMaxRank];
+    for (int i = 0; i < r; ++i) {
+        int64_t o = 1;
+        for (int k = 0; k < 3; ++k) {
+            const int j = i - (r - rk[k]);
+            x[k][i] = j >= 0 ? shp[k][j] : 1;
+            if (x[k][i] == o || x[k][i] == 1) continue;
+            if (o != 1) return EBIN_ERR_INCOMPATIBLE_SHAPES;
+            o = x[k][i];
+        }
+        so[i] = o;
+    }
+
+    const int64_t numel = elem_count(so, r), numel_a = elem_count(sa, ra),
+                  numel_b = elem_count(sb, rb), numel_c = elem_count(sc, rc);
+    if (numel < 0 || numel_a < 0 || numel_b < 0 || numel_c < 0) return EBIN_ERR_INVALID_ARG;
+
+    auto *p = new ebin_plan_s;
+    p->desc_id = d.id;
+    p->dt = d.dt;
+    p->dt_b = d.dt_b;
+    p->rank_a = ra;
+    p->rank_b = rb;
+    p->rank_c = rc;
+    for (int i = 0; i < ra; ++i) p->shape_a[i] = sa[i];
+    for (int i = 0; i < rb; ++i) p->shape_b[i] = sb[i];
+    for (int i = 0; i < rc; ++i) p->shape_c[i] = sc[i];
+    p->op = d.op;
+    p->attrs = d.attrs;
+    p->out_dt = d.out_dt;
+    p->rank_out = r;
+    for (int i = 0; i < r; ++i) p->shape_out[i] = so[i];
+    p->numel = numel;
+    p->numel_a = numel_a;
+    p->numel_b = numel_b;
+    p->numel_c = numel_c;
+    p->span_a = numel_a;
+    p->span_b = numel_b;
+    p->g = empty_geometry();
+    if (numel > 0) p->g = coalesce3(so, x, r);
     bool ok = true;
     p->family = family_of3(*p, forced, &ok);
     if (!ok) {

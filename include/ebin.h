@@ -31,6 +31,8 @@ extern "C" {
 #endif
 
 #define EBIN_MAX_RANK 8
+/* element counts and view extents stay below this (2^60) */
+#define EBIN_MAX_ELEMENTS (((int64_t)1) << 60)
 #define EBIN_PLAN_CACHE_CAPACITY 8
 #define EBIN_DEFAULT_EPSILON 1e-5f
 
@@ -238,9 +240,13 @@ void ebin_descriptor_destroy(ebin_descriptor_t desc);
  *
  * Shapes: shape_a[rank_a], shape_b[rank_b], dims >= 0.  For BatchNormalization
  * B is [4, C], for BiasPRelu [2, C] and for BiasPReluBN [6, C], with
- * C == shape_a[1] (rank_a >= 2); for Clip B is [2].
+ * C == shape_a[1] (rank_a >= 2); for Clip B is [2].  Each input's element
+ * count and the output's stay below 2^60 (EBIN_MAX_ELEMENTS), so that every
+ * element offset and byte size fits in int64_t; a shape with a zero extent is
+ * empty whatever its other extents.
  *   out            receives a plan reference; release it with ebin_plan_release
- * Errors: INVALID_ARG, RANK_TOO_LARGE, INCOMPATIBLE_SHAPES.
+ * Errors: INVALID_ARG (also an element count of 2^60 or more),
+ * RANK_TOO_LARGE, INCOMPATIBLE_SHAPES.
  */
 ebin_status ebin_plan_create(ebin_descriptor_t desc, const int64_t *shape_a, int rank_a,
                              const int64_t *shape_b, int rank_b, ebin_plan_t *out);
@@ -268,6 +274,8 @@ ebin_status ebin_plan_create_forced(ebin_descriptor_t desc, const int64_t *shape
  * parameter blocks of BatchNormalization, Clip, BiasPRelu and BiasPReluBN, and ignored with
  * with_scalar.  family: EBIN_FAMILY_AUTO (the plan is cached, keyed with the
  * strides) or a forced family as ebin_plan_create_forced (not cached).
+ * A view's storage extent (largest offset + 1) stays below 2^60, as element
+ * counts do (else INVALID_ARG).
  * A strided input is never executed in place: any overlap with out is ALIAS.
  * ebin_execute_host copies each input's whole storage extent (largest offset
  * + 1 elements) and runs strided plans without the chunked pipeline.
@@ -312,6 +320,7 @@ ebin_status ebin_plan_family(ebin_plan_t plan, ebin_family *family);
 /*
  * The coalesced traversal: *rank dims with extents n[] and element strides of
  * A and B (0 on broadcast dims); out is dense.  Arrays hold EBIN_MAX_RANK.
+ * A plan without output elements reports rank 1, n[0] = 0 and zero strides.
  */
 ebin_status ebin_plan_geometry(ebin_plan_t plan, int *rank, int64_t *n, int64_t *stride_a,
                                int64_t *stride_b);

@@ -191,6 +191,45 @@ def test_rank_and_dims_are_checked():
     assert eb.Plan(d, (1,) * 8, (2,) * 8).output_shape == (2,) * 8
 
 
+def test_element_counts_are_bounded():
+    """Every element count and view span stays below 2^60, so that offsets and
+    byte sizes fit in int64: a larger shape is refused, never wrapped.  A zero
+    extent makes any shape empty, whatever its other extents."""
+    d = eb.Descriptor("Add", "float32")
+    big = 1 << 30
+    assert eb.Plan(d, (big, big >> 1), (1,)).numel == 1 << 59
+    for sa, sb in [((big, big), (1,)),                  # exactly 2^60
+                   ((1 << 32, 1 << 32), (1,)),          # 2^64 wraps to 0
+                   ((1 << 40,) * 3, ()),                # wraps past 2^64
+                   ((1,), (1 << 61,)),                  # B alone
+                   ((big, 1), (1, big))]:               # the output alone
+        with pytest.raises(eb.EbinError) as e:
+            eb.Plan(d, sa, sb)
+        assert e.value.code == "invalid_arg", (sa, sb)
+    for sa, sb in [((1 << 40, 1 << 40, 0), (1,)), ((0, 1 << 62, 1 << 62), (1,)),
+                   ((1 << 40, 0, 1 << 40), (1, 1, 1 << 40))]:
+        p = eb.Plan(d, sa, sb)
+        assert p.numel == 0 and p.family == "empty", (sa, sb)
+        assert p.geometry() == ([0], [0], [0])
+    # a view's storage span: (n - 1) * stride summed over its dims
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (2, 64), (64,), strides_a=(1 << 60, 1))
+    assert e.value.code == "invalid_arg"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan(d, (1 << 20, 64), (64,), strides_a=(1 << 62, 1))
+    assert e.value.code == "invalid_arg"
+    assert eb.Plan(d, (0, 64), (64,), strides_a=(1 << 62, 1)).family == "empty"
+    m = eb.Descriptor("MulAdd", "float32")
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan3(m, (big,), (big, 1), (1,))
+    assert e.value.code == "invalid_arg"
+    with pytest.raises(eb.EbinError) as e:
+        eb.Plan3(m, (1,), (1,), (1 << 62, 4))
+    assert e.value.code == "invalid_arg"
+    p = eb.Plan3(m, (1 << 40, 0), (1 << 40, 1), (1,))
+    assert p.numel == 0 and p.family == "empty"
+
+
 def test_forced_families():
     d = eb.Descriptor("Add", "float32")
     for fam in ("general_strided", "inner_vector_outer"):
