@@ -662,11 +662,24 @@ ebin_status cached_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, c
     ebin_plan_s *evicted = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_cache_mu);
-        p->refs.fetch_add(1);  // the cache's reference
-        g_cache.push_front(p);
-        if ((int)g_cache.size() > EBIN_PLAN_CACHE_CAPACITY) {
-            evicted = g_cache.back();
-            g_cache.pop_back();
+        // another thread may have inserted the same key while this one built
+        // its plan: the cache keeps one entry per key, so take that one
+        for (auto it = g_cache.begin(); it != g_cache.end(); ++it) {
+            if (key_equal(**it, d.id, sa, ra, sb, rb, sc, rc, ka, kb)) {
+                evicted = p;   // never shared: freed below
+                p = *it;
+                g_cache.splice(g_cache.begin(), g_cache, it);
+                p->refs.fetch_add(1);
+                break;
+            }
+        }
+        if (!evicted) {
+            p->refs.fetch_add(1);  // the cache's reference
+            g_cache.push_front(p);
+            if ((int)g_cache.size() > EBIN_PLAN_CACHE_CAPACITY) {
+                evicted = g_cache.back();
+                g_cache.pop_back();
+            }
         }
     }
     plan_unref(evicted);

@@ -346,7 +346,10 @@ void ebin_plan_cache_clear(void);
  *   stream      cudaStream_t as void* (NULL = legacy default stream)
  * Returns once the kernel is enqueued.  Invalid elements (integer division by
  * zero, shift counts out of range) do not stop the kernel: they write 0 and set
- * bits in the stream's status word, read with ebin_get_device_status.
+ * bits in the stream's status word, read with ebin_get_device_status.  That
+ * word (4 bytes of device memory per stream handle and device) is allocated by
+ * the first validating operator on the stream and kept until the process
+ * exits; a later stream that reuses the handle's value reuses the word.
  * Stream capture: the launch path makes no allocation and no synchronising
  * call, so executions can be captured into a CUDA graph and replayed.  The one
  * exception is the first validating operator on a stream, which allocates that

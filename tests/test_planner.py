@@ -564,3 +564,24 @@ def test_plans_and_descriptors_from_many_host_threads():
     assert not errors, errors[:3]
     hits, misses, size = eb.ebin_plan_cache_stats()
     assert size <= eb.PLAN_CACHE_CAPACITY
+
+
+def test_concurrent_misses_keep_one_entry_per_key(tmp_path):
+    """Threads that miss on one key at the same time all receive the same
+    plan: the cache keeps a single entry per key.  Python threads are too
+    slow to meet inside the planner, so a C driver (tests/plan_cache_race.c)
+    releases eight pthreads together on each of 2000 new keys."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    libdir = os.path.dirname(os.path.abspath(eb.lib._name))
+    exe = str(tmp_path / "plan_cache_race")
+    subprocess.run([gcc, "-O2", "-I", os.path.join(os.path.dirname(here), "include"),
+                    os.path.join(here, "plan_cache_race.c"), "-o", exe, "-L", libdir,
+                    "-lebin", "-lpthread", "-Wl,-rpath," + libdir], check=True)
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, run.stderr
+    assert int(run.stdout) == 0, "keys that came back as more than one plan: " + run.stdout
