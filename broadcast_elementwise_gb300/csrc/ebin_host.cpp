@@ -1115,7 +1115,13 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
     if (!hp) return host_serial(p, L, host_a, host_b, host_out, dev_a, dev_b, dev_out, s);
 
     const size_t isz = ebin_dtype_size(p.dt), osz = ebin_dtype_size(p.out_dt);
-    const bool a_dense = p.numel_a == p.numel, b_dense = p.numel_b == p.numel;
+    // An operand with stride 1 moves with the output: chunk c reads its range
+    // [off, off + n).  A plain one is copied chunk by chunk; a parameter block
+    // (rows of C, plane elements apart, each moving with the output) is copied
+    // whole, first, and each chunk's kernel starts off elements into it.  An
+    // operand with stride 0 is a scalar, copied whole, first.
+    const bool a_moves = L.g.sa[0] != 0, b_moves = L.B && L.g.sb[0] != 0;
+    const bool b_chunked = b_moves && plain_b(p.op);
     const int64_t want = std::max(kPipeMinChunk, (p.numel + kPipeChunks - 1) / kPipeChunks);
     const int64_t chunk = (want + kPipeGrain - 1) / kPipeGrain * kPipeGrain;
     const int nchunks = (int)((p.numel + chunk - 1) / chunk);
@@ -1126,11 +1132,10 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
     if (!ok(cudaEventRecord(hp->start, s)) || !ok(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
         !ok(cudaStreamWaitEvent(hp->out, hp->start, 0)))
         return EBIN_ERR_CUDA;
-    // a scalar operand is copied whole, first
-    if (!a_dense && !ok(cudaMemcpyAsync(dev_a, host_a, (size_t)p.numel_a * isz,
+    if (!a_moves && !ok(cudaMemcpyAsync(dev_a, host_a, (size_t)p.numel_a * isz,
                                         cudaMemcpyHostToDevice, hp->in)))
         return EBIN_ERR_CUDA;
-    if (host_b && !b_dense && p.numel_b > 0 &&
+    if (L.B && !b_chunked && p.numel_b > 0 &&
         !ok(cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz, cudaMemcpyHostToDevice,
                             hp->in)))
         return EBIN_ERR_CUDA;
@@ -1138,10 +1143,10 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
         const int64_t off = (int64_t)c * chunk;
         const int64_t n = std::min(chunk, p.numel - off);
         const size_t ib = (size_t)off * isz, nb = (size_t)n * isz;
-        if (a_dense && !ok(cudaMemcpyAsync((char *)dev_a + ib, (const char *)host_a + ib, nb,
+        if (a_moves && !ok(cudaMemcpyAsync((char *)dev_a + ib, (const char *)host_a + ib, nb,
                                            cudaMemcpyHostToDevice, hp->in)))
             return EBIN_ERR_CUDA;
-        if (host_b && b_dense &&
+        if (b_chunked &&
             !ok(cudaMemcpyAsync((char *)dev_b + ib, (const char *)host_b + ib, nb,
                                 cudaMemcpyHostToDevice, hp->in)))
             return EBIN_ERR_CUDA;
@@ -1150,8 +1155,8 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
             return EBIN_ERR_CUDA;
         ebin::Launch Lc = L;
         Lc.numel = n;
-        Lc.A = a_dense ? (const void *)((const char *)dev_a + ib) : dev_a;
-        Lc.B = (host_b && b_dense) ? (const void *)((const char *)dev_b + ib) : L.B;
+        Lc.A = a_moves ? (const void *)((const char *)dev_a + ib) : dev_a;
+        Lc.B = b_moves ? (const void *)((const char *)dev_b + ib) : L.B;
         Lc.out = (char *)dev_out + (size_t)off * osz;
         if ((st = launch_counted(Lc)) != EBIN_OK) return st;
         if (!ok(cudaEventRecord(hp->computed[c], s)) ||

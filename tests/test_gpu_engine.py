@@ -134,6 +134,13 @@ def _host_run(op, dtype, a, b, attrs=None, stream=None):
     ("Sub", "int32", (1,), (2500000,), "left_scalar", 3),
     ("Greater", "float16", (2621447,), (2621447,), "contiguous", 3),
     ("Div", "float32", (1 << 21,), (1 << 21,), "contiguous", 2),
+    # parameter blocks whose rows move with the output: copied whole, and each
+    # chunk's kernel starts that chunk's offset into every row
+    ("BatchNormalization", "float32", (1, 2097155), (4, 2097155), "contiguous", 3),
+    ("BiasPRelu", "float16", (1, 2097155), (2, 2097155), "contiguous", 3),
+    ("BiasPReluBN", "bfloat16", (1, 2097155, 1, 1), (6, 2097155), "contiguous", 3),
+    ("Clip", "float32", (2097155,), (2,), "right_scalar", 3),
+    ("PRelu", "float32", (2097155,), (2097155,), "contiguous", 3),
 ])
 def test_execute_host_pipelined(op, dtype, sa, sb, fam, chunks):
     """Large contiguous and scalar plans run as a pipeline of chunks over two
@@ -143,7 +150,8 @@ def test_execute_host_pipelined(op, dtype, sa, sb, fam, chunks):
     got, family, launches = _host_run(op, dtype, a, b)
     assert family == fam and launches == chunks
     otype = "bool" if op == "Greater" else dtype
-    ov = {"float32": np.float32, "bfloat16": np.uint16, "int32": np.int32, "bool": np.uint8}[otype]
+    ov = {"float32": np.float32, "float16": np.float16, "bfloat16": np.uint16, "int32": np.int32,
+          "bool": np.uint8}[otype]
     assert_bits_equal(got.view(ov).reshape(want.shape), want, otype, op)
 
 
