@@ -480,22 +480,48 @@ def binary(op: str, a, b, out=None, *, stream=None, **attrs):
     import torch
     desc = descriptor(op, a.dtype, **attrs)
     plain_b = op not in ("BatchNormalization", "Clip", "BiasPRelu", "BiasPReluBN")
+    if b is not None and b.dtype != torch_dtype(desc.dtype_b):
+        raise ValueError("binary: B is %s; %s on %s takes B of %s"
+                         % (b.dtype, op, desc.dtype, desc.dtype_b))
     if not a.is_cuda:
         if not a.is_pinned() or (b is not None and not b.is_pinned()):
             raise ValueError("binary: CPU tensors must be pinned (tensor.pin_memory())")
         if not a.is_contiguous() or (b is not None and not b.is_contiguous()):
             raise ValueError("binary: pinned CPU tensors must be contiguous")
         plan = Plan(desc, a.shape, b.shape if b is not None else (2,))
-        if out is None:
-            out = torch.empty(plan.output_shape, dtype=torch_dtype(desc.out_dtype)).pin_memory()
+        out = _output(out, plan, desc, None)
         execute_mapped(plan, a, b, out, stream)
         return out
+    if b is not None and b.device != a.device:
+        raise ValueError("binary: A is on %s and B on %s" % (a.device, b.device))
     if b is not None and not plain_b:
         b = b.contiguous()
     ta = None if a.is_contiguous() else tuple(a.stride())
     tb = None if (b is None or b.is_contiguous()) else tuple(b.stride())
     plan = Plan(desc, a.shape, b.shape if b is not None else (2,), strides_a=ta, strides_b=tb)
+    out = _output(out, plan, desc, a.device)
+    with torch.cuda.device(a.device):
+        execute(plan, a, b, out, stream)
+    return out
+
+
+def _output(out, plan, desc, device):
+    """The output tensor of binary(): allocated when None (pinned host memory
+    when device is None), else checked to be what the kernel writes: the
+    output's type and shape, contiguous, on that device (or pinned)."""
+    import torch
+    want = torch_dtype(desc.out_dtype)
     if out is None:
-        out = torch.empty(plan.output_shape, dtype=torch_dtype(desc.out_dtype), device=a.device)
-    execute(plan, a, b, out, stream)
+        if device is None:
+            return torch.empty(plan.output_shape, dtype=want).pin_memory()
+        return torch.empty(plan.output_shape, dtype=want, device=device)
+    if out.dtype != want or tuple(out.shape) != tuple(plan.output_shape):
+        raise ValueError("binary: out is %s %s; the result is %s %s"
+                         % (out.dtype, tuple(out.shape), desc.out_dtype, tuple(plan.output_shape)))
+    if not out.is_contiguous():
+        raise ValueError("binary: out must be contiguous")
+    if device is None and (out.is_cuda or not out.is_pinned()):
+        raise ValueError("binary: out must be a pinned CPU tensor, as the inputs are")
+    if device is not None and out.device != device:
+        raise ValueError("binary: A is on %s and out on %s" % (device, out.device))
     return out

@@ -261,6 +261,35 @@ def test_launch_count_and_binary_helper():
     assert e.shape == (0, 5) and eb.ebin_launch_count() == before + 1
 
 
+def test_binary_helper_checks_operands_before_launching():
+    """binary() refuses, before any launch, an out the kernel would write out of
+    bounds or misread (wrong shape, type, layout or device) and a B of another
+    type or device; a correct out is written in place."""
+    x = torch.randn(4, 8, 32, device="cuda")
+    y = torch.randn(8, 1, device="cuda")
+    before = eb.ebin_launch_count()
+    bad_outs = [torch.empty(4, 8, 31, device="cuda"),                    # too small
+                torch.empty(4, 8, 32, dtype=torch.float16, device="cuda"),
+                torch.empty(4, 32, 8, device="cuda").transpose(1, 2),    # not contiguous
+                torch.empty(4, 8, 32)]                                  # host memory
+    for out in bad_outs:
+        with pytest.raises(ValueError, match="out"):
+            eb.binary("Add", x, y, out)
+    with pytest.raises(ValueError, match="takes B of float32"):
+        eb.binary("Add", x, y.half())
+    with pytest.raises(ValueError, match="B on cpu"):
+        eb.binary("Add", x, y.cpu())
+    bool_out = torch.empty(4, 8, 32, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError, match="result is bool"):
+        eb.binary("Greater", x, y, bool_out)
+    assert eb.ebin_launch_count() == before
+    out = torch.full((4, 8, 32), float("nan"), device="cuda")
+    assert eb.binary("Add", x, y, out) is out
+    torch.cuda.synchronize()
+    want, _ = oracle.run("Add", x.cpu().numpy(), y.cpu().numpy(), "float32")
+    assert_bits_equal(out.cpu().numpy(), want, "float32")
+
+
 def test_plan_outlives_cache_eviction_on_device():
     eb.ebin_plan_cache_clear()
     d = eb.descriptor("Mul", "float32")
@@ -501,6 +530,10 @@ def test_binary_helper_on_pinned_host_tensors():
     assert_bits_equal(out.numpy(), want, "float32", "binary on pinned host tensors")
     with pytest.raises(ValueError, match="pinned"):
         eb.binary("Mul", torch.from_numpy(a), tb)
+    with pytest.raises(ValueError, match="pinned CPU tensor"):
+        eb.binary("Mul", ta, tb, torch.empty(out.shape, device="cuda"))
+    with pytest.raises(ValueError, match="pinned CPU tensor"):
+        eb.binary("Mul", ta, tb, torch.empty(out.shape))
 
 
 @pytest.mark.parametrize("sb", [(1,), (1, 16, 1, 1), (4, 16, 8, 33)])

@@ -585,3 +585,19 @@ def test_concurrent_misses_keep_one_entry_per_key(tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, run.stderr
     assert int(run.stdout) == 0, "keys that came back as more than one plan: " + run.stdout
+
+
+def test_binary_helper_refuses_b_of_another_type():
+    """binary() checks B's type against the descriptor before it touches any
+    memory (no GPU needed): Pow's exponent may differ only when declared."""
+    torch = pytest.importorskip("torch")
+    a = torch.zeros(4, 8)
+    with pytest.raises(ValueError, match="takes B of float32"):
+        eb.binary("Add", a, torch.zeros(8, dtype=torch.float16))
+    with pytest.raises(ValueError, match="takes B of float32"):
+        eb.binary("Pow", a, torch.zeros(8, dtype=torch.int32))
+    with pytest.raises(ValueError, match="takes B of int32"):
+        eb.binary("Pow", a, torch.zeros(8), dtype_b="int32")
+    # the declared exponent type passes the type check (then wants pinned memory)
+    with pytest.raises(ValueError, match="pinned"):
+        eb.binary("Pow", a, torch.zeros(8, dtype=torch.int32), dtype_b="int32")
