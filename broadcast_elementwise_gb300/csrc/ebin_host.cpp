@@ -827,14 +827,18 @@ namespace {
 
 std::mutex g_dev_mu;
 std::map<std::pair<int, uintptr_t>, uint32_t *> g_status_words;
-int g_sm_count[128] = {0};
+std::atomic<int> g_sm_count[128];   // 0 until looked up (host threads race to fill it)
 
 int sm_count(int dev) {
-    if (dev >= 0 && dev < 128 && g_sm_count[dev] > 0) return g_sm_count[dev];
+    const bool slot = dev >= 0 && dev < 128;
+    if (slot) {
+        const int n = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (n > 0) return n;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         n = 1;
-    if (dev >= 0 && dev < 128) g_sm_count[dev] = n;
+    if (slot) g_sm_count[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
