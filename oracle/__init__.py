@@ -83,6 +83,9 @@ def _load():
             lib.oracle_eval.restype = i32
             lib.oracle_output_shape.argtypes = [i32, p, i32, p, i32, p, p]
             lib.oracle_output_shape.restype = i32
+            lib.oracle_eval_params.argtypes = [i32, i32, i32, f32, p, i32, p, i32, p, p, p, p,
+                                               i64, p]
+            lib.oracle_eval_params.restype = i32
             lib.oracle_eval_pow_mixed.argtypes = [i32, i32, p, i32, p, i32, p, p, p, p, i64, p]
             lib.oracle_eval_pow_mixed.restype = i32
             lib.oracle_eval3.argtypes = [i32, i32, p, i32, p, i32, p, i32, p, p, p, p, p, i64]
@@ -195,6 +198,37 @@ def run(op: str, a: np.ndarray, b: np.ndarray | None, dtype: str, *, shape_a=Non
     if rc:
         raise ValueError(RC[rc])
     return out, int(status.value)
+
+
+def run_params(op: str, a: np.ndarray, b: np.ndarray, dtype: str, dtype_b: str, *,
+               eps: float = 1e-5, idx=None):
+    """BatchNormalization / BiasPRelu / BiasPReluBN with the parameter block
+    ``b`` stored as ``dtype_b`` (float32 beside fp16, bf16 or float64 x, or
+    x's own type).  Returns the output like ``run`` (no status bits)."""
+    lib = _load()
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b)
+    if a.dtype != STORAGE[dtype] or b.dtype != STORAGE[dtype_b]:
+        raise TypeError("storage %s / %s does not match %s / %s"
+                        % (a.dtype, b.dtype, dtype, dtype_b))
+    oshape = output_shape(op, a.shape, b.shape)
+    sa, ra = _shape_arr(a.shape)
+    sb, rb = _shape_arr(b.shape)
+    if idx is None:
+        out = np.empty(oshape, STORAGE[dtype])
+        idx_p, n_idx = None, 0
+    else:
+        idx = np.ascontiguousarray(idx, dtype=np.int64)
+        out = np.empty(idx.size, STORAGE[dtype])
+        idx_p, n_idx = idx.ctypes.data, idx.size
+    status = ctypes.c_uint32(0)
+    rc = lib.oracle_eval_params(OPS.index(op), DTYPES.index(dtype), DTYPES.index(dtype_b),
+                                float(eps), sa.ctypes.data, ra, sb.ctypes.data, rb,
+                                a.ctypes.data, b.ctypes.data, out.ctypes.data, idx_p, n_idx,
+                                ctypes.byref(status))
+    if rc:
+        raise ValueError(RC[rc])
+    return out
 
 
 def run_pow_mixed(a: np.ndarray, b: np.ndarray, dtype_a: str, dtype_b: str, *, idx=None):

@@ -604,10 +604,19 @@ int oracle_output_shape(int op, const int64_t *sa, int ra, const int64_t *sb, in
     return OR_OK;
 }
 
-int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_min, int has_max,
-                const int64_t *sa, int ra, const int64_t *sb, int rb,
-                const void *A, const void *B, void *out,
-                const int64_t *idx, int64_t n_idx, uint32_t *status)
+/* A parameter of type tp, widened to binary64 (exactly). */
+static double load_param(const void *B, int tp, int64_t i)
+{
+    return tp == OT_F64 ? load_double(B, i) : (double)load_float(B, tp, i);
+}
+
+/* The evaluation behind oracle_eval and oracle_eval_params: tp is the element
+   type of BatchNormalization's, BiasPRelu's and BiasPReluBN's parameter block
+   (t for every other operator). */
+static int eval2(int op, int t, int tp, int fmod_flag, int direction, float eps, int has_min,
+                 int has_max, const int64_t *sa, int ra, const int64_t *sb, int rb,
+                 const void *A, const void *B, void *out,
+                 const int64_t *idx, int64_t n_idx, uint32_t *status)
 {
     int64_t so[OR_MAX_RANK], sta[OR_MAX_RANK], stb[OR_MAX_RANK];
     int r;
@@ -634,24 +643,24 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
         if (op == OR_BATCHNORM && t == OT_F64) {     /* the same formula in binary64 */
             int64_t C = sb[1], c = channel_of(f, so, r);
             double x = load_double(A, oa);
-            double scale = load_double(B, 0 * C + c), bias = load_double(B, 1 * C + c);
-            double mean = load_double(B, 2 * C + c), var = load_double(B, 3 * C + c);
+            double scale = load_param(B, tp, 0 * C + c), bias = load_param(B, tp, 1 * C + c);
+            double mean = load_param(B, tp, 2 * C + c), var = load_param(B, tp, 3 * C + c);
             store_double(out, k, (x - mean) / sqrt(var + (double)eps) * scale + bias);
             continue;
         }
         if (op == OR_BIAS_PRELU && t == OT_F64) {
             int64_t C = sb[1], c = channel_of(f, so, r);
-            double y = load_double(A, oa) + load_double(B, c);
-            if (!(y >= 0.0)) y = load_double(B, C + c) * y;
+            double y = load_double(A, oa) + load_param(B, tp, c);
+            if (!(y >= 0.0)) y = load_param(B, tp, C + c) * y;
             store_double(out, k, y);
             continue;
         }
         if (op == OR_BIAS_PRELU_BN && t == OT_F64) {
             int64_t C = sb[1], c = channel_of(f, so, r);
-            double y = load_double(A, oa) + load_double(B, c);
-            if (!(y >= 0.0)) y = load_double(B, C + c) * y;
-            double scale = load_double(B, 2 * C + c), bn_bias = load_double(B, 3 * C + c);
-            double mean = load_double(B, 4 * C + c), var = load_double(B, 5 * C + c);
+            double y = load_double(A, oa) + load_param(B, tp, c);
+            if (!(y >= 0.0)) y = load_param(B, tp, C + c) * y;
+            double scale = load_param(B, tp, 2 * C + c), bn_bias = load_param(B, tp, 3 * C + c);
+            double mean = load_param(B, tp, 4 * C + c), var = load_param(B, tp, 5 * C + c);
             store_double(out, k, (y - mean) / sqrt(var + (double)eps) * scale + bn_bias);
             continue;
         }
@@ -665,10 +674,10 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
         if (op == OR_BATCHNORM) {
             int64_t C = sb[1], c = channel_of(f, so, r);
             float x = load_float(A, t, oa);
-            float scale = load_float(B, t, 0 * C + c);
-            float bias = load_float(B, t, 1 * C + c);
-            float mean = load_float(B, t, 2 * C + c);
-            float var = load_float(B, t, 3 * C + c);
+            float scale = load_float(B, tp, 0 * C + c);
+            float bias = load_float(B, tp, 1 * C + c);
+            float mean = load_float(B, tp, 2 * C + c);
+            float var = load_float(B, tp, 3 * C + c);
             float y = (x - mean) / sqrtf(var + eps) * scale + bias;
             store_float(out, t, k, y);
             continue;
@@ -677,8 +686,8 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             /* y = x + bias[c]; y >= 0 ? y : slope[c] * y; binary32 steps, one
                rounding to x's type at the end */
             int64_t C = sb[1], c = channel_of(f, so, r);
-            float y = load_float(A, t, oa) + load_float(B, t, c);
-            if (!(y >= 0.0f)) y = load_float(B, t, C + c) * y;
+            float y = load_float(A, t, oa) + load_float(B, tp, c);
+            if (!(y >= 0.0f)) y = load_float(B, tp, C + c) * y;
             store_float(out, t, k, y);
             continue;
         }
@@ -686,12 +695,12 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
             /* bias add, PReLU, then the BatchNormalization formula, binary32
                steps in the order written; one rounding to x's type */
             int64_t C = sb[1], c = channel_of(f, so, r);
-            float y = load_float(A, t, oa) + load_float(B, t, c);
-            if (!(y >= 0.0f)) y = load_float(B, t, C + c) * y;
-            float scale = load_float(B, t, 2 * C + c);
-            float bn_bias = load_float(B, t, 3 * C + c);
-            float mean = load_float(B, t, 4 * C + c);
-            float var = load_float(B, t, 5 * C + c);
+            float y = load_float(A, t, oa) + load_float(B, tp, c);
+            if (!(y >= 0.0f)) y = load_float(B, tp, C + c) * y;
+            float scale = load_float(B, tp, 2 * C + c);
+            float bn_bias = load_float(B, tp, 3 * C + c);
+            float mean = load_float(B, tp, 4 * C + c);
+            float var = load_float(B, tp, 5 * C + c);
             y = (y - mean) / sqrtf(var + eps) * scale + bn_bias;
             store_float(out, t, k, y);
             continue;
@@ -739,6 +748,34 @@ int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_
         }
     }
     return OR_OK;
+}
+
+int oracle_eval(int op, int t, int fmod_flag, int direction, float eps, int has_min, int has_max,
+                const int64_t *sa, int ra, const int64_t *sb, int rb,
+                const void *A, const void *B, void *out,
+                const int64_t *idx, int64_t n_idx, uint32_t *status)
+{
+    return eval2(op, t, t, fmod_flag, direction, eps, has_min, has_max, sa, ra, sb, rb, A, B, out,
+                 idx, n_idx, status);
+}
+
+/*
+ * BatchNormalization, BiasPRelu and BiasPReluBN with the parameter block in
+ * binary32 while x is fp16, bf16 or binary64 (the block is "in x's dtype or
+ * fp32").  Reading: each parameter enters the compute type as it is -- exactly,
+ * since binary32 widens exactly into binary32 and binary64 -- so the result is
+ * the same-type formula with the parameters not first rounded to x's type.
+ * tp == t is the same-type operator.  Other operators or types: OR_TYPE.
+ */
+int oracle_eval_params(int op, int t, int tp, float eps, const int64_t *sa, int ra,
+                       const int64_t *sb, int rb, const void *A, const void *B, void *out,
+                       const int64_t *idx, int64_t n_idx, uint32_t *status)
+{
+    *status = 0;
+    if (op != OR_BATCHNORM && op != OR_BIAS_PRELU && op != OR_BIAS_PRELU_BN) return OR_TYPE;
+    if (tp != t && !(tp == OT_F32 && (t == OT_F16 || t == OT_BF16 || t == OT_F64)))
+        return OR_TYPE;
+    return eval2(op, t, tp, 0, 0, eps, 1, 1, sa, ra, sb, rb, A, B, out, idx, n_idx, status);
 }
 
 /*

@@ -910,6 +910,102 @@ def test_bias_prelu_bn_shapes():
             oracle.run("BiasPReluBN", x, np.zeros(bad, np.float32), "float32")
 
 
+# ------------------------------------------------------- float32 parameter blocks
+# The BatchNormalization block is "in x's dtype or fp32"; BiasPRelu and
+# BiasPReluBN take the same choice.  With fp32 parameters beside fp16/bf16 x,
+# each parameter enters the binary32 chain as it is (not rounded to x's type).
+
+PARAM_ROWS = {"BatchNormalization": 4, "BiasPRelu": 2, "BiasPReluBN": 6}
+
+
+def _f32_params(op, C, seed):
+    rows = [datagen.normal(seed, i + 1, C) for i in range(PARAM_ROWS[op])]
+    rows[-1] = datagen.uniform(seed, 9, C, 0.1, 2.0)     # var (BN rows) stays positive
+    if op == "BiasPRelu":
+        rows[1] = datagen.uniform(seed, 8, C, -0.5, 0.5)
+    if op == "BiasPReluBN":
+        rows[1] = datagen.uniform(seed, 8, C, -0.5, 0.5)
+    return np.stack(rows).astype(np.float32)
+
+
+def _torch_chain(op, xf, P, eps):
+    """The operator's binary32 steps on torch float32 tensors, in the order
+    written; each torch op rounds on its own."""
+    C = P.shape[1]
+    col = lambda i: P[i].view(1, C, *([1] * (xf.dim() - 2)))
+    if op == "BatchNormalization":
+        return (xf - col(2)) / torch.sqrt(col(3) + torch.tensor(eps)) * col(0) + col(1)
+    t = xf + col(0)
+    t = torch.where(t >= 0, t, col(1) * t)
+    if op == "BiasPRelu":
+        return t
+    return (t - col(4)) / torch.sqrt(col(5) + torch.tensor(eps)) * col(2) + col(3)
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16"])
+@pytest.mark.parametrize("op", ["BatchNormalization", "BiasPRelu", "BiasPReluBN"])
+def test_float32_parameters_match_the_torch_chain(op, dtype):
+    """16-bit x, binary32 parameters: the torch float32 chain on x widened and
+    the parameters as given, rounded once to x's type (torch rounds to
+    nearest even)."""
+    C = 7
+    x = datagen.make("normal", dtype, (3, C, 5, 6), 36, 0)
+    x.reshape(-1)[:SPECIALS.size] = datagen.float_to(SPECIALS, dtype)
+    P = _f32_params(op, C, 36)
+    eps = np.float32(1e-5)
+    got = oracle.run_params(op, x, P, dtype, "float32", eps=float(eps))
+    tx = torch.from_numpy(x.view(np.int16).copy()).view(
+        torch.bfloat16 if dtype == "bfloat16" else torch.float16).float()
+    y = _torch_chain(op, tx, torch.from_numpy(P), eps)
+    if dtype == "bfloat16":
+        want = y.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    else:
+        want = y.to(torch.float16).numpy()
+    assert_bits_equal(got, want, dtype, "%s fp32 parameters" % op)
+    # the parameters are not first rounded to x's type: the 16-bit block differs
+    same, _ = oracle.run(op, x, datagen.float_to(P, dtype), dtype, eps=float(eps))
+    assert (got.view(np.uint16) != same.view(np.uint16)).any()
+
+
+@pytest.mark.parametrize("op", ["BatchNormalization", "BiasPRelu", "BiasPReluBN"])
+def test_float32_parameters_beside_float64(op):
+    """float64 x, binary32 parameters widened exactly: the numpy float64 chain."""
+    C = 5
+    x = datagen.make("normal", "float64", (2, C, 9), 37, 0)
+    P = _f32_params(op, C, 37)
+    got = oracle.run_params(op, x, P, "float64", "float32", eps=1e-5)
+    y = _torch_chain(op, torch.from_numpy(x), torch.from_numpy(P.astype(np.float64)),
+                     float(np.float32(1e-5))).numpy()
+    assert_bits_equal(got, y, "float64", "%s fp32 parameters, float64 x" % op)
+
+
+@pytest.mark.parametrize("op", ["BatchNormalization", "BiasPRelu", "BiasPReluBN"])
+def test_float32_parameters_exact_in_x_type_equal_the_same_type_block(op):
+    """Parameters that x's type holds exactly give the same-type operator's
+    result, bit for bit; and a block of x's own type is that operator."""
+    C = 6
+    for dtype in ("float16", "bfloat16"):
+        x = datagen.make("normal", dtype, (4, C, 11), 38, 0)
+        Bx = datagen.float_to(_f32_params(op, C, 38), dtype)
+        P = (Bx.astype(np.float32) if dtype == "float16" else bf16_to_f32(Bx)).astype(np.float32)
+        want, _ = oracle.run(op, x, Bx, dtype)
+        assert_bits_equal(oracle.run_params(op, x, P, dtype, "float32"), want, dtype, op)
+        assert_bits_equal(oracle.run_params(op, x, Bx, dtype, dtype), want, dtype, op)
+
+
+def test_float32_parameters_refusals():
+    x16 = np.zeros((2, 3, 4), np.float16)
+    P = np.zeros((4, 3), np.float32)
+    with pytest.raises(ValueError, match="type"):
+        oracle.run_params("Add", x16, np.zeros((4,), np.float32), "float16", "float32")
+    with pytest.raises(ValueError, match="type"):      # fp16 parameters beside fp32 x
+        oracle.run_params("BatchNormalization", np.zeros((2, 3, 4), np.float32),
+                          P.astype(np.float16), "float32", "float16")
+    with pytest.raises(ValueError, match="shapes"):
+        oracle.run_params("BatchNormalization", x16, np.zeros((4, 2), np.float32), "float16",
+                          "float32")
+
+
 # --------------------------------------------------------------------------- MulAdd
 # 0verkilll/onnx ops, MulAddOp: y = (a * b) + c, shapes as the unfused Mul + Add.
 
