@@ -347,7 +347,9 @@ class Descriptor:
                  epsilon: float = 1e-5, has_min: bool = True, has_max: bool = True,
                  scalar_b: float | None = None, dtype_b=None):
         """``scalar_b`` given: ncnn binaryop's with_scalar, B is that value.
-        ``dtype_b``: B's type where it may differ from A's (Pow's exponent)."""
+        ``dtype_b``: B's type where it may differ from A's (Pow's exponent;
+        a float32 parameter block of BatchNormalization, BiasPRelu or
+        BiasPReluBN beside float16, bfloat16 or float64 x)."""
         self.op = op
         self.dtype = DTYPE_NAMES[_dtype_code(dtype)]
         self.dtype_b = self.dtype if dtype_b is None else DTYPE_NAMES[_dtype_code(dtype_b)]
@@ -478,6 +480,9 @@ def binary(op: str, a, b, out=None, *, stream=None, **attrs):
     ``out`` is allocated pinned); synchronise ``stream`` before reading it.
     """
     import torch
+    if (b is not None and op in ("BatchNormalization", "BiasPRelu", "BiasPReluBN")
+            and b.dtype != a.dtype and "dtype_b" not in attrs):
+        attrs["dtype_b"] = b.dtype      # a float32 parameter block beside 16-bit or float64 x
     desc = descriptor(op, a.dtype, **attrs)
     plain_b = op not in ("BatchNormalization", "Clip", "BiasPRelu", "BiasPReluBN")
     if b is not None and b.dtype != torch_dtype(desc.dtype_b):

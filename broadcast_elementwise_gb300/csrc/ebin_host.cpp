@@ -120,6 +120,12 @@ bool plain_b(int op) {
            op != EBIN_OP_BIAS_PRELU_BN;
 }
 
+// B is a per-channel parameter block of rows of C (BatchNormalization,
+// BiasPRelu, BiasPReluBN).
+bool param_block(int op) {
+    return op == EBIN_OP_BATCHNORM || op == EBIN_OP_BIAS_PRELU || op == EBIN_OP_BIAS_PRELU_BN;
+}
+
 // Operators with three inputs (planned by ebin_plan_create3).
 bool ternary(int op) { return op == EBIN_OP_MULADD; }
 
@@ -155,10 +161,13 @@ extern "C" ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_
     ebin_attrs a{0, 0, EBIN_DEFAULT_EPSILON, 1, 1, 0, 0.0f};
     if (attrs) a = *attrs;
     // A and B share a type, except Pow's exponent, which may be any non-BOOL
-    // type ("typed scalar adapters" for the other legal signatures)
+    // type ("typed scalar adapters" for the other legal signatures), and the
+    // parameter block of BatchNormalization, BiasPRelu and BiasPReluBN, which
+    // may be binary32 beside a 16-bit or binary64 x
     if (!type_legal(op, dtype_a)) return EBIN_ERR_UNSUPPORTED_TYPE;
     if (dtype_a != dtype_b &&
-        !(op == EBIN_OP_POW && dt_class(dtype_b) >= 0 && dtype_b != EBIN_BOOL))
+        !(op == EBIN_OP_POW && dt_class(dtype_b) >= 0 && dtype_b != EBIN_BOOL) &&
+        !(param_block(op) && dtype_b == EBIN_FLOAT32 && is_float(dtype_a)))
         return EBIN_ERR_UNSUPPORTED_TYPE;
     if (op == EBIN_OP_MOD) {
         // "Mod tracks schema version 28 while retaining minimum opset 10";
@@ -443,7 +452,7 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     // a mixed-type Pow only the general one)
     bool ok = true;
     p->family = family_of(*p, forced, &ok);
-    if (ok && p->dt_b != p->dt && p->numel > 0) {
+    if (ok && d.op == EBIN_OP_POW && p->dt_b != p->dt && p->numel > 0) {
         ok = forced == EBIN_FAMILY_AUTO || forced == EBIN_FAMILY_GENERAL_STRIDED;
         p->family = ebin::FAM_GENERAL_STRIDED;
     }
@@ -1119,6 +1128,7 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
     if (!hp) return host_serial(p, L, host_a, host_b, host_out, dev_a, dev_b, dev_out, s);
 
     const size_t isz = ebin_dtype_size(p.dt), osz = ebin_dtype_size(p.out_dt);
+    const size_t isz_b = ebin_dtype_size(p.dt_b);   // binary32 parameters beside 16-bit x
     // An operand with stride 1 moves with the output: chunk c reads its range
     // [off, off + n).  A plain one is copied chunk by chunk; a parameter block
     // (rows of C, plane elements apart, each moving with the output) is copied
@@ -1140,18 +1150,19 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
                                         cudaMemcpyHostToDevice, hp->in)))
         return EBIN_ERR_CUDA;
     if (L.B && !b_chunked && p.numel_b > 0 &&
-        !ok(cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz, cudaMemcpyHostToDevice,
+        !ok(cudaMemcpyAsync(dev_b, host_b, (size_t)p.numel_b * isz_b, cudaMemcpyHostToDevice,
                             hp->in)))
         return EBIN_ERR_CUDA;
     for (int c = 0; c < nchunks; ++c) {
         const int64_t off = (int64_t)c * chunk;
         const int64_t n = std::min(chunk, p.numel - off);
         const size_t ib = (size_t)off * isz, nb = (size_t)n * isz;
+        const size_t ib_b = (size_t)off * isz_b, nb_b = (size_t)n * isz_b;
         if (a_moves && !ok(cudaMemcpyAsync((char *)dev_a + ib, (const char *)host_a + ib, nb,
                                            cudaMemcpyHostToDevice, hp->in)))
             return EBIN_ERR_CUDA;
         if (b_chunked &&
-            !ok(cudaMemcpyAsync((char *)dev_b + ib, (const char *)host_b + ib, nb,
+            !ok(cudaMemcpyAsync((char *)dev_b + ib_b, (const char *)host_b + ib_b, nb_b,
                                 cudaMemcpyHostToDevice, hp->in)))
             return EBIN_ERR_CUDA;
         if (!ok(cudaEventRecord(hp->copied[c], hp->in)) ||
@@ -1160,7 +1171,7 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
         ebin::Launch Lc = L;
         Lc.numel = n;
         Lc.A = a_moves ? (const void *)((const char *)dev_a + ib) : dev_a;
-        Lc.B = b_moves ? (const void *)((const char *)dev_b + ib) : L.B;
+        Lc.B = b_moves ? (const void *)((const char *)dev_b + ib_b) : L.B;
         Lc.out = (char *)dev_out + (size_t)off * osz;
         if ((st = launch_counted(Lc)) != EBIN_OK) return st;
         if (!ok(cudaEventRecord(hp->computed[c], s)) ||

@@ -234,9 +234,11 @@ __global__ void __launch_bounds__(kThreads) k_contiguous(KArgs p) {
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
+    using BIn = typename BInOf<Op>::type;
+    static_assert(!Op::kPlainB || std::is_same_v<BIn, In>, "packed B shares A's type");
     constexpr int G = 16 / sizeof(In);
     const In *A = static_cast<const In *>(p.A);
-    const In *B = static_cast<const In *>(p.B);
+    const BIn *B = static_cast<const BIn *>(p.B);
     Out *O = static_cast<Out *>(p.out);
     const int64_t ng = p.numel / G;
     uint32_t err = 0;
@@ -286,11 +288,13 @@ __global__ void __launch_bounds__(kThreads) k_scalar(KArgs p) {
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BV = typename Op::BV;
+    using BIn = typename BInOf<Op>::type;
+    static_assert(!SCALAR_A || std::is_same_v<BIn, In>, "a left scalar B shares A's type");
     constexpr int G = 16 / sizeof(In);
     const In *A = static_cast<const In *>(p.A);
-    const In *B = static_cast<const In *>(p.B);
+    const BIn *B = static_cast<const BIn *>(p.B);
     Out *O = static_cast<Out *>(p.out);
-    const In *D = SCALAR_A ? B : A;
+    const In *D = SCALAR_A ? static_cast<const In *>(p.B) : A;
     In sa{};
     BV sb{};
     if constexpr (SCALAR_A) sa = A[0];

@@ -646,16 +646,19 @@ template <class C> struct BiasSlope {
     C bias, slope;
 };
 
-template <class T> struct OpBiasPRelu {
+// P: the parameter block's element type, x's own or binary32 beside a 16-bit
+// or binary64 x (a float32 runtime's parameters), widened exactly to C.
+template <class T, class P = T> struct OpBiasPRelu {
     using In = T;
     using Out = T;
+    using BIn = P;
     using C = typename Tr<T>::C;
     using BV = BiasSlope<C>;
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = is_fp_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> && is_fp_v<P>;
     static constexpr bool kValidates = false;
-    __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
-        return BV{Tr<T>::in(B[off]), Tr<T>::in(B[off + p.plane])};
+    __device__ __forceinline__ static BV loadB(const P *B, int64_t off, const OpArgs &p) {
+        return BV{(C)Tr<P>::in(B[off]), (C)Tr<P>::in(B[off + p.plane])};
     }
     __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
         const C t = add_rn(Tr<T>::in(a), q.bias);
@@ -690,23 +693,25 @@ template <class C> struct BNParams {
     C scale, bias, mean, d;
 };
 
-template <class T> struct OpBN {
+// P: the parameter block's element type, as for BiasPRelu.
+template <class T, class P = T> struct OpBN {
     using In = T;
     using Out = T;
+    using BIn = P;
     using C = typename Tr<T>::C;
     using BV = BNParams<C>;
     // at least four rows per thread in the row kernel (x[8,64,256,256]:
     // 30.9 -> 30.2 us on GB300; six rows 30.4)
     static constexpr int kMinRows = 4;
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = is_fp_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> && is_fp_v<P>;
     static constexpr bool kValidates = false;
-    __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
+    __device__ __forceinline__ static BV loadB(const P *B, int64_t off, const OpArgs &p) {
         BV r;
-        r.scale = Tr<T>::in(B[off]);
-        r.bias = Tr<T>::in(B[off + p.plane]);
-        r.mean = Tr<T>::in(B[off + 2 * p.plane]);
-        const C var = Tr<T>::in(B[off + 3 * p.plane]);
+        r.scale = (C)Tr<P>::in(B[off]);
+        r.bias = (C)Tr<P>::in(B[off + p.plane]);
+        r.mean = (C)Tr<P>::in(B[off + 2 * p.plane]);
+        const C var = (C)Tr<P>::in(B[off + 3 * p.plane]);
         r.d = sqrt_rn(add_rn(var, (C)p.eps));
         return r;
     }
@@ -729,23 +734,25 @@ template <class C> struct ChainParams {
     C bias, slope, scale, bn_bias, mean, d;
 };
 
-template <class T> struct OpBiasPReluBN {
+// P: the parameter block's element type, as for BiasPRelu.
+template <class T, class P = T> struct OpBiasPReluBN {
     using In = T;
     using Out = T;
+    using BIn = P;
     using C = typename Tr<T>::C;
     using BV = ChainParams<C>;
     static constexpr int kMinRows = 4;   // as BatchNormalization (32.6 -> 32.1 us)
     static constexpr bool kPlainB = false;
-    static constexpr bool kLegal = is_fp_v<T>;
+    static constexpr bool kLegal = is_fp_v<T> && is_fp_v<P>;
     static constexpr bool kValidates = false;
-    __device__ __forceinline__ static BV loadB(const T *B, int64_t off, const OpArgs &p) {
+    __device__ __forceinline__ static BV loadB(const P *B, int64_t off, const OpArgs &p) {
         BV r;
-        r.bias = Tr<T>::in(B[off]);
-        r.slope = Tr<T>::in(B[off + p.plane]);
-        r.scale = Tr<T>::in(B[off + 2 * p.plane]);
-        r.bn_bias = Tr<T>::in(B[off + 3 * p.plane]);
-        r.mean = Tr<T>::in(B[off + 4 * p.plane]);
-        r.d = sqrt_rn(add_rn(Tr<T>::in(B[off + 5 * p.plane]), (C)p.eps));
+        r.bias = (C)Tr<P>::in(B[off]);
+        r.slope = (C)Tr<P>::in(B[off + p.plane]);
+        r.scale = (C)Tr<P>::in(B[off + 2 * p.plane]);
+        r.bn_bias = (C)Tr<P>::in(B[off + 3 * p.plane]);
+        r.mean = (C)Tr<P>::in(B[off + 4 * p.plane]);
+        r.d = sqrt_rn(add_rn((C)Tr<P>::in(B[off + 5 * p.plane]), (C)p.eps));
         return r;
     }
     __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {

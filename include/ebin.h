@@ -80,7 +80,8 @@ typedef enum ebin_op {
     EBIN_OP_BITWISE_XOR = 16,
     EBIN_OP_BITSHIFT = 17,        /* attrs.direction */
     EBIN_OP_PRELU = 18,           /* B = slope, broadcast one way to A */
-    EBIN_OP_BATCHNORM = 19,       /* inference; B = [4, C]: scale, bias, mean, var rows */
+    EBIN_OP_BATCHNORM = 19,       /* inference; B = [4, C]: scale, bias, mean, var rows,
+                                     in A's type or FLOAT32 */
     EBIN_OP_CLIP = 20,            /* B = [2]: {min, max}; attrs.clip_has_min/max */
     /* ncnn operators.md, binaryop operation types 4, 5, 7, 8 (0-3 are ADD..DIV
      * above, 6 = POW is EBIN_OP_POW): */
@@ -193,7 +194,14 @@ typedef struct ebin_plan_s *ebin_plan_t;
  *
  *   op, opset      operator and the node's opset (only Mod reads opset: 10..28)
  *   attrs          may be NULL (defaults above); copied, not retained
- *   dtype_a/b      element types of A and B; they must be equal
+ *   dtype_a/b      element types of A and B; they must be equal, except:
+ *                  Pow's exponent B may be any non-BOOL type, and the
+ *                  parameter block B of BATCHNORM, BIAS_PRELU and
+ *                  BIAS_PRELU_BN may be FLOAT32 beside a FLOAT16, BFLOAT16
+ *                  or DOUBLE A (BatchNormalizationOp keeps its parameters in
+ *                  a float32 runtime; they enter the chain unrounded,
+ *                  widened exactly to DOUBLE for a DOUBLE A).  Such a plan
+ *                  keeps the loop family of a same-type block.
  *   out            receives the new descriptor; the caller owns it
  * Errors: INVALID_ARG (out NULL), UNSUPPORTED_OP, UNSUPPORTED_TYPE, INVALID_ATTR.
  */

@@ -111,12 +111,13 @@ def test_execute_host_round_trip():
 
 def _host_run(op, dtype, a, b, attrs=None, stream=None):
     """ebin_execute_host with pinned host buffers; returns (out, family, launches)."""
-    p = eb.Plan(eb.descriptor(op, dtype, **(attrs or {})), a.shape, b.shape)
+    desc = eb.descriptor(op, dtype, **(attrs or {}))
+    p = eb.Plan(desc, a.shape, b.shape)
     view = {1: np.uint8, 2: np.int16, 4: np.int32, 8: np.int64}
-    isz = eb.ITEMSIZE[dtype]
-    osz = eb.ITEMSIZE[eb.descriptor(op, dtype, **(attrs or {})).out_dtype]
+    isz, isz_b = eb.ITEMSIZE[dtype], eb.ITEMSIZE[desc.dtype_b]
+    osz = eb.ITEMSIZE[desc.out_dtype]
     ha = torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(view[isz]).copy()).pin_memory()
-    hb = torch.from_numpy(np.ascontiguousarray(b).reshape(-1).view(view[isz]).copy()).pin_memory()
+    hb = torch.from_numpy(np.ascontiguousarray(b).reshape(-1).view(view[isz_b]).copy()).pin_memory()
     ho = torch.empty(p.numel * osz, dtype=torch.uint8).pin_memory()
     da, db = torch.empty_like(ha, device="cuda"), torch.empty_like(hb, device="cuda")
     do = torch.empty(p.numel * osz, dtype=torch.uint8, device="cuda")
@@ -153,6 +154,43 @@ def test_execute_host_pipelined(op, dtype, sa, sb, fam, chunks):
     ov = {"float32": np.float32, "float16": np.float16, "bfloat16": np.uint16, "int32": np.int32,
           "bool": np.uint8}[otype]
     assert_bits_equal(got.view(ov).reshape(want.shape), want, otype, op)
+
+
+@pytest.mark.parametrize("op,dtype,sa,sb", [
+    ("BatchNormalization", "float16", (1, 2097155), (4, 2097155)),
+    ("BiasPReluBN", "bfloat16", (1, 2097155, 1, 1), (6, 2097155)),
+    ("BiasPRelu", "float64", (1, 2097155), (2, 2097155)),
+])
+def test_execute_host_pipelined_float32_block(op, dtype, sa, sb):
+    """A float32 parameter block that moves with a 16-bit or float64 output:
+    copied whole with its own element size, and each chunk's kernel starts that
+    chunk's offset, in float32 elements, into every row."""
+    a, _ = inputs_for(op, dtype, sa, sb, seed=83)
+    _, b = inputs_for(op, "float32", sa, sb, seed=83)
+    want = oracle.run_params(op, a, b, dtype, "float32")
+    got, family, launches = _host_run(op, dtype, a, b, attrs={"dtype_b": "float32"})
+    assert family == "contiguous" and launches == 3
+    ov = {"float16": np.float16, "bfloat16": np.uint16, "float64": np.float64}[dtype]
+    assert_bits_equal(got.view(ov).reshape(want.shape), want, dtype, op)
+
+
+def test_binary_helper_with_float32_block():
+    """binary() takes a float32 parameter block beside bfloat16 x on the device
+    and on pinned host memory (the block's type read from the tensor)."""
+    sa, sb = (2, 64, 30, 40), (6, 64)
+    a, _ = inputs_for("BiasPReluBN", "bfloat16", sa, sb, seed=84)
+    _, b = inputs_for("BiasPReluBN", "float32", sa, sb, seed=84)
+    want = oracle.run_params("BiasPReluBN", a, b, "bfloat16", "float32")
+    x = torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+    w = torch.from_numpy(b.copy())
+    y = eb.binary("BiasPReluBN", x.cuda(), w.cuda())
+    torch.cuda.synchronize()
+    assert y.dtype == torch.bfloat16 and tuple(y.shape) == sa
+    assert_bits_equal(y.cpu().view(torch.int16).numpy().view(np.uint16), want, "bfloat16",
+                      "device")
+    yh = eb.binary("BiasPReluBN", x.pin_memory(), w.pin_memory())
+    torch.cuda.synchronize()
+    assert_bits_equal(yh.view(torch.int16).numpy().view(np.uint16), want, "bfloat16", "mapped")
 
 
 def test_execute_host_pipelined_status_and_ordering():

@@ -133,6 +133,35 @@ def test_parity_all_families(op, dtype):
                 assert bits == want_bits, (what, bits, want_bits)
 
 
+PARAM_ROWS = {"BatchNormalization": 4, "BiasPRelu": 2, "BiasPReluBN": 6}
+# (family, x shape, C): the block geometries of BN_CASES plus one channel
+# (a single parameter per row, the right-scalar kernel)
+F32_BLOCK_CASES = [(fam, sa, sb[1]) for fam, sa, sb in BN_CASES] + [
+    ("right_scalar", (5, 1, 3001), 1)]
+
+
+@pytest.mark.parametrize("op", list(PARAM_ROWS))
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float64"])
+def test_float32_parameter_block(op, dtype):
+    """Parameters stored as float32 beside float16, bfloat16 or float64 x enter
+    the chain unrounded: bit-identical to the oracle on every family the block
+    reaches, natural and forced through the general kernel."""
+    for i, (fam, sa, C) in enumerate(F32_BLOCK_CASES):
+        sb = (PARAM_ROWS[op], C)
+        a, _ = inputs_for(op, dtype, sa, sb, seed=40 + i)
+        _, b = inputs_for(op, "float32", sa, sb, seed=40 + i)
+        assert b.dtype == np.float32
+        want = oracle.run_params(op, a, b, dtype, "float32")
+        for forced in (None, "general_strided"):
+            what = "%s %s x %s + float32 %s forced=%s" % (op, dtype, sa, sb, forced)
+            got, bits, family = run_engine(op, dtype, a, b, family=forced,
+                                           attrs={"dtype_b": "float32"})
+            if forced is None:
+                assert family == fam, (what, family)
+            assert_bits_equal(got, want, dtype, what)
+            assert bits == 0, what
+
+
 @pytest.mark.parametrize("op,dtype", [("Add", "float32"), ("Greater", "float16"),
                                       ("Mod", "int32"), ("Xor", "bool"), ("Sub", "uint8")])
 def test_inner_vector_kernel_on_other_geometries(op, dtype):

@@ -402,15 +402,23 @@ def test_strided_view_rules():
     assert e.value.code == "alias"
 
 
+PARAM_BLOCK_OPS = ("BatchNormalization", "BiasPRelu", "BiasPReluBN")
+
+
 def test_mixed_type_pow_rules():
-    """Pow's exponent may have any non-BOOL type (typed scalar adapters); every
-    other operator needs equal types.  Mixed plans run the general kernel."""
+    """Pow's exponent may have any non-BOOL type (typed scalar adapters), and the
+    parameter block of BatchNormalization, BiasPRelu and BiasPReluBN may be
+    float32 beside float16, bfloat16 or float64 x (scale, bias, mean and var
+    in x's type or float32); every other pair needs equal types.  Mixed Pow
+    plans run the general kernel."""
     for op in eb.OPS:
         for ta in ALL_DTYPES:
             for tb in ALL_DTYPES:
                 if ta == tb:
                     continue
-                legal = op == "Pow" and oracle.type_allowed("Pow", ta) and tb != "bool"
+                legal = ((op == "Pow" and oracle.type_allowed("Pow", ta) and tb != "bool") or
+                         (op in PARAM_BLOCK_OPS and tb == "float32" and
+                          ta in ("float16", "bfloat16", "float64")))
                 try:
                     eb.Descriptor(op, ta, dtype_b=tb).close()
                     got = True
@@ -425,6 +433,30 @@ def test_mixed_type_pow_rules():
     with pytest.raises(eb.EbinError) as e:
         eb.Plan(d, (300, 256), (256,), family="repeated_block")
     assert e.value.code == "family"
+
+
+@pytest.mark.parametrize("op", PARAM_BLOCK_OPS)
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float64"])
+def test_float32_parameter_block_keeps_the_family(op, dtype):
+    """A float32 parameter block is read one value per channel row, so it plans
+    exactly as a block of x's own type: same family and geometry for the
+    per-channel, channels-innermost, single-row and one-channel layouts."""
+    rows = {"BatchNormalization": 4, "BiasPRelu": 2, "BiasPReluBN": 6}[op]
+    same, mixed = eb.Descriptor(op, dtype), eb.Descriptor(op, dtype, dtype_b="float32")
+    assert mixed.out_dtype == dtype and mixed.dtype_b == "float32"
+    for xs in [(8, 64, 256, 256), (2, 3, 5, 7), (1000, 64), (1, 48), (4, 1, 16, 16),
+               (3, 5, 0, 2)]:
+        bs = (rows, xs[1])
+        a, b = eb.Plan(same, xs, bs), eb.Plan(mixed, xs, bs)
+        assert (b.family, b.output_shape) == (a.family, a.output_shape), (op, dtype, xs)
+        assert b.geometry() == a.geometry()
+        g = eb.Plan(mixed, xs, bs, family="general_strided")
+        assert g.family == ("empty" if 0 in xs else "general_strided")
+    for bad in ("float16", "bfloat16", "int32"):
+        if bad != dtype:
+            with pytest.raises(eb.EbinError) as e:
+                eb.Descriptor(op, dtype, dtype_b=bad)
+            assert e.value.code == "unsupported_type"
 
 
 def test_plan_cache_is_an_8_entry_lru():
