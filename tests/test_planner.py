@@ -459,6 +459,23 @@ def test_float32_parameter_block_keeps_the_family(op, dtype):
             assert e.value.code == "unsupported_type"
 
 
+def test_binary_helper_parameter_block_types():
+    """binary() takes the parameter block's type from its tensor: a float16
+    block beside bfloat16 x is refused by the descriptor rule, before any
+    memory check; a float32 block passes the rule and then meets the
+    pinned-memory check of CPU tensors."""
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((2, 3, 4), dtype=torch.bfloat16)
+    with pytest.raises(eb.EbinError) as e:
+        eb.binary("BatchNormalization", x, torch.ones((4, 3), dtype=torch.float16))
+    assert e.value.code == "unsupported_type"
+    with pytest.raises(eb.EbinError) as e:
+        eb.binary("BiasPRelu", x, torch.ones((2, 3), dtype=torch.float64))
+    assert e.value.code == "unsupported_type"
+    with pytest.raises(ValueError, match="pinned"):
+        eb.binary("BiasPReluBN", x, torch.ones((6, 3), dtype=torch.float32))
+
+
 def test_plan_cache_is_an_8_entry_lru():
     eb.ebin_plan_cache_clear()
     d = eb.Descriptor("Sub", "int32")
