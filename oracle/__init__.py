@@ -10,7 +10,8 @@ Operators and types are named by strings (ONNX operator names, numpy-style
 type names) and mapped here to the oracle's own private codes.
 
 Parity pins: see the header of ``ebin_oracle.c``.  Integer Pow with a negative
-exponent is parity unpinned beyond its closed-form cases.
+exponent follows a reading the pages leave open (the exact power truncated
+toward zero); the oracle is pinned to that reading by exact rationals.
 """
 from __future__ import annotations
 

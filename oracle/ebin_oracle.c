@@ -36,8 +36,9 @@
  * Parity pins: every function here is pinned by tests/test_oracle_pins.py
  * against numpy/Python library routines, closed forms, the sign tables that
  * follow from the Mod rules, and brute force over tiny shapes.  Integer Pow
- * with a negative exponent is the one reading with no outside pin (parity
- * unpinned beyond its closed-form cases).
+ * with a negative exponent follows a reading the pages leave open (the exact
+ * power truncated toward zero, as integer Div truncates), pinned by brute
+ * force against exact rational arithmetic.
  */
 #include <math.h>
 #include <stdint.h>

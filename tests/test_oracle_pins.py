@@ -535,8 +535,31 @@ def test_int_pow_matches_python(dtype):
     assert st == 0 and (got == want).all()
 
 
+@pytest.mark.parametrize("dtype", ["int32", "int64"])
+def test_int_pow_negative_exponent_against_exact_rationals(dtype):
+    """The negative-exponent reading (the pages leave it open) is the exact
+    power truncated toward zero, as integer Div truncates: checked by brute
+    force against Python's exact rationals, trunc(Fraction(base) ** e), for
+    every base in [-40, 40] and the type's limits, every exponent in [-70, -1]
+    and the most negative one; a zero base flags division by zero and writes 0."""
+    st_t = datagen.STORAGE[dtype]
+    lo, hi = INT_LIMITS[dtype]
+    bases = [x for x in list(range(-40, 41)) + [lo, lo + 1, hi, hi - 1] if x != 0]
+    exps = list(range(-70, 0)) + [lo]
+    pairs = [(x, y) for x in bases for y in exps if abs(x) == 1 or y >= -70]
+    a = np.array([x for x, _ in pairs], dtype=object).astype(st_t)
+    b = np.array([y for _, y in pairs], dtype=object).astype(st_t)
+    got, st = oracle.run("Pow", a, b, dtype)
+    want = [math.trunc(Fraction(x) ** y) for x, y in pairs]
+    assert st == 0 and [int(v) for v in got] == want
+    z = np.zeros(len(exps), st_t)
+    got, st = oracle.run("Pow", z, np.array(exps, dtype=object).astype(st_t), dtype)
+    assert st == oracle.STATUS_DIV_BY_ZERO and not got.any()
+
+
 def test_int_pow_negative_exponent_reading():
-    """Reading (no outside pin): trunc(1 / base^|e|), base 0 flags division by zero."""
+    """The negative-exponent reading on named cases: trunc(1 / base^|e|), base 0
+    flags division by zero."""
     a = np.array([1, -1, -1, 2, -3, 7], np.int32)
     b = np.array([-5, -3, -4, -1, -2, -1], np.int32)
     got, st = oracle.run("Pow", a, b, "int32")
