@@ -560,7 +560,9 @@ int oracle_offsets(const int64_t *sa, int ra, const int64_t *sb, int rb, const i
  *
  * Operands:
  *  - ordinary ops: A and B of types ta == tb, broadcast against each other;
- *  - PRelu: B (slope) must broadcast to A's shape, out shape == A shape;
+ *  - PRelu: B (slope) must broadcast to A's shape, out shape == A shape; a
+ *    1-D slope of C > 1 elements on data of rank >= 2 is per channel (axis 1;
+ *    see prelu_slope_shape);
  *  - BatchNormalization (inference): A = x [N, C, ...] (rank >= 2), B = [4, C]
  *    holding scale, bias, mean, var rows; per element, in binary32 and in the
  *    order written, y = (x - mean) / sqrt(var + eps) * scale + bias;
@@ -578,9 +580,39 @@ int oracle_offsets(const int64_t *sa, int ra, const int64_t *sb, int rb, const i
  *    x's type at the end (no rounding to x's type between the three).
  * Out shape: see oracle_output_shape.
  */
+/*
+ * PRelu's slope as it broadcasts (0verkilll/onnx ops, PReluOp: the slope is
+ * broadcast against the data across the channel dimension; a scalar, a 1-D
+ * [C], or a shape whose product is C with 1 everywhere but the channel axis
+ * are the per-channel forms).  A 1-D slope of more than one element on data
+ * of rank >= 2 is indexed by the channel, axis 1: it is read as the shape
+ * [C, 1, ..., 1] of rank ra - 1, which right-aligns onto axis 1.  (ONNX's own
+ * PRelu right-aligns a 1-D slope onto the last axis; the page's per-channel
+ * reading is followed.)  Every other slope shape keeps its own shape and
+ * broadcasts right-aligned.  Writes the shape into lb, its rank into *rlb.
+ */
+static void prelu_slope_shape(const int64_t *sa, int ra, const int64_t *sb, int rb,
+                              int64_t *lb, int *rlb)
+{
+    (void)sa;
+    if (ra >= 2 && rb == 1 && sb[0] != 1) {
+        lb[0] = sb[0];
+        for (int d = 1; d < ra - 1; ++d) lb[d] = 1;
+        *rlb = ra - 1;
+        return;
+    }
+    for (int d = 0; d < rb; ++d) lb[d] = sb[d];
+    *rlb = rb;
+}
+
 int oracle_output_shape(int op, const int64_t *sa, int ra, const int64_t *sb, int rb,
                         int64_t *so, int *ro)
 {
+    int64_t lb[OR_MAX_RANK];
+    if (op == OR_PRELU && rb >= 0 && rb <= OR_MAX_RANK && ra >= 0 && ra <= OR_MAX_RANK) {
+        prelu_slope_shape(sa, ra, sb, rb, lb, &rb);
+        sb = lb;
+    }
     if (op == OR_BATCHNORM || op == OR_BIAS_PRELU || op == OR_BIAS_PRELU_BN) {
         const int64_t rows = op == OR_BATCHNORM ? 4 : op == OR_BIAS_PRELU ? 2 : 6;
         if (ra < 2 || rb != 2 || sb[0] != rows || sb[1] != sa[1]) return OR_SHAPES;
@@ -619,11 +651,16 @@ static int eval2(int op, int t, int tp, int fmod_flag, int direction, float eps,
                  const void *A, const void *B, void *out,
                  const int64_t *idx, int64_t n_idx, uint32_t *status)
 {
-    int64_t so[OR_MAX_RANK], sta[OR_MAX_RANK], stb[OR_MAX_RANK];
+    int64_t so[OR_MAX_RANK], sta[OR_MAX_RANK], stb[OR_MAX_RANK], lb[OR_MAX_RANK];
     int r;
     *status = 0;
     if (op < 0 || op >= OR_NUM_OPS || !oracle_type_allowed(op, t)) return OR_TYPE;
     if (op == OR_MULADD) return OR_ARGS;              /* three inputs: oracle_eval3 */
+    if (ra < 0 || rb < 0 || ra > OR_MAX_RANK || rb > OR_MAX_RANK) return OR_ARGS;
+    if (op == OR_PRELU) {                             /* a 1-D slope is per channel */
+        prelu_slope_shape(sa, ra, sb, rb, lb, &rb);
+        sb = lb;
+    }
     int rc = oracle_output_shape(op, sa, ra, sb, rb, so, &r);
     if (rc) return rc;
     int64_t total = numel(so, r);

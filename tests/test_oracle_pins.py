@@ -774,6 +774,36 @@ def test_prelu_matches_numpy_where(dtype):
     assert_bits_equal(one, x, dtype, "PRelu slope 1 is the identity")
 
 
+def test_prelu_one_dimensional_slope_is_per_channel():
+    """A 1-D slope [C] multiplies channel c (axis 1) of the data, whatever the
+    last extent is (0verkilll/onnx ops, PReluOp: per-channel slope forms)."""
+    for shape, slope, x, want, note in read_golden("prelu_per_channel_slope.txt"):
+        xs = f32(*[float(v) for v in x.split(",")]).reshape([int(v) for v in shape.split(",")])
+        sl = f32(*[float(v) for v in slope.split(",")])
+        if want == "refused":
+            with pytest.raises(ValueError, match="incompatible_shapes"):
+                oracle.run("PRelu", xs, sl, "float32")
+            continue
+        got, st = oracle.run("PRelu", xs, sl, "float32")
+        w = f32(*[float(v) for v in want.split(",")]).reshape(xs.shape)
+        assert st == 0 and got.shape == xs.shape, note
+        assert_bits_equal(got, w, "float32", note)
+
+
+def test_prelu_one_dimensional_slope_equals_its_channel_shaped_form():
+    """[C] and [C,1,...,1] / [1,C,1,...,1] are the same per-channel slope."""
+    for shape in ((3, 5, 4, 5), (2, 5, 5), (1, 5, 7, 2, 3)):
+        x = datagen.make("normal", "float32", shape, 47, 0)
+        s = datagen.make("uniform", "float32", (5,), 47, 1, lo=0.0, hi=0.3)
+        flat, _ = oracle.run("PRelu", x, s, "float32")
+        tail = (1,) * (len(shape) - 2)
+        for form in ((5,) + tail, (1, 5) + tail):
+            shaped, _ = oracle.run("PRelu", x, s.reshape(form), "float32")
+            assert_bits_equal(flat, shaped, "float32", "%s vs %s" % (shape, form))
+        want = np.where(x >= 0, x, s.reshape((1, 5) + tail) * x)
+        assert_bits_equal(flat, want, "float32", "numpy per-channel where %s" % (shape,))
+
+
 def test_prelu_is_unidirectional():
     with pytest.raises(ValueError, match="incompatible_shapes"):
         oracle.run("PRelu", np.zeros((3, 1), np.float32), np.zeros((3, 4), np.float32), "float32")
