@@ -376,7 +376,7 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
     // The logical shape B broadcasts with.  BatchNormalization: B = [4, C]
     // holds four parameter rows of C and broadcasts as [1, C, 1, ...] along
     // x's channel axis 1.  Clip: B = [2] holds {min, max}, a scalar pair.
-    int64_t lb[kMaxRank];
+    int64_t lb[kMaxRank], lt[kMaxRank];
     int rlb = rb;
     int64_t plane = 0;
     if (d.op == EBIN_OP_BATCHNORM || d.op == EBIN_OP_BIAS_PRELU ||
@@ -394,6 +394,18 @@ ebin_status build_plan(const ebin_descriptor_s &d, const int64_t *sa, int ra, co
         rlb = 0;
     } else if (d.attrs.with_scalar) {
         rlb = 0;               // B is the attribute value: a scalar
+    } else if (d.op == EBIN_OP_PRELU && ra >= 2 && rb == 1 && sb[0] != 1) {
+        // 0verkilll/onnx ops, PReluOp: a 1-D slope [C] is per channel, broadcast
+        // across the channel dimension (axis 1), read as [C, 1, ..., 1]; its
+        // view stride, if any, moves along C and the unit dims take none
+        rlb = ra - 1;
+        lb[0] = sb[0];
+        for (int i = 1; i < rlb; ++i) lb[i] = 1;
+        if (tb) {
+            lt[0] = tb[0];
+            for (int i = 1; i < rlb; ++i) lt[i] = 0;
+            tb = lt;
+        }
     } else {
         for (int i = 0; i < rb; ++i) lb[i] = sb[i];
     }

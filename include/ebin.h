@@ -79,7 +79,9 @@ typedef enum ebin_op {
     EBIN_OP_BITWISE_OR = 15,
     EBIN_OP_BITWISE_XOR = 16,
     EBIN_OP_BITSHIFT = 17,        /* attrs.direction */
-    EBIN_OP_PRELU = 18,           /* B = slope, broadcast one way to A */
+    EBIN_OP_PRELU = 18,           /* B = slope, broadcast one way to A; a 1-D slope
+                                     [C] (C > 1) on A of rank >= 2 is per channel,
+                                     axis 1 (0verkilll/onnx ops, PReluOp) */
     EBIN_OP_BATCHNORM = 19,       /* inference; B = [4, C]: scale, bias, mean, var rows,
                                      in A's type or FLOAT32 */
     EBIN_OP_CLIP = 20,            /* B = [2]: {min, max}; attrs.clip_has_min/max */
@@ -209,15 +211,24 @@ ebin_status ebin_descriptor_create(ebin_op op, int opset, const ebin_attrs *attr
                                    ebin_dtype dtype_a, ebin_dtype dtype_b,
                                    ebin_descriptor_t *out);
 
-/* Output element type: BOOL for comparisons and logical operators, else dtype_a. */
+/*
+ * The descriptor's output element type, resolved when it was built ("Binary
+ * Kernel Design", Prepared execution: the descriptor resolves the output type;
+ * Compute, scheduling, and safety: comparisons and logical operators write
+ * one byte per BOOL): BOOL for the comparisons and And/Or/Xor, else dtype_a.
+ * Errors: INVALID_ARG (desc or out NULL).
+ */
 ebin_status ebin_descriptor_output_dtype(ebin_descriptor_t desc, ebin_dtype *out);
 
 /* The descriptor's monotonic identity (the plan cache keys on it, never on the pointer). */
 ebin_status ebin_descriptor_id(ebin_descriptor_t desc, uint64_t *id);
 
 /*
- * Free a descriptor.  Cached plans built from it are dropped from the LRU;
- * plans the caller still holds stay valid (they copy what they need).
+ * Free a descriptor ("Binary Kernel Design", Prepared execution: cache
+ * entries are keyed on the descriptor's monotonic id, never its address, so a
+ * freed descriptor's plans can never be found again).  Cached plans built
+ * from it are dropped from the LRU; plans the caller still holds stay valid
+ * (they copy what they need).  NULL is ignored.
  */
 void ebin_descriptor_destroy(ebin_descriptor_t desc);
 
@@ -227,7 +238,10 @@ void ebin_descriptor_destroy(ebin_descriptor_t desc);
  *   1. right-align the shapes (a rank-0 shape is a scalar) and check that each
  *      dimension pair is equal or contains a 1 (0 pairs only with 0 or 1);
  *      PRelu, BatchNormalization, Clip, BiasPRelu and BiasPReluBN broadcast
- *      one way: out == A's shape;
+ *      one way: out == A's shape.  A 1-D PRelu slope [C] with C > 1 on A of
+ *      rank >= 2 is per channel (0verkilll/onnx ops, PReluOp): it is read as
+ *      [C, 1, ..., 1], which right-aligns onto A's axis 1, so C must equal
+ *      shape_a[1];
  *   2. give broadcast dimensions zero strides;
  *   3. drop dimensions of output extent 1;
  *   4. merge adjacent dimensions i, i+1 when stride[i] == stride[i+1] * n[i+1]
@@ -316,13 +330,24 @@ ebin_status ebin_plan_create3_forced(ebin_descriptor_t desc, const int64_t *shap
                                      const int64_t *shape_b, int rank_b, const int64_t *shape_c,
                                      int rank_c, ebin_family family, ebin_plan_t *out);
 
-/* Output shape: `shape` must hold EBIN_MAX_RANK entries; *rank receives its rank. */
+/*
+ * The plan's output shape ("Binary Kernel Design", Operators and traversal:
+ * the right-aligned broadcast takes, per dimension, the extent that is not 1;
+ * one-way operators keep A's shape).  `shape` must hold EBIN_MAX_RANK entries;
+ * *rank receives its rank (0 for a scalar).  Errors: INVALID_ARG (a NULL
+ * argument).
+ */
 ebin_status ebin_plan_output_shape(ebin_plan_t plan, int64_t *shape, int *rank);
 
 /* Number of output elements. */
 ebin_status ebin_plan_numel(ebin_plan_t plan, int64_t *numel);
 
-/* The selected loop family. */
+/*
+ * The loop family the plan selected ("Binary Kernel Design", Operators and
+ * traversal, loop-family table; the rule is stated at ebin_plan_create).
+ * Execution may still run a 16-byte-vector family's plan on the general
+ * kernel when a buffer is off 16-byte alignment.  Errors: INVALID_ARG.
+ */
 ebin_status ebin_plan_family(ebin_plan_t plan, ebin_family *family);
 
 /*
@@ -333,7 +358,12 @@ ebin_status ebin_plan_family(ebin_plan_t plan, ebin_family *family);
 ebin_status ebin_plan_geometry(ebin_plan_t plan, int *rank, int64_t *n, int64_t *stride_a,
                                int64_t *stride_b);
 
-/* Drop one reference; the plan is freed when no caller and no cache slot holds it. */
+/*
+ * Drop one reference ("Binary Kernel Design", Prepared execution: plans live
+ * in a bounded LRU and are rebuilt on a miss; a plan evicted while a caller
+ * holds it stays valid for that caller).  The plan is freed when no caller and
+ * no cache slot holds it.  NULL is ignored.
+ */
 void ebin_plan_release(ebin_plan_t plan);
 
 /* Plan cache counters since the last clear, and its current size (<= 8). */
@@ -440,10 +470,14 @@ ebin_status ebin_execute3_mapped(ebin_plan_t plan, const void *host_a, const voi
                                  const void *host_c, void *host_out, void *stream);
 
 /*
- * Read and clear the device status word of `stream` on the current device:
- * synchronises the stream, returns the OR of the EBIN_DEVICE_* bits raised
- * since the last call, then zeroes the word (stream-ordered).  A stream that
- * never ran a validating operator reports 0.
+ * Read and clear the device status word of `stream` on the current device
+ * ("Binary Kernel Design", Compute, scheduling, and safety: invalid inputs --
+ * integer division or modulo by zero, shift counts -- are found by validation
+ * before the math; here each kernel records them as bits instead of
+ * stopping): synchronises the stream, returns the OR of the EBIN_DEVICE_*
+ * bits raised since the last call, then zeroes the word (stream-ordered).  A
+ * stream that never ran a validating operator reports 0.
+ * Errors: INVALID_ARG (bits NULL), CUDA.
  */
 ebin_status ebin_get_device_status(void *stream, uint32_t *bits);
 
@@ -483,7 +517,11 @@ uint64_t ebin_launch_count(void);
 /* Bytes per element of a type (0 if unknown). */
 size_t ebin_dtype_size(ebin_dtype dtype);
 
-/* A static, human-readable name for a status code. */
+/*
+ * A static, human-readable name for a status code ("Binary Kernel Design",
+ * Compute, scheduling, and safety: invalid inputs are reported, not acted
+ * on).  Unknown codes give "unknown status".  Never NULL; not to be freed.
+ */
 const char *ebin_status_string(ebin_status status);
 
 #ifdef __cplusplus

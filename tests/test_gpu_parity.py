@@ -51,6 +51,10 @@ PRELU_CASES = [
     ("contiguous", (50001,), (50001,)),
     ("general_strided", (2, 3, 4, 5), (3, 1, 5)),
     ("repeated_block", (300, 7), (7,)),
+    # a 1-D slope [C] is per channel (axis 1), whether or not the last extent is C
+    ("general_strided", (2, 8, 5, 8), (8,)),
+    ("general_strided", (2, 8, 5, 7), (8,)),
+    ("inner_vector_outer", (2, 16, 8, 16), (16,)),
 ]
 BN_CASES = [
     ("inner_vector_outer", (4, 16, 8, 32), (4, 16)),

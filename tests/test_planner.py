@@ -168,6 +168,36 @@ def test_repeated_block_rule_for_any_row_length():
         assert family("PRelu", "float32", (100, P), (P,))[0] == "repeated_block"
 
 
+def test_prelu_one_dimensional_slope_plans_per_channel():
+    """A 1-D PRelu slope of C > 1 elements on data of rank >= 2 is per channel
+    (0verkilll/onnx ops, PReluOp): accepted exactly where the oracle accepts it,
+    and planned as its [C, 1, ..., 1] form."""
+    d = eb.Descriptor("PRelu", "float32")
+    for sa in small_shapes():
+        for c in (0, 1, 2, 3):
+            try:
+                want = oracle.output_shape("PRelu", sa, (c,))
+            except ValueError:
+                want = None
+            try:
+                p = eb.Plan(d, sa, (c,))
+            except eb.EbinError as e:
+                assert e.code == "incompatible_shapes" and want is None, (sa, c)
+                continue
+            assert p.output_shape == want == tuple(sa), (sa, c)
+            if len(sa) >= 2 and c != 1 and p.numel:
+                q = eb.Plan(d, sa, (c,) + (1,) * (len(sa) - 2))
+                assert p.family == q.family and p.geometry() == q.geometry(), (sa, c)
+                q.close()
+            p.close()
+    f, (n, ga, gb) = family("PRelu", "bfloat16", (8, 64, 256, 256), (64,))
+    assert f == "inner_vector_outer" and n == [8, 64, 65536] and gb == [0, 1, 0]
+    for sa in ((2, 8, 5, 8), (2, 8, 5, 7)):
+        assert eb.Plan(d, sa, (8,)).output_shape == sa
+    with pytest.raises(eb.EbinError):
+        eb.Plan(d, (2, 7, 5, 8), (8,))            # the length is the last extent, not C
+
+
 def test_one_way_broadcasts():
     for op, sb in (("PRelu", (3, 4)), ("BatchNormalization", (4, 5)), ("Clip", (3,))):
         d = eb.Descriptor(op, "float32")
