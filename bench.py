@@ -9,8 +9,9 @@ algorithmic traffic.  Inputs (3 GiB) are larger than L2, so no flush is
 needed between steps.
 
 Also reported: the dominant kernel's roofline (per-launch CUDA events on the
-launching stream), an end-to-end number through ebin_execute_host (pinned
-host buffers, copies inside the timed region), the oracle timed on a bounded
+launching stream), an end-to-end number through ebin_execute_mapped (pinned
+host buffers read and written in place by the kernel inside the timed region;
+the copy pipeline of ebin_execute_host beside it), the oracle timed on a bounded
 sample on the host, SM clocks sampled during the timed region, and a table of
 every workload (one line per operator/family) timed with rotating buffers.
 
@@ -441,6 +442,31 @@ def run_ours(args, dist: Dist):
         print(json.dumps(out), flush=True)
 
 
+def host_cpu():
+    """(CPU model, logical cores) of the host the baseline runs on."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return model or platform.processor() or platform.machine(), os.cpu_count()
+
+
 def cpu_baseline_sample(a, b_mul, b_div, min_seconds=10.0, max_passes=16):
     """The oracle on the host: whole Mul+Div passes over the workload until
     about `min_seconds` of single-threaded CPU work has been done."""
@@ -454,8 +480,9 @@ def cpu_baseline_sample(a, b_mul, b_div, min_seconds=10.0, max_passes=16):
         if time.perf_counter() - t0 >= min_seconds:
             break
     dt = time.perf_counter() - t0
+    model, nproc = host_cpu()
     return {"value": round(passes * 2 * 3 * a.size * 4 / dt / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": model, "nproc": nproc,
             "sample": "%d full Mul+Div pass(es) over the %d-element workload (single-threaded C "
                       "oracle, full multi-index per element), %.1f s" % (passes, a.size, dt)}
 
@@ -492,6 +519,7 @@ def run_reference(args, dist: Dist):
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
            "config": {"workload": WORKLOAD, "ops_per_step": ["Mul", "Div"], "sample": sample},
            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "cpu_model": host_cpu()[0], "nproc": host_cpu()[1],
                             "sample": sample},
            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}

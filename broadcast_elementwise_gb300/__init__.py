@@ -104,6 +104,7 @@ def _load():
         "ebin_execute3_mapped": (i32, [vp, vp, vp, vp, vp, vp]),
         "ebin_get_device_status": (i32, [vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ebin_execute_noalloc": (i32, [vp, vp, vp, vp, vp, i32, ctypes.POINTER(ctypes.c_uint32)]),
+        "ebin_noalloc_read_status": (i32, [i32, vp, ctypes.POINTER(ctypes.c_uint32)]),
         "ebin_launch_count": (ctypes.c_uint64, []),
         "ebin_dtype_size": (ctypes.c_size_t, [i32]),
         "ebin_status_string": (ctypes.c_char_p, [i32]),
@@ -291,6 +292,14 @@ def ebin_execute_noalloc(plan, A, B, out, stream, status_slot, want_status=True)
 
 
 NOALLOC_STATUS_SLOTS = 64
+
+
+def ebin_noalloc_read_status(status_slot, stream) -> int:
+    """Marshal ebin_noalloc_read_status; returns the slot's status bits."""
+    v = ctypes.c_uint32(0)
+    _check(lib.ebin_noalloc_read_status(int(status_slot), stream, ctypes.byref(v)),
+           "ebin_noalloc_read_status")
+    return v.value
 
 
 def ebin_get_device_status(stream) -> int:

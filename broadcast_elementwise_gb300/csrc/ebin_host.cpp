@@ -926,12 +926,12 @@ cudaError_t ebin::launch(const Launch &L) {
 #undef EBIN_PICK
 }
 
-namespace {
-
-// Checks and launch description shared by the execute entry points: the
-// buffer, alias and alignment rules of ebin_execute, and the status word.
-ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, void *out,
-                           cudaStream_t s, ebin::Launch &L) {
+// Checks and launch description shared by the execute entry points (the
+// no-allocation one included): the buffer, alias and alignment rules of
+// ebin_execute, and the status word -- the stream's own, allocated on first
+// use, or `status` when the caller supplies one.
+ebin_status ebin::prepare_launch(const ebin_plan_s &p, const void *A, const void *B, void *out,
+                                 cudaStream_t s, uint32_t *status, ebin::Launch &L) {
     const bool b_needed = !(p.op == EBIN_OP_CLIP && !p.attrs.clip_has_min && !p.attrs.clip_has_max) &&
                           !p.attrs.with_scalar;
     if (!A || !out || (b_needed && !B)) return EBIN_ERR_INVALID_ARG;
@@ -979,7 +979,7 @@ ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, v
     L.num_sms = sm_count(dev);
     L.status = nullptr;
     if (validates(p.op, p.dt)) {
-        L.status = status_word(dev, s, true);
+        L.status = status ? status : status_word(dev, s, true);
         if (!L.status) return EBIN_ERR_CUDA;
     }
     // The vector families move 16-byte packs: pointers off that alignment
@@ -993,6 +993,10 @@ ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, v
     }
     return EBIN_OK;
 }
+
+namespace {
+
+using ebin::prepare_launch;
 
 ebin_status launch_counted(const ebin::Launch &L) {
     const cudaError_t e = ebin::launch(L);
@@ -1008,7 +1012,7 @@ extern "C" ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void 
     const ebin_plan_s &p = *plan;
     if (p.numel == 0) return EBIN_OK;  // empty dims: no work, nothing read
     ebin::Launch L;
-    const ebin_status st = prepare_launch(p, A, B, out, static_cast<cudaStream_t>(stream), L);
+    const ebin_status st = prepare_launch(p, A, B, out, static_cast<cudaStream_t>(stream), nullptr, L);
     if (st != EBIN_OK) return st;
     return launch_counted(L);
 }
@@ -1122,7 +1126,7 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
     if (host_b && !dev_b) return EBIN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ebin::Launch L;
-    ebin_status st = prepare_launch(p, dev_a, host_b ? dev_b : nullptr, dev_out, s, L);
+    ebin_status st = prepare_launch(p, dev_a, host_b ? dev_b : nullptr, dev_out, s, nullptr, L);
     if (st != EBIN_OK) return st;
 
     // Streaming families whose output range [o, o+n) reads only the same range
@@ -1265,7 +1269,7 @@ extern "C" ebin_status ebin_execute_mapped(ebin_plan_t plan, const void *host_a,
         mapped_range(host_out, (size_t)p.numel * ebin_dtype_size(p.out_dt)));
     if (!da || !dout) return EBIN_ERR_INVALID_ARG;
     ebin::Launch L;
-    const ebin_status st = prepare_launch(p, da, db, dout, static_cast<cudaStream_t>(stream), L);
+    const ebin_status st = prepare_launch(p, da, db, dout, static_cast<cudaStream_t>(stream), nullptr, L);
     if (st != EBIN_OK) return st;
     return launch_counted(L);
 }

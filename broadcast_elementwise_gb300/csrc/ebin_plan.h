@@ -40,4 +40,12 @@ struct ebin_plan_s {
 namespace ebin {
 // Add one to the process-wide kernel launch count (ebin_launch_count).
 void count_launch();
+
+// The checks and launch description of a two-input execution: NULL buffers,
+// the alias rule, the status word and the 16-byte alignment fallback to the
+// general kernel.  `status`: the device word a validating kernel ORs its bits
+// into, or nullptr for the stream's own word (allocated on first use).  On
+// EBIN_OK, L is ready for launch().
+ebin_status prepare_launch(const ebin_plan_s &p, const void *A, const void *B, void *out,
+                           cudaStream_t s, uint32_t *status, Launch &L);
 }  // namespace ebin

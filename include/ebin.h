@@ -391,9 +391,9 @@ void ebin_plan_cache_clear(void);
  * Stream capture: the launch path makes no allocation and no synchronising
  * call, so executions can be captured into a CUDA graph and replayed.  The one
  * exception is the first validating operator on a stream, which allocates that
- * stream's status word; for validating operators in a graph, use
- * ebin_execute_noalloc.  Launch the kernels once before the first capture,
- * because a kernel's first launch loads its module.
+ * stream's status word: run one on the capturing stream before the capture
+ * begins.  Launch the kernels once before the first capture, because a
+ * kernel's first launch loads its module.
  * Errors: INVALID_ARG, ALIAS, CUDA.
  */
 ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
@@ -500,16 +500,35 @@ ebin_status ebin_get_device_status(void *stream, uint32_t *bits);
  *                             else returns EBIN_ERR_INVALID_ARG
  *   status_bits               NULL, or a host word that receives the
  *                             EBIN_DEVICE_* bits of this call; with a non-NULL
- *                             pointer the call waits for `stream` to finish
- * The slot is zeroed (stream-ordered) at the start of every call.  All calls
- * share the array: calls that use the same slot and overlap on the GPU race on
- * it.  The first call on a device looks up the array's device address once
- * (cudaGetSymbolAddress), so make that first call before any stream capture.
- * Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ *                             pointer the call waits for `stream` to finish.
+ *                             With NULL the bits stay in the slot, to be read
+ *                             later with ebin_noalloc_read_status.
+ * The checks, the kernel choice and the alignment fallback are ebin_execute's
+ * own (one shared implementation).  The slot is zeroed (stream-ordered) at the
+ * start of every call, so it holds the bits of the last call that used it.
+ * All calls share the array: calls that use the same slot and overlap on the
+ * GPU race on it.  The first call on a device looks up the array's device
+ * address once (cudaGetSymbolAddress), so make that first call before any
+ * stream capture.  Nothing here calls cudaMalloc, cudaFree or any allocating
+ * routine.
  */
 #define EBIN_NOALLOC_STATUS_SLOTS 64
 ebin_status ebin_execute_noalloc(ebin_plan_t plan, const void *A, const void *B, void *out,
                                  void *stream, int status_slot, uint32_t *status_bits);
+
+/*
+ * Read one word of ebin_execute_noalloc's status array on the current device,
+ * without allocating.  No counterpart in the pages.  Waits for the work
+ * already queued on `stream` (the stream the calls that used the slot ran on,
+ * or one ordered after them), then returns in *bits the EBIN_DEVICE_* bits of
+ * the last ebin_execute_noalloc call that used `status_slot`; the slot is not
+ * cleared (the next call that uses it clears it).  A slot no call has used
+ * reads 0.  Like ebin_execute_noalloc, the first use on a device looks up the
+ * array's address.
+ * Errors: INVALID_ARG (bits NULL, or a slot outside [0, EBIN_NOALLOC_STATUS_SLOTS)),
+ * CUDA.
+ */
+ebin_status ebin_noalloc_read_status(int status_slot, void *stream, uint32_t *bits);
 
 /* Kernels this library has launched in this process (for launch accounting). */
 uint64_t ebin_launch_count(void);
