@@ -251,7 +251,9 @@ def test_strided_input_views(op, dtype):
     import torch
     for i, (base_n, shape, strides, shape_b) in enumerate(STRIDED_VIEWS):
         if op == "PRelu":
-            shape_b = (shape[-1],) if len(shape) else ()
+            # a slope along the inner dim: [W] on rank <= 2, [1, ..., 1, W] above
+            # (a 1-D slope on rank >= 3 data is per channel, axis 1)
+            shape_b = ((1,) * (len(shape) - 1) + (shape[-1],)) if len(shape) else ()
         base, b = inputs_for(op, dtype, (base_n,), shape_b, seed=70 + i)
         view = np.lib.stride_tricks.as_strided(base, shape, [x * base.itemsize for x in strides])
         want, _ = oracle.run(op, np.ascontiguousarray(view), b, dtype)
