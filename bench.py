@@ -56,6 +56,9 @@ def parse_args():
                     help="time one workload case alone (for profiling), e.g. mul_f32_contiguous")
     ap.add_argument("--scale-log2", type=int, default=0,
                     help="with --only: shrink the 1-D workloads by 2^S")
+    ap.add_argument("--cases", default=None,
+                    help="time these workloads (comma-separated names) with the per-workload "
+                         "table's method (rotating buffers, back-to-back launches) and exit")
     return ap.parse_args()
 
 
@@ -559,10 +562,29 @@ def run_one_case(args):
                       "gbs": round(nbytes / med / 1e9, 1)}), flush=True)
 
 
+def run_cases(args):
+    """The per-workload table for the named workloads only, one JSON line each."""
+    import torch
+
+    import broadcast_elementwise_gb300 as eb
+    from datagen import workloads
+
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2_bytes = getattr(props, "L2_cache_size", 128 << 20)
+    peak, _ = measured_peak()
+    names = [n.strip() for n in args.cases.split(",") if n.strip()]
+    rows = time_family_table(eb, torch, [workloads.by_name(n) for n in names], l2_bytes, peak)
+    for name in names:
+        print(json.dumps(dict(case=name, **rows[name])), flush=True)
+
+
 def main():
     args = parse_args()
     if args.only:
         run_one_case(args)
+        return
+    if args.cases:
+        run_cases(args)
         return
     dist = Dist()
     try:

@@ -141,6 +141,12 @@ struct MinRowsOf<Op, std::void_t<decltype(Op::kMinRows)>>
 template <class Op>
 struct HasPrep<Op, std::void_t<decltype(Op::kPrep)>> : std::bool_constant<Op::kPrep> {};
 
+// Operators with a form for a group of elements that share one B value
+// (Op::kGroup, Op::apply_group) -- e.g. BatchNormalization's prepared division.
+template <class Op, class = void> struct HasGroup : std::false_type {};
+template <class Op>
+struct HasGroup<Op, std::void_t<decltype(Op::kGroup)>> : std::bool_constant<Op::kGroup> {};
+
 struct PrepNone {
     using PB = int;
 };
@@ -162,6 +168,8 @@ __device__ __forceinline__ void compute_group(const typename Op::In *a, const ty
     if constexpr (SB && HasPrep<Op>::value) {
         const typename Op::PB pb = Op::prep(b[0]);
         Op::template apply_prep_group<G, SA>(a, pb, o, args, err);
+    } else if constexpr (SB && HasGroup<Op>::value) {
+        Op::template apply_group<G, SA>(a, b[0], o, args, err);
     } else if constexpr (HasPack<Op>::value && G % 4 == 0) {
         if constexpr (SA || SB) {
             typename Op::In ta[G], tb[G];
@@ -590,6 +598,97 @@ __global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int32_t P, FastD
     flush_err<Op>(p.status, err);
 }
 
+// ---------------------------------------------------------------- rows with one value each
+//
+// Inner-vector / repeated-block plans whose dense input covers the whole output
+// in order (x[N, C, H, W] against a per-channel operand, [M, L] against
+// [M, 1]) and whose other input is one value per row of L elements, L a
+// multiple of the pack width G.  The rows are not walked one by one: the
+// output is streamed flat, and each CTA takes `iters` consecutive runs of
+// kThreads x U packs (one contiguous chunk), so that a thread meets few row
+// boundaries.  A thread keeps the value of its current row (the parameters,
+// prepared where the operator prepares them) and reloads it only when a pack
+// lies outside that row; the row value's offset is decoded from the row
+// index only then.  ROW_A: A is the per-row input and B the dense one.
+// WIDE: a pack index may reach 2^32, and indices divide in 64 bits.
+struct RowConstArgs {
+    int64_t lp;                 // packs per row (L / G)
+    FastDiv f_lp;
+    int32_t nd;                 // outer dims (everything but the inner row)
+    int32_t iters;              // runs of kThreads x U packs per CTA
+    int64_t on[kMaxRank];       // outer extents, outermost first
+    int64_t os[kMaxRank];       // the per-row input's strides along them
+    FastDiv f_on[kMaxRank];
+};
+
+template <class Op, bool ROW_A, int U, bool WIDE>
+__global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) {
+    pdl_launch();
+    using In = typename Op::In;
+    using Out = typename Op::Out;
+    using BV = typename Op::BV;
+    using BIn = typename BInOf<Op>::type;
+    constexpr int G = 16 / sizeof(In);
+    constexpr bool kPrep = !ROW_A && HasPrep<Op>::value;
+    using PrepT = typename std::conditional_t<HasPrep<Op>::value, Op, PrepNone>::PB;
+    using RowV = std::conditional_t<ROW_A, In, std::conditional_t<kPrep, PrepT, BV>>;
+    const In *D = ROW_A ? static_cast<const In *>(p.B) : static_cast<const In *>(p.A);
+    const In *RA = static_cast<const In *>(p.A);
+    const BIn *RB = static_cast<const BIn *>(p.B);
+    Out *O = static_cast<Out *>(p.out);
+    const int64_t np = p.numel / G;
+    const int64_t first = (int64_t)blockIdx.x * r.iters * (kThreads * U) + threadIdx.x;
+    // packs [lo, hi) are the row whose value rv holds (none yet)
+    int64_t lo = 0, hi = 0;
+    RowV rv{};
+    uint32_t err = 0;
+    auto set_row = [&](int64_t g) {   // the row of pack g becomes the cached one
+        const int64_t row = udiv(g, r.lp, r.f_lp, WIDE);
+        lo = row * r.lp;
+        hi = lo + r.lp;
+        int64_t rem = row, off = 0;
+#pragma unroll
+        for (int k = kMaxRank - 1; k >= 0; --k) {
+            if (k < r.nd) {
+                const int64_t q = udiv(rem, r.on[k], r.f_on[k], WIDE);
+                off += (rem - q * r.on[k]) * r.os[k];
+                rem = q;
+            }
+        }
+        if constexpr (ROW_A) rv = RA[off];
+        else if constexpr (kPrep) rv = Op::prep(Op::loadB(RB, off, p.args));
+        else rv = Op::loadB(RB, off, p.args);
+    };
+    pdl_wait();
+#pragma unroll 1
+    for (int j = 0; j < r.iters; ++j) {
+        const int64_t base = first + (int64_t)j * (kThreads * U);
+        if (base >= np) break;
+        Pack<In, G> d[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t g = base + (int64_t)u * kThreads;
+            if (g < np) d[u] = ld_stream<In, G>(D + g * G);
+        }
+        const int64_t last = base + (int64_t)(U - 1) * kThreads;
+        const bool whole = last < np && base >= lo && last < hi;   // one cached row, all packs
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t g = base + (int64_t)u * kThreads;
+            if (whole || g < np) {
+                if (!whole && (g < lo || g >= hi)) set_row(g);
+                Pack<Out, G> o;
+                if constexpr (ROW_A) compute_group<Op, G, true, false>(&rv, d[u].v, o.v, p.args, err);
+                else if constexpr (kPrep)
+                    Op::template apply_prep_group<G, false>(d[u].v, rv, o.v, p.args, err);
+                else compute_group<Op, G, false, true>(d[u].v, &rv, o.v, p.args, err);
+                st_stream<Out, G>(O + g * G, o);
+            }
+        }
+    }
+    flush_err<Op>(p.status, err);
+}
+
 // ---------------------------------------------------------------- three inputs
 //
 // The row traversal of k_rows for an operator of three inputs (Op::apply3):
@@ -916,10 +1015,90 @@ struct RowShape {
                              : (IA == 0 || kFloatPrepRow) ? 4 : 2;
 };
 
+// Resident CTAs of a kernel per SM at kThreads threads (looked up once).
+template <class K> int resident_ctas(K kernel) {
+    static const int n = [kernel] {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess ||
+            b < 1) {
+            cudaGetLastError();
+            b = 1;
+        }
+        return b;
+    }();
+    return n;
+}
+
+// The dense input covers the whole output in order (its coalesced strides
+// are the dense ones) and the other input is one value per row: the flat
+// k_rowconst streams it.  Rows must be a whole number of packs.
+inline bool rowconst_fits(const Geom &g, int G, bool row_a) {
+    const int r = g.rank;
+    if (r < 2) return false;
+    const int64_t *sd = row_a ? g.sb : g.sa;      // the dense input
+    const int64_t *sr = row_a ? g.sa : g.sb;      // the per-row input
+    if (g.n[r - 1] % G != 0 || sd[r - 1] != 1 || sr[r - 1] != 0) return false;
+    int64_t acc = g.n[r - 1];
+    for (int i = r - 2; i >= 0; --i) {
+        if (sd[i] != acc) return false;
+        acc *= g.n[i];
+    }
+    return true;
+}
+
+// One CTA per chunk of kThreads x U x iters consecutive packs; `iters` sized
+// for about kRowConstWaves waves of resident CTAs (measured on GB300, bf16
+// x[8,64,256,256]: per-channel Add 24.6 us at two waves, 21.7 at four, 21.2
+// at eight).  A shared-memory staging of the dense input (cp.async, up to
+// three runs ahead) and two packs per thread for the costlier operators were
+// tried and gave nothing once BatchNormalization's divide was prepared.
+constexpr int kRowConstU = 4;
+template <class Op> constexpr int kRowConstWaves = HasGroup<Op>::value ? 4 : 8;
+
+template <class Op, bool ROW_A, bool WIDE>
+cudaError_t run_rowconst_kernel(const Launch &L) {
+    constexpr int G = 16 / sizeof(typename Op::In);
+    constexpr int U = kRowConstU;
+    auto kernel = k_rowconst<Op, ROW_A, U, WIDE>;
+    const Geom &g = L.g;
+    RowConstArgs r{};
+    const int rank = g.rank;
+    r.lp = g.n[rank - 1] / G;
+    r.f_lp = make_fastdiv((uint64_t)r.lp);
+    r.nd = rank - 1;
+    const int64_t *sr = ROW_A ? g.sa : g.sb;
+    for (int i = 0; i < r.nd; ++i) {
+        r.on[i] = g.n[i];
+        r.os[i] = sr[i];
+        r.f_on[i] = make_fastdiv((uint64_t)g.n[i]);
+    }
+    const int64_t np = L.numel / G;
+    const int64_t per_run = (int64_t)kThreads * U;
+    const int64_t runs = ceil_div(np, per_run);
+    const int64_t slots = (int64_t)L.num_sms * resident_ctas(kernel) * kRowConstWaves<Op>;
+    const int64_t iters = std::max<int64_t>(1, ceil_div(runs, slots));
+    if (iters > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    r.iters = (int32_t)iters;
+    const int64_t grid = ceil_div(runs, iters);
+    if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
+    return launch_pdl(kernel, grid, kThreads, L.stream, kargs<Op>(L), r);
+}
+
+template <class Op, bool ROW_A>
+cudaError_t run_rowconst(const Launch &L) {
+    constexpr int G = 16 / sizeof(typename Op::In);
+    if (L.numel / G >= (1ll << 32)) return run_rowconst_kernel<Op, ROW_A, true>(L);
+    return run_rowconst_kernel<Op, ROW_A, false>(L);
+}
+
 template <class Op, bool NOPREFIX>
 cudaError_t run_rows_vector(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
     const int64_t ia = L.g.sa[L.g.rank - 1], ib = L.g.sb[L.g.rank - 1];
+    if (ia == 1 && ib == 0 && rowconst_fits(L.g, G, false)) return run_rowconst<Op, false>(L);
+    if constexpr (Op::kPlainB) {
+        if (ia == 0 && ib == 1 && rowconst_fits(L.g, G, true)) return run_rowconst<Op, true>(L);
+    }
     if (ia == 1 && ib == 1) {
         using S = RowShape<Op, 1, 1>;
         return run_rows_kernel<Op, G, 1, 1, NOPREFIX, S::V, S::PACKED>(L);

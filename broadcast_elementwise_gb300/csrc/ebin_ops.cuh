@@ -619,6 +619,164 @@ __device__ __forceinline__ double div_rn(double a, double b) { return __ddiv_rn(
 __device__ __forceinline__ float sqrt_rn(float a) { return __fsqrt_rn(a); }
 __device__ __forceinline__ double sqrt_rn(double a) { return __dsqrt_rn(a); }
 
+// ---------------------------------------------------------------- 16-bit words
+// Groups of 16-bit elements move as 32-bit words, two elements each.
+// Two values rounded to a 16-bit type, packed (the first in the low half).
+template <class T> __device__ __forceinline__ uint32_t round2(float a, float b);
+template <> __device__ __forceinline__ uint32_t round2<__nv_bfloat16>(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    uint32_t w;
+    memcpy(&w, &v, 4);
+    return w;
+}
+template <> __device__ __forceinline__ uint32_t round2<__half>(float a, float b) {
+    const __half2 v = __floats2half2_rn(a, b);
+    uint32_t w;
+    memcpy(&w, &v, 4);
+    return w;
+}
+
+// Two 16-bit values of one 32-bit word (the first in the low half), widened
+// exactly to binary32; and the value in one half of a word.
+template <class T> __device__ __forceinline__ float2 widen2(uint32_t w);
+template <> __device__ __forceinline__ float2 widen2<__nv_bfloat16>(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <> __device__ __forceinline__ float2 widen2<__half>(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __half22float2(h);
+}
+template <class T> __device__ __forceinline__ T half_of(uint32_t w, bool high) {
+    const unsigned short b = (unsigned short)(high ? (w >> 16) : (w & 0xFFFFu));
+    T v;
+    memcpy(&v, &b, 2);
+    return v;
+}
+template <class T> __device__ __forceinline__ uint32_t bits_of(T v) {
+    unsigned short b;
+    memcpy(&b, &v, 2);
+    return b;
+}
+
+// ---------------------------------------------------------------- prepared exact division
+//
+// q = RN(t / d) for many t sharing one divisor d, without the IEEE divide: with
+// r = RN(1/d) formed once,
+//   q0 = RN(t r);  q1 = RN(q0 + RN(t - q0 d) r);  q2 = RN(q1 + RN(t - q1 d) r)
+// (every step one rounding; the remainders are FMAs).  Then q2 == RN(t/d)
+// whenever d's significand D (an integer in [2^23, 2^24)) is at most
+// 2^24 - 5 and no step leaves the normal range.  The argument, scaled to
+// d in [1, 2) (powers of two change nothing), u = 2^-24, Q = t/d, and
+// eps = d r - 1 with |eps| <= d 2^-25 = D 2^-48 (r within half an ulp):
+//  - t r = Q (1 + eps), so |q0 - Q| <= (2u + u^2) |Q|;
+//  - q0 + RN(t - q0 d) r = Q + (Q - q0)((1 + e)(1 + eps) - 1), |e| <= u, so
+//    it lies within (2u + u^2)^2 |Q| < 2^-22 ulp(Q) of Q, and q1 lies within
+//    (1/2 + 2^-22) ulp of Q;
+//  - t and q1 d are integer multiples of 2^(eq + ed), the ulps of q1 and d
+//    (t ~ q1 d and both significands are normalised), and |t - q1 d| <=
+//    (1/2 + 2^-22) D 2^(eq + ed) < 2^24 2^(eq + ed): the second remainder
+//    is exact (granularity 2^(eq + ed) >= 2^-149 within the ranges below);
+//  - q1 + (t - q1 d) r = Q + (Q - q1) eps, off Q by at most
+//    (1/2 + 2^-22) ulp D 2^-48;
+//  - Q = T/D-scaled is never a midpoint (a 25-bit odd number times D cannot
+//    equal a 24-bit T times a power of two) and lies at least ulp / (2D) from
+//    every midpoint (the distance is an integer over 2D, in ulps);
+//  - (1/2 + 2^-22) D 2^-48 < 1 / (2D) holds for D <= 2^24 - 5, so rounding
+//    Q's neighbour rounds as Q does.
+// This is the final-correction scheme of P. Markstein ("Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990), applied twice.
+//
+// Ranges.  A row takes it when 2^-20 <= d <= 2^20 and D <= 2^24 - 5; an
+// element keeps q2 when |t| >= tlow and |q2| <= 2^100.  With |t| >= 2^-100 the
+// remainders' granularity 2^(eq + ed) ~ |t| 2^-46 stays at or above 2^-149
+// and every quantity is normal; |q2| <= 2^100 keeps every step finite (an
+// infinite or NaN t, or an overflowing quotient, gives a NaN or infinite q2).
+// For t = +0 the steps give q2 = +0 exactly, but t = -0 comes out as +0.
+// The chains divide t = t' - mean with t' and mean binary32 values; when
+// |mean| >= 2^-75, t is +0 or at least 2^-99 in magnitude (two binary32 values
+// at or above 2^-76 differ by a multiple of 2^-99), and never -0, so such
+// rows take tlow = 0; other rows take tlow = 2^-100 and send their zeros to
+// the IEEE divide, as they do tiny, huge, infinite and NaN quotients.
+struct DivPrep {
+    float r, nd, tlow;      // RN(1/d), -d, the least |t| kept (+inf: the row is refused)
+};
+
+__device__ __forceinline__ DivPrep div_prep(float d, float mean) {
+    DivPrep v;
+    v.r = __frcp_rn(d);
+    v.nd = -d;
+    const bool ok = d >= 0x1p-20f && d <= 0x1p20f && (__float_as_uint(d) & 0x7FFFFFu) <= 0x7FFFFBu;
+    v.tlow = !ok ? INFINITY : fabsf(mean) >= 0x1p-75f ? 0.0f : 0x1p-100f;
+    return v;
+}
+
+// Two quotients t / d (both lanes one divisor); *ok is cleared when a lane
+// falls outside the proven ranges.
+__device__ __forceinline__ float2 div2_prepared(float2 t, const DivPrep &v, bool *ok) {
+    const float2 r = make_float2(v.r, v.r), nd = make_float2(v.nd, v.nd);
+    const float2 q0 = __fmul2_rn(t, r);
+    const float2 q1 = __ffma2_rn(__ffma2_rn(q0, nd, t), r, q0);
+    const float2 q2 = __ffma2_rn(__ffma2_rn(q1, nd, t), r, q1);
+    *ok = *ok & (fabsf(t.x) >= v.tlow) & (fabsf(t.y) >= v.tlow) & (fabsf(q2.x) <= 0x1p100f) &
+          (fabsf(q2.y) <= 0x1p100f);
+    return q2;
+}
+
+// A group of G 16-bit elements whose chain divides by the row's d: pre(x)
+// forms two elements' t (x: their binary32 values) exactly as the chain does,
+// the quotient is div2_prepared's, tail(q) finishes one element's chain in
+// binary32 and exact(x) is the whole chain with the IEEE divide, for the
+// elements outside the proven ranges.  The group moves as 32-bit words, two
+// elements each; the rare refused pairs are recomputed in one rolled loop
+// (the words rotate through slot 0, so every index stays a constant and the
+// arrays stay in registers).
+template <class T, int G, bool SA, class Pre, class Tail, class Exact>
+__device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &v, Pre pre,
+                                               Tail tail, Exact exact) {
+    if constexpr (G % 2 == 0 && !SA) {
+        constexpr int W = G / 2;
+        uint32_t aw[W], ow[W];
+        memcpy(aw, a, sizeof(aw));
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            const float2 q = div2_prepared(pre(widen2<T>(aw[k])), v, &ok);
+            ow[k] = round2<T>(tail(q.x), tail(q.y));
+        }
+        if (!ok) {   // rare (zeros, extreme quotients): those elements again, exactly
+#pragma unroll 1
+            for (int k = 0; k < W; ++k) {
+                const uint32_t x = aw[0];
+                bool pok = true;
+                div2_prepared(pre(widen2<T>(x)), v, &pok);
+                uint32_t r = ow[0];
+                if (!pok)
+                    r = bits_of(exact(half_of<T>(x, false))) |
+                        (bits_of(exact(half_of<T>(x, true))) << 16);
+#pragma unroll
+                for (int i = 0; i + 1 < W; ++i) {
+                    aw[i] = aw[i + 1];
+                    ow[i] = ow[i + 1];
+                }
+                aw[W - 1] = x;
+                ow[W - 1] = r;
+            }
+        }
+        memcpy(o, ow, sizeof(ow));
+    } else {
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+            const T x = a[SA ? 0 : k];
+            bool ok = true;
+            const float xf = Tr<T>::in(x);
+            const float2 q = div2_prepared(pre(make_float2(xf, xf)), v, &ok);
+            o[k] = ok ? Tr<T>::out(tail(q.x)) : exact(x);
+        }
+    }
+}
+
 template <class T> struct OpPRelu : PlainB<T, T> {
     static constexpr bool kLegal = is_fp_v<T> || is_pow_int_v<T> ||      // ONNX PRelu T
                                    std::is_same_v<T, uint32_t> || std::is_same_v<T, uint64_t>;
@@ -686,12 +844,18 @@ template <class T> struct OpMulAdd {
 // Inference BatchNormalization: y = (x - mean) / sqrt(var + eps) * scale + bias,
 // each step rounded in the compute type (binary32, or binary64 for DOUBLE) in
 // the order written.  B holds four rows (scale, bias, mean, var) of `plane`
-// elements; the per-channel sqrt is formed when the parameters are loaded.  (A
-// per-channel reciprocal with a remainder-checked correction was measured
-// slower than the IEEE divide on GB300, so the divide stays.)
+// elements; the per-channel sqrt is formed when the parameters are loaded.
+// For float16 and bfloat16 x the per-channel divisor is prepared once (its
+// reciprocal) and each quotient is formed by the exact prepared division
+// (div_prep / div2_prepared), the IEEE divide only outside its ranges.
 template <class C> struct BNParams {
     C scale, bias, mean, d;
+    DivPrep v;          // 16-bit outputs: the prepared division's row constants
 };
+
+// float16 and bfloat16 outputs (a binary32 chain) divide with the prepared
+// exact division, a group of elements at a time
+template <class T> constexpr bool prepared_v = is_half_like_v<T>;
 
 // P: the parameter block's element type, as for BiasPRelu.
 template <class T, class P = T> struct OpBN {
@@ -706,6 +870,7 @@ template <class T, class P = T> struct OpBN {
     static constexpr bool kPlainB = false;
     static constexpr bool kLegal = is_fp_v<T> && is_fp_v<P>;
     static constexpr bool kValidates = false;
+    static constexpr bool kGroup = prepared_v<T>;    // apply_group: the prepared division
     __device__ __forceinline__ static BV loadB(const P *B, int64_t off, const OpArgs &p) {
         BV r;
         r.scale = (C)Tr<P>::in(B[off]);
@@ -713,6 +878,7 @@ template <class T, class P = T> struct OpBN {
         r.mean = (C)Tr<P>::in(B[off + 2 * p.plane]);
         const C var = (C)Tr<P>::in(B[off + 3 * p.plane]);
         r.d = sqrt_rn(add_rn(var, (C)p.eps));
+        if constexpr (prepared_v<T>) r.v = div_prep(r.d, r.mean);
         return r;
     }
     __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
@@ -720,6 +886,18 @@ template <class T, class P = T> struct OpBN {
         t = div_rn(t, q.d);
         t = mul_rn(t, q.scale);
         return Tr<T>::out(add_rn(t, q.bias));
+    }
+    // G elements sharing one channel's parameters (16-bit outputs): the same
+    // chain with the quotient from the prepared exact division (div_prep).
+    template <int G, bool SA>
+    __device__ __forceinline__ static void apply_group(const T *a, const BV &q, T *o,
+                                                       const OpArgs &p, uint32_t &err) {
+        // t = x - mean; t / d prepared; then * scale + bias with the scalar _rn
+        // operations (never contracted into a fused multiply-add)
+        prepared_group<T, G, SA>(
+            a, o, q.v, [&](float2 x) { return __fadd2_rn(x, make_float2(-q.mean, -q.mean)); },
+            [&](float qd) { return __fadd_rn(__fmul_rn(qd, q.scale), q.bias); },
+            [&](T x) { return apply(x, q, p, err); });
     }
 };
 
@@ -732,6 +910,7 @@ template <class T, class P = T> struct OpBN {
 // var) of `plane` elements, read once per row with the sqrt formed there.
 template <class C> struct ChainParams {
     C bias, slope, scale, bn_bias, mean, d;
+    DivPrep v;          // 16-bit outputs: the prepared division's row constants
 };
 
 // P: the parameter block's element type, as for BiasPRelu.
@@ -753,6 +932,7 @@ template <class T, class P = T> struct OpBiasPReluBN {
         r.bn_bias = (C)Tr<P>::in(B[off + 3 * p.plane]);
         r.mean = (C)Tr<P>::in(B[off + 4 * p.plane]);
         r.d = sqrt_rn(add_rn((C)Tr<P>::in(B[off + 5 * p.plane]), (C)p.eps));
+        if constexpr (prepared_v<T>) r.v = div_prep(r.d, r.mean);
         return r;
     }
     __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
@@ -760,6 +940,24 @@ template <class T, class P = T> struct OpBiasPReluBN {
         if (!(t >= 0)) t = mul_rn(q.slope, t);
         t = div_rn(sub_rn(t, q.mean), q.d);
         return Tr<T>::out(add_rn(mul_rn(t, q.scale), q.bn_bias));
+    }
+    static constexpr bool kGroup = prepared_v<T>;
+    // G elements of one channel (16-bit outputs): the same chain with the
+    // quotient from the prepared exact division (div_prep).
+    template <int G, bool SA>
+    __device__ __forceinline__ static void apply_group(const T *a, const BV &q, T *o,
+                                                       const OpArgs &p, uint32_t &err) {
+        // the bias add, PReLU and mean subtraction one element at a time with
+        // the scalar _rn operations (never contracted into a fused multiply-add)
+        auto pre1 = [&](float x) {
+            float t = __fadd_rn(x, q.bias);
+            if (!(t >= 0.0f)) t = __fmul_rn(q.slope, t);
+            return __fsub_rn(t, q.mean);
+        };
+        prepared_group<T, G, SA>(
+            a, o, q.v, [&](float2 x) { return make_float2(pre1(x.x), pre1(x.y)); },
+            [&](float qd) { return __fadd_rn(__fmul_rn(qd, q.scale), q.bn_bias); },
+            [&](T x) { return apply(x, q, p, err); });
     }
 };
 
