@@ -689,18 +689,19 @@ template <class T> __device__ __forceinline__ uint32_t bits_of(T v) {
 // Dev. 34(1), 1990), applied twice.
 //
 // Ranges.  A row takes it when 2^-20 <= d <= 2^20 and D <= 2^24 - 5; an
-// element keeps q2 when |t| >= tlow and |q2| <= 2^100.  With |t| >= 2^-100 the
-// remainders' granularity 2^(eq + ed) ~ |t| 2^-46 stays at or above 2^-149
-// and every quantity is normal; |q2| <= 2^100 keeps every step finite (an
-// infinite or NaN t, or an overflowing quotient, gives a NaN or infinite q2).
-// For t = +0 the steps give q2 = +0 exactly, but t = -0 comes out as +0.
-// The chains divide t = t' - mean with t' and mean binary32 values; when
-// |mean| >= 2^-75, t is +0 or at least 2^-99 in magnitude (two binary32 values
-// at or above 2^-76 differ by a multiple of 2^-99), and never -0, so such
-// rows take tlow = 0; other rows take tlow = 2^-100 and send their zeros to
-// the IEEE divide, as they do tiny, huge, infinite and NaN quotients.
+// element keeps q2 when tlow <= |t| <= thigh = RD(2^99 d).  The upper bound
+// keeps |t / d| <= 2^99 and every step finite (and fails for an infinite or NaN
+// t).  With |t| >= 2^-100 the remainders' granularity 2^(eq + ed) ~ |t| 2^-46
+// stays at or above 2^-149 and every quantity is normal.  For t = +0 the steps
+// give q2 = +0 exactly, but t = -0 comes out as +0.  The chains divide
+// t = t' - mean with t' and mean binary32 values; when |mean| >= 2^-75, t is +0
+// or at least 2^-99 in magnitude (two binary32 values at or above 2^-76 differ
+// by a multiple of 2^-99), and never -0, so such rows need no lower test
+// (tlow = 0); other rows take tlow = 2^-100 and send their zeros to the IEEE
+// divide, as they do tiny, huge, infinite and NaN quotients.
 struct DivPrep {
-    float r, nd, tlow;      // RN(1/d), -d, the least |t| kept (+inf: the row is refused)
+    float r, nd;            // RN(1/d), -d
+    float tlow, thigh;      // |t| kept in [tlow, thigh] (thigh = -1: the row is refused)
 };
 
 __device__ __forceinline__ DivPrep div_prep(float d, float mean) {
@@ -708,19 +709,23 @@ __device__ __forceinline__ DivPrep div_prep(float d, float mean) {
     v.r = __frcp_rn(d);
     v.nd = -d;
     const bool ok = d >= 0x1p-20f && d <= 0x1p20f && (__float_as_uint(d) & 0x7FFFFFu) <= 0x7FFFFBu;
-    v.tlow = !ok ? INFINITY : fabsf(mean) >= 0x1p-75f ? 0.0f : 0x1p-100f;
+    v.tlow = fabsf(mean) >= 0x1p-75f ? 0.0f : 0x1p-100f;
+    v.thigh = ok ? __fmul_rd(d, 0x1p99f) : -1.0f;
     return v;
 }
 
 // Two quotients t / d (both lanes one divisor); *ok is cleared when a lane
-// falls outside the proven ranges.
+// falls outside the proven ranges.  LOW: test the lower bound too (rows with
+// tlow > 0).
+template <bool LOW>
 __device__ __forceinline__ float2 div2_prepared(float2 t, const DivPrep &v, bool *ok) {
     const float2 r = make_float2(v.r, v.r), nd = make_float2(v.nd, v.nd);
     const float2 q0 = __fmul2_rn(t, r);
     const float2 q1 = __ffma2_rn(__ffma2_rn(q0, nd, t), r, q0);
     const float2 q2 = __ffma2_rn(__ffma2_rn(q1, nd, t), r, q1);
-    *ok = *ok & (fabsf(t.x) >= v.tlow) & (fabsf(t.y) >= v.tlow) & (fabsf(q2.x) <= 0x1p100f) &
-          (fabsf(q2.y) <= 0x1p100f);
+    const float ax = fabsf(t.x), ay = fabsf(t.y);
+    *ok = *ok & (ax <= v.thigh) & (ay <= v.thigh);
+    if constexpr (LOW) *ok = *ok & (ax >= v.tlow) & (ay >= v.tlow);
     return q2;
 }
 
@@ -740,17 +745,25 @@ __device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &
         uint32_t aw[W], ow[W];
         memcpy(aw, a, sizeof(aw));
         bool ok = true;
+        if (v.tlow == 0.0f) {   // uniform per row: the common rows test one bound
 #pragma unroll
-        for (int k = 0; k < W; ++k) {
-            const float2 q = div2_prepared(pre(widen2<T>(aw[k])), v, &ok);
-            ow[k] = round2<T>(tail(q.x), tail(q.y));
+            for (int k = 0; k < W; ++k) {
+                const float2 q = div2_prepared<false>(pre(widen2<T>(aw[k])), v, &ok);
+                ow[k] = round2<T>(tail(q.x), tail(q.y));
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                const float2 q = div2_prepared<true>(pre(widen2<T>(aw[k])), v, &ok);
+                ow[k] = round2<T>(tail(q.x), tail(q.y));
+            }
         }
         if (!ok) {   // rare (zeros, extreme quotients): those elements again, exactly
 #pragma unroll 1
             for (int k = 0; k < W; ++k) {
                 const uint32_t x = aw[0];
                 bool pok = true;
-                div2_prepared(pre(widen2<T>(x)), v, &pok);
+                div2_prepared<true>(pre(widen2<T>(x)), v, &pok);
                 uint32_t r = ow[0];
                 if (!pok)
                     r = bits_of(exact(half_of<T>(x, false))) |
@@ -771,7 +784,7 @@ __device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &
             const T x = a[SA ? 0 : k];
             bool ok = true;
             const float xf = Tr<T>::in(x);
-            const float2 q = div2_prepared(pre(make_float2(xf, xf)), v, &ok);
+            const float2 q = div2_prepared<true>(pre(make_float2(xf, xf)), v, &ok);
             o[k] = ok ? Tr<T>::out(tail(q.x)) : exact(x);
         }
     }
@@ -782,7 +795,12 @@ template <class T> struct OpPRelu : PlainB<T, T> {
                                    std::is_same_v<T, uint32_t> || std::is_same_v<T, uint64_t>;
     static constexpr bool kValidates = false;
     __device__ __forceinline__ static T apply(T a, T slope, const OpArgs &, uint32_t &) {
-        if constexpr (is_fp_v<T>) {
+        if constexpr (is_half_like_v<T>) {
+            // x >= 0 goes back through the rounding unchanged (-0 included), so
+            // both branches round once and pairs of results convert together
+            const float x = Tr<T>::in(a);
+            return Tr<T>::out(x >= 0.0f ? x : __fmul_rn(Tr<T>::in(slope), x));
+        } else if constexpr (is_fp_v<T>) {
             const auto x = Tr<T>::in(a);
             if (x >= 0) return a;                                // keeps -0 and exact bits
             return Tr<T>::out(mul_rn(Tr<T>::in(slope), x));

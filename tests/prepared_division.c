@@ -4,9 +4,9 @@
  * with the engine or the oracle).  Restated from the algorithm:
  *     r = RN(1/d);  q0 = RN(t r);  q1 = RN(q0 + RN(t - q0 d) r);
  *     q2 = RN(q1 + RN(t - q1 d) r)                   (remainders and updates: FMAs)
- * kept when 2^-20 <= d <= 2^20, d's significand is at most 2^24 - 5,
- * |t| >= tlow and |q2| <= 2^100 (tlow = 2^-100, or 0 where the caller's t
- * is known to be +0 or at least 2^-99 in magnitude).  pd_check counts, over
+ * kept when 2^-20 <= d <= 2^20, d's significand is at most 2^24 - 5 and
+ * tlow <= |t| <= RD(2^99 d) (tlow = 2^-100, or 0 where the caller's t is
+ * known to be +0 or at least 2^-99 in magnitude).  pd_check counts, over
  * pairs (t, d), the quotients kept, refused, and kept but different from the
  * correctly rounded t / d.
  * `corrections` = 2 is the engine's scheme; 0 plants a scheme without them.
@@ -31,7 +31,9 @@ void pd_check(const float *ts, const float *ds, int64_t n, int corrections, floa
             float rem = fmaf(q, -d, t);
             q = fmaf(rem, r, q);
         }
-        if (!(row_ok && fabsf(t) >= tlow && fabsf(q) <= 0x1p100f)) { counts[1]++; continue; }
+        /* RD(2^99 d): 2^99 d is exact (d is a binary32 value well inside the range) */
+        float thigh = d * 0x1p99f;
+        if (!(row_ok && fabsf(t) >= tlow && fabsf(t) <= thigh)) { counts[1]++; continue; }
         counts[0]++;
         volatile float vt = t;
         float want = vt / vd;                     /* IEEE division, round to nearest */
