@@ -950,7 +950,12 @@ template <class T, class P = T> struct OpBiasPReluBN {
         r.bn_bias = (C)Tr<P>::in(B[off + 3 * p.plane]);
         r.mean = (C)Tr<P>::in(B[off + 4 * p.plane]);
         r.d = sqrt_rn(add_rn((C)Tr<P>::in(B[off + 5 * p.plane]), (C)p.eps));
-        if constexpr (prepared_v<T>) r.v = div_prep(r.d, r.mean);
+        if constexpr (prepared_v<T>) {
+            r.v = div_prep(r.d, r.mean);
+            // the group form takes PReLU as max(t, slope t): rows whose slope is
+            // above 1, infinite or NaN take the exact chain throughout
+            if (!(r.slope <= 1.0f && r.slope >= -INFINITY)) r.v.thigh = -1.0f;
+        }
         return r;
     }
     __device__ __forceinline__ static T apply(T a, const BV &q, const OpArgs &, uint32_t &) {
@@ -965,15 +970,22 @@ template <class T, class P = T> struct OpBiasPReluBN {
     template <int G, bool SA>
     __device__ __forceinline__ static void apply_group(const T *a, const BV &q, T *o,
                                                        const OpArgs &p, uint32_t &err) {
-        // the bias add, PReLU and mean subtraction one element at a time with
-        // the scalar _rn operations (never contracted into a fused multiply-add)
-        auto pre1 = [&](float x) {
-            float t = __fadd_rn(x, q.bias);
-            if (!(t >= 0.0f)) t = __fmul_rn(q.slope, t);
-            return __fsub_rn(t, q.mean);
+        // The bias add, PReLU and mean subtraction on pairs.  PReLU as
+        // max(t1, slope t1): for a finite slope <= 1 this is t1 for t1 > 0 and
+        // slope t1 for t1 < 0, as the select; for t1 = +-0 the two may give
+        // zeros of other signs, which t1' - mean turns into the same t when
+        // mean != 0 (rows with |mean| < 2^-75 send zero t to the exact chain);
+        // an infinite t1 makes t infinite, outside the range.  No product
+        // feeds an addition here (the max stands between), so nothing can be
+        // contracted into a fused multiply-add.
+        auto pre2 = [&](float2 x) {
+            const float2 t1 = __fadd2_rn(x, make_float2(q.bias, q.bias));
+            const float2 s1 = __fmul2_rn(t1, make_float2(q.slope, q.slope));
+            return __fadd2_rn(make_float2(fmaxf(t1.x, s1.x), fmaxf(t1.y, s1.y)),
+                              make_float2(-q.mean, -q.mean));
         };
         prepared_group<T, G, SA>(
-            a, o, q.v, [&](float2 x) { return make_float2(pre1(x.x), pre1(x.y)); },
+            a, o, q.v, pre2,
             [&](float qd) { return __fadd_rn(__fmul_rn(qd, q.scale), q.bn_bias); },
             [&](T x) { return apply(x, q, p, err); });
     }
