@@ -534,53 +534,89 @@ __global__ void __launch_bounds__(kThreads) k_rows(KArgs p, RowArgs r) {
 
 // ---------------------------------------------------------------- short rows
 //
-// REPEATED_BLOCK whose rows are not a whole number of 16-byte packs (a
-// channels-last per-channel operand of 3 or 4 channels, rows of 13): the
-// dense input and the output are flat arrays, read and written in packs of G
-// as in k_scalar; the other input is X[e mod P] (a row block reused) or
-// X[e / P] (one value per row) for output element e, with P the row length.
-// The row position is decoded once per pack and stepped with selects.
-// Indices are 32-bit: the launcher sends plans of 2^31 elements or more to the
-// general kernel.
-template <class Op, bool DENSE_A, bool PER_ROW, int U>
-__global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int32_t P, FastDiv fP) {
+// Plans whose rows are short or off the 16-byte pack width: a channels-last
+// per-channel operand of 3 or 4 channels, rows of 13, and the general shapes
+// [a, 1, k] x [1, b, k] and [a, 1] x [1, k] with small k.  The output is
+// streamed flat in packs of G elements, as in k_scalar.  After coalescing the
+// plan is [n0,] n1, n2: an optional outer index over blocks of Lb = n1 n2
+// elements, and in each block rows of P = n2.  For output element e, with
+// (i0, f) = (e / Lb, e mod Lb) and (q, r) = (f / P, f mod P), each input is
+// read at i0 s0 + one of
+//   DENSE     f   (dense within the block; read in 16-byte packs),
+//   ROWVAL    q   (one value per row),
+//   ROWBLOCK  r   (one row of P values reused by every row).
+// The position (i0, f, q, r) is decoded once per pack and stepped with
+// selects; a pack never crosses a block (Lb is a multiple of G when there is
+// an outer index).  Indices are 32-bit: the launcher sends plans of 2^31
+// elements or more to the row kernel.
+enum PMode { PM_DENSE = 0, PM_ROWVAL = 1, PM_ROWBLOCK = 2 };
+
+struct PeriodicArgs {
+    int32_t P;          // row length (innermost extent)
+    int32_t Lb;         // block length (numel when there is no outer index)
+    int32_t sa0, sb0;   // A's and B's element strides along the outer index
+    FastDiv fP, fLb;
+};
+
+template <class Op, int MA, int MB, int U>
+__global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, PeriodicArgs a) {
     pdl_launch();
     using In = typename Op::In;
     using Out = typename Op::Out;
     using BIn = typename BInOf<Op>::type;
+    using BV = typename Op::BV;
+    static_assert(!(MA == PM_DENSE && MB == PM_DENSE), "one input at least repeats");
+    static_assert(MB != PM_DENSE || Op::kPlainB, "a dense B is read in packs of A's type");
     constexpr int G = 16 / sizeof(In);
     const In *A = static_cast<const In *>(p.A);
     const BIn *B = static_cast<const BIn *>(p.B);
     Out *O = static_cast<Out *>(p.out);
-    const In *D = DENSE_A ? A : reinterpret_cast<const In *>(B);
     const int64_t ng = p.numel / G;
     const int64_t step = (int64_t)gridDim.x * (kThreads * U);
     uint32_t err = 0;
+    // offsets of element e = i0 Lb + f
+    auto decode = [&](int32_t e, int32_t &i0, int32_t &f) {
+        i0 = (int32_t)fastdiv((uint32_t)e, a.fLb);
+        f = e - i0 * a.Lb;
+    };
     pdl_wait();
     for (int64_t base = (int64_t)blockIdx.x * (kThreads * U) + threadIdx.x; base < ng;
          base += step) {
-        Pack<In, G> d[U];
+        Pack<In, G> da[MA == PM_DENSE ? U : 1];
+        Pack<In, G> db[MB == PM_DENSE ? U : 1];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t g = base + (int64_t)u * kThreads;
-            if (g < ng) d[u] = ld_stream<In, G>(D + g * G);
+            if (g < ng) {
+                int32_t i0, f;
+                decode((int32_t)(g * G), i0, f);
+                if constexpr (MA == PM_DENSE) da[u] = ld_stream<In, G>(A + i0 * a.sa0 + f);
+                if constexpr (MB == PM_DENSE)
+                    db[u] = ld_stream<In, G>(reinterpret_cast<const In *>(B) + i0 * a.sb0 + f);
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t g = base + (int64_t)u * kThreads;
             if (g < ng) {
                 const int32_t e0 = (int32_t)(g * G);
-                int32_t q = (int32_t)fastdiv((uint32_t)e0, fP);
-                int32_t r = e0 - q * P;
+                int32_t i0, f;
+                decode(e0, i0, f);
+                int32_t q = (int32_t)fastdiv((uint32_t)f, a.fP);
+                int32_t r = f - q * a.P;
+                const In *pa = A + i0 * a.sa0;
+                const BIn *pb = B + i0 * a.sb0;
                 Pack<Out, G> o;
 #pragma unroll
                 for (int k = 0; k < G; ++k) {
-                    const int32_t xi = PER_ROW ? q : r;
-                    if constexpr (DENSE_A)
-                        o.v[k] = Op::apply(d[u].v[k], Op::loadB(B, xi, p.args), p.args, err);
-                    else
-                        o.v[k] = Op::apply(A[xi], d[u].v[k], p.args, err);
-                    const bool wrap = ++r == P;
+                    In xa;
+                    if constexpr (MA == PM_DENSE) xa = da[u].v[k];
+                    else xa = pa[MA == PM_ROWVAL ? q : r];
+                    BV xb;
+                    if constexpr (MB == PM_DENSE) xb = db[u].v[k];
+                    else xb = Op::loadB(pb, MB == PM_ROWVAL ? q : r, p.args);
+                    o.v[k] = Op::apply(xa, xb, p.args, err);
+                    const bool wrap = ++r == a.P;
                     r = wrap ? 0 : r;
                     q += wrap ? 1 : 0;
                 }
@@ -588,12 +624,104 @@ __global__ void __launch_bounds__(kThreads) k_periodic(KArgs p, int32_t P, FastD
             }
         }
     }
+    // the last numel % G elements, one by one
     for (int64_t e = ng * G + (int64_t)blockIdx.x * kThreads + threadIdx.x; e < p.numel;
          e += (int64_t)gridDim.x * kThreads) {
-        const int32_t q = (int32_t)fastdiv((uint32_t)e, fP);
-        const int32_t xi = PER_ROW ? q : (int32_t)e - q * P;
-        if constexpr (DENSE_A) O[e] = Op::apply(A[e], Op::loadB(B, xi, p.args), p.args, err);
-        else O[e] = Op::apply(A[xi], D[e], p.args, err);
+        int32_t i0, f;
+        decode((int32_t)e, i0, f);
+        const int32_t q = (int32_t)fastdiv((uint32_t)f, a.fP);
+        const int32_t r = f - q * a.P;
+        const int32_t oa = i0 * a.sa0 + (MA == PM_DENSE ? f : MA == PM_ROWVAL ? q : r);
+        const int32_t ob = i0 * a.sb0 + (MB == PM_DENSE ? f : MB == PM_ROWVAL ? q : r);
+        O[e] = Op::apply(A[oa], Op::loadB(B, ob, p.args), p.args, err);
+    }
+    flush_err<Op>(p.status, err);
+}
+
+// ---------------------------------------------------------------- a short row reused in blocks
+//
+// The k_periodic pattern with one input X a row of P <= kBlockRowMaxP values
+// reused by every row of a block (ROWBLOCK) and the other, D, dense in the
+// block: [a, 1, k] x [1, b, k], [n, k] x [k].  The 16-byte pack of X that an
+// output pack needs depends only on the row position r0 = f mod P where the
+// pack starts, so each CTA first lays out in shared memory, for the (at most
+// two) blocks its tile touches, the P rotations of the row:
+//   pat[s][r0][j] = X[(i0 + s) sx0 + (r0 + j) mod P],  j < G,
+// behind one barrier; then each output pack is one 16-byte shared load of X,
+// one 16-byte load of D and one 16-byte store.  One tile of kThreads x U
+// packs per CTA; a block holds at least that many elements (the launcher
+// checks), so a tile spans at most two blocks.  X_IS_A: X is A (else B).
+constexpr int kBlockRowMaxP = 32;
+
+struct BlockRowArgs {
+    int32_t P;          // row length
+    int32_t Lb;         // block length (numel when there is no outer index)
+    int32_t n0;         // blocks
+    int32_t sx0, sd0;   // X's and D's element strides along the outer index
+    FastDiv fP, fLb;
+};
+
+template <class Op, bool X_IS_A, int U>
+__global__ void __launch_bounds__(kThreads) k_blockrow(KArgs p, BlockRowArgs a) {
+    pdl_launch();
+    using In = typename Op::In;
+    using Out = typename Op::Out;
+    static_assert(Op::kPlainB, "both inputs are plain tensors of one type");
+    constexpr int G = 16 / sizeof(In);
+    __shared__ Pack<In, G> pat[2][kBlockRowMaxP];
+    const In *X = static_cast<const In *>(X_IS_A ? p.A : p.B);
+    const In *D = static_cast<const In *>(X_IS_A ? p.B : p.A);
+    Out *O = static_cast<Out *>(p.out);
+    const int64_t ng = p.numel / G;
+    const int64_t tile0 = (int64_t)blockIdx.x * (kThreads * U);
+    const int32_t ib = (int32_t)fastdiv((uint32_t)(tile0 * G), a.fLb);   // the tile's first block
+    pdl_wait();
+    // the rotations of the row of blocks ib and ib + 1
+    for (int idx = threadIdx.x; idx < 2 * a.P * G; idx += kThreads) {
+        const int s = idx / (a.P * G), rem = idx - s * (a.P * G);
+        const int r0 = rem / G, j = rem - r0 * G;
+        if (ib + s < a.n0) {
+            int rj = r0 + j;
+            while (rj >= a.P) rj -= a.P;   // (r0 + j) mod P, at most G / P + 1 steps
+            pat[s][r0].v[j] = X[(ib + s) * a.sx0 + rj];
+        }
+    }
+    __syncthreads();
+    uint32_t err = 0;
+    Pack<In, G> d[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t g = tile0 + (int64_t)u * kThreads + threadIdx.x;
+        if (g < ng) {
+            const int32_t e0 = (int32_t)(g * G);
+            const int32_t i0 = (int32_t)fastdiv((uint32_t)e0, a.fLb);
+            d[u] = ld_stream<In, G>(D + i0 * a.sd0 + (e0 - i0 * a.Lb));
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t g = tile0 + (int64_t)u * kThreads + threadIdx.x;
+        if (g < ng) {
+            const int32_t e0 = (int32_t)(g * G);
+            const int32_t i0 = (int32_t)fastdiv((uint32_t)e0, a.fLb);
+            const int32_t f = e0 - i0 * a.Lb;
+            const int32_t r0 = f - (int32_t)fastdiv((uint32_t)f, a.fP) * a.P;
+            const Pack<In, G> x = pat[i0 - ib][r0];
+            Pack<Out, G> o;
+            if constexpr (X_IS_A) compute_group<Op, G>(x.v, d[u].v, o.v, p.args, err);
+            else compute_group<Op, G>(d[u].v, x.v, o.v, p.args, err);
+            st_stream<Out, G>(O + e0, o);
+        }
+    }
+    // the last numel % G elements (tile 0 is the one that holds them... every
+    // CTA strides over them, one element per thread)
+    for (int64_t e = ng * G + (int64_t)blockIdx.x * kThreads + threadIdx.x; e < p.numel;
+         e += (int64_t)gridDim.x * kThreads) {
+        const int32_t i0 = (int32_t)fastdiv((uint32_t)e, a.fLb);
+        const int32_t f = (int32_t)e - i0 * a.Lb;
+        const int32_t r = f - (int32_t)fastdiv((uint32_t)f, a.fP) * a.P;
+        const In xv = X[i0 * a.sx0 + r], dv = D[i0 * a.sd0 + f];
+        O[e] = X_IS_A ? Op::apply(xv, dv, p.args, err) : Op::apply(dv, xv, p.args, err);
     }
     flush_err<Op>(p.status, err);
 }
@@ -1119,36 +1247,104 @@ cudaError_t run_general(const Launch &L) {
     return run_rows_kernel<Op, 1, 2, 2, false, 2, false>(L);
 }
 
-// REPEATED_BLOCK with rows off the pack width: rank 2, one input dense
-// (strides (P, 1)), the other (0, 1) or (1, 0).
+// The pattern of one input over the last two coalesced dims (n1, n2), for
+// k_periodic: dense (n2, 1), one value per row (1, 0), a reused row (0, 1).
+inline int pmode_of(int64_t s1, int64_t s2, int64_t n2) {
+    if (s1 == n2 && s2 == 1) return PM_DENSE;
+    if (s1 == 1 && s2 == 0) return PM_ROWVAL;
+    if (s1 == 0 && s2 == 1) return PM_ROWBLOCK;
+    return -1;
+}
+
+// Whether k_periodic can stream a plan (rank 2, or rank 3 with an outer
+// index), and its arguments: 32-bit indices, one input at least repeating,
+// packs that stay inside a block and dense inputs whose packs stay aligned.
+// A dense B only for operators whose B is a plain tensor of A's type.
 template <class Op>
-cudaError_t run_periodic(const Launch &L) {
+bool periodic_fits(const Launch &L, int *ma, int *mb, PeriodicArgs *pa) {
+    constexpr int64_t G = 16 / sizeof(typename Op::In);
+    const Geom &g = L.g;
+    if (L.numel >= (1ll << 31) || (g.rank != 2 && g.rank != 3)) return false;
+    const int o = g.rank - 2;          // first of the two inner dims
+    const int64_t n1 = g.n[o], n2 = g.n[o + 1];
+    *ma = pmode_of(g.sa[o], g.sa[o + 1], n2);
+    *mb = pmode_of(g.sb[o], g.sb[o + 1], n2);
+    if (*ma < 0 || *mb < 0 || (*ma == PM_DENSE && *mb == PM_DENSE)) return false;
+    if (*mb == PM_DENSE && !Op::kPlainB) return false;
+    const int64_t sa0 = o ? g.sa[0] : 0, sb0 = o ? g.sb[0] : 0;
+    if (o && (n1 * n2) % G != 0) return false;
+    if ((*ma == PM_DENSE && sa0 % G != 0) || (*mb == PM_DENSE && sb0 % G != 0)) return false;
+    pa->P = (int32_t)n2;
+    pa->Lb = (int32_t)(o ? n1 * n2 : L.numel);
+    pa->sa0 = (int32_t)sa0;
+    pa->sb0 = (int32_t)sb0;
+    pa->fP = make_fastdiv((uint64_t)pa->P);
+    pa->fLb = make_fastdiv((uint64_t)pa->Lb);
+    return true;
+}
+
+// A reused short row against data dense in the block, in blocks of at least
+// one k_blockrow tile: the shared-memory rotations instead of per-element reads.
+constexpr int kBlockRowU = 4;
+
+template <class Op, bool X_IS_A>
+cudaError_t launch_blockrow(const Launch &L, const PeriodicArgs &pa) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    if (L.numel >= (1ll << 31)) return run_general<Op>(L);   // 32-bit indices below
-    const int32_t P = (int32_t)L.g.n[1];
-    const bool a_dense = L.g.sa[0] == P && L.g.sa[1] == 1;
-    const int64_t *xs = a_dense ? L.g.sb : L.g.sa;      // the broadcast input's strides
-    const bool per_row = xs[0] == 1 && xs[1] == 0;
-    const FastDiv fP = make_fastdiv((uint64_t)P);
+    BlockRowArgs b{};
+    b.P = pa.P;
+    b.Lb = pa.Lb;
+    b.n0 = (int32_t)(L.numel / pa.Lb);
+    b.sx0 = X_IS_A ? pa.sa0 : pa.sb0;
+    b.sd0 = X_IS_A ? pa.sb0 : pa.sa0;
+    b.fP = pa.fP;
+    b.fLb = pa.fLb;
+    const int64_t ng = L.numel / G;
+    const int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kBlockRowU);
+    if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
+    return launch_pdl(k_blockrow<Op, X_IS_A, kBlockRowU>, grid, kThreads, L.stream, kargs<Op>(L),
+                      b);
+}
+
+template <class Op, int MA, int MB>
+cudaError_t launch_periodic(const Launch &L, const PeriodicArgs &pa) {
+    constexpr int G = 16 / sizeof(typename Op::In);
     const int64_t ng = L.numel / G;
     int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kUnrollFlat);
     grid = std::min<int64_t>(grid, kMaxGrid);
-    if (a_dense) {
-        if (per_row)
-            return launch_pdl(k_periodic<Op, true, true, kUnrollFlat>, grid, kThreads, L.stream,
-                              kargs<Op>(L), P, fP);
-        return launch_pdl(k_periodic<Op, true, false, kUnrollFlat>, grid, kThreads, L.stream,
-                          kargs<Op>(L), P, fP);
+    return launch_pdl(k_periodic<Op, MA, MB, kUnrollFlat>, grid, kThreads, L.stream, kargs<Op>(L),
+                      pa);
+}
+
+// Short rows and general shapes that k_periodic streams, else the row kernel
+// (the general traversal).  Pointers off 16-byte alignment never reach here
+// (the host sends them to the general family first).
+template <class Op>
+cudaError_t run_periodic(const Launch &L) {
+    int ma, mb;
+    PeriodicArgs pa{};
+    if (!periodic_fits<Op>(L, &ma, &mb, &pa)) return run_general<Op>(L);
+    if constexpr (Op::kPlainB) {
+        constexpr int64_t G = 16 / sizeof(typename Op::In);
+        const bool blockrow = pa.P <= kBlockRowMaxP && pa.Lb >= (int64_t)kThreads * kBlockRowU * G &&
+                              L.numel % pa.Lb == 0;
+        if (blockrow && ma == PM_ROWBLOCK && mb == PM_DENSE) return launch_blockrow<Op, true>(L, pa);
+        if (blockrow && ma == PM_DENSE && mb == PM_ROWBLOCK) return launch_blockrow<Op, false>(L, pa);
+    }
+    switch (ma * 3 + mb) {
+    case PM_DENSE * 3 + PM_ROWVAL: return launch_periodic<Op, PM_DENSE, PM_ROWVAL>(L, pa);
+    case PM_DENSE * 3 + PM_ROWBLOCK: return launch_periodic<Op, PM_DENSE, PM_ROWBLOCK>(L, pa);
+    default: break;
     }
     if constexpr (Op::kPlainB) {
-        if (per_row)
-            return launch_pdl(k_periodic<Op, false, true, kUnrollFlat>, grid, kThreads, L.stream,
-                              kargs<Op>(L), P, fP);
-        return launch_pdl(k_periodic<Op, false, false, kUnrollFlat>, grid, kThreads, L.stream,
-                          kargs<Op>(L), P, fP);
-    } else {
-        return cudaErrorInvalidValue;
+        switch (ma * 3 + mb) {
+        case PM_ROWVAL * 3 + PM_DENSE: return launch_periodic<Op, PM_ROWVAL, PM_DENSE>(L, pa);
+        case PM_ROWBLOCK * 3 + PM_DENSE: return launch_periodic<Op, PM_ROWBLOCK, PM_DENSE>(L, pa);
+        case PM_ROWVAL * 3 + PM_ROWBLOCK: return launch_periodic<Op, PM_ROWVAL, PM_ROWBLOCK>(L, pa);
+        case PM_ROWBLOCK * 3 + PM_ROWVAL: return launch_periodic<Op, PM_ROWBLOCK, PM_ROWVAL>(L, pa);
+        default: break;
+        }
     }
+    return run_general<Op>(L);
 }
 
 // Operators that accept a scalar B given as an attribute (Op::kScalarAttr).
@@ -1169,6 +1365,15 @@ cudaError_t launch_with_scalar(const Launch &L) {
     case FAM_GENERAL_STRIDED: return run_general<W>(L);
     default: return cudaErrorInvalidValue;
     }
+}
+
+// The buffers allow 16-byte input packs and packs of G outputs (the host
+// sends unaligned buffers to the general family, whose row traversal reads
+// element by element).
+template <class Op> bool packs_aligned(const Launch &L) {
+    constexpr uintptr_t G = 16 / sizeof(typename Op::In);
+    return (uintptr_t)L.A % 16 == 0 && (!L.B || (uintptr_t)L.B % 16 == 0) &&
+           (uintptr_t)L.out % (G * sizeof(typename Op::Out)) == 0;
 }
 
 // Launch the kernel of L.family for operator functor Op.
@@ -1193,7 +1398,11 @@ cudaError_t launch_op(const Launch &L) {
             if (L.g.rank == 2) return run_rows_vector<Op, true>(L);
             return run_rows_vector<Op, false>(L);
         case FAM_INNER_VECTOR_OUTER: return run_rows_vector<Op, false>(L);
-        case FAM_GENERAL_STRIDED: return run_general<Op>(L);
+        case FAM_GENERAL_STRIDED:
+            // short rows and outer products stream flat when the buffers allow
+            // 16-byte packs; anything else takes the general row traversal
+            if (packs_aligned<Op>(L)) return run_periodic<Op>(L);
+            return run_general<Op>(L);
         default: return cudaErrorInvalidValue;
         }
     }

@@ -20,6 +20,10 @@ operand j of a workload uses stream seed*16 + j.
   5  Greater fp16 A[64,1,512,1] vs B[1,32,1,1024] ~ N(0,1) -> 1-byte BOOL
      [64,32,512,1024]; BitShift RIGHT uint32 A[2^26] raw bits by B[1] in
      [0,31]                                                               seed 4
+Not from the pages:
+  6  Add fp32 [2^24,3] ~ N(0,1) + [3] ~ U(-0.5,0.5) (channels-last)       seed 5
+  7  general strided, short rows: Add fp32 [8192,1,5] + [1,4096,5] and
+     Mul bf16 [16384,1,3] x [1,8192,3], all ~ N(0,1)                      seed 6
 """
 from __future__ import annotations
 
@@ -150,6 +154,20 @@ def cases(scale_log2: int = 0) -> list[Case]:
                     lambda: make("normal", "float32", nhwc, 5, 0),
                     lambda: make("uniform", "float32", (3,), 5, 1, lo=-0.5, hi=0.5),
                     "repeated_block", 6, ["extra"]))
+    # not from the pages: general-strided broadcasts with short rows, both
+    # operands broadcast ([a, 1, k] against [1, b, k]), several times the L2
+    # in output bytes: Add fp32 out [8192, 4096, 5] (671 MB) and Mul bf16
+    # out [16384, 8192, 3] (805 MB)
+    ga, gb = (1 << max(13 - scale_log2, 4), 1, 5), (1, 1 << max(12 - scale_log2, 4), 5)
+    out.append(Case("add_f32_general_short_rows", "Add", "float32", {}, ga, gb,
+                    lambda: make("normal", "float32", ga, 6, 0),
+                    lambda: make("normal", "float32", gb, 6, 1),
+                    "general_strided", 7, ["extra"]))
+    ma, mb = (1 << max(14 - scale_log2, 4), 1, 3), (1, 1 << max(13 - scale_log2, 4), 3)
+    out.append(Case("mul_bf16_general_short_rows", "Mul", "bfloat16", {}, ma, mb,
+                    lambda: make("normal", "bfloat16", ma, 6, 2),
+                    lambda: make("normal", "bfloat16", mb, 6, 3),
+                    "general_strided", 7, ["extra"]))
     return out
 
 

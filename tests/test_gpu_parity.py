@@ -372,3 +372,80 @@ def test_prepared_division_on_every_16bit_value(op, dtype):
                 assert family == fam, what
                 assert_bits_equal(got, want, dtype, what)
                 assert bits == 0, what
+
+
+# k_periodic: [n0,] n1, n2 with each input dense in the block, one value per
+# row, or one reused row; (shape A, shape B, the pattern of A and of B)
+PERIODIC_CASES = [
+    ((7, 1, 5), (1, 12, 5)),        # reused row x dense block (the [a,1,k] x [1,b,k] shape)
+    ((6, 8, 3), (6, 1, 3)),         # dense x reused row, outer strides 24 and 3
+    ((5, 8, 3), (1, 8, 1)),         # dense x one value per row (per channel, short rows)
+    ((1, 8, 1), (5, 8, 3)),         # one value per row x dense
+    ((4, 8, 1), (4, 1, 6)),         # one value per row x reused row, with an outer index
+    ((9, 1), (1, 7)),               # short outer products, both orders
+    ((1, 7), (9, 1)),
+    ((300, 7), (7,)),               # rank 2: dense x reused row
+    # blocks of at least one k_blockrow tile (row rotations in shared memory)
+    ((3, 1, 5), (1, 4000, 5)),      # reused row x dense block
+    ((1, 4000, 5), (3, 1, 5)),      # dense block x reused row
+    ((4001, 3), (3,)),              # rank 2, with a ragged tail of numel % 16-byte packs
+    ((3, 1, 32), (1, 700, 32)),     # the longest row taken (32)
+    ((3, 1, 33), (1, 700, 33)),     # one longer: element by element
+]
+
+
+def _run_offset(op, dtype, a, b, offset, attrs=None):
+    """The engine on buffers shifted `offset` bytes off 16-byte alignment."""
+    import torch
+    desc = eb.descriptor(op, dtype, **(attrs or {}))
+    plan = eb.Plan(desc, a.shape, b.shape)
+    bufs = []
+    for x in (a, b):
+        raw = np.ascontiguousarray(x).reshape(-1).view(np.uint8)
+        bufs.append(to_device(np.concatenate([np.zeros(offset, np.uint8), raw,
+                                              np.zeros(16, np.uint8)])))
+    osz = eb.ITEMSIZE[desc.out_dtype]
+    out = torch.zeros(plan.numel * osz + offset + 16, dtype=torch.uint8, device="cuda")
+    eb.ebin_execute(plan.handle, bufs[0].data_ptr() + offset, bufs[1].data_ptr() + offset,
+                    out.data_ptr() + offset, None)
+    bits = eb.get_device_status()
+    host = out.cpu().numpy()[offset:offset + plan.numel * osz]
+    return host.view(datagen.STORAGE[desc.out_dtype]).reshape(plan.output_shape), bits
+
+
+@pytest.mark.parametrize("op,dtype", [("Add", "float32"), ("Mul", "bfloat16"),
+                                      ("Sub", "float64"), ("Greater", "float16"),
+                                      ("Mod", "int32"), ("BitwiseXor", "uint8"),
+                                      ("Max", "int64")])
+def test_short_rows_stream_flat(op, dtype):
+    """Short-row repeated blocks, [a,1,k] x [1,b,k] general broadcasts and short
+    outer products stream flat (k_periodic) when the buffers are aligned, and
+    through the general row traversal when they are not: bit-identical to the
+    oracle either way, status bits included."""
+    attrs = {"fmod": 0} if op == "Mod" else {}
+    for i, (sa, sb) in enumerate(PERIODIC_CASES):
+        a, b = inputs_for(op, dtype, sa, sb, seed=60 + i)
+        want, want_bits = oracle.run(op, a, b, dtype, **oracle_kwargs(attrs))
+        for forced in (None, "general_strided"):
+            got, bits, fam = run_engine(op, dtype, a, b, family=forced, attrs=attrs)
+            what = "%s %s %s x %s forced=%s family %s" % (op, dtype, sa, sb, forced, fam)
+            compare(op, dtype, got, want, what)
+            assert bits == want_bits, what
+        got, bits = _run_offset(op, dtype, a, b, eb.ITEMSIZE[dtype], attrs)
+        compare(op, dtype, got, want, "%s %s %s x %s unaligned" % (op, dtype, sa, sb))
+        assert bits == want_bits
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+def test_per_channel_short_rows_stream_flat(dtype):
+    """BatchNormalization and PRelu per channel on short spatial rows (NCW with
+    W = 3): one value per row against dense data, with an outer index."""
+    for op, sb in (("BatchNormalization", (4, 8)), ("PRelu", (8, 1)), ("BiasPReluBN", (6, 8))):
+        sa = (5, 8, 3)
+        a, b = inputs_for(op, dtype, sa, sb, seed=77)
+        want, _ = oracle.run(op, a, b, dtype, **({"eps": 1e-5} if op != "PRelu" else {}))
+        for forced in (None, "general_strided"):
+            got, bits, fam = run_engine(op, dtype, a, b, family=forced,
+                                        attrs={"epsilon": 1e-5} if op != "PRelu" else {})
+            assert_bits_equal(got, want, dtype, "%s %s forced=%s" % (op, dtype, forced))
+            assert bits == 0

@@ -149,6 +149,9 @@ def test_families_of_the_benchmark_workloads():
     assert family("Clip", "float32", (30, 40), (2,))[0] == "right_scalar"
     assert family("BatchNormalization", "float32", (300, 64), (4, 64))[0] == "repeated_block"
     assert family("Add", "float32", (1 << 24, 3), (3,))[0] == "repeated_block"
+    f, (n, sa, sb) = family("Add", "float32", (8192, 1, 5), (1, 4096, 5))
+    assert f == "general_strided" and n == [8192, 4096, 5] and sa == [5, 0, 1] and sb == [0, 5, 1]
+    assert family("Mul", "bfloat16", (16384, 1, 3), (1, 8192, 3))[0] == "general_strided"
 
 
 def test_repeated_block_rule_for_any_row_length():
