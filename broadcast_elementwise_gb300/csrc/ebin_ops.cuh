@@ -120,6 +120,50 @@ template <class T, class O> struct PlainB {
     }
 };
 
+// float16 and bfloat16: computed through binary32
+template <class T> constexpr bool is_half_like_v = std::is_same_v<T, __half> ||
+                                                   std::is_same_v<T, __nv_bfloat16>;
+
+// ---------------------------------------------------------------- 16-bit words
+// Groups of 16-bit elements move as 32-bit words, two elements each.
+// Two values rounded to a 16-bit type, packed (the first in the low half).
+template <class T> __device__ __forceinline__ uint32_t round2(float a, float b);
+template <> __device__ __forceinline__ uint32_t round2<__nv_bfloat16>(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    uint32_t w;
+    memcpy(&w, &v, 4);
+    return w;
+}
+template <> __device__ __forceinline__ uint32_t round2<__half>(float a, float b) {
+    const __half2 v = __floats2half2_rn(a, b);
+    uint32_t w;
+    memcpy(&w, &v, 4);
+    return w;
+}
+
+// Two 16-bit values of one 32-bit word (the first in the low half), widened
+// exactly to binary32; and the value in one half of a word.
+template <class T> __device__ __forceinline__ float2 widen2(uint32_t w);
+template <> __device__ __forceinline__ float2 widen2<__nv_bfloat16>(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <> __device__ __forceinline__ float2 widen2<__half>(uint32_t w) {
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __half22float2(h);
+}
+template <class T> __device__ __forceinline__ T half_of(uint32_t w, bool high) {
+    const unsigned short b = (unsigned short)(high ? (w >> 16) : (w & 0xFFFFu));
+    T v;
+    memcpy(&v, &b, 2);
+    return v;
+}
+template <class T> __device__ __forceinline__ uint32_t bits_of(T v) {
+    unsigned short b;
+    memcpy(&b, &v, 2);
+    return b;
+}
+
 // ---------------------------------------------------------------- exact fmod
 //
 // Truncated remainder r = a - trunc(a/b)*b, exact, for finite a and nonzero
@@ -163,6 +207,29 @@ template <class T, int K> struct OpArith : PlainB<T, T> {
     static constexpr bool kLegal = is_fp_v<T> || is_int_v<T>;
     static constexpr bool kValidates = (K == K_DIV || K == K_RDIV) && is_int_v<T>;
     static constexpr bool kScalarAttr = is_fp_v<T>;        // ncnn binaryop with_scalar
+    // Add, Sub, Mul and RSub of float16 / bfloat16 on pairs: two elements
+    // widened from one 32-bit word, one binary32 pair operation (each lane
+    // rounded on its own), the two results rounded by one conversion -- the
+    // values of apply.  Division keeps the element form (the IEEE divide).
+    static constexpr bool kPack = is_half_like_v<T> && K != K_DIV && K != K_RDIV;
+    template <int G>
+    __device__ __forceinline__ static void apply_pack(const T *a, const T *b, T *o) {
+        constexpr int W = G / 2;
+        uint32_t aw[W], bw[W], ow[W];
+        memcpy(aw, a, sizeof(aw));
+        memcpy(bw, b, sizeof(bw));
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            const float2 x = widen2<T>(aw[k]), y = widen2<T>(bw[k]);
+            float2 r;
+            if constexpr (K == K_ADD) r = __fadd2_rn(x, y);
+            else if constexpr (K == K_SUB) r = __fadd2_rn(x, make_float2(-y.x, -y.y));
+            else if constexpr (K == K_RSUB) r = __fadd2_rn(y, make_float2(-x.x, -x.y));
+            else r = __fmul2_rn(x, y);
+            ow[k] = round2<T>(r.x, r.y);
+        }
+        memcpy(o, ow, sizeof(ow));
+    }
     __device__ __forceinline__ static T apply(T a, T b, const OpArgs &, uint32_t &err) {
         if constexpr (K == K_RSUB || K == K_RDIV) {
             // the same operation with the operands exchanged
@@ -513,8 +580,6 @@ template <class C, int K> __device__ __forceinline__ bool compare(C x, C y) {
     else return x >= y;
 }
 
-template <class T> constexpr bool is_half_like_v = std::is_same_v<T, __half> ||
-                                                   std::is_same_v<T, __nv_bfloat16>;
 
 // Two-lane comparison masks (0xFFFF per true lane, NaN compares false).
 template <int K, class T2>
@@ -618,46 +683,6 @@ __device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, 
 __device__ __forceinline__ double div_rn(double a, double b) { return __ddiv_rn(a, b); }
 __device__ __forceinline__ float sqrt_rn(float a) { return __fsqrt_rn(a); }
 __device__ __forceinline__ double sqrt_rn(double a) { return __dsqrt_rn(a); }
-
-// ---------------------------------------------------------------- 16-bit words
-// Groups of 16-bit elements move as 32-bit words, two elements each.
-// Two values rounded to a 16-bit type, packed (the first in the low half).
-template <class T> __device__ __forceinline__ uint32_t round2(float a, float b);
-template <> __device__ __forceinline__ uint32_t round2<__nv_bfloat16>(float a, float b) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    uint32_t w;
-    memcpy(&w, &v, 4);
-    return w;
-}
-template <> __device__ __forceinline__ uint32_t round2<__half>(float a, float b) {
-    const __half2 v = __floats2half2_rn(a, b);
-    uint32_t w;
-    memcpy(&w, &v, 4);
-    return w;
-}
-
-// Two 16-bit values of one 32-bit word (the first in the low half), widened
-// exactly to binary32; and the value in one half of a word.
-template <class T> __device__ __forceinline__ float2 widen2(uint32_t w);
-template <> __device__ __forceinline__ float2 widen2<__nv_bfloat16>(uint32_t w) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-template <> __device__ __forceinline__ float2 widen2<__half>(uint32_t w) {
-    __half2 h;
-    memcpy(&h, &w, 4);
-    return __half22float2(h);
-}
-template <class T> __device__ __forceinline__ T half_of(uint32_t w, bool high) {
-    const unsigned short b = (unsigned short)(high ? (w >> 16) : (w & 0xFFFFu));
-    T v;
-    memcpy(&v, &b, 2);
-    return v;
-}
-template <class T> __device__ __forceinline__ uint32_t bits_of(T v) {
-    unsigned short b;
-    memcpy(&b, &v, 2);
-    return b;
-}
 
 // ---------------------------------------------------------------- prepared exact division
 //
