@@ -655,9 +655,10 @@ constexpr int kBlockRowMaxP = 32;
 
 struct BlockRowArgs {
     int32_t P;          // row length
-    int32_t Lb;         // block length (numel when there is no outer index)
+    int32_t Lb;         // block length, a multiple of P (numel when there is no outer index)
     int32_t n0;         // blocks
     int32_t sx0, sd0;   // X's and D's element strides along the outer index
+    int32_t dr;         // (kThreads * G) mod P: the row position's step between a thread's packs
     FastDiv fP, fLb;
 };
 
@@ -674,7 +675,12 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(KArgs p, BlockRowArgs a) 
     Out *O = static_cast<Out *>(p.out);
     const int64_t ng = p.numel / G;
     const int64_t tile0 = (int64_t)blockIdx.x * (kThreads * U);
-    const int32_t ib = (int32_t)fastdiv((uint32_t)(tile0 * G), a.fLb);   // the tile's first block
+    // the tile's first block ib; packs from pb on lie in block ib + 1 (Lb is a
+    // multiple of G when there is an outer index; else pb >= ng)
+    const int32_t ib = (int32_t)fastdiv((uint32_t)(tile0 * G), a.fLb);
+    const int64_t pb = (int64_t)(ib + 1) * a.Lb / G;
+    // D's element index of output element e in block i0 is i0 (sd0 - Lb) + e
+    const int64_t off0 = (int64_t)ib * (a.sd0 - a.Lb), off1 = off0 + (a.sd0 - a.Lb);
     pdl_wait();
     // the rotations of the row of blocks ib and ib + 1
     for (int idx = threadIdx.x; idx < 2 * a.P * G; idx += kThreads) {
@@ -692,35 +698,33 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(KArgs p, BlockRowArgs a) 
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t g = tile0 + (int64_t)u * kThreads + threadIdx.x;
-        if (g < ng) {
-            const int32_t e0 = (int32_t)(g * G);
-            const int32_t i0 = (int32_t)fastdiv((uint32_t)e0, a.fLb);
-            d[u] = ld_stream<In, G>(D + i0 * a.sd0 + (e0 - i0 * a.Lb));
-        }
+        if (g < ng) d[u] = ld_stream<In, G>(D + ((g >= pb ? off1 : off0) + g * G));
     }
+    // the row position of the thread's first pack (Lb is a multiple of P, so
+    // it does not depend on the block), then stepped by dr from pack to pack
+    const int32_t e_first = (int32_t)((tile0 + threadIdx.x) * G);
+    int32_t r = e_first - (int32_t)fastdiv((uint32_t)e_first, a.fP) * a.P;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t g = tile0 + (int64_t)u * kThreads + threadIdx.x;
         if (g < ng) {
-            const int32_t e0 = (int32_t)(g * G);
-            const int32_t i0 = (int32_t)fastdiv((uint32_t)e0, a.fLb);
-            const int32_t f = e0 - i0 * a.Lb;
-            const int32_t r0 = f - (int32_t)fastdiv((uint32_t)f, a.fP) * a.P;
-            const Pack<In, G> x = pat[i0 - ib][r0];
+            const Pack<In, G> x = pat[g >= pb ? 1 : 0][r];
             Pack<Out, G> o;
             if constexpr (X_IS_A) compute_group<Op, G>(x.v, d[u].v, o.v, p.args, err);
             else compute_group<Op, G>(d[u].v, x.v, o.v, p.args, err);
-            st_stream<Out, G>(O + e0, o);
+            st_stream<Out, G>(O + g * G, o);
         }
+        r += a.dr;
+        r -= r >= a.P ? a.P : 0;
     }
-    // the last numel % G elements (tile 0 is the one that holds them... every
-    // CTA strides over them, one element per thread)
+    // the last numel % G elements, one per thread (rank-2 plans only: with an
+    // outer index the element count is a multiple of G)
     for (int64_t e = ng * G + (int64_t)blockIdx.x * kThreads + threadIdx.x; e < p.numel;
          e += (int64_t)gridDim.x * kThreads) {
         const int32_t i0 = (int32_t)fastdiv((uint32_t)e, a.fLb);
         const int32_t f = (int32_t)e - i0 * a.Lb;
-        const int32_t r = f - (int32_t)fastdiv((uint32_t)f, a.fP) * a.P;
-        const In xv = X[i0 * a.sx0 + r], dv = D[i0 * a.sd0 + f];
+        const int32_t rr = f - (int32_t)fastdiv((uint32_t)f, a.fP) * a.P;
+        const In xv = X[i0 * a.sx0 + rr], dv = D[i0 * a.sd0 + f];
         O[e] = X_IS_A ? Op::apply(xv, dv, p.args, err) : Op::apply(dv, xv, p.args, err);
     }
     flush_err<Op>(p.status, err);
@@ -1298,6 +1302,7 @@ cudaError_t launch_blockrow(const Launch &L, const PeriodicArgs &pa) {
     b.sd0 = X_IS_A ? pa.sb0 : pa.sa0;
     b.fP = pa.fP;
     b.fLb = pa.fLb;
+    b.dr = (int32_t)(((int64_t)kThreads * G) % pa.P);
     const int64_t ng = L.numel / G;
     const int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * kBlockRowU);
     if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
