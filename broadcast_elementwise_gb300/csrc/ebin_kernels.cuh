@@ -742,7 +742,8 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(KArgs p, BlockRowArgs a) 
 // prepared where the operator prepares them) and reloads it only when a pack
 // lies outside that row; the row value's offset is decoded from the row
 // index only then.  ROW_A: A is the per-row input and B the dense one.
-// WIDE: a pack index may reach 2^32, and indices divide in 64 bits.
+// WIDE: pack indices are 64-bit and divide in 64 bits (plans of 2^31 - 2^20
+// packs or more); else they are 32-bit.
 struct RowConstArgs {
     int64_t lp;                 // packs per row (L / G)
     FastDiv f_lp;
@@ -760,6 +761,8 @@ __global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) 
     using Out = typename Op::Out;
     using BV = typename Op::BV;
     using BIn = typename BInOf<Op>::type;
+    // pack indices: 32-bit unless the plan's packs reach the launcher's bound
+    using I = std::conditional_t<WIDE, int64_t, int32_t>;
     constexpr int G = 16 / sizeof(In);
     constexpr bool kPrep = !ROW_A && HasPrep<Op>::value;
     using PrepT = typename std::conditional_t<HasPrep<Op>::value, Op, PrepNone>::PB;
@@ -768,16 +771,17 @@ __global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) 
     const In *RA = static_cast<const In *>(p.A);
     const BIn *RB = static_cast<const BIn *>(p.B);
     Out *O = static_cast<Out *>(p.out);
-    const int64_t np = p.numel / G;
-    const int64_t first = (int64_t)blockIdx.x * r.iters * (kThreads * U) + threadIdx.x;
+    const I np = (I)(p.numel / G);
+    const I lp = (I)r.lp;
+    const I first = (I)blockIdx.x * (I)r.iters * (I)(kThreads * U) + (I)threadIdx.x;
     // packs [lo, hi) are the row whose value rv holds (none yet)
-    int64_t lo = 0, hi = 0;
+    I lo = 0, hi = 0;
     RowV rv{};
     uint32_t err = 0;
-    auto set_row = [&](int64_t g) {   // the row of pack g becomes the cached one
+    auto set_row = [&](I g) {   // the row of pack g becomes the cached one
         const int64_t row = udiv(g, r.lp, r.f_lp, WIDE);
-        lo = row * r.lp;
-        hi = lo + r.lp;
+        lo = (I)row * lp;
+        hi = lo + lp;
         int64_t rem = row, off = 0;
 #pragma unroll
         for (int k = kMaxRank - 1; k >= 0; --k) {
@@ -794,19 +798,19 @@ __global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) 
     pdl_wait();
 #pragma unroll 1
     for (int j = 0; j < r.iters; ++j) {
-        const int64_t base = first + (int64_t)j * (kThreads * U);
+        const I base = first + (I)j * (I)(kThreads * U);
         if (base >= np) break;
         Pack<In, G> d[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t g = base + (int64_t)u * kThreads;
-            if (g < np) d[u] = ld_stream<In, G>(D + g * G);
+            const I g = base + (I)(u * kThreads);
+            if (g < np) d[u] = ld_stream<In, G>(D + (int64_t)g * G);
         }
-        const int64_t last = base + (int64_t)(U - 1) * kThreads;
+        const I last = base + (I)((U - 1) * kThreads);
         const bool whole = last < np && base >= lo && last < hi;   // one cached row, all packs
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t g = base + (int64_t)u * kThreads;
+            const I g = base + (I)(u * kThreads);
             if (whole || g < np) {
                 if (!whole && (g < lo || g >= hi)) set_row(g);
                 Pack<Out, G> o;
@@ -814,7 +818,7 @@ __global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) 
                 else if constexpr (kPrep)
                     Op::template apply_prep_group<G, false>(d[u].v, rv, o.v, p.args, err);
                 else compute_group<Op, G, false, true>(d[u].v, &rv, o.v, p.args, err);
-                st_stream<Out, G>(O + g * G, o);
+                st_stream<Out, G>(O + (int64_t)g * G, o);
             }
         }
     }
@@ -1219,7 +1223,9 @@ cudaError_t run_rowconst_kernel(const Launch &L) {
 template <class Op, bool ROW_A>
 cudaError_t run_rowconst(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    if (L.numel / G >= (1ll << 32)) return run_rowconst_kernel<Op, ROW_A, true>(L);
+    // 32-bit pack indices below 2^31 - 2^20 packs (a run's last pack and the
+    // row bounds then stay below 2^31)
+    if (L.numel / G >= (1ll << 31) - (1ll << 20)) return run_rowconst_kernel<Op, ROW_A, true>(L);
     return run_rowconst_kernel<Op, ROW_A, false>(L);
 }
 

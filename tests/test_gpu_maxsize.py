@@ -8,7 +8,8 @@ ragged tail, and check sampled outputs against the oracle: the oracle maps
 each sampled flat output index to its A and B offsets, the test gathers those
 input elements from the device and the oracle evaluates them.  The samples
 hold the whole first and last tiles and the elements on either side of
-2^31 and 2^32, where a truncated index would land.
+2^31 and 2^32 (and of 2^35, where 16-byte pack indices of one-byte elements
+pass 2^31), where a truncated index would land.
 
 Inputs are drawn on the device from a seeded torch generator (a host copy of
 several GiB would dominate the test); the oracle reads back the elements it
@@ -45,7 +46,7 @@ def _samples(numel, seed=2024):
     edge = 1 << 14
     parts = [np.arange(min(edge, numel)), np.arange(max(numel - edge, 0), numel),
              rng.integers(0, numel, 1 << 18)]
-    for wall in (1 << 31, 1 << 32):
+    for wall in (1 << 31, 1 << 32, 1 << 35):
         if wall < numel:
             parts.append(np.arange(max(wall - edge, 0), min(wall + edge, numel)))
     return np.unique(np.concatenate(parts)).astype(np.int64)
@@ -66,13 +67,17 @@ CASES = [
     # 2^31 elements, and the general kernel past it
     ("Add", "uint8", (715827882, 3), (3,), "repeated_block"),
     ("Sub", "uint8", ((1 << 31) + 3, 3), ((1 << 31) + 3, 1), "repeated_block"),
+    # one value per row past 2^31 packs of 16 bytes (2^35 elements): the flat
+    # per-row kernel's 64-bit pack indices (two 32 GiB buffers)
+    ("Add", "uint8", ((1 << 24) + 3, 2048), ((1 << 24) + 3, 1), "repeated_block"),
 ]
 
 
 @pytest.mark.parametrize("op,dtype,sa,sb,family", CASES,
                          ids=["xor_u8_2p32", "add_u8_scalar_2p32", "add_u8_general_wide",
                               "mul_f32_channel_2p31", "xor_i64_rows_8GiB",
-                              "add_u8_block3_below_2p31", "sub_u8_rows3_past_2p31"])
+                              "add_u8_block3_below_2p31", "sub_u8_rows3_past_2p31",
+                              "add_u8_rows_past_2p31_packs"])
 def test_past_32bit_indices(op, dtype, sa, sb, family):
     import broadcast_elementwise_gb300 as eb
     plan = eb.Plan(eb.descriptor(op, dtype), sa, sb)
