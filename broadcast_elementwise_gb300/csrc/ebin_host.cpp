@@ -975,6 +975,7 @@ ebin_status ebin::prepare_launch(const ebin_plan_s &p, const void *A, const void
     L.args.plane = p.plane;
     L.args.with_scalar = p.attrs.with_scalar;
     L.args.scalar_b = p.attrs.scalar_b;
+    L.args.one = 1.0f;
     L.stream = s;
     L.num_sms = sm_count(dev);
     L.status = nullptr;

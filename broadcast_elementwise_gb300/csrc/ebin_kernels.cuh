@@ -741,7 +741,9 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(KArgs p, BlockRowArgs a) 
 // boundaries.  A thread keeps the value of its current row (the parameters,
 // prepared where the operator prepares them) and reloads it only when a pack
 // lies outside that row; the row value's offset is decoded from the row
-// index only then.  ROW_A: A is the per-row input and B the dense one.
+// index only then.  A run whose packs all lie in bounds and in the cached row
+// (nearly every run) takes no per-pack test: its U x G elements are computed
+// as one group.  ROW_A: A is the per-row input and B the dense one.
 // WIDE: pack indices are 64-bit and divide in 64 bits (plans of 2^31 - 2^20
 // packs or more); else they are 32-bit.
 struct RowConstArgs {
@@ -754,8 +756,19 @@ struct RowConstArgs {
     FastDiv f_on[kMaxRank];
 };
 
+// The smallest number of resident CTAs per SM asked of the compiler for an
+// operator's k_rowconst (0: none asked).  Measured on GB300, bf16
+// x[8,64,256,256] against a per-channel operand: BiasPReluBN takes 66
+// registers unbounded (three CTAs per SM, 25.9 us) and 53 when asked for four
+// (24.1 us), BatchNormalization 22.6 -> 22.3 us; Add 21.0 -> 20.7 us and fp32
+// Mod rows 21.7 -> 21.5 us asked for one, while PRelu and BiasPRelu lose 10%
+// when asked for one (20.8 -> 22.9 us), so they ask nothing.
+template <class Op> struct RowConstMinCtas : std::integral_constant<int, HasGroup<Op>::value ? 4 : 0> {};
+template <class T, int K> struct RowConstMinCtas<OpArith<T, K>> : std::integral_constant<int, 1> {};
+template <class T> struct RowConstMinCtas<OpMod<T>> : std::integral_constant<int, 1> {};
+
 template <class Op, bool ROW_A, int U, bool WIDE>
-__global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) {
+__device__ __forceinline__ void rowconst_body(const KArgs &p, const RowConstArgs &r) {
     pdl_launch();
     using In = typename Op::In;
     using Out = typename Op::Out;
@@ -806,13 +819,29 @@ __global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) 
             const I g = base + (I)(u * kThreads);
             if (g < np) d[u] = ld_stream<In, G>(D + (int64_t)g * G);
         }
+        // the loads are in flight: bring the row of the run's first pack in
+        if (base < lo || base >= hi) set_row(base);
         const I last = base + (I)((U - 1) * kThreads);
-        const bool whole = last < np && base >= lo && last < hi;   // one cached row, all packs
+        if (last < np && last < hi) {
+            // the common run: every pack in bounds and in the cached row, so
+            // no per-pack test, and the stores are one base plus constants
+            Out *dst = O + (int64_t)base * G;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                Pack<Out, G> o;
+                if constexpr (ROW_A) compute_group<Op, G, true, false>(&rv, d[u].v, o.v, p.args, err);
+                else if constexpr (kPrep)
+                    Op::template apply_prep_group<G, false>(d[u].v, rv, o.v, p.args, err);
+                else compute_group<Op, G, false, true>(d[u].v, &rv, o.v, p.args, err);
+                st_stream<Out, G>(dst + u * kThreads * G, o);
+            }
+            continue;
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const I g = base + (I)(u * kThreads);
-            if (whole || g < np) {
-                if (!whole && (g < lo || g >= hi)) set_row(g);
+            if (g < np) {
+                if (g < lo || g >= hi) set_row(g);
                 Pack<Out, G> o;
                 if constexpr (ROW_A) compute_group<Op, G, true, false>(&rv, d[u].v, o.v, p.args, err);
                 else if constexpr (kPrep)
@@ -823,6 +852,16 @@ __global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) 
         }
     }
     flush_err<Op>(p.status, err);
+}
+
+template <class Op, bool ROW_A, int U, bool WIDE>
+__global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) {
+    rowconst_body<Op, ROW_A, U, WIDE>(p, r);
+}
+
+template <class Op, bool ROW_A, int U, bool WIDE, int MINCTAS>
+__global__ void __launch_bounds__(kThreads, MINCTAS) k_rowconst_bounded(KArgs p, RowConstArgs r) {
+    rowconst_body<Op, ROW_A, U, WIDE>(p, r);
 }
 
 // ---------------------------------------------------------------- three inputs
@@ -1195,7 +1234,11 @@ template <class Op, bool ROW_A, bool WIDE>
 cudaError_t run_rowconst_kernel(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
     constexpr int U = kRowConstU;
-    auto kernel = k_rowconst<Op, ROW_A, U, WIDE>;
+    constexpr int kMin = RowConstMinCtas<Op>::value;
+    auto kernel = [] {
+        if constexpr (kMin > 0) return k_rowconst_bounded<Op, ROW_A, U, WIDE, kMin>;
+        else return k_rowconst<Op, ROW_A, U, WIDE>;
+    }();
     const Geom &g = L.g;
     RowConstArgs r{};
     const int rank = g.rank;

@@ -37,6 +37,7 @@ struct OpArgs {
     int64_t plane;       // BatchNormalization, BiasPRelu(BN): elements between parameter rows
     int32_t with_scalar; // B is scalar_b, not a tensor (ncnn binaryop with_scalar)
     float scalar_b;
+    float one;           // exactly 1.0f: a multiplier the device code cannot fold away
 };
 
 // Coalesced traversal: rank dims, extents n, element strides of A and B.

@@ -724,6 +724,17 @@ __device__ __forceinline__ double sqrt_rn(double a) { return __dsqrt_rn(a); }
 // by a multiple of 2^-99), and never -0, so such rows need no lower test
 // (tlow = 0); other rows take tlow = 2^-100 and send their zeros to the IEEE
 // divide, as they do tiny, huge, infinite and NaN quotients.
+// p + c for two binary32 products p (each already rounded on its own), as a
+// fused multiply-add by `one`, which the host sets to exactly 1.0: the
+// result is RN(p + c) lane by lane, as an addition.  A paired addition
+// written as such was merged with the paired multiply that formed p into one
+// fused multiply-add (a few outputs per million one unit off in the last
+// place), even with contraction disabled; a multiplier the compiler cannot
+// know to be 1 leaves nothing to merge.
+__device__ __forceinline__ float2 add2_after_mul(float2 p, float2 c, float one) {
+    return __ffma2_rn(p, make_float2(one, one), c);
+}
+
 struct DivPrep {
     float r, nd;            // RN(1/d), -d
     float tlow, thigh;      // |t| kept in [tlow, thigh] (thigh = -1: the row is refused)
@@ -756,8 +767,8 @@ __device__ __forceinline__ float2 div2_prepared(float2 t, const DivPrep &v, bool
 
 // A group of G 16-bit elements whose chain divides by the row's d: pre(x)
 // forms two elements' t (x: their binary32 values) exactly as the chain does,
-// the quotient is div2_prepared's, tail(q) finishes one element's chain in
-// binary32 and exact(x) is the whole chain with the IEEE divide, for the
+// the quotient is div2_prepared's, tail(q) finishes two elements' chains in
+// binary32 (lane by lane, as the scalar steps would) and exact(x) is the whole chain with the IEEE divide, for the
 // elements outside the proven ranges.  The group moves as 32-bit words, two
 // elements each; the rare refused pairs are recomputed in one rolled loop
 // (the words rotate through slot 0, so every index stays a constant and the
@@ -773,14 +784,14 @@ __device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &
         if (v.tlow == 0.0f) {   // uniform per row: the common rows test one bound
 #pragma unroll
             for (int k = 0; k < W; ++k) {
-                const float2 q = div2_prepared<false>(pre(widen2<T>(aw[k])), v, &ok);
-                ow[k] = round2<T>(tail(q.x), tail(q.y));
+                const float2 y = tail(div2_prepared<false>(pre(widen2<T>(aw[k])), v, &ok));
+                ow[k] = round2<T>(y.x, y.y);
             }
         } else {
 #pragma unroll
             for (int k = 0; k < W; ++k) {
-                const float2 q = div2_prepared<true>(pre(widen2<T>(aw[k])), v, &ok);
-                ow[k] = round2<T>(tail(q.x), tail(q.y));
+                const float2 y = tail(div2_prepared<true>(pre(widen2<T>(aw[k])), v, &ok));
+                ow[k] = round2<T>(y.x, y.y);
             }
         }
         if (!ok) {   // rare (zeros, extreme quotients): those elements again, exactly
@@ -810,7 +821,7 @@ __device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &
             bool ok = true;
             const float xf = Tr<T>::in(x);
             const float2 q = div2_prepared<true>(pre(make_float2(xf, xf)), v, &ok);
-            o[k] = ok ? Tr<T>::out(tail(q.x)) : exact(x);
+            o[k] = ok ? Tr<T>::out(tail(q).x) : exact(x);
         }
     }
 }
@@ -935,11 +946,14 @@ template <class T, class P = T> struct OpBN {
     template <int G, bool SA>
     __device__ __forceinline__ static void apply_group(const T *a, const BV &q, T *o,
                                                        const OpArgs &p, uint32_t &err) {
-        // t = x - mean; t / d prepared; then * scale + bias with the scalar _rn
-        // operations (never contracted into a fused multiply-add)
+        // t = x - mean; t / d prepared; then * scale + bias, each lane's
+        // product and sum rounded on their own (add2_after_mul)
         prepared_group<T, G, SA>(
             a, o, q.v, [&](float2 x) { return __fadd2_rn(x, make_float2(-q.mean, -q.mean)); },
-            [&](float qd) { return __fadd_rn(__fmul_rn(qd, q.scale), q.bias); },
+            [&](float2 qd) {
+                return add2_after_mul(__fmul2_rn(qd, make_float2(q.scale, q.scale)),
+                                      make_float2(q.bias, q.bias), p.one);
+            },
             [&](T x) { return apply(x, q, p, err); });
     }
 };
@@ -1011,7 +1025,10 @@ template <class T, class P = T> struct OpBiasPReluBN {
         };
         prepared_group<T, G, SA>(
             a, o, q.v, pre2,
-            [&](float qd) { return __fadd_rn(__fmul_rn(qd, q.scale), q.bn_bias); },
+            [&](float2 qd) {
+                return add2_after_mul(__fmul2_rn(qd, make_float2(q.scale, q.scale)),
+                                      make_float2(q.bn_bias, q.bn_bias), p.one);
+            },
             [&](T x) { return apply(x, q, p, err); });
     }
 };

@@ -26,6 +26,37 @@ MANIFEST = {
     "BiasPRelu": FLOATS, "BiasPReluBN": FLOATS,
 }
 ONE_WAY = ("PRelu", "BatchNormalization", "Clip", "BiasPRelu", "BiasPReluBN")
+# parameter rows of the per-channel operators' B blocks
+PARAM_ROWS = {"BatchNormalization": 4, "BiasPRelu": 2, "BiasPReluBN": 6}
+
+
+def every_16bit_value(shape):
+    """x[n, c, ...] whose every channel holds every 16-bit pattern (NaNs,
+    infinities, subnormals and both zeros included), at least once."""
+    N, C = shape[0], shape[1]
+    S = int(np.prod(shape[2:]))
+    n = np.arange(N, dtype=np.int64)[:, None, None]
+    c = np.arange(C, dtype=np.int64)[None, :, None]
+    s = np.arange(S, dtype=np.int64)[None, None, :]
+    return ((n * S + s + 977 * c) % 65536).astype(np.uint16).reshape(shape)
+
+
+def chain_params(op, C, seed, wide):
+    """Seeded binary32 parameter rows of a per-channel chain, [rows, C]:
+    ordinary normal values, or (wide) magnitudes over many binades with signs
+    mixed and some exact zeros; the variance row positive, BiasPReluBN's slope
+    row in [0, 1)."""
+    rows = PARAM_ROWS[op]
+    rng = np.random.default_rng(seed)
+    p = rng.standard_normal((rows, C)).astype(np.float32)
+    if wide:       # magnitudes over many binades, signs mixed, some exact zeros
+        p *= np.float32(2.0) ** rng.integers(-30, 30, (rows, C)).astype(np.float32)
+        p[rng.random((rows, C)) < 0.05] = 0.0
+    p[-1] = np.abs(p[-1]) + np.float32(0.05)                  # variance
+    if op == "BiasPReluBN":
+        p[1] = np.abs(p[1]) * np.float32(0.3)                 # slope
+    return p
+
 
 
 def to_device(arr: np.ndarray):

@@ -12,7 +12,8 @@ import pytest
 import datagen
 import oracle
 from conftest import assert_bits_equal, ulp_distance
-from engine_util import FLOATS, MANIFEST, ONE_WAY, inputs_for, run_engine, to_device
+from engine_util import (FLOATS, MANIFEST, ONE_WAY, PARAM_ROWS, chain_params,
+                         every_16bit_value, inputs_for, run_engine, to_device)
 
 eb = pytest.importorskip("broadcast_elementwise_gb300")
 
@@ -137,7 +138,6 @@ def test_parity_all_families(op, dtype):
                 assert bits == want_bits, (what, bits, want_bits)
 
 
-PARAM_ROWS = {"BatchNormalization": 4, "BiasPRelu": 2, "BiasPReluBN": 6}
 # (family, x shape, C): the block geometries of BN_CASES plus one channel
 # (a single parameter per row, the right-scalar kernel)
 F32_BLOCK_CASES = [(fam, sa, sb[1]) for fam, sa, sb in BN_CASES] + [
@@ -319,30 +319,6 @@ def test_pow_with_exponent_of_another_type(ta, tb):
 
 
 
-def _every_16bit_value(shape):
-    """x[n, c, ...] whose every channel holds every 16-bit pattern (NaNs,
-    infinities, subnormals and both zeros included), at least once."""
-    N, C = shape[0], shape[1]
-    S = int(np.prod(shape[2:]))
-    n = np.arange(N, dtype=np.int64)[:, None, None]
-    c = np.arange(C, dtype=np.int64)[None, :, None]
-    s = np.arange(S, dtype=np.int64)[None, None, :]
-    return ((n * S + s + 977 * c) % 65536).astype(np.uint16).reshape(shape)
-
-
-def _chain_params(op, C, seed, wide):
-    rows = PARAM_ROWS[op]
-    rng = np.random.default_rng(seed)
-    p = rng.standard_normal((rows, C)).astype(np.float32)
-    if wide:       # magnitudes over many binades, signs mixed, some exact zeros
-        p *= np.float32(2.0) ** rng.integers(-30, 30, (rows, C)).astype(np.float32)
-        p[rng.random((rows, C)) < 0.05] = 0.0
-    p[-1] = np.abs(p[-1]) + np.float32(0.05)                  # variance
-    if op == "BiasPReluBN":
-        p[1] = np.abs(p[1]) * np.float32(0.3)                 # slope
-    return p
-
-
 @pytest.mark.parametrize("op", ["BatchNormalization", "BiasPReluBN"])
 @pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
 def test_prepared_division_on_every_16bit_value(op, dtype):
@@ -352,13 +328,16 @@ def test_prepared_division_on_every_16bit_value(op, dtype):
     ranges): every bfloat16 / float16 x pattern, in every channel, through the
     flat per-row kernel (pairs of elements), the general kernel (single
     elements) and rows of odd length, with 16-bit and float32 parameter blocks
-    of ordinary and wide-ranging values, bit-identical to the oracle."""
+    of ordinary and wide-ranging values, bit-identical to the oracle.  The
+    inputs hold elements whose result changes when the chain's last multiply
+    and add are merged into one fused multiply-add (test_chain_inputs checks
+    that on the CPU), so a merged tail fails here."""
     C = 64
     for shape, fams in (((16, C, 64, 64), ("inner_vector_outer", "general_strided")),
                         ((16, C, 4097), ("general_strided",))):
-        x = _every_16bit_value(shape).view(datagen.STORAGE[dtype])
+        x = every_16bit_value(shape).view(datagen.STORAGE[dtype])
         for k, (wide, ptype) in enumerate(((False, dtype), (True, dtype), (True, "float32"))):
-            p = _chain_params(op, C, 90 + k, wide)
+            p = chain_params(op, C, 90 + k, wide)
             b = datagen.float_to(p, ptype) if ptype != "float32" else p
             want = oracle.run_params(op, x, b, dtype, ptype)
             attrs = {"epsilon": 1e-5}
