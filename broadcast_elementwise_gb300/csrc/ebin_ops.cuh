@@ -152,6 +152,31 @@ template <> __device__ __forceinline__ float2 widen2<__half>(uint32_t w) {
     memcpy(&h, &w, 4);
     return __half22float2(h);
 }
+// The two 16-bit values of a word, each widened exactly and added to c with
+// one binary32 rounding: RN(x + c) for both halves.  One mixed-precision add
+// per half (PTX add.rn.f32.bf16 / .f32.f16, sm_100 and later), the word's
+// halves taken as 16-bit registers, in place of a widening and a binary32 add.
+template <class T> __device__ __forceinline__ float2 widen_add2(uint32_t w, float c);
+template <> __device__ __forceinline__ float2 widen_add2<__nv_bfloat16>(uint32_t w, float c) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %3;\n\t"
+        "add.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(c));
+    return make_float2(lo, hi);
+}
+template <> __device__ __forceinline__ float2 widen_add2<__half>(uint32_t w, float c) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %3;\n\t"
+        "add.rn.f32.f16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(c));
+    return make_float2(lo, hi);
+}
 template <class T> __device__ __forceinline__ T half_of(uint32_t w, bool high) {
     const unsigned short b = (unsigned short)(high ? (w >> 16) : (w & 0xFFFFu));
     T v;
@@ -767,15 +792,16 @@ __device__ __forceinline__ float2 div2_prepared(float2 t, const DivPrep &v, bool
 
 // A group of G 16-bit elements whose chain divides by the row's d: pre(x)
 // forms two elements' t (x: their binary32 values) exactly as the chain does,
-// the quotient is div2_prepared's, tail(q) finishes two elements' chains in
-// binary32 (lane by lane, as the scalar steps would) and exact(x) is the whole chain with the IEEE divide, for the
-// elements outside the proven ranges.  The group moves as 32-bit words, two
+// pre_w(w) the same from the word w that holds them, the quotient is
+// div2_prepared's, tail(q) finishes two elements' chains in binary32 (lane by
+// lane, as the scalar steps would) and exact(x) is the whole chain with the
+// IEEE divide, for the elements outside the proven ranges.  The group moves as 32-bit words, two
 // elements each; the rare refused pairs are recomputed in one rolled loop
 // (the words rotate through slot 0, so every index stays a constant and the
 // arrays stay in registers).
-template <class T, int G, bool SA, class Pre, class Tail, class Exact>
+template <class T, int G, bool SA, class Pre, class PreW, class Tail, class Exact>
 __device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &v, Pre pre,
-                                               Tail tail, Exact exact) {
+                                               PreW pre_w, Tail tail, Exact exact) {
     if constexpr (G % 2 == 0 && !SA) {
         constexpr int W = G / 2;
         uint32_t aw[W], ow[W];
@@ -784,13 +810,13 @@ __device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &
         if (v.tlow == 0.0f) {   // uniform per row: the common rows test one bound
 #pragma unroll
             for (int k = 0; k < W; ++k) {
-                const float2 y = tail(div2_prepared<false>(pre(widen2<T>(aw[k])), v, &ok));
+                const float2 y = tail(div2_prepared<false>(pre_w(aw[k]), v, &ok));
                 ow[k] = round2<T>(y.x, y.y);
             }
         } else {
 #pragma unroll
             for (int k = 0; k < W; ++k) {
-                const float2 y = tail(div2_prepared<true>(pre(widen2<T>(aw[k])), v, &ok));
+                const float2 y = tail(div2_prepared<true>(pre_w(aw[k]), v, &ok));
                 ow[k] = round2<T>(y.x, y.y);
             }
         }
@@ -799,7 +825,7 @@ __device__ __forceinline__ void prepared_group(const T *a, T *o, const DivPrep &
             for (int k = 0; k < W; ++k) {
                 const uint32_t x = aw[0];
                 bool pok = true;
-                div2_prepared<true>(pre(widen2<T>(x)), v, &pok);
+                div2_prepared<true>(pre_w(x), v, &pok);
                 uint32_t r = ow[0];
                 if (!pok)
                     r = bits_of(exact(half_of<T>(x, false))) |
@@ -948,8 +974,10 @@ template <class T, class P = T> struct OpBN {
                                                        const OpArgs &p, uint32_t &err) {
         // t = x - mean; t / d prepared; then * scale + bias, each lane's
         // product and sum rounded on their own (add2_after_mul)
+        // (x - mean and x + (-mean) are the same IEEE operation)
         prepared_group<T, G, SA>(
             a, o, q.v, [&](float2 x) { return __fadd2_rn(x, make_float2(-q.mean, -q.mean)); },
+            [&](uint32_t w) { return widen_add2<T>(w, -q.mean); },
             [&](float2 qd) {
                 return add2_after_mul(__fmul2_rn(qd, make_float2(q.scale, q.scale)),
                                       make_float2(q.bias, q.bias), p.one);
@@ -1017,14 +1045,14 @@ template <class T, class P = T> struct OpBiasPReluBN {
         // an infinite t1 makes t infinite, outside the range.  No product
         // feeds an addition here (the max stands between), so nothing can be
         // contracted into a fused multiply-add.
-        auto pre2 = [&](float2 x) {
-            const float2 t1 = __fadd2_rn(x, make_float2(q.bias, q.bias));
+        auto rest = [&](float2 t1) {
             const float2 s1 = __fmul2_rn(t1, make_float2(q.slope, q.slope));
             return __fadd2_rn(make_float2(fmaxf(t1.x, s1.x), fmaxf(t1.y, s1.y)),
                               make_float2(-q.mean, -q.mean));
         };
         prepared_group<T, G, SA>(
-            a, o, q.v, pre2,
+            a, o, q.v, [&](float2 x) { return rest(__fadd2_rn(x, make_float2(q.bias, q.bias))); },
+            [&](uint32_t w) { return rest(widen_add2<T>(w, q.bias)); },
             [&](float2 qd) {
                 return add2_after_mul(__fmul2_rn(qd, make_float2(q.scale, q.scale)),
                                       make_float2(q.bn_bias, q.bn_bias), p.one);
