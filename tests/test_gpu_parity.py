@@ -353,6 +353,37 @@ def test_prepared_division_on_every_16bit_value(op, dtype):
                 assert bits == 0, what
 
 
+@pytest.mark.parametrize("op", ["Add", "Sub", "Mul", "RSub"])
+@pytest.mark.parametrize("dtype", ["bfloat16", "float16"])
+def test_pair_forms_on_every_16bit_value(op, dtype):
+    """16-bit Add, Sub, Mul and RSub run two elements per 32-bit word through
+    mixed-precision operations (Mul: a 16-bit by 16-bit fused multiply-add
+    with a -0 addend; the others: one operand widened, one 16-bit add).  Every
+    bfloat16 / float16 pattern (NaNs, infinities, subnormals, both zeros) as
+    each operand, against a seeded permutation of every pattern, through the
+    contiguous kernel; every pattern against a value per row (the per-row flat
+    kernel) and against a short reused row (the block-row kernel): bit-identical
+    to the oracle."""
+    st = datagen.STORAGE[dtype]
+    every = np.arange(65536, dtype=np.uint16)
+    rng = np.random.default_rng(2024)
+    perm = rng.permutation(every)
+    cases = [
+        ("contiguous", every, perm),
+        ("contiguous", perm, every),
+        ("repeated_block", every.reshape(256, 256), rng.permutation(every)[:256].reshape(256, 1)),
+        ("repeated_block", every.reshape(16384, 4), rng.permutation(every)[:4]),
+    ]
+    for fam, a16, b16 in cases:
+        a, b = np.ascontiguousarray(a16).view(st), np.ascontiguousarray(b16).view(st)
+        want, _ = oracle.run(op, a, b, dtype)
+        got, bits, family = run_engine(op, dtype, a, b)
+        what = "%s %s %s x %s" % (op, dtype, a.shape, b.shape)
+        assert family == fam, what
+        assert_bits_equal(got, want, dtype, what)
+        assert bits == 0, what
+
+
 # k_periodic: [n0,] n1, n2 with each input dense in the block, one value per
 # row, or one reused row; (shape A, shape B, the pattern of A and of B)
 PERIODIC_CASES = [
