@@ -1075,13 +1075,21 @@ cudaError_t run_contiguous(const Launch &L) {
     return launch_pdl(k_contiguous<Op, kUnrollFlat>, grid, kThreads, L.stream, kargs<Op>(L));
 }
 
+template <class Op, bool ROW_A> cudaError_t run_rowconst(const Launch &L);
+
 template <class Op, bool SCALAR_A>
 cudaError_t run_scalar(const Launch &L) {
+    constexpr int G = 16 / sizeof(typename Op::In);
+    if constexpr (HasPrep<Op>::value && !SCALAR_A) {
+        // a prepared right scalar over a whole number of packs is one row of
+        // the per-row flat kernel, the divisor prepared once per thread (fp32
+        // Mod fmod0 vs a scalar, A[4096,4096]: 21.98 -> 21.42 us on GB300)
+        if (L.numel % G == 0) return run_rowconst<Op, false>(L);
+    }
     // an operator that prepares the scalar (Mod's divisor) spreads the
     // preparation over four packs per thread (fp32 Mod fmod0 vs a scalar:
     // 23.7 -> 22.2 us on GB300; one pack 30.7 us, eight 21.8 but int32 worse)
     constexpr int U = HasPrep<Op>::value ? 4 : kUnrollFlat;
-    constexpr int G = 16 / sizeof(typename Op::In);
     const int64_t ng = L.numel / G;
     int64_t grid = ceil_div(ng > 0 ? ng : 1, (int64_t)kThreads * U);
     grid = std::min<int64_t>(grid, kMaxGrid);
