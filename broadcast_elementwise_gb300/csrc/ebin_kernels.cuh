@@ -742,10 +742,10 @@ __global__ void __launch_bounds__(kThreads) k_blockrow(KArgs p, BlockRowArgs a) 
 // prepared where the operator prepares them) and reloads it only when a pack
 // lies outside that row; the row value's offset is decoded from the row
 // index only then.  A run whose packs all lie in bounds and in the cached row
-// (nearly every run) takes no per-pack test: its U x G elements are computed
-// as one group.  ROW_A: A is the per-row input and B the dense one.
-// WIDE: pack indices are 64-bit and divide in 64 bits (plans of 2^31 - 2^20
-// packs or more); else they are 32-bit.
+// (nearly every run) takes no per-pack test.  ROW_A: A is the per-row input
+// and B the dense one.  WIDE: pack indices are 64-bit and divide in 64 bits
+// (the launcher takes it when some run start would reach 2^31 packs); else
+// they are 32-bit.
 struct RowConstArgs {
     int64_t lp;                 // packs per row (L / G)
     FastDiv f_lp;
@@ -862,6 +862,95 @@ __global__ void __launch_bounds__(kThreads) k_rowconst(KArgs p, RowConstArgs r) 
 template <class Op, bool ROW_A, int U, bool WIDE, int MINCTAS>
 __global__ void __launch_bounds__(kThreads, MINCTAS) k_rowconst_bounded(KArgs p, RowConstArgs r) {
     rowconst_body<Op, ROW_A, U, WIDE>(p, r);
+}
+
+// ---------------------------------------------------------------- three inputs, one value per row
+//
+// k_rowconst for a three-input operator (Op::apply3): two inputs dense over
+// the output in order and the third, operand RP (0 = a, 1 = b, 2 = c), one
+// value per row of L elements, L a multiple of the pack width G (MulAdd with
+// a per-channel multiplier: x[N, C, H, W] * s[1, C, 1, 1] + y).  The same flat
+// stream of runs, cached row value and common run as k_rowconst.
+template <class Op, int RP, int U, bool WIDE>
+__global__ void __launch_bounds__(kThreads) k_rowconst3(KArgs p, RowConstArgs r) {
+    pdl_launch();
+    using In = typename Op::In;
+    using Out = typename Op::Out;
+    using I = std::conditional_t<WIDE, int64_t, int32_t>;
+    constexpr int G = 16 / sizeof(In);
+    const In *A = static_cast<const In *>(p.A);
+    const In *B = static_cast<const In *>(p.B);
+    const In *C = static_cast<const In *>(p.C);
+    const In *D0 = RP == 0 ? B : A;             // the dense inputs, in operand order
+    const In *D1 = RP == 2 ? B : C;
+    const In *R = RP == 0 ? A : RP == 1 ? B : C;
+    Out *O = static_cast<Out *>(p.out);
+    const I np = (I)(p.numel / G);
+    const I lp = (I)r.lp;
+    const I first = (I)blockIdx.x * (I)r.iters * (I)(kThreads * U) + (I)threadIdx.x;
+    I lo = 0, hi = 0;                           // packs [lo, hi): the row rv belongs to
+    In rv{};
+    auto set_row = [&](I g) {
+        const int64_t row = udiv(g, r.lp, r.f_lp, WIDE);
+        lo = (I)row * lp;
+        hi = lo + lp;
+        int64_t rem = row, off = 0;
+#pragma unroll
+        for (int k = kMaxRank - 1; k >= 0; --k) {
+            if (k < r.nd) {
+                const int64_t q = udiv(rem, r.on[k], r.f_on[k], WIDE);
+                off += (rem - q * r.on[k]) * r.os[k];
+                rem = q;
+            }
+        }
+        rv = R[off];
+    };
+    auto compute = [&](const Pack<In, G> &x, const Pack<In, G> &y, Pack<Out, G> &o) {
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+            if constexpr (RP == 0) o.v[k] = Op::apply3(rv, x.v[k], y.v[k]);
+            else if constexpr (RP == 1) o.v[k] = Op::apply3(x.v[k], rv, y.v[k]);
+            else o.v[k] = Op::apply3(x.v[k], y.v[k], rv);
+        }
+    };
+    pdl_wait();
+#pragma unroll 1
+    for (int j = 0; j < r.iters; ++j) {
+        const I base = first + (I)j * (I)(kThreads * U);
+        if (base >= np) break;
+        Pack<In, G> d0[U], d1[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const I g = base + (I)(u * kThreads);
+            if (g < np) {
+                d0[u] = ld_stream<In, G>(D0 + (int64_t)g * G);
+                d1[u] = ld_stream<In, G>(D1 + (int64_t)g * G);
+            }
+        }
+        // the loads are in flight: bring the row of the run's first pack in
+        if (base < lo || base >= hi) set_row(base);
+        const I last = base + (I)((U - 1) * kThreads);
+        if (last < np && last < hi) {           // the common run: no per-pack test
+            Out *dst = O + (int64_t)base * G;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                Pack<Out, G> o;
+                compute(d0[u], d1[u], o);
+                st_stream<Out, G>(dst + u * kThreads * G, o);
+            }
+            continue;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const I g = base + (I)(u * kThreads);
+            if (g < np) {
+                if (g < lo || g >= hi) set_row(g);
+                Pack<Out, G> o;
+                compute(d0[u], d1[u], o);
+                st_stream<Out, G>(O + (int64_t)g * G, o);
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------------------- three inputs
@@ -1198,11 +1287,14 @@ struct RowShape {
                              : (IA == 0 || kFloatPrepRow) ? 4 : 2;
 };
 
-// Resident CTAs of a kernel per SM at kThreads threads (looked up once).
-template <class K> int resident_ctas(K kernel) {
-    static const int n = [kernel] {
+// Resident CTAs of KERNEL per SM at kThreads threads, looked up once per
+// kernel (the kernel is the template argument: kernels of one signature share
+// a pointer type, so a cache keyed on the type would hand every one of them
+// the first kernel's count).
+template <auto KERNEL> int resident_ctas() {
+    static const int n = [] {
         int b = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, KERNEL, kThreads, 0) != cudaSuccess ||
             b < 1) {
             cudaGetLastError();
             b = 1;
@@ -1238,46 +1330,93 @@ inline bool rowconst_fits(const Geom &g, int G, bool row_a) {
 constexpr int kRowConstU = 4;
 template <class Op> constexpr int kRowConstWaves = HasGroup<Op>::value ? 4 : 8;
 
-template <class Op, bool ROW_A, bool WIDE>
-cudaError_t run_rowconst_kernel(const Launch &L) {
-    constexpr int G = 16 / sizeof(typename Op::In);
-    constexpr int U = kRowConstU;
-    constexpr int kMin = RowConstMinCtas<Op>::value;
-    auto kernel = [] {
-        if constexpr (kMin > 0) return k_rowconst_bounded<Op, ROW_A, U, WIDE, kMin>;
-        else return k_rowconst<Op, ROW_A, U, WIDE>;
-    }();
-    const Geom &g = L.g;
+// The per-row launch description: rows of g.n[rank - 1] elements (packs of
+// G), the outer dims, and the per-row input's strides `sr` along them.
+inline RowConstArgs rowconst_args(const Geom &g, int G, const int64_t *sr) {
     RowConstArgs r{};
     const int rank = g.rank;
     r.lp = g.n[rank - 1] / G;
     r.f_lp = make_fastdiv((uint64_t)r.lp);
     r.nd = rank - 1;
-    const int64_t *sr = ROW_A ? g.sa : g.sb;
     for (int i = 0; i < r.nd; ++i) {
         r.on[i] = g.n[i];
         r.os[i] = sr[i];
         r.f_on[i] = make_fastdiv((uint64_t)g.n[i]);
     }
+    return r;
+}
+
+// Launch a per-row flat kernel: runs of kThreads x U packs, `iters` of them
+// per CTA, for about `waves` waves of resident CTAs.  K32 indexes packs in 32
+// bits, K64 in 64: K32 runs when every run start a thread forms, and every
+// row bound, stays below 2^31 packs (grid x iters runs of kThreads x U packs
+// cover them all), whatever the occupancy behind `iters`.
+template <class Op, auto K32, auto K64>
+cudaError_t launch_rowconst(const Launch &L, RowConstArgs r, int G, int U, int waves) {
     const int64_t np = L.numel / G;
     const int64_t per_run = (int64_t)kThreads * U;
     const int64_t runs = ceil_div(np, per_run);
-    const int64_t slots = (int64_t)L.num_sms * resident_ctas(kernel) * kRowConstWaves<Op>;
-    const int64_t iters = std::max<int64_t>(1, ceil_div(runs, slots));
-    if (iters > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    auto shape = [&](int resident, int64_t &iters, int64_t &grid) {
+        const int64_t slots = (int64_t)L.num_sms * resident * waves;
+        iters = std::max<int64_t>(1, ceil_div(runs, slots));
+        grid = ceil_div(runs, iters);
+    };
+    int64_t iters = 0, grid = 0;
+    shape(resident_ctas<K32>(), iters, grid);
+    const bool narrow = grid * iters * per_run < (1ll << 31);
+    if (!narrow) shape(resident_ctas<K64>(), iters, grid);
+    if (iters > 0x7FFFFFFF || grid > kMaxGrid) return cudaErrorInvalidConfiguration;
     r.iters = (int32_t)iters;
-    const int64_t grid = ceil_div(runs, iters);
-    if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
-    return launch_pdl(kernel, grid, kThreads, L.stream, kargs<Op>(L), r);
+    if (narrow) return launch_pdl(K32, grid, kThreads, L.stream, kargs<Op>(L), r);
+    return launch_pdl(K64, grid, kThreads, L.stream, kargs<Op>(L), r);
 }
 
 template <class Op, bool ROW_A>
 cudaError_t run_rowconst(const Launch &L) {
     constexpr int G = 16 / sizeof(typename Op::In);
-    // 32-bit pack indices below 2^31 - 2^20 packs (a run's last pack and the
-    // row bounds then stay below 2^31)
-    if (L.numel / G >= (1ll << 31) - (1ll << 20)) return run_rowconst_kernel<Op, ROW_A, true>(L);
-    return run_rowconst_kernel<Op, ROW_A, false>(L);
+    constexpr int U = kRowConstU;
+    constexpr int kMin = RowConstMinCtas<Op>::value;
+    const RowConstArgs r = rowconst_args(L.g, G, ROW_A ? L.g.sa : L.g.sb);
+    if constexpr (kMin > 0)
+        return launch_rowconst<Op, k_rowconst_bounded<Op, ROW_A, U, false, kMin>,
+                               k_rowconst_bounded<Op, ROW_A, U, true, kMin>>(
+            L, r, G, U, kRowConstWaves<Op>);
+    else
+        return launch_rowconst<Op, k_rowconst<Op, ROW_A, U, false>, k_rowconst<Op, ROW_A, U, true>>(
+            L, r, G, U, kRowConstWaves<Op>);
+}
+
+// Three inputs: operand rp one value per row, the other two dense over the
+// output in order (their coalesced strides the dense ones), rows a whole
+// number of packs.
+inline bool rowconst3_fits(const Geom &g, int G, int rp) {
+    const int r = g.rank;
+    if (r < 2 || g.n[r - 1] % G != 0) return false;
+    const int64_t *st[3] = {g.sa, g.sb, g.sc};
+    for (int k = 0; k < 3; ++k)
+        if (st[k][r - 1] != (k == rp ? 0 : 1)) return false;
+    int64_t acc = g.n[r - 1];
+    for (int i = r - 2; i >= 0; --i) {
+        for (int k = 0; k < 3; ++k)
+            if (k != rp && st[k][i] != acc) return false;
+        acc *= g.n[i];
+    }
+    return true;
+}
+
+// two packs of each dense input per thread and run (MulAdd bf16
+// x[8,64,256,256] * s[1,64,1,1] + y on GB300: 30.25 us, against 32.08 with
+// four packs at 111 registers and 32.27 on the row traversal k_rows3)
+constexpr int kRowConst3U = 2;
+
+template <class Op, int RP>
+cudaError_t run_rowconst3(const Launch &L) {
+    constexpr int G = 16 / sizeof(typename Op::In);
+    constexpr int U = kRowConst3U;
+    const int64_t *sr = RP == 0 ? L.g.sa : RP == 1 ? L.g.sb : L.g.sc;
+    const RowConstArgs r = rowconst_args(L.g, G, sr);
+    return launch_rowconst<Op, k_rowconst3<Op, RP, U, false>, k_rowconst3<Op, RP, U, true>>(
+        L, r, G, U, 8);
 }
 
 template <class Op, bool NOPREFIX>
@@ -1517,6 +1656,11 @@ cudaError_t launch_op3(const Launch &L) {
             default: return cudaErrorInvalidValue;
             }
         }
+        // one input one value per row, the other two dense: the per-row flat
+        // kernel
+        if (code == 5 && rowconst3_fits(L.g, G, 1)) return run_rowconst3<Op, 1>(L);
+        if (code == 3 && rowconst3_fits(L.g, G, 0)) return run_rowconst3<Op, 0>(L);
+        if (code == 6 && rowconst3_fits(L.g, G, 2)) return run_rowconst3<Op, 2>(L);
         switch (code) {
         case 7: return run_rows3_kernel<Op, G, 1, 1, 1, V>(L);
         case 6: return run_rows3_kernel<Op, G, 1, 1, 0, V>(L);

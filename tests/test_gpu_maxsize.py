@@ -100,3 +100,28 @@ def test_past_32bit_indices(op, dtype, sa, sb, family):
     assert_bits_equal(got, want, dtype, "%s %s %s x %s" % (op, dtype, sa, sb))
     del a, b, out
     torch.cuda.empty_cache()
+
+
+def test_muladd_per_row_past_2p31_packs():
+    """MulAdd x * s + y with s one value per row past 2^31 packs of 16 bytes
+    (2^35 uint8 elements): the three-input per-row flat kernel's 64-bit pack
+    indices (three 32 GiB buffers).  x and y are shaped like the output, so
+    their offsets are the output index; s's come from the oracle's mapping."""
+    import broadcast_elementwise_gb300 as eb
+    sx, ss = ((1 << 24) + 3, 2048), ((1 << 24) + 3, 1)
+    plan = eb.Plan3(eb.descriptor("MulAdd", "uint8"), sx, ss, sx)
+    assert plan.family == "inner_vector_outer"
+    numel = plan.numel
+    assert numel // 16 >= 1 << 31
+    x = _device_input(sx, "uint8", 21)
+    s = _device_input(ss, "uint8", 22)
+    y = _device_input(sx, "uint8", 23)
+    out = torch.empty(numel, dtype=torch.uint8, device="cuda")
+    eb.execute3(plan, x.data_ptr(), s.data_ptr(), y.data_ptr(), out.data_ptr())
+    torch.cuda.synchronize()
+    idx = _samples(numel)
+    ox, os_ = oracle.offsets(sx, ss, idx)
+    want = oracle.run3("MulAdd", _gather(x, ox), _gather(s, os_), _gather(y, ox), "uint8")
+    assert_bits_equal(_gather(out, idx), want, "uint8", "MulAdd uint8 %s * %s + %s" % (sx, ss, sx))
+    del x, s, y, out
+    torch.cuda.empty_cache()

@@ -201,6 +201,14 @@ MULADD_CASES = [
     ("inner_vector_outer", (4, 16, 8, 64), (1, 16, 1, 1), (4, 16, 8, 64)),
     ("inner_vector_outer", (1, 16, 1, 1), (4, 16, 8, 64), (4, 16, 8, 64)),
     ("inner_vector_outer", (6, 256), (256,), (6, 1)),
+    # one operand one value per row, the other two dense: the per-row flat
+    # kernel, with rows shorter than a thread's run (rows change inside runs)
+    # and rows long enough for runs that stay in one row
+    ("inner_vector_outer", (6, 256), (6, 256), (6, 1)),
+    ("inner_vector_outer", (3, 37, 528), (1, 37, 1), (3, 37, 528)),
+    ("inner_vector_outer", (2, 6, 16384), (1, 6, 1), (2, 6, 16384)),
+    ("inner_vector_outer", (6, 1), (2, 6, 16384), (2, 6, 16384)),
+    ("inner_vector_outer", (2, 6, 16384), (2, 6, 16384), (2, 6, 1)),
     ("general_strided", (3, 1, 5), (1, 4, 1), (4, 5)),
     ("general_strided", (7, 1, 93), (1, 5, 93), (93,)),
     ("empty", (0, 4), (4,), (1, 4)),
