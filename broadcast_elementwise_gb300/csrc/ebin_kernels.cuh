@@ -774,7 +774,7 @@ __device__ __forceinline__ void rowconst_body(const KArgs &p, const RowConstArgs
     using Out = typename Op::Out;
     using BV = typename Op::BV;
     using BIn = typename BInOf<Op>::type;
-    // pack indices: 32-bit unless the plan's packs reach the launcher's bound
+    // pack indices: 32-bit unless a run start of the launch reaches 2^31 packs
     using I = std::conditional_t<WIDE, int64_t, int32_t>;
     constexpr int G = 16 / sizeof(In);
     constexpr bool kPrep = !ROW_A && HasPrep<Op>::value;
