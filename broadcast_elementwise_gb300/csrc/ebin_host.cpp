@@ -1187,6 +1187,7 @@ extern "C" ebin_status ebin_execute_host(ebin_plan_t plan, const void *host_a, c
             return EBIN_ERR_CUDA;
         ebin::Launch Lc = L;
         Lc.numel = n;
+        if (Lc.g.rank == 1) Lc.g.n[0] = n;   // the chunk's own extent
         Lc.A = a_moves ? (const void *)((const char *)dev_a + ib) : dev_a;
         Lc.B = b_moves ? (const void *)((const char *)dev_b + ib_b) : L.B;
         Lc.out = (char *)dev_out + (size_t)off * osz;

@@ -141,6 +141,9 @@ def _host_run(op, dtype, a, b, attrs=None, stream=None):
     ("BiasPRelu", "float16", (1, 2097155), (2, 2097155), "contiguous", 3),
     ("BiasPReluBN", "bfloat16", (1, 2097155, 1, 1), (6, 2097155), "contiguous", 3),
     ("Clip", "float32", (2097155,), (2,), "right_scalar", 3),
+    # a prepared scalar: whole-pack chunks on the per-row kernel as one row,
+    # the short last chunk on the scalar kernel
+    ("Mod", "float32", (3000001,), (), "right_scalar", 3),
     ("PRelu", "float32", (2097155,), (2097155,), "contiguous", 3),
 ])
 def test_execute_host_pipelined(op, dtype, sa, sb, fam, chunks):
