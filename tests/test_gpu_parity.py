@@ -277,6 +277,50 @@ def test_strided_input_views(op, dtype):
                     (op, dtype, shape, strides, forced, plan.family))
 
 
+# (M, N, ld): output [M, N]; the transposed input is a buffer of N * ld
+# elements read as (i, j) -> i + j * ld (a transposed view, padded when ld > M)
+TRANSPOSED = [(300, 257, 300), (1000, 70, 1003), (33, 2049, 40)]
+
+
+@pytest.mark.parametrize("op,dtype", [("Add", "float32"), ("Mul", "bfloat16"),
+                                      ("Sub", "float16"), ("Greater", "float32"),
+                                      ("Div", "int32"), ("BitwiseXor", "uint8"),
+                                      ("Max", "float64"), ("Mod", "int64"), ("RSub", "int32")])
+def test_transposed_input(op, dtype):
+    """A transposed view beside a dense input (general family, the tiled
+    kernel): both orders, tiles cut by the edges, a padded leading dimension,
+    1- to 8-byte elements, a BOOL output, and an integer divide whose zero
+    divisor sets the status word; each against the oracle on contiguous
+    copies."""
+    import torch
+    for i, (M, N, ld) in enumerate(TRANSPOSED):
+        for t_is_b in (True, False):
+            if t_is_b:
+                a, base = inputs_for(op, dtype, (M, N), (N * ld,), seed=90 + i)
+                if op in ("Div", "Mod") and dtype not in FLOATS:
+                    base[2 * ld + 3] = 0                    # divisor (3, 2)
+            else:
+                base, b = inputs_for(op, dtype, (N * ld,), (M, N), seed=90 + i)
+            t = np.lib.stride_tricks.as_strided(base, (M, N), (base.itemsize, ld * base.itemsize))
+            a_c, b_c = (a, np.ascontiguousarray(t)) if t_is_b else (np.ascontiguousarray(t), b)
+            want, wbits = oracle.run(op, a_c, b_c, dtype)
+            desc = eb.descriptor(op, dtype)
+            strides = (1, ld)
+            plan = eb.Plan(desc, (M, N), (M, N), strides_a=None if t_is_b else strides,
+                           strides_b=strides if t_is_b else None)
+            assert plan.family == "general_strided"
+            dA, dB = (to_device(a), to_device(base)) if t_is_b else (to_device(base), to_device(b))
+            osz = eb.ITEMSIZE[desc.out_dtype]
+            out = torch.empty(plan.numel * osz, dtype=torch.uint8, device="cuda")
+            eb.execute(plan, dA, dB, out)
+            bits = eb.get_device_status()
+            got = out.cpu().numpy().view(datagen.STORAGE[desc.out_dtype]).reshape(want.shape)
+            what = "%s %s [%d,%d] ld %d, %s transposed" % (op, dtype, M, N, ld,
+                                                            "B" if t_is_b else "A")
+            compare(op, dtype, got, want, what)
+            assert bits == wbits, (what, bits, wbits)
+
+
 MIXED_POW = [(ta, tb) for ta in ("float32", "float16", "bfloat16", "float64", "int32", "int64")
              for tb in ("float32", "float16", "bfloat16", "float64", "int32", "int64", "uint8",
                         "uint32", "int8", "int16", "uint16", "uint64")
