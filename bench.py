@@ -199,7 +199,8 @@ def _case_plan(eb, c):
     if c.make_c is not None:
         plan = eb.Plan3(desc, c.shape_a, c.shape_b, c.shape_c)
         return desc, plan, [c.make_a(), c.make_b(), c.make_c()]
-    return desc, eb.Plan(desc, c.shape_a, c.shape_b), [c.make_a(), c.make_b()]
+    return desc, eb.Plan(desc, c.shape_a, c.shape_b, strides_b=c.strides_b), \
+        [c.make_a(), c.make_b()]
 
 
 def _case_run(eb, plan, bufs, stream):

@@ -24,6 +24,9 @@ Not from the pages:
   6  Add fp32 [2^24,3] ~ N(0,1) + [3] ~ U(-0.5,0.5) (channels-last)       seed 5
   7  general strided, short rows: Add fp32 [8192,1,5] + [1,4096,5] and
      Mul bf16 [16384,1,3] x [1,8192,3], all ~ N(0,1)                      seed 6
+  8  general strided, a transposed view: Add fp32 A[8192,8192] + B and Mul
+     bf16 the same, B read through element strides (1, 8192) from an
+     [8192,8192] buffer (a transposed tensor), all ~ N(0,1)               seed 7
 """
 from __future__ import annotations
 
@@ -50,6 +53,7 @@ class Case:
     tags: list = field(default_factory=list)
     shape_c: tuple | None = None                 # three-input operators (MulAdd)
     make_c: Callable[[], np.ndarray] | None = None
+    strides_b: tuple | None = None               # B a view of make_b()'s buffer
 
 
 def _bn_params(seed: int, C: int, dtype: str) -> np.ndarray:
@@ -168,6 +172,13 @@ def cases(scale_log2: int = 0) -> list[Case]:
                     lambda: make("normal", "bfloat16", ma, 6, 2),
                     lambda: make("normal", "bfloat16", mb, 6, 3),
                     "general_strided", 7, ["extra"]))
+    t = 1 << max(13 - scale_log2 // 2, 6)
+    for name, op, dt, k in (("add_f32_transposed", "Add", "float32", 0),
+                            ("mul_bf16_transposed", "Mul", "bfloat16", 2)):
+        out.append(Case(name, op, dt, {}, (t, t), (t, t),
+                        lambda dt=dt, k=k: make("normal", dt, (t, t), 7, k),
+                        lambda dt=dt, k=k: make("normal", dt, (t * t,), 7, k + 1),
+                        "general_strided", 8, ["extra"], strides_b=(1, t)))
     return out
 
 

@@ -145,6 +145,8 @@ def test_families_of_the_benchmark_workloads():
     assert f == "inner_vector_outer" and n == [64, 32, 512, 1024]
     assert family("BitShift", "uint32", (1 << 26,), (1,), direction=1)[0] == "right_scalar"
     assert family("Add", "float32", (1,), (1 << 20,))[0] == "left_scalar"
+    assert eb.Plan(eb.descriptor("Add", "float32"), (8192, 8192), (8192, 8192),
+                   strides_b=(1, 8192)).family == "general_strided"      # a transposed view
     assert family("Add", "float32", (0, 5), (5,))[0] == "empty"
     assert family("Clip", "float32", (30, 40), (2,))[0] == "right_scalar"
     assert family("BatchNormalization", "float32", (300, 64), (4, 64))[0] == "repeated_block"
