@@ -393,7 +393,8 @@ void ebin_plan_cache_clear(void);
  * exception is the first validating operator on a stream, which allocates that
  * stream's status word: run one on the capturing stream before the capture
  * begins.  Launch the kernels once before the first capture, because a
- * kernel's first launch loads its module.
+ * kernel's first launch loads its module (and, for the per-row kernels, looks
+ * up its occupancy once to size the grid).
  * Errors: INVALID_ARG, ALIAS, CUDA.
  */
 ebin_status ebin_execute(ebin_plan_t plan, const void *A, const void *B, void *out,
